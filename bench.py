@@ -1,0 +1,535 @@
+#!/usr/bin/env python3
+"""Benchmark of the deterministic rank-ordered all-gather (and, beside it,
+the fixed-order BF16 reductions) on one GB300.
+
+Metric: all-gather / all-reduce GB/s and us per call vs size, and the
+fraction of the HBM roofline (bytes read + bytes written per call).
+
+Workload of the headline line: the all-gather sweep with P=8 and P=2
+simulated ranks, per-rank sizes 1, 8, 32, 64, 128 KiB, 1 MiB and 4 MiB of
+BF16 bit patterns, 16-byte aligned (the sizes of the results tables of
+"perf(cuda): vectorize the deterministic all-gather copy and right-size its
+single-block path").  One step = the 14 gathers of the sweep.  Inputs are
+resident in HBM before timing; every call is preceded (outside its CUDA-event
+interval) by an L2 flush that writes and then reads a buffer four times the
+L2 size, so each call reads its inputs from HBM.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W]        # this library
+  python bench.py --impl reference [--steps K] [--warmup W]  # the oracle on host cores
+  python bench.py --crossover                                 # single/multi-CTA sweep
+For N > 1 launch one process per GPU with torch.distributed.run; each rank
+runs the same workload on its own GPU (replicas: the path has no exchange
+step between GPUs) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "all-gather / all-reduce GB/s and us per call vs size at 1 GB300; % HBM roofline"
+UNIT = "GB/s"
+WORKLOAD = ("all-gather sweep: P=8 and P=2 simulated ranks x {1, 8, 32, 64, 128 KiB, 1 MiB, "
+            "4 MiB} per rank of BF16 bit patterns, 16-byte aligned; one step = the 14 gathers")
+FALLBACK_HBM_GBS = 6800.0
+KIB = 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["dc", "reference"], default="dc")
+    ap.add_argument("--no-reductions", action="store_true",
+                    help="skip the all_reduce / reduce_scatter / all_gather_many block")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--crossover", action="store_true", help="run the single/multi-CTA sweep")
+    ap.add_argument("--out", default=None, help="also write the JSON line to this file")
+    args = ap.parse_args(argv)
+    if args.warmup < 0 or args.steps < 1:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    return args
+
+
+# ------------------------------------------------------------ workload ---
+
+def sweep_cases():
+    """(P, bytes_per_rank, seed) of the 14 gathers, in step order."""
+    return [(c.P, c.bytes_per_rank, c.seed) for c in W.config2_cases()]
+
+
+def algorithmic_bytes(P: int, B: int) -> int:
+    """Bytes read plus bytes written by one gather: P*B read, P*B written."""
+    return 2 * P * B
+
+
+# ------------------------------------------------------------- helpers ---
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "reduce_copy_rank_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken from the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for ln in lines:
+        if ln.startswith("#") or not ln.strip():
+            continue
+        parts = dict(kv.split("=", 1) for kv in ln.split() if "=" in kv)
+        if parts.get("kernel") == kernel and parts.get("source") == kernel_source_digest():
+            try:
+                return float(parts["bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.split(",") for ln in self.file.read().splitlines() if ln.count(",") >= 8]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------- the oracle arm ---
+
+def cpu_oracle_sample(seconds: float):
+    """Time the oracle (single-threaded C byte-loop gather) on the host over
+    whole passes of the sweep until `seconds` have elapsed (at least one)."""
+    import oracle
+
+    cases = sweep_cases()
+    host = [[W.random_bf16_patterns(seed, r, B // 2).view(np.uint8) for r in range(P)]
+            for (P, B, seed) in cases]
+    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
+    oracle.all_gather(host[0])  # load the library outside the timing
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        for peers in host:
+            oracle.all_gather(peers)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": step_bytes * passes / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{passes} full passes of the 14-gather sweep ({step_bytes} algorithmic bytes "
+                      f"each) through the single-threaded C oracle, {el:.1f} s"}
+
+
+def run_reference(args) -> int:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+
+    cases = sweep_cases()
+    host = [[W.random_bf16_patterns(seed, r, B // 2).view(np.uint8) for r in range(P)]
+            for (P, B, seed) in cases]
+    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
+    for _ in range(args.warmup):
+        for peers in host:
+            oracle.all_gather(peers)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for peers in host:
+            oracle.all_gather(peers)
+    el = time.perf_counter() - t0
+    value = step_bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded random BF16 bit patterns)",
+        "config": {"workload": WORKLOAD, "l2": "host oracle (no GPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full passes of the 14-gather sweep through the "
+                                   "single-threaded C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    emit(line, args)
+    return 0
+
+
+# ----------------------------------------------------------- GPU arm ---
+
+class Flusher:
+    """Writes, then reads, a buffer four times the L2 size: afterwards L2 holds
+    only clean lines of this buffer, so the next call's inputs come from HBM
+    and no dirty line of ours is left to be written back inside its timing."""
+
+    def __init__(self, torch, device):
+        l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20)
+        n = max(4 * l2, 256 << 20)
+        self.buf = torch.empty(n // 4, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.buf.zero_()
+        self.buf.sum()
+
+
+def timed_calls(torch, stream, flush, calls, reps):
+    """Run each call `reps` times, each preceded by a flush outside its
+    events; return per-call lists of microseconds."""
+    evs = []
+    for _ in range(reps):
+        for fn in calls:
+            flush()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            evs.append((s, e))
+    torch.cuda.synchronize()
+    out = [[] for _ in calls]
+    for i, (s, e) in enumerate(evs):
+        out[i % len(calls)].append(s.elapsed_time(e) * 1e3)
+    return out
+
+
+def build_gather_calls(torch, dc, device, cases):
+    calls, keep = [], []
+    for (P, B, seed) in cases:
+        peers = [torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)).to(device)
+                 for r in range(P)]
+        out = torch.empty(P * B, dtype=torch.uint8, device=device)
+        keep.append((peers, out))
+        calls.append(lambda peers=peers, out=out: dc.all_gather(peers, out))
+    return calls, keep
+
+
+def reductions_block(torch, dc, device, stream, flush, peak):
+    """The other paths, each measured like the sweep (flush, CUDA events,
+    median of 5): all_reduce at the five per-rank sizes, reduce_scatter
+    16384x8192 per rank, all_gather_many of the six mixed tensors (P=8)."""
+    rows = []
+    P = W.CONFIG4_P
+    for name, n in W.CONFIG4_COUNTS.items():
+        seed = W.seed_for(4, list(W.CONFIG4_COUNTS).index(name))
+        ins = [W.normal_bf16_device(seed, r, n, device) for r in range(P)]
+        outs = [torch.empty_like(x) for x in ins]
+        us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_reduce(ins, outs)], 5)[0])
+        nbytes = 4 * P * n
+        rows.append({"op": "all_reduce_bf16", "P": P, "count": n, "shape": name, "us": us,
+                     "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+        del ins, outs
+    c = W.CONFIG5_RS
+    n = c["rows"] * c["cols"]
+    ins = [W.normal_bf16_device(W.seed_for(5, 0), r, n, device) for r in range(c["P"])]
+    outs = [torch.empty(n // c["P"], dtype=torch.bfloat16, device=device) for _ in range(c["P"])]
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.reduce_scatter(ins, outs)], 5)[0])
+    nbytes = 2 * c["P"] * n + 2 * n
+    rows.append({"op": "reduce_scatter_bf16", "P": c["P"], "count": n, "shape": "16384x8192",
+                 "us": us, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    del ins, outs
+    P = W.CONFIG5_MANY_P
+    tens = [[W.random_bytes_device(W.seed_for(5, 1), r, B, device, tensor=t) for r in range(P)]
+            for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
+    outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in W.CONFIG5_MANY_SIZES]
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather_many(tens, outs)], 5)[0])
+    nbytes = 2 * P * sum(W.CONFIG5_MANY_SIZES)
+    rows.append({"op": "all_gather_many", "P": P, "count": len(W.CONFIG5_MANY_SIZES),
+                 "shape": "{3 B, 4 KiB, 100000 B, 1 MiB, 7 MiB+5 B, 32 MiB}", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    return rows
+
+
+def e2e_measure(torch, dc, device, stream, cases, steps):
+    """The same sweep through the public API with host buffers: each step
+    copies every call's inputs from pinned host memory, gathers, and copies
+    each output back to pinned host memory."""
+    host_in, dev_in, dev_out, host_out = [], [], [], []
+    for (P, B, seed) in cases:
+        hin = [torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)).pin_memory()
+               for r in range(P)]
+        host_in.append(hin)
+        dev_in.append([torch.empty(B, dtype=torch.uint8, device=device) for _ in range(P)])
+        dev_out.append(torch.empty(P * B, dtype=torch.uint8, device=device))
+        host_out.append(torch.empty(P * B, dtype=torch.uint8).pin_memory())
+    h2d = sum(P * B for (P, B, _s) in cases)
+
+    def step():
+        for i in range(len(cases)):
+            for d, h in zip(dev_in[i], host_in[i]):
+                d.copy_(h, non_blocking=True)
+            dc.all_gather(dev_in[i], dev_out[i])
+            host_out[i].copy_(dev_out[i], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    for i, (P, B, seed) in enumerate(cases[:1]):  # the round trip really happened
+        want = np.concatenate([W.random_bf16_patterns(seed, r, B // 2).view(np.uint8) for r in range(P)])
+        assert np.array_equal(host_out[i].numpy(), want)
+    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
+    return {"value": step_bytes / ms / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": steps}
+
+
+def run_dc(args) -> int:
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (this arm times the library's kernels)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+
+    import reduce_copy_rank_gb300 as dc
+
+    dc.lib()
+    stream = torch.cuda.current_stream()
+    flush = Flusher(torch, device)
+    peak, peak_src = load_peaks()
+    cases = sweep_cases()
+    calls, _keep = build_gather_calls(torch, dc, device, cases)
+    single_max = dc.get_option("gather_single_max_bytes")
+    paths = ["single" if P * B <= single_max else "multi" for (P, B, _s) in cases]
+
+    timed_calls(torch, stream, flush, calls, max(args.warmup, 0))  # warm-up steps
+
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    launches0 = dc.launch_count()
+    t_wall = time.perf_counter()
+    per_call = timed_calls(torch, stream, flush, calls, args.steps)  # ends with a synchronize
+    t_wall = time.perf_counter() - t_wall
+    launches = dc.launch_count() - launches0
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
+    gpu_ms_total = sum(sum(x) for x in per_call) / 1e3
+    if dist:
+        t = torch.tensor([gpu_ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        gpu_ms_total = float(t.item())
+    ms_per_step = gpu_ms_total / args.steps
+    value = world * step_bytes / ms_per_step / 1e6  # GB/s over all ranks
+
+    table = []
+    kern_time = {"multi": 0.0, "single": 0.0}
+    kern_bytes = {"multi": 0, "single": 0}
+    kern_launches = {"multi": 0, "single": 0}
+    for (P, B, _s), path, us_list in zip(cases, paths, per_call):
+        med = statistics.median(us_list)
+        nbytes = algorithmic_bytes(P, B)
+        table.append({"P": P, "bytes_per_rank": B, "path": path, "us_median": med,
+                      "us_p10": float(np.percentile(us_list, 10)),
+                      "us_p90": float(np.percentile(us_list, 90)),
+                      "gbs": nbytes / med / 1e3, "frac": nbytes / med / 1e3 / peak})
+        kern_time[path] += sum(us_list)
+        kern_bytes[path] += nbytes * len(us_list)
+        kern_launches[path] += len(us_list)
+    dom = max(kern_time, key=kern_time.get)
+    kname = {"multi": "dc_gather_kernel<1,64,true>", "single": "dc_gather_single_kernel<1,64,true>"}[dom]
+    achieved = kern_bytes[dom] / kern_time[dom] / 1e3  # GB/s
+    traffic = load_traffic(kname)
+    big = [row for row in table if row["P"] == 8 and row["bytes_per_rank"] == 4 << 20][0]
+
+    extra = None
+    if not args.no_reductions:
+        extra = reductions_block(torch, dc, device, stream, flush, peak)
+    e2e = e2e_measure(torch, dc, device, stream, cases, min(args.steps, 20))
+    if dist:
+        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["value"] = world * step_bytes / float(t.item()) / 1e6
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded random BF16 bit patterns, resident in HBM)",
+        "config": {"workload": WORKLOAD, "P": [8, 2], "bytes_per_rank": W.CONFIG2_SIZES,
+                   "l2": "flushed before every call (write + read of 4x L2), outside the events",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "gather_single_max_bytes": single_max},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "launches": kern_launches[dom],
+                     "share": kern_time[dom] / sum(kern_time.values()),
+                     "algorithmic_bytes_per_launch": kern_bytes[dom] / max(kern_launches[dom], 1)},
+        "headline_4MiB_P8": {"us": big["us_median"], "gbs": big["gbs"], "frac": big["frac"]},
+        "per_call": table,
+        "gpu_launches": launches,
+        "wall_s_timed_region": t_wall,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if extra is not None:
+        line["other_ops"] = extra
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(args.cpu_seconds)
+    if rank == 0:
+        emit(line, args)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_crossover(args) -> int:
+    """Single-CTA vs multi-CTA time per call across output sizes, for the
+    gather (P=2 and P=8) and the all_reduce (P=8); prints one JSON line per
+    point and the largest size where the single CTA is not slower."""
+    import torch
+
+    import reduce_copy_rank_gb300 as dc
+
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = Flusher(torch, device)
+    result = {"gather": {}, "all_reduce": {}}
+    sizes = [256, 512, 1 * KIB, 2 * KIB, 4 * KIB, 8 * KIB, 16 * KIB, 32 * KIB, 64 * KIB,
+             128 * KIB, 256 * KIB]
+    for P in (2, 8):
+        best = 0
+        for B in sizes:
+            peers = [torch.randint(0, 256, (B,), dtype=torch.uint8, device=device) for _ in range(P)]
+            out = torch.empty(P * B, dtype=torch.uint8, device=device)
+            t = {}
+            for path in (1, 2):
+                with dc.options(force_path=path):
+                    t[path] = statistics.median(timed_calls(torch, stream, flush,
+                                                            [lambda: dc.all_gather(peers, out)], 30)[0])
+            print(json.dumps({"op": "all_gather", "P": P, "out_bytes": P * B,
+                              "single_us": t[1], "multi_us": t[2]}), flush=True)
+            if t[1] <= t[2]:
+                best = P * B
+        result["gather"][P] = best
+    P = 8
+    best = 0
+    for B in sizes:
+        n = B // 2
+        ins = [torch.randn(n, device=device).to(torch.bfloat16) for _ in range(P)]
+        outs = [torch.empty_like(x) for x in ins]
+        t = {}
+        for path in (1, 2):
+            with dc.options(force_path=path):
+                t[path] = statistics.median(timed_calls(torch, stream, flush,
+                                                        [lambda: dc.all_reduce(ins, outs)], 30)[0])
+        print(json.dumps({"op": "all_reduce", "P": P, "in_bytes_per_rank": B,
+                          "single_us": t[1], "multi_us": t[2]}), flush=True)
+        if t[1] <= t[2]:
+            best = B
+    result["all_reduce"][P] = best
+    print(json.dumps({"crossover": result}), flush=True)
+    return 0
+
+
+def emit(line, args):
+    s = json.dumps(line)
+    print(s, flush=True)
+    if args.out:
+        with open(args.out, "w") as fh:
+            fh.write(s + "\n")
+
+
+def main(argv=None) -> int:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.crossover:
+        return run_crossover(args)
+    return run_dc(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,162 @@
+/*
+ * dc.h -- C ABI of libdc: the data-parallel core of a deterministic
+ * collective on one GPU, with the world's P ranks held as P buffers in the
+ * GPU's own memory.
+ *
+ * Pages cited by title:
+ *   [PR491] "perf(cuda): vectorize the deterministic all-gather copy and
+ *           right-size its single-block path" (RL-Kernel pull request 491).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_ptrs / outs / bytes_per_rank are HOST arrays that the
+ *     call reads before it returns; the pointers stored in them are DEVICE
+ *     addresses of the current device (cudaMalloc, torch CUDA tensors, or
+ *     managed memory).  The caller owns all memory.
+ *   - The work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     runs asynchronously.  A call allocates no memory, never synchronises,
+ *     launches at most one kernel, and copies every pointer and size into the
+ *     kernel's parameters, so it may be captured into a CUDA graph and the
+ *     host arrays may be freed as soon as it returns.
+ *   - Arguments are checked before any CUDA call; a rejected call launches
+ *     nothing and returns a status with a message in dc_last_error().  A
+ *     launch failure returns DC_ERR_CUDA.  Faults inside the kernel surface at
+ *     the caller's next synchronisation, as for any CUDA kernel.
+ *   - A call whose size is zero succeeds without launching anything (after P
+ *     has been checked).
+ *   - Results never depend on the path, grid size or stream timing: the
+ *     gathers are exact byte copies and the reductions use one fixed
+ *     per-element order.
+ *   - Calls are thread-safe; options (dc_set_option) are process-wide.
+ */
+#ifndef DC_H
+#define DC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *dc_stream_t;
+
+typedef enum {
+    DC_OK = 0,
+    DC_ERR_INVALID = 1,  /* bad count, null pointer, size overflow */
+    DC_ERR_ALIGN = 2,    /* a BF16 pointer that is not 2-byte aligned */
+    DC_ERR_OVERLAP = 3,  /* an output range overlaps an input or another output */
+    DC_ERR_TOO_MANY = 4, /* all_gather_many table larger than the limits below */
+    DC_ERR_CUDA = 5,     /* the CUDA runtime refused the launch */
+    DC_ERR_TIMEOUT = 6   /* reserved for bounded device waits; no current kernel waits */
+} dc_status_t;
+
+#define DC_MAX_RANKS 64          /* P <= 64 */
+#define DC_MANY_MAX_TENSORS 256  /* all_gather_many: T <= 256 */
+#define DC_MANY_MAX_SEGMENTS 1024 /* all_gather_many: T * P <= 1024 */
+
+/*
+ * dc_all_gather -- rank-ordered all-gather ([PR491] section "What",
+ * copy_rank_ordered bullet; the Python API there is all_gather(input, out=)).
+ *
+ *   out[r*bytes_per_rank + j] = peer_ptrs[r][j]   for r < P, j < bytes_per_rank.
+ *
+ * peer_ptrs: host array of P device pointers, each to bytes_per_rank bytes
+ *            (any alignment; peers may overlap or repeat each other).
+ * P:         1..DC_MAX_RANKS.
+ * out:       device pointer to P*bytes_per_rank bytes, any alignment; it must
+ *            not overlap any peer range (DC_ERR_OVERLAP).
+ * Bytes outside [out, out + P*bytes_per_rank) are never written.
+ * Path: the 16-byte flat vector copy when out, bytes_per_rank and every peer
+ * are 16-byte aligned, the realigning per-rank copy otherwise; one CTA below
+ * the measured single-block threshold (output bytes), a grid sized from the
+ * 16-byte vector count and the SM count above it.
+ */
+dc_status_t dc_all_gather(const void *const *peer_ptrs, int P, size_t bytes_per_rank,
+                          void *out, dc_stream_t stream);
+
+/*
+ * dc_all_gather_many -- T independent all-gathers in one launch, each into
+ * its own output, with no packing ([PR491] results paragraph and the
+ * author's reply on all_gather_many: several gathers, one handshake, no
+ * packing).
+ *
+ * peer_ptrs:      host array of T*P device pointers, tensor-major:
+ *                 peer_ptrs[t*P + r] is rank r's payload of tensor t.
+ * bytes_per_rank: host array of T sizes (zero allowed).
+ * outs:           host array of T device pointers; outs[t] receives
+ *                 P*bytes_per_rank[t] bytes in rank order.  Outputs must not
+ *                 overlap each other or any payload.
+ * T:              0..DC_MANY_MAX_TENSORS, and T*P <= DC_MANY_MAX_SEGMENTS
+ *                 (DC_ERR_TOO_MANY otherwise).
+ */
+dc_status_t dc_all_gather_many(const void *const *peer_ptrs, const size_t *bytes_per_rank,
+                               void *const *outs, int T, int P, dc_stream_t stream);
+
+/*
+ * dc_all_reduce_bf16 -- deterministic all_reduce of P BF16 buffers
+ * ([PR491] sections "What" and "Not in this PR"; the page does not print the
+ * arithmetic, and this is the reading used): for every i < count,
+ *
+ *   acc = f32(in_ptrs[0][i]);  acc = acc + f32(in_ptrs[q][i]) for q = 1..P-1
+ *   (binary32, round to nearest even, in that order);
+ *   out_ptrs[r][i] = bf16_round_nearest_even(acc) for every r < P.
+ *
+ * in_ptrs, out_ptrs: host arrays of P device pointers to `count` BF16
+ *            elements each, 2-byte aligned (DC_ERR_ALIGN).  out_ptrs[r] may
+ *            be exactly equal to an input pointer (in place); any other
+ *            overlap between outputs and inputs, or between outputs, is
+ *            DC_ERR_OVERLAP.  Inputs may overlap each other.
+ * Subnormals are kept; NaN inputs give a NaN (payload unspecified).
+ */
+dc_status_t dc_all_reduce_bf16(const void *const *in_ptrs, void *const *out_ptrs, int P,
+                               size_t count, dc_stream_t stream);
+
+/*
+ * dc_reduce_scatter_bf16 -- deterministic reduce_scatter: input = world x
+ * output, as the author's reply on [PR491] describes it.  Each input holds
+ * P*count_per_shard BF16 elements; rank r receives shard r:
+ *
+ *   out_ptrs[r][j] = fold over q = 0..P-1 of in_ptrs[q][r*count_per_shard + j]
+ *
+ * with the fold of dc_all_reduce_bf16.  out_ptrs[r] may be exactly
+ * in_ptrs[q] + r*count_per_shard for some q (in place); other overlaps are
+ * DC_ERR_OVERLAP.  Pointers must be 2-byte aligned.
+ */
+dc_status_t dc_reduce_scatter_bf16(const void *const *in_ptrs, void *const *out_ptrs, int P,
+                                   size_t count_per_shard, dc_stream_t stream);
+
+/* Message describing the last failed call on this thread ("" if none). */
+const char *dc_last_error(void);
+
+/* Name of a status code, e.g. "DC_ERR_OVERLAP". */
+const char *dc_status_name(int status);
+
+/*
+ * Process-wide tuning and test options.  Keys:
+ *   "force_path"              0 = automatic, 1 = single CTA, 2 = multi CTA
+ *   "force_generic"           1 = never use the flat aligned gather path
+ *   "gather_single_max_bytes" single-CTA gather up to this many output bytes
+ *   "reduce_single_max_bytes" single-CTA reductions up to this many input
+ *                             bytes per rank
+ *   "grid_ctas"               0 = automatic, else the multi-CTA grid size
+ *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
+ * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
+ * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES and DC_GRID_CTAS set
+ * the initial values (read once, at the first call).
+ * dc_set_option returns 0, or -1 for an unknown key or a negative value.
+ * dc_get_option returns the value, or -1 for an unknown key.
+ */
+int dc_set_option(const char *key, long long value);
+long long dc_get_option(const char *key);
+
+/* Kernels launched by this library since it was loaded (all threads). */
+unsigned long long dc_launch_count(void);
+
+/* ABI version: 1. */
+int dc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DC_H */

@@ -1,0 +1,519 @@
+// dc_api.cu -- the C ABI of libdc: argument checks, path planning, launch.
+//
+// Pages cited by title:
+//   [PR491] "perf(cuda): vectorize the deterministic all-gather copy and
+//           right-size its single-block path" (RL-Kernel pull request 491).
+//
+// Planning follows what [PR491] learned on B200 and re-measures it here:
+//  * the single-block path only pays below a crossover on OUTPUT bytes for
+//    the gather (section "What", kAllGatherSingleBlockMaxBytes) and on INPUT
+//    bytes per rank for the reductions (author's reply:
+//    input_bytes <= kSingleBlockFastPathMaxBytes); both thresholds here are
+//    measured on GB300 and can be changed at run time;
+//  * the multi-block grid is sized from the 16-byte vector (or 8-element
+//    group) count, not from bytes (review nitpick on
+//    DeterministicCollectiveState::all_gather: a byte-sized grid left 15 of
+//    16 blocks idle), and capped at the resident CTAs of the whole GPU.
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "dc.h"
+#include "dc_internal.h"
+
+namespace {
+
+using namespace dc;
+
+thread_local char g_err[512] = "";
+std::atomic<unsigned long long> g_launches{0};
+
+// Measured single-CTA crossovers (bytes); see the crossover sweep of the
+// benchmark.  Initial values, replaced by the measured ones.
+constexpr long long kDefaultGatherSingleMax = 32 * 1024;
+constexpr long long kDefaultReduceSingleMax = 16 * 1024;
+
+struct Options {
+  std::atomic<long long> force_path{0};
+  std::atomic<long long> force_generic{0};
+  std::atomic<long long> gather_single_max{kDefaultGatherSingleMax};
+  std::atomic<long long> reduce_single_max{kDefaultReduceSingleMax};
+  std::atomic<long long> grid_ctas{0};
+  std::atomic<long long> test_fail_launch{0};
+};
+Options g_opt;
+std::once_flag g_env_once;
+
+struct OptionKey {
+  const char* key;
+  const char* env;
+  std::atomic<long long>* slot;
+};
+const OptionKey kKeys[] = {
+    {"force_path", "DC_FORCE_PATH", &g_opt.force_path},
+    {"force_generic", "DC_FORCE_GENERIC", &g_opt.force_generic},
+    {"gather_single_max_bytes", "DC_GATHER_SINGLE_MAX_BYTES", &g_opt.gather_single_max},
+    {"reduce_single_max_bytes", "DC_REDUCE_SINGLE_MAX_BYTES", &g_opt.reduce_single_max},
+    {"grid_ctas", "DC_GRID_CTAS", &g_opt.grid_ctas},
+    {"test_fail_launch", nullptr, &g_opt.test_fail_launch},
+};
+
+void read_env_once() {
+  std::call_once(g_env_once, [] {
+    for (const OptionKey& k : kKeys) {
+      if (!k.env) continue;
+      const char* v = std::getenv(k.env);
+      if (!v || !*v) continue;
+      char* end = nullptr;
+      long long x = std::strtoll(v, &end, 0);
+      if (end && *end == '\0' && x >= 0) k.slot->store(x);
+    }
+  });
+}
+
+dc_status_t fail(dc_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+dc_status_t ok() {
+  g_err[0] = '\0';
+  return DC_OK;
+}
+
+bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
+  return na > 0 && nb > 0 && a < b + nb && b < a + na;
+}
+
+// ---------------------------------------------------- device properties ---
+constexpr int kMaxDevices = 64;
+constexpr int kFamilies = 16;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_occ[kMaxDevices][kFamilies];
+
+dc_status_t current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DC_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+  }
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(DC_ERR_CUDA, "device index %d out of range", *dev);
+  return DC_OK;
+}
+
+dc_status_t sm_count(int dev, int* sms) {
+  int v = g_sms[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      return fail(DC_ERR_CUDA, "cannot read the SM count: %s", cudaGetErrorString(e));
+    }
+    g_sms[dev].store(v, std::memory_order_relaxed);
+  }
+  *sms = v;
+  return DC_OK;
+}
+
+template <class F>
+int occupancy(int dev, int family, F query) {
+  int v = g_occ[dev][family].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    v = std::max(1, query());
+    g_occ[dev][family].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+// Multi-CTA grid: enough CTAs that each thread has about `per_thread` units
+// in one pass, at most the CTAs that fit on the GPU at once (later passes
+// loop inside the CTA).  Each CTA then owns `chunk` contiguous units.
+void plan_grid(uint64_t total, int block, int per_thread, int sms, int ctas_per_sm, int* grid,
+               uint64_t* chunk) {
+  const uint64_t per_cta = static_cast<uint64_t>(block) * per_thread;
+  uint64_t g = (total + per_cta - 1) / per_cta;
+  const uint64_t cap = static_cast<uint64_t>(sms) * ctas_per_sm;
+  g = std::min<uint64_t>(std::max<uint64_t>(g, 1), cap);
+  const long long forced = g_opt.grid_ctas.load();
+  if (forced > 0) g = std::min<uint64_t>(static_cast<uint64_t>(forced), std::max<uint64_t>(total, 1));
+  // keep every CTA's run below 2^31 units (32-bit loop counters)
+  const uint64_t min_g = (total + (1ull << 31) - 1) >> 31;
+  g = std::max<uint64_t>(g, std::max<uint64_t>(min_g, 1));
+  uint64_t c = (total + g - 1) / g;
+  g = (total + c - 1) / c;
+  *grid = static_cast<int>(g);
+  *chunk = c;
+}
+
+bool use_single(uint64_t size_bytes, long long threshold, uint64_t total_units) {
+  const long long f = g_opt.force_path.load();
+  if (total_units >= (1ull << 31)) return false;
+  if (f == 1) return true;
+  if (f == 2) return false;
+  return size_bytes <= static_cast<uint64_t>(threshold);
+}
+
+dc_status_t check_launch(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DC_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+  }
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ok();
+}
+
+// --------------------------------------------------------------- gather ---
+struct GatherTensor {
+  uint64_t out;
+  uint64_t bytes;
+  const void* const* peers;  // P pointers
+};
+
+// Fill jobs and sources of a gather parameter block from T tensors.
+template <class Params>
+void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_flat) {
+  uint64_t v = 0;
+  int nj = 0;
+  for (int t = 0; t < T; ++t) {
+    const GatherTensor& g = ts[t];
+    if (g.bytes == 0) continue;
+    GatherJob& J = prm.job[nj];
+    J.out = g.out;
+    J.bytes = g.bytes;
+    J.src0 = static_cast<uint32_t>(nj * P);
+    bool aligned = allow_flat && (g.out & 15u) == 0 && (g.bytes & 15u) == 0;
+    for (int r = 0; r < P; ++r) {
+      const uint64_t s = reinterpret_cast<uint64_t>(g.peers[r]);
+      prm.src[nj * P + r] = s;
+      aligned = aligned && (s & 15u) == 0;
+    }
+    J.flags = aligned ? kJobFlat : (g.bytes < kGatherSmallBytes ? kJobSmall : 0u);
+    const uint64_t end = g.out + static_cast<uint64_t>(P) * g.bytes;
+    J.nvec = ((end - 1) >> 4) - (g.out >> 4) + 1;
+    J.vfirst = v;
+    v += J.nvec;
+    ++nj;
+  }
+  prm.njobs = nj;
+  prm.P = P;
+  prm.total_vec = v;
+}
+
+template <class Params>
+dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cudaStream_t stream) {
+  if (g_opt.test_fail_launch.load())
+    return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
+  int dev = 0, sms = 0;
+  dc_status_t st = current_device(&dev);
+  if (st != DC_OK) return st;
+  st = sm_count(dev, &sms);
+  if (st != DC_OK) return st;
+  const bool single = use_single(out_bytes, g_opt.gather_single_max.load(), prm.total_vec);
+  int grid = 1;
+  if (single) {
+    prm.chunk_vec = prm.total_vec;
+  } else {
+    const int occ = occupancy(dev, family, [family] { return gather_ctas_per_sm(family); });
+    plan_grid(prm.total_vec, kGatherBlock, kGatherUnroll, sms, occ, &grid, &prm.chunk_vec);
+  }
+  return check_launch(launch_gather(prm, grid, single, stream), "all-gather");
+}
+
+// --------------------------------------------------------------- reduce ---
+template <class Params>
+void set_reduce_job(Params& prm, int j, uint64_t in_off, uint64_t count, uint32_t out0,
+                    uint32_t nout, const uint64_t* in, const uint64_t* out_ptrs, int P,
+                    uint64_t* units) {
+  ReduceJob& J = prm.job[j];
+  J.in_off = in_off;
+  J.count = count;
+  J.out0 = out0;
+  J.nout = nout;
+  const uint32_t o = static_cast<uint32_t>((in[0] + 2 * in_off) & 15u);
+  bool vec = true;
+  for (int q = 0; q < P; ++q) vec = vec && ((in[q] + 2 * in_off) & 15u) == o;
+  for (uint32_t m = 0; m < nout; ++m) vec = vec && (out_ptrs[out0 + m] & 15u) == o;
+  if (vec) {
+    uint64_t head = ((16u - o) & 15u) / 2;
+    if (head > count) head = count;
+    const uint64_t rest = count - head;
+    J.head = static_cast<uint32_t>(head);
+    J.flags = kJobVec;
+    J.nunits = (head ? 1 : 0) + rest / 8 + ((rest & 7u) ? 1 : 0);
+  } else {
+    J.head = 0;
+    J.flags = 0;
+    J.nunits = count;
+  }
+  J.ufirst = *units;
+  *units += J.nunits;
+}
+
+template <class Params>
+dc_status_t launch_reduce_plan(Params& prm, int family, uint64_t in_bytes_per_rank,
+                               cudaStream_t stream, const char* what) {
+  if (g_opt.test_fail_launch.load())
+    return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
+  int dev = 0, sms = 0;
+  dc_status_t st = current_device(&dev);
+  if (st != DC_OK) return st;
+  st = sm_count(dev, &sms);
+  if (st != DC_OK) return st;
+  const bool single = use_single(in_bytes_per_rank, g_opt.reduce_single_max.load(), prm.total_units);
+  int grid = 1;
+  if (single) {
+    prm.chunk_units = prm.total_units;
+  } else {
+    const int P = prm.P;
+    const bool scatter = prm.njobs > 1 || family >= 8;
+    const int occ = occupancy(dev, family, [P, scatter] { return reduce_ctas_per_sm(P, scatter); });
+    plan_grid(prm.total_units, kReduceBlock, kReduceUnroll, sms, occ, &grid, &prm.chunk_units);
+  }
+  return check_launch(launch_reduce(prm, grid, single, stream), what);
+}
+
+int reduce_family(int P, bool scatter) {
+  const int pt = P == 8 ? 0 : P == 4 ? 1 : P == 2 ? 2 : 3;
+  return (scatter ? 8 : 4) + pt;
+}
+
+dc_status_t check_bf16_ptrs(const void* const* ptrs, int P, const char* name) {
+  for (int r = 0; r < P; ++r) {
+    if (!ptrs[r]) return fail(DC_ERR_INVALID, "%s[%d] is NULL", name, r);
+    if (reinterpret_cast<uint64_t>(ptrs[r]) & 1u)
+      return fail(DC_ERR_ALIGN, "%s[%d] = %p is not 2-byte aligned (BF16)", name, r, ptrs[r]);
+  }
+  return DC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dc_status_t dc_all_gather(const void* const* peer_ptrs, int P, size_t bytes_per_rank, void* out,
+                          dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (bytes_per_rank == 0) return ok();
+  if (!peer_ptrs) return fail(DC_ERR_INVALID, "peer_ptrs is NULL");
+  if (!out) return fail(DC_ERR_INVALID, "out is NULL");
+  const uint64_t B = bytes_per_rank;
+  if (B > UINT64_MAX / static_cast<uint64_t>(P))
+    return fail(DC_ERR_INVALID, "P * bytes_per_rank overflows");
+  const uint64_t o = reinterpret_cast<uint64_t>(out);
+  const uint64_t total = B * static_cast<uint64_t>(P);
+  if (o + total < o) return fail(DC_ERR_INVALID, "output range wraps around the address space");
+  for (int r = 0; r < P; ++r) {
+    const uint64_t s = reinterpret_cast<uint64_t>(peer_ptrs[r]);
+    if (!s) return fail(DC_ERR_INVALID, "peer_ptrs[%d] is NULL", r);
+    if (s + B < s) return fail(DC_ERR_INVALID, "peer %d range wraps around", r);
+    if (overlaps(o, total, s, B))
+      return fail(DC_ERR_OVERLAP, "output overlaps the payload of rank %d", r);
+  }
+  GatherParams1 prm{};
+  GatherTensor t{o, B, peer_ptrs};
+  fill_gather(prm, &t, 1, P, g_opt.force_generic.load() == 0);
+  return launch_gather_plan(prm, 0, total, static_cast<cudaStream_t>(stream));
+}
+
+dc_status_t dc_all_gather_many(const void* const* peer_ptrs, const size_t* bytes_per_rank,
+                               void* const* outs, int T, int P, dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (T < 0) return fail(DC_ERR_INVALID, "T = %d is negative", T);
+  if (T > kManyMaxTensors)
+    return fail(DC_ERR_TOO_MANY, "T = %d exceeds %d tensors per call", T, kManyMaxTensors);
+  if (static_cast<long long>(T) * P > kManyMaxSegments)
+    return fail(DC_ERR_TOO_MANY, "T * P = %lld exceeds %d segments per call",
+                static_cast<long long>(T) * P, kManyMaxSegments);
+  if (T == 0) return ok();
+  if (!peer_ptrs || !bytes_per_rank || !outs)
+    return fail(DC_ERR_INVALID, "peer_ptrs, bytes_per_rank and outs must not be NULL");
+  GatherTensor ts[kManyMaxTensors];
+  uint64_t out_total = 0;
+  int live = 0;
+  for (int t = 0; t < T; ++t) {
+    const uint64_t B = bytes_per_rank[t];
+    ts[t] = GatherTensor{reinterpret_cast<uint64_t>(outs[t]), B, peer_ptrs + static_cast<size_t>(t) * P};
+    if (B == 0) continue;
+    ++live;
+    if (!outs[t]) return fail(DC_ERR_INVALID, "outs[%d] is NULL", t);
+    if (B > UINT64_MAX / static_cast<uint64_t>(P))
+      return fail(DC_ERR_INVALID, "P * bytes_per_rank[%d] overflows", t);
+    const uint64_t tot = B * static_cast<uint64_t>(P);
+    if (ts[t].out + tot < ts[t].out) return fail(DC_ERR_INVALID, "outs[%d] range wraps around", t);
+    out_total += tot;
+    for (int r = 0; r < P; ++r) {
+      const uint64_t s = reinterpret_cast<uint64_t>(ts[t].peers[r]);
+      if (!s) return fail(DC_ERR_INVALID, "peer_ptrs[%d] (tensor %d, rank %d) is NULL", t * P + r, t, r);
+      if (s + B < s) return fail(DC_ERR_INVALID, "tensor %d rank %d range wraps around", t, r);
+    }
+  }
+  if (live == 0) return ok();
+  // every output against every output and every payload
+  for (int t = 0; t < T; ++t) {
+    if (ts[t].bytes == 0) continue;
+    const uint64_t ot = ts[t].out, nt = ts[t].bytes * P;
+    for (int u = 0; u < T; ++u) {
+      if (ts[u].bytes == 0) continue;
+      if (u > t && overlaps(ot, nt, ts[u].out, ts[u].bytes * P))
+        return fail(DC_ERR_OVERLAP, "outputs of tensors %d and %d overlap", t, u);
+      for (int r = 0; r < P; ++r)
+        if (overlaps(ot, nt, reinterpret_cast<uint64_t>(ts[u].peers[r]), ts[u].bytes))
+          return fail(DC_ERR_OVERLAP, "output of tensor %d overlaps the payload of tensor %d rank %d",
+                      t, u, r);
+    }
+  }
+  const bool allow_flat = g_opt.force_generic.load() == 0;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (live <= kManySmallTensors && live * P <= kManySmallSegments) {
+    GatherParamsS prm{};
+    GatherTensor packed[kManySmallTensors];
+    int n = 0;
+    for (int t = 0; t < T; ++t)
+      if (ts[t].bytes) packed[n++] = ts[t];
+    fill_gather(prm, packed, n, P, allow_flat);
+    return launch_gather_plan(prm, 1, out_total, s);
+  }
+  static thread_local GatherParamsL prm;  // 18 KB: keep it off the stack
+  std::memset(&prm, 0, sizeof prm);
+  fill_gather(prm, ts, T, P, allow_flat);
+  return launch_gather_plan(prm, 2, out_total, s);
+}
+
+dc_status_t dc_all_reduce_bf16(const void* const* in_ptrs, void* const* out_ptrs, int P,
+                               size_t count, dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (count == 0) return ok();
+  if (!in_ptrs || !out_ptrs) return fail(DC_ERR_INVALID, "in_ptrs and out_ptrs must not be NULL");
+  if (count > UINT64_MAX / 2) return fail(DC_ERR_INVALID, "count overflows");
+  dc_status_t st = check_bf16_ptrs(in_ptrs, P, "in_ptrs");
+  if (st != DC_OK) return st;
+  st = check_bf16_ptrs(const_cast<const void* const*>(out_ptrs), P, "out_ptrs");
+  if (st != DC_OK) return st;
+  const uint64_t nb = 2 * static_cast<uint64_t>(count);
+  uint64_t in[kMaxRanks], out[kMaxRanks];
+  for (int r = 0; r < P; ++r) {
+    in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
+    out[r] = reinterpret_cast<uint64_t>(out_ptrs[r]);
+    if (in[r] + nb < in[r] || out[r] + nb < out[r])
+      return fail(DC_ERR_INVALID, "buffer of rank %d wraps around", r);
+  }
+  for (int r = 0; r < P; ++r) {
+    for (int u = r + 1; u < P; ++u)
+      if (overlaps(out[r], nb, out[u], nb))
+        return fail(DC_ERR_OVERLAP, "outputs of ranks %d and %d overlap", r, u);
+    for (int q = 0; q < P; ++q)
+      if (out[r] != in[q] && overlaps(out[r], nb, in[q], nb))
+        return fail(DC_ERR_OVERLAP,
+                    "output of rank %d overlaps input %d without being the same buffer", r, q);
+  }
+  ReduceParams1 prm{};
+  prm.P = P;
+  prm.njobs = 1;
+  for (int r = 0; r < P; ++r) {
+    prm.in[r] = in[r];
+    prm.out[r] = out[r];
+  }
+  uint64_t units = 0;
+  set_reduce_job(prm, 0, 0, count, 0, static_cast<uint32_t>(P), in, out, P, &units);
+  prm.total_units = units;
+  return launch_reduce_plan(prm, reduce_family(P, false), nb, static_cast<cudaStream_t>(stream),
+                            "all_reduce");
+}
+
+dc_status_t dc_reduce_scatter_bf16(const void* const* in_ptrs, void* const* out_ptrs, int P,
+                                   size_t count_per_shard, dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (count_per_shard == 0) return ok();
+  if (!in_ptrs || !out_ptrs) return fail(DC_ERR_INVALID, "in_ptrs and out_ptrs must not be NULL");
+  const uint64_t C = count_per_shard;
+  if (C > UINT64_MAX / 2 / static_cast<uint64_t>(P))
+    return fail(DC_ERR_INVALID, "P * count_per_shard overflows");
+  dc_status_t st = check_bf16_ptrs(in_ptrs, P, "in_ptrs");
+  if (st != DC_OK) return st;
+  st = check_bf16_ptrs(const_cast<const void* const*>(out_ptrs), P, "out_ptrs");
+  if (st != DC_OK) return st;
+  const uint64_t nb_out = 2 * C, nb_in = nb_out * static_cast<uint64_t>(P);
+  uint64_t in[kMaxRanks], out[kMaxRanks];
+  for (int r = 0; r < P; ++r) {
+    in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
+    out[r] = reinterpret_cast<uint64_t>(out_ptrs[r]);
+    if (in[r] + nb_in < in[r] || out[r] + nb_out < out[r])
+      return fail(DC_ERR_INVALID, "buffer of rank %d wraps around", r);
+  }
+  for (int r = 0; r < P; ++r) {
+    for (int u = r + 1; u < P; ++u)
+      if (overlaps(out[r], nb_out, out[u], nb_out))
+        return fail(DC_ERR_OVERLAP, "outputs of ranks %d and %d overlap", r, u);
+    for (int q = 0; q < P; ++q) {
+      if (out[r] == in[q] + static_cast<uint64_t>(r) * nb_out) continue;  // in place: shard r
+      if (overlaps(out[r], nb_out, in[q], nb_in))
+        return fail(DC_ERR_OVERLAP,
+                    "output of rank %d overlaps input %d outside that input's shard %d", r, q, r);
+    }
+  }
+  ReduceParamsP prm{};
+  prm.P = P;
+  prm.njobs = P;
+  for (int r = 0; r < P; ++r) {
+    prm.in[r] = in[r];
+    prm.out[r] = out[r];
+  }
+  uint64_t units = 0;
+  for (int r = 0; r < P; ++r)
+    set_reduce_job(prm, r, static_cast<uint64_t>(r) * C, C, static_cast<uint32_t>(r), 1, in, out, P,
+                   &units);
+  prm.total_units = units;
+  return launch_reduce_plan(prm, reduce_family(P, true), nb_in, static_cast<cudaStream_t>(stream),
+                            "reduce_scatter");
+}
+
+const char* dc_last_error(void) { return g_err; }
+
+const char* dc_status_name(int status) {
+  switch (status) {
+    case DC_OK: return "DC_OK";
+    case DC_ERR_INVALID: return "DC_ERR_INVALID";
+    case DC_ERR_ALIGN: return "DC_ERR_ALIGN";
+    case DC_ERR_OVERLAP: return "DC_ERR_OVERLAP";
+    case DC_ERR_TOO_MANY: return "DC_ERR_TOO_MANY";
+    case DC_ERR_CUDA: return "DC_ERR_CUDA";
+    case DC_ERR_TIMEOUT: return "DC_ERR_TIMEOUT";
+    default: return "DC_ERR_UNKNOWN";
+  }
+}
+
+int dc_set_option(const char* key, long long value) {
+  read_env_once();
+  if (!key || value < 0) return -1;
+  for (const OptionKey& k : kKeys)
+    if (std::strcmp(k.key, key) == 0) {
+      k.slot->store(value);
+      return 0;
+    }
+  return -1;
+}
+
+long long dc_get_option(const char* key) {
+  read_env_once();
+  if (!key) return -1;
+  for (const OptionKey& k : kKeys)
+    if (std::strcmp(k.key, key) == 0) return k.slot->load();
+  return -1;
+}
+
+unsigned long long dc_launch_count(void) { return g_launches.load(); }
+
+int dc_version(void) { return 1; }
+
+}  // extern "C"

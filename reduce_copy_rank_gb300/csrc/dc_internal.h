@@ -1,0 +1,116 @@
+// dc_internal.h -- definitions shared by the host planner (dc_api.cu) and the
+// kernels (dc_gather.cu, dc_reduce.cu).  Not part of the public C ABI.
+//
+// Everything a kernel needs travels by value in one parameter block, so a
+// launch allocates nothing, reads no host memory after it is enqueued and can
+// be captured in a CUDA graph.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dc {
+
+constexpr int kMaxRanks = 64;            // P limit (pointer tables stay small)
+constexpr int kManyMaxTensors = 256;     // all_gather_many: tensors per call
+constexpr int kManyMaxSegments = 1024;   // all_gather_many: tensors x ranks
+constexpr int kManySmallTensors = 16;    // the small parameter block of all_gather_many
+constexpr int kManySmallSegments = 128;
+
+// Threads per CTA of each kernel family.
+constexpr int kGatherBlock = 512;
+constexpr int kGatherSingleBlock = 1024;       // aligned (flat) jobs only
+constexpr int kGatherSingleBlockGeneral = 512;  // any job: the realigning path needs registers
+constexpr int kGatherUnroll = 4;         // 16-byte vectors in flight per thread
+constexpr int kGatherRealignUnroll = 2;  // realigned vectors (two loads each) per thread
+constexpr int kReduceBlock = 256;
+constexpr int kReduceSingleBlock = 512;
+constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread
+
+// Below this many bytes per rank a gather job is copied byte by byte: each
+// rank then spans at most a handful of 16-byte output vectors, the total is
+// at most kMaxRanks * 127 bytes, and the vector machinery would cost more
+// than it saves.
+constexpr uint64_t kGatherSmallBytes = 128;
+
+// ------------------------------------------------------------- gather ---
+enum : uint32_t {
+  kJobFlat = 1u,   // out, bytes and every source are 16-byte aligned
+  kJobSmall = 2u,  // bytes < kGatherSmallBytes: byte path
+};
+
+// One rank-ordered gather: P sources of `bytes` bytes into out[0, P*bytes).
+// Its output is covered by the 16-byte-aligned vectors
+// [out/16, (out + P*bytes - 1)/16]; `nvec` counts them and `vfirst` is the
+// global index of the first one (prefix over the jobs of one launch).
+struct GatherJob {
+  uint64_t out;
+  uint64_t bytes;
+  uint64_t vfirst;
+  uint64_t nvec;
+  uint32_t src0;   // index of rank 0's source pointer in GatherParams::src
+  uint32_t flags;
+};
+
+template <int MAXJ, int MAXS>
+struct GatherParams {
+  uint64_t total_vec;   // sum of nvec over the jobs
+  uint64_t chunk_vec;   // contiguous output vectors per CTA
+  int32_t njobs;
+  int32_t P;
+  GatherJob job[MAXJ];
+  uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
+};
+
+using GatherParams1 = GatherParams<1, kMaxRanks>;
+using GatherParamsS = GatherParams<kManySmallTensors, kManySmallSegments>;
+using GatherParamsL = GatherParams<kManyMaxTensors, kManyMaxSegments>;
+
+// ---------------------------------------------------------- reduction ---
+enum : uint32_t {
+  kJobVec = 1u,    // every pointer of the job has the same address mod 16
+};
+
+// One fixed-order reduction over `count` elements: element i reads
+// in[q][in_off + i] for q = 0..P-1 and writes out[out0 + m][i] for
+// m = 0..nout-1.  Work units: an optional scalar head (elements before the
+// first 16-byte boundary), 8-element groups, and an optional scalar tail;
+// for a job without kJobVec every unit is one element.
+struct ReduceJob {
+  uint64_t in_off;
+  uint64_t count;
+  uint64_t ufirst;
+  uint64_t nunits;
+  uint32_t out0;
+  uint32_t nout;
+  uint32_t head;
+  uint32_t flags;
+};
+
+template <int MAXJ>
+struct ReduceParams {
+  uint64_t total_units;
+  uint64_t chunk_units;
+  int32_t njobs;
+  int32_t P;
+  uint64_t in[kMaxRanks];
+  uint64_t out[kMaxRanks];
+  ReduceJob job[MAXJ];
+};
+
+using ReduceParams1 = ReduceParams<1>;          // all_reduce
+using ReduceParamsP = ReduceParams<kMaxRanks>;  // reduce_scatter: one job per rank
+
+// ------------------------------------------------- launch entry points ---
+// Each returns the error of the launch itself (cudaGetLastError).
+cudaError_t launch_gather(const GatherParams1& p, int grid, bool single, cudaStream_t s);
+cudaError_t launch_gather(const GatherParamsS& p, int grid, bool single, cudaStream_t s);
+cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceParams1& p, int grid, bool single, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, cudaStream_t s);
+
+// Resident CTAs per SM of the multi-CTA kernels (occupancy API, per device).
+int gather_ctas_per_sm(int which);  // 0: one job, 1: small many, 2: large many
+int reduce_ctas_per_sm(int P, bool scatter);
+
+}  // namespace dc

@@ -1,0 +1,229 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/dc.h, and rejects bad arguments before any CUDA call.
+
+Pointers here are fake device addresses: every rejected call returns before
+touching them.  Calls that pass validation use the ``test_fail_launch``
+option, which makes the library report a launch failure instead of
+launching, so nothing here ever reaches a GPU.
+"""
+from __future__ import annotations
+
+import os
+import re
+import threading
+
+import pytest
+
+import reduce_copy_rank_gb300 as dc
+from reduce_copy_rank_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dc.h")
+
+OK, INVALID, ALIGN, OVERLAP, TOO_MANY, CUDA = 0, 1, 2, 3, 4, 5
+BASE = 0x7F00_0000_0000  # a fake, 256-byte aligned device address
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    _build.build()
+    dc.lib()
+    yield
+
+
+@pytest.fixture
+def no_launch():
+    with dc.options(test_fail_launch=1):
+        yield
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for needed in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
+                   "dc_reduce_scatter_bf16", "dc_last_error", "dc_set_option"):
+        assert needed in names
+
+
+def test_library_exports_every_declared_function():
+    L = dc.lib()
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_names():
+    assert dc.lib().dc_version() == 1
+    for code, name in dc.STATUS.items():
+        assert dc.lib().dc_status_name(code).decode() == name
+
+
+# ------------------------------------------------------------- all_gather ---
+
+def test_gather_rejects_bad_rank_counts():
+    assert dc.dc_all_gather([], 0, 16, BASE) == INVALID
+    assert "P = 0" in dc.last_error()
+    assert dc.dc_all_gather([BASE] * 65, 65, 16, BASE + (1 << 30)) == INVALID
+
+
+def test_gather_zero_bytes_is_a_noop_without_launch():
+    before = dc.launch_count()
+    assert dc.dc_all_gather([0, 0], 2, 0, 0) == OK
+    assert dc.launch_count() == before
+
+
+def test_gather_rejects_null_pointers():
+    assert dc.dc_all_gather([BASE, 0], 2, 16, BASE + 4096) == INVALID
+    assert dc.dc_all_gather([BASE, BASE + 64], 2, 16, 0) == INVALID
+
+
+@pytest.mark.parametrize("out_off", [-31, -1, 0, 1, 15])
+def test_gather_rejects_overlap(out_off):
+    peers = [BASE + 1024, BASE + 2048]
+    out = peers[1] + out_off  # a 32-byte output starting here touches rank 1's 16 bytes
+    assert dc.dc_all_gather(peers, 2, 16, out) == OVERLAP
+    assert "overlaps" in dc.last_error()
+
+
+@pytest.mark.parametrize("out_off", [-32, 16])
+def test_gather_adjacent_is_not_overlap(no_launch, out_off):
+    peers = [BASE + 1024, BASE + 2048]
+    assert dc.dc_all_gather(peers, 2, 16, peers[1] + out_off) == CUDA  # passed validation
+    assert "injected" in dc.last_error()
+
+
+def test_gather_peers_may_repeat(no_launch):
+    assert dc.dc_all_gather([BASE, BASE, BASE], 3, 100, BASE + 4096) == CUDA
+
+
+def test_gather_rejects_size_overflow():
+    assert dc.dc_all_gather([BASE, BASE], 2, (1 << 63) + 1, BASE + 4096) == INVALID
+
+
+# -------------------------------------------------------- all_gather_many ---
+
+def test_many_limits():
+    P = 8
+    T = 129  # 1032 segments
+    assert dc.dc_all_gather_many([BASE] * (T * P), [16] * T, [BASE + 4096] * T, T, P) == TOO_MANY
+    assert dc.dc_all_gather_many([BASE] * 257, [16] * 257, [BASE] * 257, 257, 1) == TOO_MANY
+    assert dc.dc_all_gather_many([], [], [], 0, 4) == OK
+
+
+def test_many_rejects_overlapping_outputs():
+    P = 2
+    peers = [BASE, BASE + 64, BASE + 128, BASE + 192]
+    outs = [BASE + 4096, BASE + 4096 + 16]  # first output is 32 bytes long
+    assert dc.dc_all_gather_many(peers, [16, 16], outs, 2, P) == OVERLAP
+
+
+def test_many_rejects_output_over_another_tensors_payload():
+    P = 2
+    peers = [BASE, BASE + 64, BASE + 4096, BASE + 128]  # tensor 1 rank 0 sits in output 0
+    outs = [BASE + 4096, BASE + 8192]
+    assert dc.dc_all_gather_many(peers, [16, 16], outs, 2, P) == OVERLAP
+
+
+def test_many_zero_sized_tensors_are_skipped(no_launch):
+    before = dc.launch_count()
+    assert dc.dc_all_gather_many([0, 0, 0, 0], [0, 0], [0, 0], 2, 2) == OK
+    assert dc.launch_count() == before
+    peers = [0, 0, BASE, BASE + 64]
+    assert dc.dc_all_gather_many(peers, [0, 32], [0, BASE + 4096], 2, 2) == CUDA
+
+
+# ------------------------------------------------------------- reductions ---
+
+def test_reduce_rejects_misaligned_bf16():
+    ins = [BASE, BASE + 1024 + 1]
+    outs = [BASE + 4096, BASE + 8192]
+    assert dc.dc_all_reduce_bf16(ins, outs, 2, 8) == ALIGN
+    assert dc.dc_reduce_scatter_bf16(ins, outs, 2, 8) == ALIGN
+
+
+def test_reduce_zero_count_is_a_noop():
+    before = dc.launch_count()
+    assert dc.dc_all_reduce_bf16([0] * 4, [0] * 4, 4, 0) == OK
+    assert dc.dc_reduce_scatter_bf16([0] * 4, [0] * 4, 4, 0) == OK
+    assert dc.launch_count() == before
+
+
+def test_all_reduce_in_place_allowed(no_launch):
+    ins = [BASE + i * 4096 for i in range(4)]
+    assert dc.dc_all_reduce_bf16(ins, ins, 4, 100) == CUDA  # validation passed
+    # outputs that are other ranks' inputs are also exact aliases
+    assert dc.dc_all_reduce_bf16(ins, ins[::-1], 4, 100) == CUDA
+
+
+def test_all_reduce_rejects_partial_overlap():
+    ins = [BASE + i * 4096 for i in range(4)]
+    outs = [BASE + 64 * 1024 + i * 4096 for i in range(4)]
+    outs[2] = ins[1] + 2  # shifted by one element
+    assert dc.dc_all_reduce_bf16(ins, outs, 4, 100) == OVERLAP
+    outs[2] = outs[1] + 100  # two outputs overlap
+    assert dc.dc_all_reduce_bf16(ins, outs, 4, 100) == OVERLAP
+
+
+def test_reduce_scatter_in_place_shard_allowed(no_launch):
+    P, C = 4, 64
+    ins = [BASE + i * 4096 for i in range(P)]
+    outs = [ins[r] + 2 * r * C for r in range(P)]  # each rank's own shard
+    assert dc.dc_reduce_scatter_bf16(ins, outs, P, C) == CUDA
+
+
+def test_reduce_scatter_rejects_other_shard():
+    P, C = 4, 64
+    ins = [BASE + i * 4096 for i in range(P)]
+    outs = [BASE + 64 * 1024 + r * 1024 for r in range(P)]
+    outs[1] = ins[0]  # shard 0 of input 0 is not rank 1's shard
+    assert dc.dc_reduce_scatter_bf16(ins, outs, P, C) == OVERLAP
+
+
+def test_reduce_rejects_null():
+    assert dc.dc_all_reduce_bf16([BASE, 0], [BASE + 4096, BASE + 8192], 2, 8) == INVALID
+
+
+# ---------------------------------------------------------------- options ---
+
+def test_options_roundtrip():
+    assert dc.get_option("force_path") in (0, 1, 2)
+    with dc.options(force_path=2, grid_ctas=7):
+        assert dc.get_option("force_path") == 2
+        assert dc.get_option("grid_ctas") == 7
+    assert dc.lib().dc_set_option(b"no_such_option", 1) == -1
+    assert dc.lib().dc_get_option(b"no_such_option") == -1
+    assert dc.lib().dc_set_option(b"grid_ctas", -5) == -1
+
+
+def test_rejected_calls_launch_nothing():
+    before = dc.launch_count()
+    dc.dc_all_gather([BASE], 1, 16, BASE + 8)
+    dc.dc_all_reduce_bf16([BASE + 1], [BASE + 4096], 1, 4)
+    assert dc.launch_count() == before
+
+
+def test_last_error_is_per_thread():
+    msgs = {}
+
+    def worker(name, P):
+        dc.dc_all_gather([BASE] * max(P, 1), P, 16, BASE + 4096)
+        msgs[name] = dc.last_error()
+
+    t1 = threading.Thread(target=worker, args=("a", 0))
+    t1.start()
+    t1.join()
+    dc.dc_all_gather([BASE, BASE], 2, 16, BASE + 8)  # overlap on this thread
+    assert "P = 0" in msgs["a"]
+    assert "overlaps" in dc.last_error()
+
+
+def test_tensor_api_requires_cuda_tensors():
+    import torch
+
+    x = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        dc.all_gather([x], torch.zeros(16, dtype=torch.uint8))

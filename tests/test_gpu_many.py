@@ -1,0 +1,158 @@
+"""GPU parity of all_gather_many (several gathers in one launch, one output
+per tensor) against the oracle, bit exact, plus CUDA-graph capture and
+replay of every entry point.
+
+Workload: 6 tensors per rank of {3 B, 4 KiB, 100000 B, 1 MiB, 7 MiB+5 B,
+32 MiB}, P=8, random bytes.  Page, by title: "perf(cuda): vectorize the
+deterministic all-gather copy and right-size its single-block path"
+(results paragraph and the author's reply on all_gather_many: several
+gathers, one handshake, no packing).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import Placed, assert_bf16_equal, bf16_tensor, bits_of
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import reduce_copy_rank_gb300 as dc  # noqa: E402
+
+
+def run_many(tensors_np, in_offs, out_offs, **opts):
+    T = len(tensors_np)
+    P = len(tensors_np[0])
+    srcs, outs, ptrs, sizes = [], [], [], []
+    for t in range(T):
+        B = tensors_np[t][0].size
+        sizes.append(B)
+        for r in range(P):
+            s = Placed(B, in_offs[t][r])
+            s.write(tensors_np[t][r])
+            srcs.append(s)
+            ptrs.append(s.ptr())
+        outs.append(Placed(P * B, out_offs[t]))
+    with dc.options(**opts):
+        st = dc.dc_all_gather_many(ptrs, sizes, [o.ptr() for o in outs], T, P,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == 0, dc.last_error()
+    torch.cuda.synchronize()
+    return [o.read() for o in outs], all(o.guards_intact() for o in outs)
+
+
+def test_config5_gather_many_full_size():
+    P = W.CONFIG5_MANY_P
+    seed = W.seed_for(5, 1)
+    tensors = [[W.random_bytes(seed, r, B, tensor=t) for r in range(P)]
+               for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
+    want = oracle.all_gather_many(tensors)
+    T = len(tensors)
+    for opts in ({}, {"force_generic": 1}):
+        got, guards = run_many(tensors, [[0] * P] * T, [0] * T, **opts)
+        for t in range(T):
+            assert np.array_equal(got[t], want[t]), (t, opts)
+        assert guards
+
+
+def test_many_random_layouts():
+    rng = np.random.default_rng(W.seed_for(5, 9000))
+    for trial in range(12):
+        P = int(rng.choice([1, 2, 3, 8]))
+        T = int(rng.integers(1, 20))
+        tensors = [[rng.integers(0, 256, int(B), dtype=np.uint8) for _ in range(P)]
+                   for B in rng.choice([0, 1, 15, 16, 17, 127, 128, 129, 4096, 65537, 300000], T)]
+        in_offs = [[int(x) for x in rng.integers(0, 16, P)] for _ in range(T)]
+        out_offs = [int(x) for x in rng.integers(0, 16, T)]
+        want = oracle.all_gather_many(tensors)
+        got, guards = run_many(tensors, in_offs, out_offs)
+        for t in range(T):
+            assert np.array_equal(got[t], want[t]), (trial, t)
+        assert guards
+
+
+def test_many_large_table():
+    """More tensors than the small parameter block holds (T=100, P=8)."""
+    rng = np.random.default_rng(W.seed_for(5, 9001))
+    P, T = 8, 100
+    tensors = [[rng.integers(0, 256, int(B), dtype=np.uint8) for _ in range(P)]
+               for B in rng.integers(1, 3000, T)]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, [[0] * P] * T, [int(x) for x in rng.integers(0, 16, T)])
+    for t in range(T):
+        assert np.array_equal(got[t], want[t]), t
+    assert guards
+
+
+def test_many_tensor_api():
+    P = 4
+    tensors = [[torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda") for _ in range(P)]
+               for n in (5, 4096, 777)]
+    outs = [torch.empty(P * p[0].numel(), dtype=torch.uint8, device="cuda") for p in tensors]
+    ret = dc.all_gather_many(tensors, outs)
+    assert ret is outs
+    for p, o in zip(tensors, outs):
+        assert torch.equal(o, torch.cat(p))
+
+
+def test_cuda_graph_capture_and_replay():
+    """Every entry point captured into one CUDA graph and replayed with new
+    input values: the launches read no host memory after capture."""
+    P, n, B = 8, 65536 + 8, 4096 * 3 + 4
+    ar_in = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ar_out = [torch.empty_like(x) for x in ar_in]
+    rs_in = [torch.empty(P * 1024, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    rs_out = [torch.empty(1024, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    g_in = [torch.empty(B, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    g_out = torch.empty(P * B, dtype=torch.uint8, device="cuda")
+    m_in = [[torch.empty(s, dtype=torch.uint8, device="cuda") for _ in range(P)] for s in (3, 5000)]
+    m_out = [torch.empty(P * s, dtype=torch.uint8, device="cuda") for s in (3, 5000)]
+
+    def fill(seed):
+        for r in range(P):
+            ar_in[r].copy_(bf16_tensor(W.normal_bf16(seed, r, n)))
+            rs_in[r].copy_(bf16_tensor(W.normal_bf16(seed + 1, r, P * 1024)))
+            g_in[r].copy_(torch.from_numpy(W.random_bytes(seed, r, B)))
+            for t in range(2):
+                m_in[t][r].copy_(torch.from_numpy(W.random_bytes(seed, r, m_in[t][r].numel(), t + 1)))
+
+    def body():
+        dc.all_reduce(ar_in, ar_out)
+        dc.reduce_scatter(rs_in, rs_out)
+        dc.all_gather(g_in, g_out)
+        dc.all_gather_many(m_in, m_out)
+
+    fill(W.seed_for(5, 9100))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        body()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    before = dc.launch_count()
+    with torch.cuda.graph(g):
+        body()
+    assert dc.launch_count() - before == 4
+    for seed in (W.seed_for(5, 9101), W.seed_for(5, 9102)):
+        fill(seed)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        host_ar = [bits_of(x) for x in ar_in]
+        want = oracle.all_reduce_bf16(host_ar)
+        for r in range(P):
+            assert_bf16_equal(bits_of(ar_out[r]), want, "graph all_reduce")
+        want_rs = oracle.reduce_scatter_bf16([bits_of(x) for x in rs_in])
+        for r in range(P):
+            assert_bf16_equal(bits_of(rs_out[r]), want_rs[r], "graph reduce_scatter")
+        assert np.array_equal(g_out.cpu().numpy(), oracle.all_gather([x.cpu().numpy() for x in g_in]))
+        for t in range(2):
+            assert np.array_equal(m_out[t].cpu().numpy(),
+                                  oracle.all_gather([x.cpu().numpy() for x in m_in[t]]))
