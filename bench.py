@@ -63,6 +63,9 @@ def parse_args(argv=None):
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--crossover", action="store_true", help="run the single/multi-CTA sweep")
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
+    ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
+                    help="profiling helper: run one call REPS times and exit, e.g. "
+                         "gather:8:4194304:3 or allreduce:8:268435456:2 (BYTES per rank)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps must be >= 1 and --warmup >= 0")
@@ -514,6 +517,36 @@ def run_crossover(args) -> int:
     return 0
 
 
+def run_case(args) -> int:
+    """Run one operation a few times with nothing else on the GPU (for ncu)."""
+    import torch
+
+    import reduce_copy_rank_gb300 as dc
+
+    op, P, nbytes, reps = args.case.split(":")
+    P, nbytes, reps = int(P), int(nbytes), int(reps)
+    device = torch.device("cuda", 0)
+    if op == "gather":
+        peers = [torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=device) for _ in range(P)]
+        out = torch.empty(P * nbytes, dtype=torch.uint8, device=device)
+        fn = lambda: dc.all_gather(peers, out)  # noqa: E731
+    elif op == "allreduce":
+        ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
+        outs = [torch.empty_like(x) for x in ins]
+        fn = lambda: dc.all_reduce(ins, outs)  # noqa: E731
+    elif op == "reducescatter":
+        ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
+        outs = [torch.empty(nbytes // 2 // P, dtype=torch.bfloat16, device=device) for _ in range(P)]
+        fn = lambda: dc.reduce_scatter(ins, outs)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown op {op}")
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    print(f"ran {op} P={P} bytes_per_rank={nbytes} x{reps}")
+    return 0
+
+
 def emit(line, args):
     s = json.dumps(line)
     print(s, flush=True)
@@ -528,6 +561,8 @@ def main(argv=None) -> int:
         return run_reference(args)
     if args.crossover:
         return run_crossover(args)
+    if args.case:
+        return run_case(args)
     return run_dc(args)
 
 

@@ -47,17 +47,23 @@ __device__ __forceinline__ void st16(uint4* p, const uint4& v) {
                : "memory");
 }
 
-// Output bytes [s, s+16) of the 32-byte little-endian sequence lo || hi,
-// where s = 4*Q + t/8 (t in {0, 8, 16, 24}).  Word j of the result is the
-// 32-bit window starting t bits into word Q+j of the sequence.
-template <int Q>
-__device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uint32_t t) {
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+// Output bytes [s, s+16) of the 32-byte little-endian sequence lo || hi
+// (s in 0..15): the 32-bit words starting at word s/4 of the sequence, each
+// shifted right by 8*(s%4) bits with the next word's low bytes funnelled in.
+__device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uint32_t s) {
+  const uint32_t t = (s & 3u) * 8u;
+  uint32_t w0, w1, w2, w3, w4;
+  switch (s >> 2) {
+    case 0: w0 = lo.x; w1 = lo.y; w2 = lo.z; w3 = lo.w; w4 = hi.x; break;
+    case 1: w0 = lo.y; w1 = lo.z; w2 = lo.w; w3 = hi.x; w4 = hi.y; break;
+    case 2: w0 = lo.z; w1 = lo.w; w2 = hi.x; w3 = hi.y; w4 = hi.z; break;
+    default: w0 = lo.w; w1 = hi.x; w2 = hi.y; w3 = hi.z; w4 = hi.w; break;
+  }
   uint4 r;
-  r.x = __funnelshift_r(w[Q + 0], w[Q + 1], t);
-  r.y = __funnelshift_r(w[Q + 1], w[Q + 2], t);
-  r.z = __funnelshift_r(w[Q + 2], w[Q + 3], t);
-  r.w = __funnelshift_r(w[Q + 3], w[Q + 4], t);
+  r.x = __funnelshift_r(w0, w1, t);
+  r.y = __funnelshift_r(w1, w2, t);
+  r.z = __funnelshift_r(w2, w3, t);
+  r.w = __funnelshift_r(w3, w4, t);
   return r;
 }
 

@@ -13,21 +13,21 @@
 //  * The unit of work is a 16-byte-aligned OUTPUT vector.  A launch covers
 //    the output vectors of one or more jobs (all_gather_many packs several
 //    gathers into one launch), numbered by a prefix over the jobs.  Each CTA
-//    owns one contiguous run of them, so no thread ever searches for its rank
-//    per element: the CTA finds its first job and rank once (one 64-bit
-//    division per CTA and job), then walks ranks in order.
-//  * Aligned job (flat): rank r owns output vectors [r*B/16, (r+1)*B/16); all
-//    threads of a CTA stream each rank's part of its run with LDG.128 /
-//    STG.128, UNROLL vectors in flight per thread.
-//  * Unaligned job: the vectors that lie inside one rank's bytes are
-//    "interior"; their source starts at a fixed offset s = (src - dst) mod 16.
-//    For s = 0 they are copied like the flat case; otherwise each output
-//    vector is built from the two aligned source blocks that cover it with a
-//    funnel shift, so loads and stores both stay 16 bytes wide and aligned.
-//    The few vectors that mix two ranks' bytes (one per rank boundary) or
-//    stick out of the output (first and last) are written byte by byte by one
-//    warp.  Reads never leave the 16-byte blocks that hold source bytes, so
-//    they stay inside the source allocation.
+//    owns one contiguous run of them and finds its first job once.
+//  * Inside a run, thread t takes vectors t, t+BLOCK, t+2*BLOCK, ..., UNROLL
+//    of them at a time with all loads issued before the first store, across
+//    rank boundaries: the flat loop of the page.  (The page's first version
+//    copied rank by rank, leaving threads idle and serialising the ranks'
+//    reads; a per-rank walk inside a CTA has the same defect.)  A thread's
+//    vector index only grows, so it finds its rank by walking forward from
+//    the rank of the run's first vector: comparisons, never a division per
+//    element.
+//  * Aligned job (flat): plain LDG.128 / STG.128.
+//  * Unaligned job: each output vector that lies inside one rank's bytes is
+//    built from the two aligned source blocks that cover it with a funnel
+//    shift, so loads and stores stay 16 bytes wide and aligned; the few
+//    vectors that straddle two ranks or stick out of the output (at most P+1
+//    per job) are written byte by byte.
 //  * Jobs with fewer than kGatherSmallBytes per rank are copied byte by byte.
 #include "dc_device.cuh"
 #include "dc_internal.h"
@@ -35,129 +35,116 @@
 namespace dc {
 namespace {
 
-template <int BLOCK, int UNROLL>
-__device__ __forceinline__ void copy_aligned(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                             uint32_t n) {
-  for (uint32_t i = threadIdx.x; i < n; i += BLOCK * UNROLL) {
+// Aligned job (flat): rank r owns output vectors [r*vp, (r+1)*vp), vp = B/16.
+// Thread t copies vectors a+t, a+t+BLOCK, ... of the CTA's run [a, b), UNROLL
+// at a time with every load issued before the first store, so the whole
+// CTA's run is in flight at once whatever the rank boundaries.  A thread's
+// vector index only grows, so its rank is found by walking forward from the
+// rank of the run's first vector: one 64-bit division per thread, then
+// comparisons (at most P steps in total).
+template <int BLOCK, int UNROLL, int MAXJ, int MAXS>
+__device__ __forceinline__ void gather_flat(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
+                                            uint64_t a, uint64_t b) {
+  const uint64_t vp = J.bytes >> 4;
+  uint64_t r = a / vp;
+  uint64_t rbeg = r * vp, rend = rbeg + vp;
+  uint4* out = reinterpret_cast<uint4*>(J.out);
+  for (uint64_t i = a + threadIdx.x; i < b; i += static_cast<uint64_t>(BLOCK) * UNROLL) {
     uint4 v[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      const uint32_t k = i + u * BLOCK;
-      if (k < n) v[u] = ld_nc_stream(src + k);
-    }
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const uint32_t k = i + u * BLOCK;
-      if (k < n) st16(dst + k, v[u]);
-    }
-  }
-}
-
-// dst[k] = bytes [s, s+16) of src[k] || src[k+1], s = 4*Q + t/8, for k < n.
-// Both blocks hold source bytes of output vector k, so they are in bounds.
-template <int BLOCK, int UNROLL, int Q>
-__device__ __forceinline__ void copy_realign_q(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                               uint32_t n, uint32_t t) {
-  for (uint32_t i = threadIdx.x; i < n; i += BLOCK * UNROLL) {
-    uint4 lo[UNROLL], hi[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const uint32_t k = i + u * BLOCK;
-      if (k < n) {
-        lo[u] = ld_nc_cached(src + k);
-        hi[u] = ld_nc_cached(src + k + 1);
+      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
+      if (k < b) {
+        while (k >= rend) {
+          ++r;
+          rbeg = rend;
+          rend += vp;
+        }
+        v[u] = ld_nc_stream(reinterpret_cast<const uint4*>(p.src[J.src0 + r]) + (k - rbeg));
       }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      const uint32_t k = i + u * BLOCK;
-      if (k < n) st16(dst + k, realign16<Q>(lo[u], hi[u], t));
+      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
+      if (k < b) st16(out + k, v[u]);
     }
   }
 }
 
-template <int BLOCK>
-__device__ __forceinline__ void copy_realign(const uint4* src, uint4* dst, uint32_t n, uint32_t s) {
-  constexpr int U = kGatherRealignUnroll;
-  const uint32_t t = (s & 3u) * 8u;
-  switch (s >> 2) {  // uniform across the CTA
-    case 0: copy_realign_q<BLOCK, U, 0>(src, dst, n, t); break;
-    case 1: copy_realign_q<BLOCK, U, 1>(src, dst, n, t); break;
-    case 2: copy_realign_q<BLOCK, U, 2>(src, dst, n, t); break;
-    default: copy_realign_q<BLOCK, U, 3>(src, dst, n, t); break;
-  }
-}
-
-// Output vectors [k0, k1) of a job that lie inside rank r's bytes
-// [d_r, d_r + B); the source of output byte x is src_r + (x - d_r).
-template <int BLOCK, int UNROLL>
-__device__ __forceinline__ void copy_interior(uint64_t src_r, uint64_t d_r, uint64_t vbase,
-                                              uint64_t k0, uint64_t k1) {
-  const uint64_t dst_addr = (vbase + k0) << 4;
-  const uint64_t src_addr = src_r + (dst_addr - d_r);
-  const uint32_t s = static_cast<uint32_t>(src_addr & 15u);
-  const uint32_t n = static_cast<uint32_t>(k1 - k0);
-  uint4* dst = reinterpret_cast<uint4*>(dst_addr);
-  if (s == 0)
-    copy_aligned<BLOCK, UNROLL>(reinterpret_cast<const uint4*>(src_addr), dst, n);
-  else
-    copy_realign<BLOCK>(reinterpret_cast<const uint4*>(src_addr - s), dst, n, s);
-}
-
-// One output vector that holds bytes of rank r and possibly rank r+1, or
-// bytes outside the job's output (first and last vector): lanes 0..15 of warp
-// 0 copy the bytes that belong to the output, one each.
-template <int MAXJ, int MAXS>
-__device__ __forceinline__ void copy_boundary(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
-                                              uint64_t vbase, uint64_t k, uint32_t r) {
-  const uint32_t lane = threadIdx.x;
-  if (lane >= 16) return;
-  const uint64_t x = ((vbase + k) << 4) + lane;
-  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
-  if (x < J.out || x >= out_end) return;
-  uint64_t d = J.out + static_cast<uint64_t>(r) * J.bytes;
-  uint32_t q = r;
-  if (x >= d + J.bytes) {  // B >= kGatherSmallBytes > 16: at most the next rank
-    ++q;
-    d += J.bytes;
-  }
-  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.src[J.src0 + q]);
-  *reinterpret_cast<uint8_t*>(x) = src[x - d];
-}
-
-template <int BLOCK, int UNROLL, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_flat(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
-                                            uint64_t a, uint64_t b) {
-  const uint64_t vp = J.bytes >> 4;  // vectors per rank
-  uint64_t r = a / vp;                // once per CTA and job
-  uint64_t k = a;
-  uint4* out = reinterpret_cast<uint4*>(J.out);
-  while (k < b) {
-    const uint64_t e = min(b, (r + 1) * vp);
-    const uint4* src = reinterpret_cast<const uint4*>(p.src[J.src0 + r]) + (k - r * vp);
-    copy_aligned<BLOCK, UNROLL>(src, out + k, static_cast<uint32_t>(e - k));
-    k = e;
-    ++r;
-  }
-}
-
+// Unaligned job (B >= kGatherSmallBytes).  Output vector k covers bytes
+// [x, x+16), x = 16*(vbase+k).  It is "interior" when all 16 bytes belong to
+// one rank r (d_r <= x and x+16 <= d_r + B): its source starts at
+// src_r + (x - d_r), at offset s = that address mod 16, so it is built from
+// the aligned source block holding that byte and the next one (one block
+// when s = 0) and stored as one aligned 16-byte vector.  The other vectors
+// (one per rank boundary, plus the first and last vector when the output is
+// not aligned) are written byte by byte by the thread that owns them; since
+// B > 16 they hold bytes of at most two ranks.  Both aligned source blocks
+// of an interior vector contain bytes of [src_r, src_r + B), so no read
+// leaves the 16-byte blocks of the source buffer.  Threads walk ranks
+// forward as in the flat case.
 template <int BLOCK, int UNROLL, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_unaligned(const GatherParams<MAXJ, MAXS>& p,
                                                  const GatherJob& J, uint64_t a, uint64_t b) {
   const uint64_t B = J.bytes;
   const uint64_t vbase = J.out >> 4;
+  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * B;
   const uint64_t first_byte = max(J.out, (vbase + a) << 4);
-  uint32_t r = static_cast<uint32_t>((first_byte - J.out) / B);  // once per CTA and job
-  if (a == 0 && (J.out & 15u)) copy_boundary(p, J, vbase, 0, 0);
-  for (; r < static_cast<uint32_t>(p.P); ++r) {
-    const uint64_t d = J.out + static_cast<uint64_t>(r) * B;
-    const uint64_t e = d + B;
-    const uint64_t lo = ((d + 15) >> 4) - vbase;  // first vector inside rank r
-    const uint64_t hi = (e >> 4) - vbase;         // one past the last one
-    if (lo >= b) break;
-    const uint64_t ia = max(a, lo), ib = min(b, hi);
-    if (ia < ib) copy_interior<BLOCK, UNROLL>(p.src[J.src0 + r], d, vbase, ia, ib);
-    if ((e & 15u) && hi >= a && hi < b) copy_boundary(p, J, vbase, hi, r);
+  uint32_t r = static_cast<uint32_t>((first_byte - J.out) / B);
+  uint64_t d = J.out + static_cast<uint64_t>(r) * B;  // rank r's first output byte
+  uint64_t e = d + B;                                  // one past its last
+  for (uint64_t i = a + threadIdx.x; i < b; i += static_cast<uint64_t>(BLOCK) * UNROLL) {
+    uint4 lo[UNROLL], hi[UNROLL];
+    uint32_t shift[UNROLL];
+    bool interior[UNROLL];
+    uint32_t rank[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
+      interior[u] = false;
+      if (k < b) {
+        const uint64_t x = (vbase + k) << 4;
+        while (x >= e) {
+          ++r;
+          d = e;
+          e += B;
+        }
+        rank[u] = r;
+        if (x >= d && x + 16 <= e) {
+          interior[u] = true;
+          const uint64_t src = p.src[J.src0 + r] + (x - d);
+          const uint32_t s = static_cast<uint32_t>(src & 15u);
+          const uint4* blk = reinterpret_cast<const uint4*>(src - s);
+          shift[u] = s;
+          if (s == 0) {
+            lo[u] = ld_nc_stream(blk);
+            hi[u] = lo[u];
+          } else {
+            lo[u] = ld_nc_cached(blk);
+            hi[u] = ld_nc_cached(blk + 1);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
+      if (k >= b) continue;
+      const uint64_t x = (vbase + k) << 4;
+      if (interior[u]) {
+        st16(reinterpret_cast<uint4*>(x), realign16(lo[u], hi[u], shift[u]));
+      } else {
+        const uint32_t q0 = rank[u];
+        const uint64_t dq = J.out + static_cast<uint64_t>(q0) * B;
+        for (uint32_t j = 0; j < 16; ++j) {
+          const uint64_t y = x + j;
+          if (y < J.out || y >= out_end) continue;
+          const bool next = y >= dq + B;  // byte of rank q0 + 1
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.src[J.src0 + q0 + (next ? 1 : 0)]);
+          *reinterpret_cast<uint8_t*>(y) = src[y - dq - (next ? B : 0)];
+        }
+      }
+    }
   }
 }
 
@@ -209,12 +196,12 @@ __device__ __forceinline__ void gather_cta(const GatherParams<MAXJ, MAXS>& p, ui
 // Multi-CTA gather: CTA c owns output vectors [c*chunk, (c+1)*chunk).
 // FLAT: every job of the launch is 16-byte aligned (the flat path only).
 template <int MAXJ, int MAXS, bool FLAT>
-__global__ void __launch_bounds__(kGatherBlock)
+__global__ void __launch_bounds__(kGatherBlock, FLAT ? 4 : 2)
     dc_gather_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
   const uint64_t g0 = static_cast<uint64_t>(blockIdx.x) * p.chunk_vec;
   if (g0 >= p.total_vec) return;
   const uint64_t g1 = min(g0 + p.chunk_vec, p.total_vec);
-  gather_cta<kGatherBlock, kGatherUnroll, FLAT>(p, g0, g1);
+  gather_cta<kGatherBlock, FLAT ? kGatherUnroll : kGatherUnrollGeneral, FLAT>(p, g0, g1);
 }
 
 // Single-CTA gather for small outputs: one CTA copies everything.
@@ -222,7 +209,7 @@ template <int MAXJ, int MAXS, bool FLAT>
 __global__ void __launch_bounds__(FLAT ? kGatherSingleBlock : kGatherSingleBlockGeneral)
     dc_gather_single_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
   constexpr int kBlock = FLAT ? kGatherSingleBlock : kGatherSingleBlockGeneral;
-  gather_cta<kBlock, kGatherUnroll, FLAT>(p, 0, p.total_vec);
+  gather_cta<kBlock, FLAT ? kGatherUnroll : kGatherUnrollGeneral, FLAT>(p, 0, p.total_vec);
 }
 
 template <int MAXJ, int MAXS>

@@ -21,8 +21,8 @@ constexpr int kManySmallSegments = 128;
 constexpr int kGatherBlock = 512;
 constexpr int kGatherSingleBlock = 1024;       // aligned (flat) jobs only
 constexpr int kGatherSingleBlockGeneral = 512;  // any job: the realigning path needs registers
-constexpr int kGatherUnroll = 4;         // 16-byte vectors in flight per thread
-constexpr int kGatherRealignUnroll = 2;  // realigned vectors (two loads each) per thread
+constexpr int kGatherUnroll = 4;         // 16-byte vectors in flight per thread (aligned)
+constexpr int kGatherUnrollGeneral = 2;  // realigned vectors (up to two loads each) per thread
 constexpr int kReduceBlock = 256;
 constexpr int kReduceSingleBlock = 512;
 constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread
