@@ -9,10 +9,16 @@ Workload of the headline line: the all-gather sweep with P=8 and P=2
 simulated ranks, per-rank sizes 1, 8, 32, 64, 128 KiB, 1 MiB and 4 MiB of
 BF16 bit patterns, 16-byte aligned (the sizes of the results tables of
 "perf(cuda): vectorize the deterministic all-gather copy and right-size its
-single-block path").  One step = the 14 gathers of the sweep.  Inputs are
-resident in HBM before timing; every call is preceded (outside its CUDA-event
-interval) by an L2 flush that writes and then reads a buffer four times the
-L2 size, so each call reads its inputs from HBM.
+single-block path").  One step = the 14 gathers of the sweep, captured once
+into a CUDA graph and replayed: an L2 flush (write, then read, of a buffer
+four times the L2 size), a timing event, the 14 calls back to back, a timing
+event.  Inputs are resident in HBM; every call reads inputs that no kernel
+has touched since the flush, so they come from HBM.  `value` = algorithmic
+bytes of a step / the time between the two events.  In the same timed
+region every call is also timed on its own (flush, event, the one launch,
+event): that gives `per_call` (us per call vs size, as the page reports it)
+and the roofline's per-launch duration.  Events between back-to-back calls
+would add about 3 us each, so the step is timed at its two ends only.
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W]        # this library
@@ -317,25 +323,48 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     return rows
 
 
+def build_step_graph(torch, flush, calls):
+    """Capture flush, an event, the calls back to back and an event into one
+    CUDA graph (events recorded as graph nodes)."""
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first use of every call outside the capture
+        flush()
+        for fn in calls:
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        flush()
+        evs[0].record()
+        for fn in calls:
+            fn()
+        evs[1].record()
+    torch.cuda.synchronize()
+    return g, evs
+
+
 def e2e_measure(torch, dc, device, stream, cases, steps):
     """The same sweep through the public API with host buffers: each step
-    copies every call's inputs from pinned host memory, gathers, and copies
-    each output back to pinned host memory."""
+    copies every call's P payloads from one pinned host buffer to the device,
+    gathers, and copies each output back to pinned host memory."""
     host_in, dev_in, dev_out, host_out = [], [], [], []
     for (P, B, seed) in cases:
-        hin = [torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)).pin_memory()
-               for r in range(P)]
-        host_in.append(hin)
-        dev_in.append([torch.empty(B, dtype=torch.uint8, device=device) for _ in range(P)])
+        h = torch.empty(P * B, dtype=torch.uint8).pin_memory()
+        for r in range(P):
+            h[r * B:(r + 1) * B].copy_(torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)))
+        host_in.append(h)
+        dev_in.append(torch.empty(P * B, dtype=torch.uint8, device=device))
         dev_out.append(torch.empty(P * B, dtype=torch.uint8, device=device))
         host_out.append(torch.empty(P * B, dtype=torch.uint8).pin_memory())
     h2d = sum(P * B for (P, B, _s) in cases)
 
     def step():
-        for i in range(len(cases)):
-            for d, h in zip(dev_in[i], host_in[i]):
-                d.copy_(h, non_blocking=True)
-            dc.all_gather(dev_in[i], dev_out[i])
+        for i, (P, B, _s) in enumerate(cases):
+            dev_in[i].copy_(host_in[i], non_blocking=True)
+            dc.all_gather([dev_in[i][r * B:(r + 1) * B] for r in range(P)], dev_out[i])
             host_out[i].copy_(dev_out[i], non_blocking=True)
 
     step()
@@ -348,12 +377,16 @@ def e2e_measure(torch, dc, device, stream, cases, steps):
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
-    for i, (P, B, seed) in enumerate(cases[:1]):  # the round trip really happened
-        want = np.concatenate([W.random_bf16_patterns(seed, r, B // 2).view(np.uint8) for r in range(P)])
-        assert np.array_equal(host_out[i].numpy(), want)
+    for i in range(len(cases)):  # the round trip really happened
+        assert torch.equal(host_out[i], host_in[i]), "e2e output differs from its input payloads"
     step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
     return {"value": step_bytes / ms / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": steps}
+
+
+def stats(xs):
+    return {"us_mean": float(np.mean(xs)), "us_median": float(np.median(xs)),
+            "us_p10": float(np.percentile(xs, 10)), "us_p90": float(np.percentile(xs, 90))}
 
 
 def run_dc(args) -> int:
@@ -382,8 +415,15 @@ def run_dc(args) -> int:
     calls, _keep = build_gather_calls(torch, dc, device, cases)
     single_max = dc.get_option("gather_single_max_bytes")
     paths = ["single" if P * B <= single_max else "multi" for (P, B, _s) in cases]
+    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
 
-    timed_calls(torch, stream, flush, calls, max(args.warmup, 0))  # warm-up steps
+    launches0 = dc.launch_count()
+    graph, evs = build_step_graph(torch, flush, calls)
+    kernels_per_step = dc.launch_count() - launches0 - len(calls)  # launches captured in the graph
+    for _ in range(max(args.warmup, 0)):
+        graph.replay()
+        timed_calls(torch, stream, flush, calls, 1)
+    torch.cuda.synchronize()
 
     if dist:
         dist.barrier()
@@ -391,15 +431,21 @@ def run_dc(args) -> int:
     sampler = ClockSampler(local)
     launches0 = dc.launch_count()
     t_wall = time.perf_counter()
-    per_call = timed_calls(torch, stream, flush, calls, args.steps)  # ends with a synchronize
+    step_ms, per_call = [], [[] for _ in calls]
+    for _ in range(args.steps):
+        graph.replay()
+        iso = timed_calls(torch, stream, flush, calls, 1)  # synchronizes
+        step_ms.append(evs[0].elapsed_time(evs[1]))
+        for i in range(len(calls)):
+            per_call[i].extend(iso[i])
+    torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
-    launches = dc.launch_count() - launches0
+    eager_launches = dc.launch_count() - launches0
     if dist:
         dist.barrier()
     clocks = sampler.stop()
 
-    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
-    gpu_ms_total = sum(sum(x) for x in per_call) / 1e3
+    gpu_ms_total = float(sum(step_ms))
     if dist:
         t = torch.tensor([gpu_ms_total], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -412,17 +458,15 @@ def run_dc(args) -> int:
     kern_bytes = {"multi": 0, "single": 0}
     kern_launches = {"multi": 0, "single": 0}
     for (P, B, _s), path, us_list in zip(cases, paths, per_call):
-        med = statistics.median(us_list)
         nbytes = algorithmic_bytes(P, B)
-        table.append({"P": P, "bytes_per_rank": B, "path": path, "us_median": med,
-                      "us_p10": float(np.percentile(us_list, 10)),
-                      "us_p90": float(np.percentile(us_list, 90)),
-                      "gbs": nbytes / med / 1e3, "frac": nbytes / med / 1e3 / peak})
+        st = stats(us_list)
+        table.append({"P": P, "bytes_per_rank": B, "path": path, **st,
+                      "gbs": nbytes / st["us_mean"] / 1e3, "frac": nbytes / st["us_mean"] / 1e3 / peak})
         kern_time[path] += sum(us_list)
         kern_bytes[path] += nbytes * len(us_list)
         kern_launches[path] += len(us_list)
     dom = max(kern_time, key=kern_time.get)
-    kname = {"multi": "dc_gather_kernel<1,64,true>", "single": "dc_gather_single_kernel<1,64,true>"}[dom]
+    kname = {"multi": "dc_gather_kernel<1,64,2>", "single": "dc_gather_single_kernel<1,64,2>"}[dom]
     achieved = kern_bytes[dom] / kern_time[dom] / 1e3  # GB/s
     traffic = load_traffic(kname)
     big = [row for row in table if row["P"] == 8 and row["bytes_per_rank"] == 4 << 20][0]
@@ -442,7 +486,12 @@ def run_dc(args) -> int:
         "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded random BF16 bit patterns, resident in HBM)",
         "config": {"workload": WORKLOAD, "P": [8, 2], "bytes_per_rank": W.CONFIG2_SIZES,
-                   "l2": "flushed before every call (write + read of 4x L2), outside the events",
+                   "timing": "value: one CUDA graph per step (L2 flush, event, the 14 calls back "
+                             "to back, event); per_call and roofline: each call alone (L2 flush, "
+                             "event, the launch, event), in the same timed region",
+                   "l2": "flushed before every step and before every separately timed call "
+                         "(write + read of 4x L2); each call's inputs are untouched since",
+                   "programmatic_dependent_launch": bool(dc.get_option("pdl")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "gather_single_max_bytes": single_max},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
@@ -450,9 +499,9 @@ def run_dc(args) -> int:
                      "traffic": traffic, "launches": kern_launches[dom],
                      "share": kern_time[dom] / sum(kern_time.values()),
                      "algorithmic_bytes_per_launch": kern_bytes[dom] / max(kern_launches[dom], 1)},
-        "headline_4MiB_P8": {"us": big["us_median"], "gbs": big["gbs"], "frac": big["frac"]},
+        "headline_4MiB_P8": {"us": big["us_mean"], "gbs": big["gbs"], "frac": big["frac"]},
         "per_call": table,
-        "gpu_launches": launches,
+        "gpu_launches": kernels_per_step * args.steps + eager_launches,
         "wall_s_timed_region": t_wall,
         "clocks": clocks,
         "e2e": e2e,

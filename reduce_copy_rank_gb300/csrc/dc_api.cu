@@ -32,10 +32,13 @@ using namespace dc;
 thread_local char g_err[512] = "";
 std::atomic<unsigned long long> g_launches{0};
 
-// Measured single-CTA crossovers (bytes); see the crossover sweep of the
-// benchmark.  Initial values, replaced by the measured ones.
-constexpr long long kDefaultGatherSingleMax = 32 * 1024;
-constexpr long long kDefaultReduceSingleMax = 16 * 1024;
+// Single-CTA thresholds measured on GB300 (bench.py --crossover, CUDA events,
+// L2 flushed before every call): one CTA is as fast as the multi-CTA grid up
+// to 64 KiB of gathered output (P = 2 and P = 8) and slower from 128 KiB; for
+// the P = 8 all_reduce it is as fast up to 8 KiB of input per rank and slower
+// from 32 KiB.  Above these sizes every extra CTA adds bandwidth.
+constexpr long long kDefaultGatherSingleMax = 64 * 1024;
+constexpr long long kDefaultReduceSingleMax = 8 * 1024;
 
 struct Options {
   std::atomic<long long> force_path{0};
@@ -44,6 +47,7 @@ struct Options {
   std::atomic<long long> reduce_single_max{kDefaultReduceSingleMax};
   std::atomic<long long> grid_ctas{0};
   std::atomic<long long> test_fail_launch{0};
+  std::atomic<long long> pdl{1};
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -60,6 +64,7 @@ const OptionKey kKeys[] = {
     {"reduce_single_max_bytes", "DC_REDUCE_SINGLE_MAX_BYTES", &g_opt.reduce_single_max},
     {"grid_ctas", "DC_GRID_CTAS", &g_opt.grid_ctas},
     {"test_fail_launch", nullptr, &g_opt.test_fail_launch},
+    {"pdl", "DC_PDL", &g_opt.pdl},
 };
 
 void read_env_once() {
@@ -132,29 +137,25 @@ int occupancy(int dev, int family, F query) {
   return v;
 }
 
-// Multi-CTA grid: enough CTAs that each thread has about `per_thread` units
-// in one pass, at most the CTAs that fit on the GPU at once (later passes
-// loop inside the CTA).  Each CTA then owns `chunk` contiguous units.
-void plan_grid(uint64_t total, int block, int per_thread, int sms, int ctas_per_sm, int* grid,
-               uint64_t* chunk) {
-  const uint64_t per_cta = static_cast<uint64_t>(block) * per_thread;
-  uint64_t g = (total + per_cta - 1) / per_cta;
-  const uint64_t cap = static_cast<uint64_t>(sms) * ctas_per_sm;
-  g = std::min<uint64_t>(std::max<uint64_t>(g, 1), cap);
+// Multi-CTA grid for `tiles` tiles of work taken round robin: at most the
+// CTAs that fit on the GPU at once, and the fewest CTAs that still finish in
+// the same number of rounds (so every CTA does the same number of tiles,
+// give or take one).
+int plan_grid(uint64_t tiles, int sms, int ctas_per_sm) {
+  const uint64_t cap = std::max<uint64_t>(1, static_cast<uint64_t>(sms) * ctas_per_sm);
+  uint64_t g;
   const long long forced = g_opt.grid_ctas.load();
-  if (forced > 0) g = std::min<uint64_t>(static_cast<uint64_t>(forced), std::max<uint64_t>(total, 1));
-  // keep every CTA's run below 2^31 units (32-bit loop counters)
-  const uint64_t min_g = (total + (1ull << 31) - 1) >> 31;
-  g = std::max<uint64_t>(g, std::max<uint64_t>(min_g, 1));
-  uint64_t c = (total + g - 1) / g;
-  g = (total + c - 1) / c;
-  *grid = static_cast<int>(g);
-  *chunk = c;
+  if (forced > 0) {
+    g = std::min<uint64_t>(static_cast<uint64_t>(forced), std::max<uint64_t>(tiles, 1));
+  } else {
+    const uint64_t rounds = (tiles + cap - 1) / cap;
+    g = std::max<uint64_t>(1, (tiles + rounds - 1) / std::max<uint64_t>(rounds, 1));
+  }
+  return static_cast<int>(std::min<uint64_t>(g, 0x7FFFFFFFull));
 }
 
-bool use_single(uint64_t size_bytes, long long threshold, uint64_t total_units) {
+bool use_single(uint64_t size_bytes, long long threshold) {
   const long long f = g_opt.force_path.load();
-  if (total_units >= (1ull << 31)) return false;
   if (f == 1) return true;
   if (f == 2) return false;
   return size_bytes <= static_cast<uint64_t>(threshold);
@@ -215,15 +216,17 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   if (st != DC_OK) return st;
   st = sm_count(dev, &sms);
   if (st != DC_OK) return st;
-  const bool single = use_single(out_bytes, g_opt.gather_single_max.load(), prm.total_vec);
+  const bool single = use_single(out_bytes, g_opt.gather_single_max.load());
   int grid = 1;
-  if (single) {
-    prm.chunk_vec = prm.total_vec;
-  } else {
-    const int occ = occupancy(dev, family, [family] { return gather_ctas_per_sm(family); });
-    plan_grid(prm.total_vec, kGatherBlock, kGatherUnroll, sms, occ, &grid, &prm.chunk_vec);
+  if (!single) {
+    bool flat = true;
+    for (int j = 0; j < prm.njobs; ++j) flat = flat && (prm.job[j].flags & kJobFlat);
+    const int fam = family * 2 + (flat ? 1 : 0);
+    const int occ = occupancy(dev, fam, [family, flat] { return gather_ctas_per_sm(family, flat); });
+    const uint64_t tile = static_cast<uint64_t>(kGatherBlock) * (flat ? kGatherUnroll : kGatherUnrollGeneral);
+    grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
   }
-  return check_launch(launch_gather(prm, grid, single, stream), "all-gather");
+  return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather");
 }
 
 // --------------------------------------------------------------- reduce ---
@@ -266,22 +269,21 @@ dc_status_t launch_reduce_plan(Params& prm, int family, uint64_t in_bytes_per_ra
   if (st != DC_OK) return st;
   st = sm_count(dev, &sms);
   if (st != DC_OK) return st;
-  const bool single = use_single(in_bytes_per_rank, g_opt.reduce_single_max.load(), prm.total_units);
+  const bool single = use_single(in_bytes_per_rank, g_opt.reduce_single_max.load());
   int grid = 1;
-  if (single) {
-    prm.chunk_units = prm.total_units;
-  } else {
+  if (!single) {
     const int P = prm.P;
-    const bool scatter = prm.njobs > 1 || family >= 8;
+    const bool scatter = family >= 12;
     const int occ = occupancy(dev, family, [P, scatter] { return reduce_ctas_per_sm(P, scatter); });
-    plan_grid(prm.total_units, kReduceBlock, kReduceUnroll, sms, occ, &grid, &prm.chunk_units);
+    const uint64_t tile = static_cast<uint64_t>(kReduceBlock) * kReduceUnroll;
+    grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
   }
-  return check_launch(launch_reduce(prm, grid, single, stream), what);
+  return check_launch(launch_reduce(prm, grid, single, g_opt.pdl.load() != 0, stream), what);
 }
 
-int reduce_family(int P, bool scatter) {
+int reduce_family(int P, bool scatter) {  // occupancy cache slots 8..15 (gather uses 0..5)
   const int pt = P == 8 ? 0 : P == 4 ? 1 : P == 2 ? 2 : 3;
-  return (scatter ? 8 : 4) + pt;
+  return (scatter ? 12 : 8) + pt;
 }
 
 dc_status_t check_bf16_ptrs(const void* const* ptrs, int P, const char* name) {

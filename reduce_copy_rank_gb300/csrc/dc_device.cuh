@@ -7,6 +7,19 @@
 
 namespace dc {
 
+// Programmatic dependent launch.  When a kernel is launched with
+// programmatic stream serialization, the GPU may start it before the previous
+// kernel in the stream has finished; griddepcontrol.wait then blocks until
+// that kernel has completed and its writes are visible, so every global
+// access below it sees the finished predecessor.  Without that launch
+// attribute the wait returns at once.  launch_dependents lets the next
+// kernel in the stream (if it was launched the same way) start its launch
+// while this one runs; it still waits for this one to finish.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Streaming 16-byte load through the read-only path without allocating in
 // L1: each source byte of an aligned copy is read exactly once.  Only for
 // data that no thread writes during the launch (gather sources).

@@ -35,214 +35,292 @@
 namespace dc {
 namespace {
 
-// Aligned job (flat): rank r owns output vectors [r*vp, (r+1)*vp), vp = B/16.
-// Thread t copies vectors a+t, a+t+BLOCK, ... of the CTA's run [a, b), UNROLL
-// at a time with every load issued before the first store, so the whole
-// CTA's run is in flight at once whatever the rank boundaries.  A thread's
-// vector index only grows, so its rank is found by walking forward from the
-// rank of the run's first vector: one 64-bit division per thread, then
-// comparisons (at most P steps in total).
-template <int BLOCK, int UNROLL, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_flat(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
-                                            uint64_t a, uint64_t b) {
+// Per-thread position among the jobs and ranks of a launch.  A thread's
+// output vector indices only grow, so the cursor only moves forward: the job
+// by comparison with the job table, the rank by comparison with the rank
+// boundaries.  Entering a job costs one 64-bit division (the rank of the
+// thread's first vector in it); after that, nothing per element but
+// comparisons.
+struct Cursor {
+  int j;           // current job
+  uint64_t jbeg;   // its first global vector
+  uint64_t jend;   // one past its last
+  bool fresh;      // rank state not yet set for job j
+  uint32_t r;      // current rank
+  uint64_t lo;     // flat: first job-local vector of rank r; unaligned: its first output byte
+  uint64_t hi;     // one past its last (same units)
+};
+
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ void cursor_to_job(const GatherParams<MAXJ, MAXS>& p, Cursor& c,
+                                              uint64_t k) {
+  while (k >= c.jend) {
+    ++c.j;
+    c.jbeg = p.job[c.j].vfirst;
+    c.jend = c.jbeg + p.job[c.j].nvec;
+    c.fresh = true;
+  }
+}
+
+// Flat job: rank r owns job-local vectors [r*vp, (r+1)*vp), vp = B/16.
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ const uint4* flat_source(const GatherParams<MAXJ, MAXS>& p, Cursor& c,
+                                                    const GatherJob& J, uint64_t kl) {
   const uint64_t vp = J.bytes >> 4;
-  uint64_t r = a / vp;
-  uint64_t rbeg = r * vp, rend = rbeg + vp;
-  uint4* out = reinterpret_cast<uint4*>(J.out);
-  for (uint64_t i = a + threadIdx.x; i < b; i += static_cast<uint64_t>(BLOCK) * UNROLL) {
+  if (c.fresh) {
+    c.r = static_cast<uint32_t>(kl / vp);
+    c.lo = static_cast<uint64_t>(c.r) * vp;
+    c.hi = c.lo + vp;
+    c.fresh = false;
+  }
+  while (kl >= c.hi) {
+    ++c.r;
+    c.lo = c.hi;
+    c.hi += vp;
+  }
+  return reinterpret_cast<const uint4*>(p.src[J.src0 + c.r]) + (kl - c.lo);
+}
+
+// Unaligned job: rank r owns output bytes [d_r, d_r + B), d_r = out + r*B;
+// x is the first byte of the output vector.
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ void unaligned_rank(Cursor& c, const GatherJob& J, uint64_t x) {
+  if (c.fresh) {
+    c.r = static_cast<uint32_t>((max(x, J.out) - J.out) / J.bytes);
+    c.lo = J.out + static_cast<uint64_t>(c.r) * J.bytes;
+    c.hi = c.lo + J.bytes;
+    c.fresh = false;
+  }
+  while (x >= c.hi) {
+    ++c.r;
+    c.lo = c.hi;
+    c.hi += J.bytes;
+  }
+}
+
+// Bytes [x, x+16) of a job's output that are not one rank's aligned-source
+// vector: copied one by one.  `r` is the rank of the vector's first output
+// byte; for jobs of at least kGatherSmallBytes per rank the vector holds
+// bytes of rank r and r+1 only, for smaller jobs the rank of each byte is
+// found by a 32-bit division (the whole job is under kMaxRanks*128 bytes).
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ void copy_bytes(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
+                                           uint64_t x, uint32_t r, bool small) {
+  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
+  for (uint32_t i = 0; i < 16; ++i) {
+    const uint64_t y = x + i;
+    if (y < J.out || y >= out_end) continue;
+    uint32_t q;
+    uint64_t off;
+    if (small) {
+      const uint32_t o = static_cast<uint32_t>(y - J.out), B = static_cast<uint32_t>(J.bytes);
+      q = o / B;
+      off = o - q * B;
+    } else {
+      const uint64_t d = J.out + static_cast<uint64_t>(r) * J.bytes;
+      q = r + (y >= d + J.bytes ? 1u : 0u);
+      off = y - d - (q > r ? J.bytes : 0);
+    }
+    *reinterpret_cast<uint8_t*>(y) = reinterpret_cast<const uint8_t*>(p.src[J.src0 + q])[off];
+  }
+}
+
+// Copy output vectors, tile by tile: tile t covers global vectors
+// [t*TILE, (t+1)*TILE), TILE = BLOCK*UNROLL; this CTA takes tiles
+// first, first + step, ...  Thread i of the CTA owns vectors
+// t*TILE + i + u*BLOCK, u < UNROLL: all its loads are issued before its
+// first store.
+//  * Flat job vector: one LDG.128 from its rank's payload.
+//  * Unaligned job vector lying inside one rank's bytes: source start s =
+//    src address mod 16; the aligned block holding it and, if s != 0, the
+//    next one; a funnel shift gives the 16 output bytes.  Both blocks hold
+//    source bytes of this vector, so they lie in the source allocation.
+//  * Any other vector (rank boundary, output ends, jobs under
+//    kGatherSmallBytes per rank): byte copies.
+// One aligned job (dc_all_gather with everything 16-byte aligned): the hot
+// loop with the least state, so it fits the 32 registers of full occupancy.
+// Idx is uint32_t when the output has fewer than 2^31 vectors (32 GiB).
+template <int BLOCK, int UNROLL, typename Idx, int MAXS>
+__device__ __forceinline__ void gather_tiles_flat1(const GatherParams<1, MAXS>& p, Idx first,
+                                                   Idx step) {
+  constexpr Idx kTile = static_cast<Idx>(BLOCK) * UNROLL;
+  const Idx total = static_cast<Idx>(p.total_vec);
+  const Idx ntiles = (total + kTile - 1) / kTile;
+  const Idx vp = static_cast<Idx>(p.job[0].bytes >> 4);
+  uint4* out = reinterpret_cast<uint4*>(p.job[0].out);
+  uint32_t r = 0;
+  Idx rlo = 0, rhi = vp;
+  bool fresh = true;
+  for (Idx t = first; t < ntiles; t += step) {
+    const Idx base = t * kTile + threadIdx.x;
     uint4 v[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
-      if (k < b) {
-        while (k >= rend) {
+      const Idx k = base + static_cast<Idx>(u) * BLOCK;
+      if (k < total) {
+        if (fresh) {
+          r = static_cast<uint32_t>(k / vp);
+          rlo = static_cast<Idx>(r) * vp;
+          rhi = rlo + vp;
+          fresh = false;
+        }
+        while (k >= rhi) {
           ++r;
-          rbeg = rend;
-          rend += vp;
+          rlo = rhi;
+          rhi += vp;
         }
-        v[u] = ld_nc_stream(reinterpret_cast<const uint4*>(p.src[J.src0 + r]) + (k - rbeg));
+        v[u] = ld_nc_stream(reinterpret_cast<const uint4*>(p.src[r]) + (k - rlo));
       }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
-      if (k < b) st16(out + k, v[u]);
+      const Idx k = base + static_cast<Idx>(u) * BLOCK;
+      if (k < total) st16(out + k, v[u]);
     }
-  }
-}
-
-// Unaligned job (B >= kGatherSmallBytes).  Output vector k covers bytes
-// [x, x+16), x = 16*(vbase+k).  It is "interior" when all 16 bytes belong to
-// one rank r (d_r <= x and x+16 <= d_r + B): its source starts at
-// src_r + (x - d_r), at offset s = that address mod 16, so it is built from
-// the aligned source block holding that byte and the next one (one block
-// when s = 0) and stored as one aligned 16-byte vector.  The other vectors
-// (one per rank boundary, plus the first and last vector when the output is
-// not aligned) are written byte by byte by the thread that owns them; since
-// B > 16 they hold bytes of at most two ranks.  Both aligned source blocks
-// of an interior vector contain bytes of [src_r, src_r + B), so no read
-// leaves the 16-byte blocks of the source buffer.  Threads walk ranks
-// forward as in the flat case.
-template <int BLOCK, int UNROLL, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_unaligned(const GatherParams<MAXJ, MAXS>& p,
-                                                 const GatherJob& J, uint64_t a, uint64_t b) {
-  const uint64_t B = J.bytes;
-  const uint64_t vbase = J.out >> 4;
-  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * B;
-  const uint64_t first_byte = max(J.out, (vbase + a) << 4);
-  uint32_t r = static_cast<uint32_t>((first_byte - J.out) / B);
-  uint64_t d = J.out + static_cast<uint64_t>(r) * B;  // rank r's first output byte
-  uint64_t e = d + B;                                  // one past its last
-  for (uint64_t i = a + threadIdx.x; i < b; i += static_cast<uint64_t>(BLOCK) * UNROLL) {
-    uint4 lo[UNROLL], hi[UNROLL];
-    uint32_t shift[UNROLL];
-    bool interior[UNROLL];
-    uint32_t rank[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
-      interior[u] = false;
-      if (k < b) {
-        const uint64_t x = (vbase + k) << 4;
-        while (x >= e) {
-          ++r;
-          d = e;
-          e += B;
-        }
-        rank[u] = r;
-        if (x >= d && x + 16 <= e) {
-          interior[u] = true;
-          const uint64_t src = p.src[J.src0 + r] + (x - d);
-          const uint32_t s = static_cast<uint32_t>(src & 15u);
-          const uint4* blk = reinterpret_cast<const uint4*>(src - s);
-          shift[u] = s;
-          if (s == 0) {
-            lo[u] = ld_nc_stream(blk);
-            hi[u] = lo[u];
-          } else {
-            lo[u] = ld_nc_cached(blk);
-            hi[u] = ld_nc_cached(blk + 1);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const uint64_t k = i + static_cast<uint64_t>(u) * BLOCK;
-      if (k >= b) continue;
-      const uint64_t x = (vbase + k) << 4;
-      if (interior[u]) {
-        st16(reinterpret_cast<uint4*>(x), realign16(lo[u], hi[u], shift[u]));
-      } else {
-        const uint32_t q0 = rank[u];
-        const uint64_t dq = J.out + static_cast<uint64_t>(q0) * B;
-        for (uint32_t j = 0; j < 16; ++j) {
-          const uint64_t y = x + j;
-          if (y < J.out || y >= out_end) continue;
-          const bool next = y >= dq + B;  // byte of rank q0 + 1
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.src[J.src0 + q0 + (next ? 1 : 0)]);
-          *reinterpret_cast<uint8_t*>(y) = src[y - dq - (next ? B : 0)];
-        }
-      }
-    }
-  }
-}
-
-// Fewer than kGatherSmallBytes per rank: every output byte of the CTA's
-// vectors is copied on its own.  P*B < kMaxRanks*kGatherSmallBytes, so the
-// rank lookup is a 32-bit division over a few thousand bytes in total.
-template <int BLOCK, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_small(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
-                                             uint64_t a, uint64_t b) {
-  const uint64_t vbase = J.out >> 4;
-  const uint32_t B = static_cast<uint32_t>(J.bytes);
-  const uint32_t total = static_cast<uint32_t>(p.P) * B;
-  const uint32_t nbytes = static_cast<uint32_t>(b - a) * 16u;
-  const uint64_t x0 = (vbase + a) << 4;
-  for (uint32_t i = threadIdx.x; i < nbytes; i += BLOCK) {
-    const uint64_t x = x0 + i;
-    if (x < J.out) continue;
-    const uint32_t off = static_cast<uint32_t>(x - J.out);
-    if (off >= total) continue;
-    const uint32_t r = off / B;
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.src[J.src0 + r]);
-    *reinterpret_cast<uint8_t*>(x) = src[off - r * B];
   }
 }
 
 template <int BLOCK, int UNROLL, bool FLAT, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_cta(const GatherParams<MAXJ, MAXS>& p, uint64_t g0,
-                                           uint64_t g1) {
-  int j = 0;
-  while (j + 1 < p.njobs && p.job[j].vfirst + p.job[j].nvec <= g0) ++j;
-  for (; j < p.njobs && p.job[j].vfirst < g1; ++j) {
-    const GatherJob& J = p.job[j];
-    const uint64_t a = max(g0, J.vfirst) - J.vfirst;
-    const uint64_t b = min(g1, J.vfirst + J.nvec) - J.vfirst;
-    if (a >= b) continue;
-    if constexpr (FLAT) {
-      gather_flat<BLOCK, UNROLL>(p, J, a, b);
-    } else {
-      if (J.flags & kJobFlat)
-        gather_flat<BLOCK, UNROLL>(p, J, a, b);
-      else if (J.flags & kJobSmall)
-        gather_small<BLOCK>(p, J, a, b);
+__device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
+                                             uint64_t step) {
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
+  const uint64_t ntiles = (p.total_vec + kTile - 1) / kTile;
+  Cursor c{0, p.job[0].vfirst, p.job[0].vfirst + p.job[0].nvec, true, 0, 0, 0};
+  for (uint64_t t = first; t < ntiles; t += step) {
+    const uint64_t base = t * kTile + threadIdx.x;
+    uint4 lo[UNROLL], hi[UNROLL];
+    uint64_t dst[UNROLL];
+    uint32_t meta[UNROLL];  // FLAT: unused; else shift | kind << 8 | rank << 16
+    int job[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const uint64_t k = base + static_cast<uint64_t>(u) * BLOCK;
+      dst[u] = 0;
+      if (k >= p.total_vec) continue;
+      cursor_to_job(p, c, k);
+      const GatherJob& J = p.job[c.j];
+      const uint64_t kl = k - c.jbeg;
+      job[u] = c.j;
+      if (FLAT) {
+        lo[u] = ld_nc_stream(flat_source(p, c, J, kl));
+        dst[u] = J.out + 16 * kl;
+        continue;
+      }
+      if (J.flags & kJobFlat) {
+        lo[u] = ld_nc_stream(flat_source(p, c, J, kl));
+        hi[u] = lo[u];
+        dst[u] = J.out + 16 * kl;
+        meta[u] = 0;  // kind 0: aligned vector, shift 0
+        continue;
+      }
+      const uint64_t x = ((J.out >> 4) + kl) << 4;
+      dst[u] = x;
+      if (J.flags & kJobSmall) {
+        meta[u] = 2u << 8;  // kind 2: bytes, small job
+        continue;
+      }
+      unaligned_rank<MAXJ, MAXS>(c, J, x);
+      if (x >= c.lo && x + 16 <= c.hi) {
+        const uint64_t src = p.src[J.src0 + c.r] + (x - c.lo);
+        const uint32_t s = static_cast<uint32_t>(src & 15u);
+        const uint4* blk = reinterpret_cast<const uint4*>(src - s);
+        if (s == 0) {
+          lo[u] = ld_nc_stream(blk);
+          hi[u] = lo[u];
+        } else {
+          lo[u] = ld_nc_cached(blk);
+          hi[u] = ld_nc_cached(blk + 1);
+        }
+        meta[u] = s;  // kind 0
+      } else {
+        meta[u] = (1u << 8) | (c.r << 16);  // kind 1: bytes at a rank boundary
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      if (!dst[u]) continue;
+      if (FLAT) {
+        st16(reinterpret_cast<uint4*>(dst[u]), lo[u]);
+        continue;
+      }
+      const uint32_t kind = (meta[u] >> 8) & 0xFFu;
+      if (kind == 0)
+        st16(reinterpret_cast<uint4*>(dst[u]), realign16(lo[u], hi[u], meta[u] & 15u));
       else
-        gather_unaligned<BLOCK, UNROLL>(p, J, a, b);
+        copy_bytes(p, p.job[job[u]], dst[u], meta[u] >> 16, kind == 2);
     }
   }
 }
 
-// Multi-CTA gather: CTA c owns output vectors [c*chunk, (c+1)*chunk).
-// FLAT: every job of the launch is 16-byte aligned (the flat path only).
-template <int MAXJ, int MAXS, bool FLAT>
-__global__ void __launch_bounds__(kGatherBlock, FLAT ? 4 : 2)
+// Kernel modes: kGeneral (any jobs), kFlat (all jobs 16-byte aligned),
+// kFlat1 (one aligned job with fewer than 2^31 output vectors).
+enum Mode : int { kGeneral = 0, kFlat = 1, kFlat1 = 2 };
+
+template <int BLOCK, int UNROLL, int MODE, int MAXJ, int MAXS>
+__device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
+                                            uint64_t step) {
+  if constexpr (MODE == kFlat1 && MAXJ == 1)
+    gather_tiles_flat1<BLOCK, UNROLL, uint32_t>(p, static_cast<uint32_t>(first),
+                                                static_cast<uint32_t>(step));
+  else
+    gather_tiles<BLOCK, UNROLL, MODE != kGeneral>(p, first, step);
+}
+
+// Multi-CTA gather: CTA c copies tiles c, c + gridDim.x, ...
+template <int MAXJ, int MAXS, int MODE>
+__global__ void __launch_bounds__(kGatherBlock, MODE == kFlat1 ? 4 : 2)
     dc_gather_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
-  const uint64_t g0 = static_cast<uint64_t>(blockIdx.x) * p.chunk_vec;
-  if (g0 >= p.total_vec) return;
-  const uint64_t g1 = min(g0 + p.chunk_vec, p.total_vec);
-  gather_cta<kGatherBlock, FLAT ? kGatherUnroll : kGatherUnrollGeneral, FLAT>(p, g0, g1);
+  pdl_enter();
+  gather_mode<kGatherBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(
+      p, blockIdx.x, gridDim.x);
 }
 
 // Single-CTA gather for small outputs: one CTA copies everything.
-template <int MAXJ, int MAXS, bool FLAT>
-__global__ void __launch_bounds__(FLAT ? kGatherSingleBlock : kGatherSingleBlockGeneral)
+template <int MAXJ, int MAXS, int MODE>
+__global__ void __launch_bounds__(MODE == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock)
     dc_gather_single_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
-  constexpr int kBlock = FLAT ? kGatherSingleBlock : kGatherSingleBlockGeneral;
-  gather_cta<kBlock, FLAT ? kGatherUnroll : kGatherUnrollGeneral, FLAT>(p, 0, p.total_vec);
+  constexpr int kBlock = MODE == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock;
+  pdl_enter();
+  gather_mode<kBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(p, 0, 1);
 }
 
 template <int MAXJ, int MAXS>
-bool all_flat(const GatherParams<MAXJ, MAXS>& p) {
+int mode_of(const GatherParams<MAXJ, MAXS>& p) {
   for (int j = 0; j < p.njobs; ++j)
-    if (!(p.job[j].flags & kJobFlat)) return false;
-  return true;
+    if (!(p.job[j].flags & kJobFlat)) return kGeneral;
+  return (MAXJ == 1 && p.total_vec < (1ull << 31)) ? kFlat1 : kFlat;
+}
+
+template <int MAXJ, int MAXS, int MODE>
+cudaError_t launch_mode(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, bool pdl,
+                        cudaStream_t s) {
+  if (single)
+    return launch_ex(dc_gather_single_kernel<MAXJ, MAXS, MODE>, 1,
+                     MODE == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock, pdl, s, p);
+  return launch_ex(dc_gather_kernel<MAXJ, MAXS, MODE>, grid, kGatherBlock, pdl, s, p);
 }
 
 template <int MAXJ, int MAXS>
-cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, cudaStream_t s) {
-  const bool flat = all_flat(p);
-  if (single) {
-    if (flat)
-      dc_gather_single_kernel<MAXJ, MAXS, true><<<1, kGatherSingleBlock, 0, s>>>(p);
-    else
-      dc_gather_single_kernel<MAXJ, MAXS, false><<<1, kGatherSingleBlockGeneral, 0, s>>>(p);
-  } else {
-    if (flat)
-      dc_gather_kernel<MAXJ, MAXS, true><<<grid, kGatherBlock, 0, s>>>(p);
-    else
-      dc_gather_kernel<MAXJ, MAXS, false><<<grid, kGatherBlock, 0, s>>>(p);
+cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, bool pdl,
+                        cudaStream_t s) {
+  switch (mode_of(p)) {
+    case kGeneral: return launch_mode<MAXJ, MAXS, kGeneral>(p, grid, single, pdl, s);
+    case kFlat: return launch_mode<MAXJ, MAXS, kFlat>(p, grid, single, pdl, s);
+    default:
+      if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);
+      return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
-// Resident CTAs per SM of the general (heavier) instantiation, so a grid
-// planned from it never exceeds what either instantiation can hold at once.
 template <int MAXJ, int MAXS>
-int occupancy_impl() {
+int occupancy_impl(bool flat) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, false>,
-                                                    kGatherBlock, 0) != cudaSuccess) {
+  const cudaError_t e =
+      flat ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                 &n, dc_gather_kernel<MAXJ, MAXS, MAXJ == 1 ? kFlat1 : kFlat>, kGatherBlock, 0)
+           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kGeneral>,
+                                                           kGatherBlock, 0);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     n = 1;
   }
@@ -251,21 +329,21 @@ int occupancy_impl() {
 
 }  // namespace
 
-cudaError_t launch_gather(const GatherParams1& p, int grid, bool single, cudaStream_t s) {
-  return launch_impl(p, grid, single, s);
+cudaError_t launch_gather(const GatherParams1& p, int grid, bool single, bool pdl, cudaStream_t s) {
+  return launch_impl(p, grid, single, pdl, s);
 }
-cudaError_t launch_gather(const GatherParamsS& p, int grid, bool single, cudaStream_t s) {
-  return launch_impl(p, grid, single, s);
+cudaError_t launch_gather(const GatherParamsS& p, int grid, bool single, bool pdl, cudaStream_t s) {
+  return launch_impl(p, grid, single, pdl, s);
 }
-cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, cudaStream_t s) {
-  return launch_impl(p, grid, single, s);
+cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, bool pdl, cudaStream_t s) {
+  return launch_impl(p, grid, single, pdl, s);
 }
 
-int gather_ctas_per_sm(int which) {
+int gather_ctas_per_sm(int which, bool flat) {
   switch (which) {
-    case 0: return occupancy_impl<1, kMaxRanks>();
-    case 1: return occupancy_impl<kManySmallTensors, kManySmallSegments>();
-    default: return occupancy_impl<kManyMaxTensors, kManyMaxSegments>();
+    case 0: return occupancy_impl<1, kMaxRanks>(flat);
+    case 1: return occupancy_impl<kManySmallTensors, kManySmallSegments>(flat);
+    default: return occupancy_impl<kManyMaxTensors, kManyMaxSegments>(flat);
   }
 }
 

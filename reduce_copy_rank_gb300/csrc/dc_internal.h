@@ -55,7 +55,6 @@ struct GatherJob {
 template <int MAXJ, int MAXS>
 struct GatherParams {
   uint64_t total_vec;   // sum of nvec over the jobs
-  uint64_t chunk_vec;   // contiguous output vectors per CTA
   int32_t njobs;
   int32_t P;
   GatherJob job[MAXJ];
@@ -90,7 +89,6 @@ struct ReduceJob {
 template <int MAXJ>
 struct ReduceParams {
   uint64_t total_units;
-  uint64_t chunk_units;
   int32_t njobs;
   int32_t P;
   uint64_t in[kMaxRanks];
@@ -102,15 +100,33 @@ using ReduceParams1 = ReduceParams<1>;          // all_reduce
 using ReduceParamsP = ReduceParams<kMaxRanks>;  // reduce_scatter: one job per rank
 
 // ------------------------------------------------- launch entry points ---
-// Each returns the error of the launch itself (cudaGetLastError).
-cudaError_t launch_gather(const GatherParams1& p, int grid, bool single, cudaStream_t s);
-cudaError_t launch_gather(const GatherParamsS& p, int grid, bool single, cudaStream_t s);
-cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, cudaStream_t s);
-cudaError_t launch_reduce(const ReduceParams1& p, int grid, bool single, cudaStream_t s);
-cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, cudaStream_t s);
+// Each returns the error of the launch itself.  pdl: launch with
+// programmatic stream serialization (the kernel may start while the previous
+// kernel of the stream drains; it waits for it before touching memory).
+cudaError_t launch_gather(const GatherParams1& p, int grid, bool single, bool pdl, cudaStream_t s);
+cudaError_t launch_gather(const GatherParamsS& p, int grid, bool single, bool pdl, cudaStream_t s);
+cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, bool pdl, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceParams1& p, int grid, bool single, bool pdl, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, bool pdl, cudaStream_t s);
+
+// cudaLaunchKernelEx with an optional programmatic-serialization attribute.
+template <typename Kernel, typename Params>
+cudaError_t launch_ex(Kernel kernel, int grid, int block, bool pdl, cudaStream_t s, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 
 // Resident CTAs per SM of the multi-CTA kernels (occupancy API, per device).
-int gather_ctas_per_sm(int which);  // 0: one job, 1: small many, 2: large many
+int gather_ctas_per_sm(int which, bool flat);  // which: 0 one job, 1 small many, 2 large many
 int reduce_ctas_per_sm(int P, bool scatter);
 
 }  // namespace dc

@@ -21,8 +21,9 @@
 // scalar head up to the first 16-byte boundary, a body of 8-element groups
 // (one 16-byte load per rank and one 16-byte store per output, P loads in
 // flight per group) and a scalar tail.  Otherwise every element is folded
-// with 2-byte accesses.  Each CTA owns a contiguous run of units and finds its
-// job once; there is no per-element division.
+// with 2-byte accesses.  CTAs take tiles of units round robin and find a
+// tile's job by walking the job table forward; there is no per-element
+// division.
 #include "dc_device.cuh"
 #include "dc_internal.h"
 
@@ -142,53 +143,60 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ>& p, cons
   }
 }
 
+// Tile t covers global units [t*TILE, (t+1)*TILE), TILE = BLOCK*UNROLL; a
+// CTA takes tiles first, first + step, ...  so that all CTAs sweep the
+// buffers together (neighbouring CTAs read neighbouring addresses), which
+// keeps DRAM rows and TLB entries shared between them.
 template <int BLOCK, int UNROLL, int PT, int MAXJ>
-__device__ __forceinline__ void reduce_cta(const ReduceParams<MAXJ>& p, uint64_t g0, uint64_t g1) {
+__device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ>& p, uint64_t first,
+                                             uint64_t step) {
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
+  const uint64_t ntiles = (p.total_units + kTile - 1) / kTile;
   int j = 0;
-  while (j + 1 < p.njobs && p.job[j].ufirst + p.job[j].nunits <= g0) ++j;
-  for (; j < p.njobs && p.job[j].ufirst < g1; ++j) {
-    const ReduceJob& J = p.job[j];
-    const uint64_t a = max(g0, J.ufirst) - J.ufirst;
-    const uint64_t b = min(g1, J.ufirst + J.nunits) - J.ufirst;
-    if (a >= b) continue;
-    if (J.flags & kJobVec)
-      reduce_job_vec<BLOCK, UNROLL, PT>(p, J, a, b);
-    else
-      fold_scalar(p, J, a + threadIdx.x, b, BLOCK);
+  for (uint64_t t = first; t < ntiles; t += step) {
+    const uint64_t g0 = t * kTile, g1 = min(g0 + kTile, p.total_units);
+    while (j + 1 < p.njobs && p.job[j].ufirst + p.job[j].nunits <= g0) ++j;
+    for (int jj = j; jj < p.njobs && p.job[jj].ufirst < g1; ++jj) {
+      const ReduceJob& J = p.job[jj];
+      const uint64_t a = max(g0, J.ufirst) - J.ufirst;
+      const uint64_t b = min(g1, J.ufirst + J.nunits) - J.ufirst;
+      if (a >= b) continue;
+      if (J.flags & kJobVec)
+        reduce_job_vec<BLOCK, UNROLL, PT>(p, J, a, b);
+      else
+        fold_scalar(p, J, a + threadIdx.x, b, BLOCK);
+    }
   }
 }
 
 template <int MAXJ, int PT>
 __global__ void __launch_bounds__(kReduceBlock)
     dc_reduce_kernel(const __grid_constant__ ReduceParams<MAXJ> p) {
-  const uint64_t g0 = static_cast<uint64_t>(blockIdx.x) * p.chunk_units;
-  if (g0 >= p.total_units) return;
-  const uint64_t g1 = min(g0 + p.chunk_units, p.total_units);
-  reduce_cta<kReduceBlock, kReduceUnroll, PT>(p, g0, g1);
+  pdl_enter();
+  reduce_tiles<kReduceBlock, kReduceUnroll, PT>(p, blockIdx.x, gridDim.x);
 }
 
 template <int MAXJ, int PT>
 __global__ void __launch_bounds__(kReduceSingleBlock)
     dc_reduce_single_kernel(const __grid_constant__ ReduceParams<MAXJ> p) {
-  reduce_cta<kReduceSingleBlock, kReduceUnroll, PT>(p, 0, p.total_units);
+  pdl_enter();
+  reduce_tiles<kReduceSingleBlock, kReduceUnroll, PT>(p, 0, 1);
 }
 
 template <int MAXJ, int PT>
-cudaError_t launch_pt(const ReduceParams<MAXJ>& p, int grid, bool single, cudaStream_t s) {
-  if (single)
-    dc_reduce_single_kernel<MAXJ, PT><<<1, kReduceSingleBlock, 0, s>>>(p);
-  else
-    dc_reduce_kernel<MAXJ, PT><<<grid, kReduceBlock, 0, s>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_pt(const ReduceParams<MAXJ>& p, int grid, bool single, bool pdl, cudaStream_t s) {
+  if (single) return launch_ex(dc_reduce_single_kernel<MAXJ, PT>, 1, kReduceSingleBlock, pdl, s, p);
+  return launch_ex(dc_reduce_kernel<MAXJ, PT>, grid, kReduceBlock, pdl, s, p);
 }
 
 template <int MAXJ>
-cudaError_t launch_impl(const ReduceParams<MAXJ>& p, int grid, bool single, cudaStream_t s) {
+cudaError_t launch_impl(const ReduceParams<MAXJ>& p, int grid, bool single, bool pdl,
+                        cudaStream_t s) {
   switch (p.P) {
-    case 8: return launch_pt<MAXJ, 8>(p, grid, single, s);
-    case 4: return launch_pt<MAXJ, 4>(p, grid, single, s);
-    case 2: return launch_pt<MAXJ, 2>(p, grid, single, s);
-    default: return launch_pt<MAXJ, 0>(p, grid, single, s);
+    case 8: return launch_pt<MAXJ, 8>(p, grid, single, pdl, s);
+    case 4: return launch_pt<MAXJ, 4>(p, grid, single, pdl, s);
+    case 2: return launch_pt<MAXJ, 2>(p, grid, single, pdl, s);
+    default: return launch_pt<MAXJ, 0>(p, grid, single, pdl, s);
   }
 }
 
@@ -215,11 +223,11 @@ int occupancy_impl(int P) {
 
 }  // namespace
 
-cudaError_t launch_reduce(const ReduceParams1& p, int grid, bool single, cudaStream_t s) {
-  return launch_impl(p, grid, single, s);
+cudaError_t launch_reduce(const ReduceParams1& p, int grid, bool single, bool pdl, cudaStream_t s) {
+  return launch_impl(p, grid, single, pdl, s);
 }
-cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, cudaStream_t s) {
-  return launch_impl(p, grid, single, s);
+cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, bool pdl, cudaStream_t s) {
+  return launch_impl(p, grid, single, pdl, s);
 }
 
 int reduce_ctas_per_sm(int P, bool scatter) {
