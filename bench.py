@@ -466,7 +466,7 @@ def run_dc(args) -> int:
         kern_bytes[path] += nbytes * len(us_list)
         kern_launches[path] += len(us_list)
     dom = max(kern_time, key=kern_time.get)
-    kname = {"multi": "dc_gather_kernel<1,64,2>", "single": "dc_gather_single_kernel<1,64,2>"}[dom]
+    kname = {"multi": "dc_gather_kernel<1,64,3>" if dc.get_option("gather_staged") else "dc_gather_kernel<1,64,2>", "single": "dc_gather_single_kernel<1,64,2>"}[dom]
     achieved = kern_bytes[dom] / kern_time[dom] / 1e3  # GB/s
     traffic = load_traffic(kname)
     big = [row for row in table if row["P"] == 8 and row["bytes_per_rank"] == 4 << 20][0]

@@ -140,10 +140,16 @@ const char *dc_status_name(int status);
  *   "reduce_single_max_bytes" single-CTA reductions up to this many input
  *                             bytes per rank
  *   "grid_ctas"               0 = automatic, else the multi-CTA grid size
+ *   "pdl"                     1 (default) = launch with programmatic stream
+ *                             serialization, so a kernel's launch overlaps the
+ *                             end of the previous kernel in the stream (it still
+ *                             waits for that kernel before touching memory)
+ *   "gather_staged"           1 (default) = aligned gathers stage their loads
+ *                             through shared memory with cp.async
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
- * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES and DC_GRID_CTAS set
- * the initial values (read once, at the first call).
+ * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL
+ * and DC_GATHER_STAGED set the initial values (read once, at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.
  */

@@ -48,6 +48,7 @@ struct Options {
   std::atomic<long long> grid_ctas{0};
   std::atomic<long long> test_fail_launch{0};
   std::atomic<long long> pdl{1};
+  std::atomic<long long> gather_staged{1};
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -65,6 +66,7 @@ const OptionKey kKeys[] = {
     {"grid_ctas", "DC_GRID_CTAS", &g_opt.grid_ctas},
     {"test_fail_launch", nullptr, &g_opt.test_fail_launch},
     {"pdl", "DC_PDL", &g_opt.pdl},
+    {"gather_staged", "DC_GATHER_STAGED", &g_opt.gather_staged},
 };
 
 void read_env_once() {
@@ -99,7 +101,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 16;
+constexpr int kFamilies = 24;
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -217,13 +219,14 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   st = sm_count(dev, &sms);
   if (st != DC_OK) return st;
   const bool single = use_single(out_bytes, g_opt.gather_single_max.load());
+  prm.staged = g_opt.gather_staged.load() ? 1 : 0;
   int grid = 1;
   if (!single) {
-    bool flat = true;
-    for (int j = 0; j < prm.njobs; ++j) flat = flat && (prm.job[j].flags & kJobFlat);
-    const int fam = family * 2 + (flat ? 1 : 0);
-    const int occ = occupancy(dev, fam, [family, flat] { return gather_ctas_per_sm(family, flat); });
-    const uint64_t tile = static_cast<uint64_t>(kGatherBlock) * (flat ? kGatherUnroll : kGatherUnrollGeneral);
+    const int mode = gather_mode_of(prm);
+    const int fam = family * 4 + mode;
+    const int occ = occupancy(dev, fam, [family, mode] { return gather_ctas_per_sm(family, mode); });
+    const int unroll = mode == 0 ? kGatherUnrollGeneral : mode == 3 ? kStagedVectors : kGatherUnroll;
+    const uint64_t tile = static_cast<uint64_t>(kGatherBlock) * unroll;
     grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
   }
   return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather");
@@ -273,7 +276,7 @@ dc_status_t launch_reduce_plan(Params& prm, int family, uint64_t in_bytes_per_ra
   int grid = 1;
   if (!single) {
     const int P = prm.P;
-    const bool scatter = family >= 12;
+    const bool scatter = family >= 20;
     const int occ = occupancy(dev, family, [P, scatter] { return reduce_ctas_per_sm(P, scatter); });
     const uint64_t tile = static_cast<uint64_t>(kReduceBlock) * kReduceUnroll;
     grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
@@ -281,9 +284,9 @@ dc_status_t launch_reduce_plan(Params& prm, int family, uint64_t in_bytes_per_ra
   return check_launch(launch_reduce(prm, grid, single, g_opt.pdl.load() != 0, stream), what);
 }
 
-int reduce_family(int P, bool scatter) {  // occupancy cache slots 8..15 (gather uses 0..5)
+int reduce_family(int P, bool scatter) {  // occupancy cache slots 16..23 (gather uses 0..11)
   const int pt = P == 8 ? 0 : P == 4 ? 1 : P == 2 ? 2 : 3;
-  return (scatter ? 12 : 8) + pt;
+  return (scatter ? 20 : 16) + pt;
 }
 
 dc_status_t check_bf16_ptrs(const void* const* ptrs, int P, const char* name) {

@@ -80,6 +80,26 @@ __device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uin
   return r;
 }
 
+// Asynchronous 16-byte copy global -> shared (cp.async, cached in L2 only).
+// The data travels without passing through registers; the issuing thread
+// waits for its own copies with cp.async.wait_group, a hardware wait.
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared16(uint32_t smem_addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr)
+               : "memory");
+  return v;
+}
+
 // BF16 -> binary32 is exact: the 16 bits become the high half of the word.
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -180,6 +180,69 @@ __device__ __forceinline__ void gather_tiles_flat1(const GatherParams<1, MAXS>& 
   }
 }
 
+// One aligned job, staged through shared memory.  Same tiles and rank walk
+// as gather_tiles_flat1 (tile = BLOCK*V vectors), but the loads are cp.async
+// copies into a ring of S shared-memory slots per thread: while tile i is
+// stored (shared -> registers -> STG.128), the copies of tiles i+1..i+S-1
+// are already in flight, and in-flight data costs shared memory instead of
+// registers (192 KB per SM instead of 128 KB).  Each thread only reads back
+// the slots it filled itself, so no barrier is needed; the waits are
+// cp.async.wait_group, a hardware wait on the thread's own copies.
+template <int BLOCK, int V, int S, int MAXS>
+__device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>& p, uint32_t first,
+                                                    uint32_t step) {
+  extern __shared__ uint4 stage_buf[];  // [S][V][BLOCK]
+  constexpr uint32_t kTile = static_cast<uint32_t>(BLOCK) * V;
+  const uint32_t total = static_cast<uint32_t>(p.total_vec);
+  const uint32_t ntiles = (total + kTile - 1) / kTile;
+  const uint32_t vp = static_cast<uint32_t>(p.job[0].bytes >> 4);
+  uint4* out = reinterpret_cast<uint4*>(p.job[0].out);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
+  uint32_t r = 0, rlo = 0, rhi = vp;
+  bool fresh = true;
+  auto issue = [&](uint32_t slot, uint32_t t) {
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint32_t k = t * kTile + u * BLOCK + threadIdx.x;
+      if (t < ntiles && k < total) {
+        if (fresh) {
+          r = k / vp;
+          rlo = r * vp;
+          rhi = rlo + vp;
+          fresh = false;
+        }
+        while (k >= rhi) {
+          ++r;
+          rlo = rhi;
+          rhi += vp;
+        }
+        cp_async16(sbase + 16u * BLOCK * (slot * V + u),
+                   reinterpret_cast<const uint4*>(p.src[r]) + (k - rlo));
+      }
+    }
+    cp_async_commit();  // one group per slot fill, empty past the last tile
+  };
+  uint32_t t_issue = first;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    issue(s, t_issue);
+    t_issue += step;
+  }
+  uint32_t slot = 0;
+  for (uint32_t t = first; t < ntiles; t += step) {
+    cp_async_wait<S - 1>();  // the oldest group: tile t
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint32_t k = t * kTile + u * BLOCK + threadIdx.x;
+      if (k < total) st16(out + k, ld_shared16(sbase + 16u * BLOCK * (slot * V + u)));
+    }
+    issue(slot, t_issue);  // refill the slot just drained
+    t_issue += step;
+    slot = (slot + 1 == S) ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
 template <int BLOCK, int UNROLL, bool FLAT, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
                                              uint64_t step) {
@@ -254,7 +317,7 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
 
 // Kernel modes: kGeneral (any jobs), kFlat (all jobs 16-byte aligned),
 // kFlat1 (one aligned job with fewer than 2^31 output vectors).
-enum Mode : int { kGeneral = 0, kFlat = 1, kFlat1 = 2 };
+enum Mode : int { kGeneral = 0, kFlat = 1, kFlat1 = 2, kFlat1Staged = 3 };
 
 template <int BLOCK, int UNROLL, int MODE, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
@@ -262,13 +325,16 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
   if constexpr (MODE == kFlat1 && MAXJ == 1)
     gather_tiles_flat1<BLOCK, UNROLL, uint32_t>(p, static_cast<uint32_t>(first),
                                                 static_cast<uint32_t>(step));
+  else if constexpr (MODE == kFlat1Staged && MAXJ == 1)
+    gather_tiles_staged<BLOCK, kStagedVectors, kStagedStages>(p, static_cast<uint32_t>(first),
+                                                              static_cast<uint32_t>(step));
   else
     gather_tiles<BLOCK, UNROLL, MODE != kGeneral>(p, first, step);
 }
 
 // Multi-CTA gather: CTA c copies tiles c, c + gridDim.x, ...
 template <int MAXJ, int MAXS, int MODE>
-__global__ void __launch_bounds__(kGatherBlock, MODE == kFlat1 ? 4 : 2)
+__global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat1Staged) ? 4 : 2)
     dc_gather_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
   pdl_enter();
   gather_mode<kGatherBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(
@@ -288,16 +354,24 @@ template <int MAXJ, int MAXS>
 int mode_of(const GatherParams<MAXJ, MAXS>& p) {
   for (int j = 0; j < p.njobs; ++j)
     if (!(p.job[j].flags & kJobFlat)) return kGeneral;
-  return (MAXJ == 1 && p.total_vec < (1ull << 31)) ? kFlat1 : kFlat;
+  if (MAXJ == 1 && p.total_vec < (1ull << 31)) return p.staged ? kFlat1Staged : kFlat1;
+  return kFlat;
+}
+
+constexpr size_t staged_smem(int block) {
+  return static_cast<size_t>(kStagedStages) * kStagedVectors * block * 16;
 }
 
 template <int MAXJ, int MAXS, int MODE>
 cudaError_t launch_mode(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, bool pdl,
                         cudaStream_t s) {
-  if (single)
-    return launch_ex(dc_gather_single_kernel<MAXJ, MAXS, MODE>, 1,
-                     MODE == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock, pdl, s, p);
-  return launch_ex(dc_gather_kernel<MAXJ, MAXS, MODE>, grid, kGatherBlock, pdl, s, p);
+  if (single) {  // small outputs: staging buys nothing, use the register path
+    constexpr int kMode = MODE == kFlat1Staged ? kFlat1 : MODE;
+    constexpr int block = kMode == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock;
+    return launch_ex(dc_gather_single_kernel<MAXJ, MAXS, kMode>, 1, block, pdl, s, p);
+  }
+  return launch_ex(dc_gather_kernel<MAXJ, MAXS, MODE>, grid, kGatherBlock, pdl, s, p,
+                   MODE == kFlat1Staged ? staged_smem(kGatherBlock) : 0);
 }
 
 template <int MAXJ, int MAXS>
@@ -306,20 +380,32 @@ cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
   switch (mode_of(p)) {
     case kGeneral: return launch_mode<MAXJ, MAXS, kGeneral>(p, grid, single, pdl, s);
     case kFlat: return launch_mode<MAXJ, MAXS, kFlat>(p, grid, single, pdl, s);
-    default:
+    case kFlat1:
       if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);
+      return cudaErrorInvalidValue;
+    default:
+      if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1Staged>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
   }
 }
 
 template <int MAXJ, int MAXS>
-int occupancy_impl(bool flat) {
+int occupancy_impl(int mode) {
   int n = 0;
-  const cudaError_t e =
-      flat ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                 &n, dc_gather_kernel<MAXJ, MAXS, MAXJ == 1 ? kFlat1 : kFlat>, kGatherBlock, 0)
-           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kGeneral>,
-                                                           kGatherBlock, 0);
+  cudaError_t e;
+  if (mode == kGeneral)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kGeneral>,
+                                                      kGatherBlock, 0);
+  else if (mode == kFlat || MAXJ != 1)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kFlat>,
+                                                      kGatherBlock, 0);
+  else if (mode == kFlat1)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, dc_gather_kernel<MAXJ, MAXS, MAXJ == 1 ? kFlat1 : kFlat>, kGatherBlock, 0);
+  else
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, dc_gather_kernel<MAXJ, MAXS, MAXJ == 1 ? kFlat1Staged : kFlat>, kGatherBlock,
+        MAXJ == 1 ? staged_smem(kGatherBlock) : 0);
   if (e != cudaSuccess) {
     cudaGetLastError();
     n = 1;
@@ -339,12 +425,16 @@ cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, bool pd
   return launch_impl(p, grid, single, pdl, s);
 }
 
-int gather_ctas_per_sm(int which, bool flat) {
+int gather_ctas_per_sm(int which, int mode) {
   switch (which) {
-    case 0: return occupancy_impl<1, kMaxRanks>(flat);
-    case 1: return occupancy_impl<kManySmallTensors, kManySmallSegments>(flat);
-    default: return occupancy_impl<kManyMaxTensors, kManyMaxSegments>(flat);
+    case 0: return occupancy_impl<1, kMaxRanks>(mode);
+    case 1: return occupancy_impl<kManySmallTensors, kManySmallSegments>(mode);
+    default: return occupancy_impl<kManyMaxTensors, kManyMaxSegments>(mode);
   }
 }
+
+int gather_mode_of(const GatherParams1& p) { return mode_of(p); }
+int gather_mode_of(const GatherParamsS& p) { return mode_of(p); }
+int gather_mode_of(const GatherParamsL& p) { return mode_of(p); }
 
 }  // namespace dc

@@ -23,6 +23,11 @@ constexpr int kGatherSingleBlock = 1024;       // aligned (flat) jobs only
 constexpr int kGatherSingleBlockGeneral = 512;  // any job: the realigning path needs registers
 constexpr int kGatherUnroll = 4;         // 16-byte vectors in flight per thread (aligned)
 constexpr int kGatherUnrollGeneral = 2;  // realigned vectors (up to two loads each) per thread
+// Shared-memory staged aligned copy: kStagedStages ring slots of
+// kStagedVectors 16-byte vectors per thread (2 x 3 x 512 x 16 B = 48 KB per
+// CTA, four CTAs = 192 KB in flight per SM, no registers held).
+constexpr int kStagedStages = 2;
+constexpr int kStagedVectors = 3;
 constexpr int kReduceBlock = 256;
 constexpr int kReduceSingleBlock = 512;
 constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread
@@ -57,6 +62,8 @@ struct GatherParams {
   uint64_t total_vec;   // sum of nvec over the jobs
   int32_t njobs;
   int32_t P;
+  int32_t staged;       // aligned single job: stage through shared memory with cp.async
+  int32_t pad;
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
 };
@@ -111,11 +118,12 @@ cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, bool pd
 
 // cudaLaunchKernelEx with an optional programmatic-serialization attribute.
 template <typename Kernel, typename Params>
-cudaError_t launch_ex(Kernel kernel, int grid, int block, bool pdl, cudaStream_t s, const Params& p) {
+cudaError_t launch_ex(Kernel kernel, int grid, int block, bool pdl, cudaStream_t s, const Params& p,
+                      size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(static_cast<unsigned>(block));
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -126,7 +134,12 @@ cudaError_t launch_ex(Kernel kernel, int grid, int block, bool pdl, cudaStream_t
 }
 
 // Resident CTAs per SM of the multi-CTA kernels (occupancy API, per device).
-int gather_ctas_per_sm(int which, bool flat);  // which: 0 one job, 1 small many, 2 large many
+int gather_ctas_per_sm(int which, int mode);  // which: 0 one job, 1 small many, 2 large many
+// Kernel mode a launch will use: 0 general, 1 aligned jobs, 2 one aligned job,
+// 3 one aligned job staged through shared memory.
+int gather_mode_of(const GatherParams1& p);
+int gather_mode_of(const GatherParamsS& p);
+int gather_mode_of(const GatherParamsL& p);
 int reduce_ctas_per_sm(int P, bool scatter);
 
 }  // namespace dc

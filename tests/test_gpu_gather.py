@@ -67,9 +67,10 @@ def test_config2_aligned_sweep(case):
     peers = [W.random_bf16_patterns(case.seed, r, case.bytes_per_rank // 2).view(np.uint8)
              for r in range(case.P)]
     want = oracle.all_gather(peers)
-    got, guards = run_gather(peers, [0] * case.P, 0)
-    assert np.array_equal(got, want)
-    assert guards
+    for opts in ({}, {"gather_staged": 1}):
+        got, guards = run_gather(peers, [0] * case.P, 0, **opts)
+        assert np.array_equal(got, want), opts
+        assert guards
 
 
 def _config3_by_size():
@@ -150,6 +151,9 @@ def test_independent_per_rank_offsets():
     {"force_path": 2, "grid_ctas": 1}, {"force_path": 2, "grid_ctas": 3},
     {"force_path": 2, "grid_ctas": 151}, {"force_path": 2, "grid_ctas": 5000},
     {"force_generic": 1, "force_path": 1},
+    {"gather_staged": 1}, {"gather_staged": 1, "force_path": 2, "grid_ctas": 3},
+    {"gather_staged": 1, "force_path": 2, "grid_ctas": 7000}, {"gather_staged": 1, "force_path": 1},
+    {"pdl": 0},
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_path_and_grid_independence(opts):
     """The bytes never depend on the path, the grid or the flat/generic
