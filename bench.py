@@ -384,6 +384,25 @@ def e2e_measure(torch, dc, device, stream, cases, steps):
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": steps}
 
 
+def rank_max(value: float, dist=None, device=None) -> float:
+    """The largest `value` over all ranks (the slowest replica sets the
+    job's time); the local value when there is no process group."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, bytes_per_rank_step: int, slowest_ms_per_step: float) -> float:
+    """GB/s of the whole job: every replica moves `bytes_per_rank_step` per
+    step, and the job's step takes as long as its slowest replica's."""
+    return world * bytes_per_rank_step / slowest_ms_per_step / 1e6
+
+
 def stats(xs):
     return {"us_mean": float(np.mean(xs)), "us_median": float(np.median(xs)),
             "us_p10": float(np.percentile(xs, 10)), "us_p90": float(np.percentile(xs, 90))}
@@ -445,13 +464,9 @@ def run_dc(args) -> int:
         dist.barrier()
     clocks = sampler.stop()
 
-    gpu_ms_total = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([gpu_ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        gpu_ms_total = float(t.item())
+    gpu_ms_total = rank_max(float(sum(step_ms)), dist, device)
     ms_per_step = gpu_ms_total / args.steps
-    value = world * step_bytes / ms_per_step / 1e6  # GB/s over all ranks
+    value = job_throughput(world, step_bytes, ms_per_step)  # GB/s over all ranks
 
     table = []
     kern_time = {"multi": 0.0, "single": 0.0}
@@ -475,10 +490,7 @@ def run_dc(args) -> int:
     if not args.no_reductions:
         extra = reductions_block(torch, dc, device, stream, flush, peak)
     e2e = e2e_measure(torch, dc, device, stream, cases, min(args.steps, 20))
-    if dist:
-        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["value"] = world * step_bytes / float(t.item()) / 1e6
+    e2e["value"] = job_throughput(world, step_bytes, rank_max(e2e["ms_per_step"], dist, device))
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
