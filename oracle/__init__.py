@@ -40,10 +40,17 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
                                       ctypes.c_size_t]
     L.orc_reduce_scatter_bf16.argtypes = [ctypes.POINTER(P), ctypes.POINTER(P),
                                           ctypes.c_int, ctypes.c_size_t]
+    L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_f16_to_f32.restype = ctypes.c_float
+    L.orc_f32_to_f16_rne_array.argtypes = [P, P, ctypes.c_size_t]
+    L.orc_all_reduce.argtypes = [ctypes.POINTER(P), ctypes.POINTER(P), ctypes.c_int,
+                                 ctypes.c_size_t, ctypes.c_int, ctypes.c_int]
+    L.orc_reduce_scatter.argtypes = [ctypes.POINTER(P), ctypes.POINTER(P), ctypes.c_int,
+                                     ctypes.c_size_t, ctypes.c_int, ctypes.c_int]
     L.orc_subnormals_preserved.argtypes = []
     for f in ("orc_all_gather", "orc_all_gather_many", "orc_all_reduce_bf16",
-              "orc_f32_to_bf16_rne_array", "orc_reduce_scatter_bf16",
-              "orc_subnormals_preserved"):
+              "orc_f32_to_bf16_rne_array", "orc_reduce_scatter_bf16", "orc_f32_to_f16_rne_array",
+              "orc_all_reduce", "orc_reduce_scatter", "orc_subnormals_preserved"):
         getattr(L, f).restype = ctypes.c_int
     if L.orc_subnormals_preserved() != 1:
         raise RuntimeError("oracle host flushes binary32 subnormals; results would be wrong")
@@ -57,6 +64,22 @@ def _ptrs(arrs: Sequence[np.ndarray]):
 def _u8(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
     return a.view(np.uint8).reshape(-1)
+
+
+DTYPES = {"bf16": (0, np.uint16), "f16": (1, np.uint16), "f32": (2, np.float32)}
+ORDERS = {"linear": 0, "tree": 1}
+
+
+def _as_elems(a, dtype: str) -> np.ndarray:
+    """A contiguous 1-D view of the payload as the oracle's element type
+    (16-bit patterns for bf16 / f16, binary32 for f32)."""
+    want = DTYPES[dtype][1]
+    a = np.ascontiguousarray(a)
+    if a.dtype != want:
+        if a.dtype.itemsize != np.dtype(want).itemsize:
+            raise TypeError(f"{dtype} payloads need {np.dtype(want).itemsize}-byte elements")
+        a = a.view(want)
+    return a.reshape(-1)
 
 
 def _as_bf16_bits(a) -> np.ndarray:
@@ -162,6 +185,56 @@ class Oracle:
             raise ValueError(f"orc_reduce_scatter_bf16 rejected its arguments ({rc})")
         return outs
 
+    # ------------------------------------------- other types and orders ---
+    def f16_to_f32(self, h: int) -> float:
+        return float(self.L.orc_f16_to_f32(int(h) & 0xFFFF))
+
+    def f32_to_f16_rne_array(self, f32: np.ndarray) -> np.ndarray:
+        a = np.ascontiguousarray(f32)
+        if a.dtype == np.uint32:
+            a = a.view(np.float32)
+        a = a.astype(np.float32, copy=False).reshape(-1)
+        out = np.empty(a.size, dtype=np.uint16)
+        if self.L.orc_f32_to_f16_rne_array(a.ctypes.data, out.ctypes.data, a.size) != 0:
+            raise ValueError("orc_f32_to_f16_rne_array rejected its arguments")
+        return out
+
+    def all_reduce_all_outputs(self, inputs, dtype="bf16", order="linear") -> list[np.ndarray]:
+        """Every rank's output of the fixed-order all_reduce of element type
+        `dtype` ("bf16", "f16", "f32") in summation order `order` ("linear",
+        "tree")."""
+        ins = [_as_elems(x, dtype) for x in inputs]
+        P = len(ins)
+        n = ins[0].size
+        if any(x.size != n for x in ins):
+            raise ValueError("all inputs must have the same element count")
+        outs = [np.empty(n, dtype=DTYPES[dtype][1]) for _ in range(P)]
+        rc = self.L.orc_all_reduce(_ptrs(ins), _ptrs(outs), P, n, DTYPES[dtype][0], ORDERS[order])
+        if rc != 0:
+            raise ValueError(f"orc_all_reduce rejected its arguments ({rc})")
+        return outs
+
+    def all_reduce(self, inputs, dtype="bf16", order="linear") -> np.ndarray:
+        outs = self.all_reduce_all_outputs(inputs, dtype, order)
+        for r in range(1, len(outs)):
+            if not np.array_equal(outs[0].view(np.uint8), outs[r].view(np.uint8)):
+                raise AssertionError("oracle wrote different values to different ranks")
+        return outs[0]
+
+    def reduce_scatter(self, inputs, dtype="bf16", order="linear") -> list[np.ndarray]:
+        ins = [_as_elems(x, dtype) for x in inputs]
+        P = len(ins)
+        n = ins[0].size
+        if any(x.size != n for x in ins) or n % P != 0:
+            raise ValueError("inputs must be equal length and divisible by P")
+        C = n // P
+        outs = [np.empty(C, dtype=DTYPES[dtype][1]) for _ in range(P)]
+        rc = self.L.orc_reduce_scatter(_ptrs(ins), _ptrs(outs), P, C, DTYPES[dtype][0],
+                                       ORDERS[order])
+        if rc != 0:
+            raise ValueError(f"orc_reduce_scatter rejected its arguments ({rc})")
+        return outs
+
     def reduce_bf16_at(self, inputs, index: np.ndarray) -> np.ndarray:
         """The fold evaluated only at the given element indices (for sampled
         checks of full-size outputs)."""
@@ -208,3 +281,11 @@ def reduce_scatter_bf16(inputs):
 
 def reduce_bf16_at(inputs, index):
     return default().reduce_bf16_at(inputs, index)
+
+
+def all_reduce(inputs, dtype="bf16", order="linear"):
+    return default().all_reduce(inputs, dtype, order)
+
+
+def reduce_scatter(inputs, dtype="bf16", order="linear"):
+    return default().reduce_scatter(inputs, dtype, order)

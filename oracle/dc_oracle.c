@@ -130,6 +130,164 @@ int orc_reduce_scatter_bf16(const uint16_t *const *in, uint16_t *const *out,
     return 0;
 }
 
+/* ------------------------------------------------------------------------
+ * binary16.  Layout: sign (1), exponent (5, bias 15), fraction (10).  Normal
+ * values are (1 + f/1024) * 2^(e-15); subnormals f * 2^-24. */
+float orc_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    uint32_t e = (h >> 10) & 0x1Fu;
+    uint32_t f = h & 0x3FFu;
+    uint32_t u;
+    if (e == 0x1Fu) {                /* inf, or NaN (made quiet, payload kept) */
+        u = sign | 0x7F800000u | (f << 13) | (f ? 0x00400000u : 0u);
+    } else if (e != 0) {             /* normal: rebias the exponent */
+        u = sign | ((e - 15u + 127u) << 23) | (f << 13);
+    } else if (f == 0) {             /* signed zero */
+        u = sign;
+    } else {                         /* subnormal: f * 2^-24, exact in binary32 */
+        float v = (float)f * 5.9604644775390625e-8f; /* 2^-24 */
+        memcpy(&u, &v, sizeof u);
+        u |= sign;
+    }
+    float out;
+    memcpy(&out, &u, sizeof out);
+    return out;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even.
+ * Normal range (|x| >= 2^-14): drop the low 13 fraction bits with the same
+ * bias-and-truncate rule as the BF16 rounding, then move the exponent from
+ * bias 127 to bias 15 (a carry out of the fraction correctly bumps the
+ * exponent).  |x| >= 65520 is at or beyond the halfway point between the
+ * largest binary16 value 65504 (odd significand) and 2^16, so it becomes
+ * infinity.  Below 2^-14 the result is a multiple k of 2^-24: k is |x| / 2^-24
+ * rounded to nearest even, computed on the integer significand. */
+uint16_t orc_f32_to_f16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u)
+        return (uint16_t)(sign | 0x7E00u);
+    if (a >= 0x477FF000u)            /* 65520 and above, infinity included */
+        return (uint16_t)(sign | 0x7C00u);
+    if (a >= 0x38800000u) {          /* 2^-14 and above: normal binary16 */
+        uint32_t r = a + 0x0FFFu + ((a >> 13) & 1u);
+        return (uint16_t)(sign | ((r >> 13) - (112u << 10)));
+    }
+    if (a < 0x00800000u)             /* binary32 subnormal or zero: below 2^-126 */
+        return sign;
+    uint32_t sig = (a & 0x007FFFFFu) | 0x00800000u;   /* 24-bit significand */
+    int e = (int)(a >> 23) - 127;                      /* |x| = sig * 2^(e-23) */
+    int sh = -(e + 1);                                 /* k = sig * 2^(e+1) = sig >> sh */
+    if (sh >= 25)
+        return sign;                 /* k < 1/2: below half of 2^-24, rounds to 0 */
+    uint32_t q = sig >> sh;
+    uint32_t rem = sig & ((1u << sh) - 1u);
+    uint32_t half = 1u << (sh - 1);
+    if (rem > half || (rem == half && (q & 1u)))
+        ++q;
+    return (uint16_t)(sign | q);     /* q = 1024 is the smallest normal, 0x0400 */
+}
+
+int orc_f32_to_f16_rne_array(const float *in, uint16_t *out, size_t n)
+{
+    if (n > 0 && (in == NULL || out == NULL))
+        return -1;
+    for (size_t i = 0; i < n; ++i)
+        out[i] = orc_f32_to_f16_rne(in[i]);
+    return 0;
+}
+
+/* Element i of input q, widened to binary32 (exact for every type). */
+static float load_as_f32(const void *const *in, int q, size_t i, int dtype)
+{
+    if (dtype == ORC_F32)
+        return ((const float *)in[q])[i];
+    uint16_t h = ((const uint16_t *)in[q])[i];
+    return dtype == ORC_F16 ? orc_f16_to_f32(h) : orc_bf16_to_f32(h);
+}
+
+static void store_from_f32(void *const *out, int r, size_t i, float v, int dtype)
+{
+    if (dtype == ORC_F32)
+        ((float *)out[r])[i] = v;
+    else if (dtype == ORC_F16)
+        ((uint16_t *)out[r])[i] = orc_f32_to_f16_rne(v);
+    else
+        ((uint16_t *)out[r])[i] = orc_f32_to_bf16_rne(v);
+}
+
+/* The tree fold over x[lo..hi): split at the largest power of two below the
+ * count, fold each side, add left + right. */
+static float fold_tree(const float *x, int lo, int hi)
+{
+    int n = hi - lo;
+    if (n == 1)
+        return x[lo];
+    int m = 1;
+    while (m * 2 < n)
+        m *= 2;
+    float left = fold_tree(x, lo, lo + m);
+    float right = fold_tree(x, lo + m, hi);
+    return left + right;
+}
+
+static float fold_element(const void *const *in, int P, size_t i, int dtype, int order)
+{
+    float x[64] = {0.0f};
+    for (int q = 0; q < P; ++q)
+        x[q] = load_as_f32(in, q, i, dtype);
+    if (order == ORC_ORDER_TREE)
+        return fold_tree(x, 0, P);
+    float acc = x[0];
+    for (int q = 1; q < P; ++q)
+        acc = acc + x[q];
+    return acc;
+}
+
+static int check_args(const void *const *in, void *const *out, int P, size_t n, int dtype,
+                      int order)
+{
+    if (P < 1 || P > 64 || dtype < ORC_BF16 || dtype > ORC_F32 ||
+        (order != ORC_ORDER_LINEAR && order != ORC_ORDER_TREE))
+        return -1;
+    if (n == 0)
+        return 0;
+    if (in == NULL || out == NULL)
+        return -1;
+    for (int r = 0; r < P; ++r)
+        if (in[r] == NULL || out[r] == NULL)
+            return -1;
+    return 0;
+}
+
+int orc_all_reduce(const void *const *in, void *const *out, int P, size_t count, int dtype,
+                   int order)
+{
+    if (check_args(in, out, P, count, dtype, order) != 0)
+        return -1;
+    for (size_t i = 0; i < count; ++i) {
+        float y = fold_element(in, P, i, dtype, order);
+        for (int r = 0; r < P; ++r)
+            store_from_f32(out, r, i, y, dtype);
+    }
+    return 0;
+}
+
+int orc_reduce_scatter(const void *const *in, void *const *out, int P, size_t C, int dtype,
+                       int order)
+{
+    if (check_args(in, out, P, C, dtype, order) != 0)
+        return -1;
+    for (int r = 0; r < P; ++r)
+        for (size_t j = 0; j < C; ++j)
+            store_from_f32(out, r, j, fold_element(in, P, (size_t)r * C + j, dtype, order), dtype);
+    return 0;
+}
+
 int orc_subnormals_preserved(void)
 {
     /* 2^-140 is a binary32 subnormal; with FTZ/DAZ either the operand or

@@ -63,6 +63,40 @@ int orc_all_reduce_bf16(const uint16_t *const *in, uint16_t *const *out,
 int orc_reduce_scatter_bf16(const uint16_t *const *in, uint16_t *const *out,
                             int P, size_t C);
 
+/* ------------------------------------------------------------------------
+ * Other element types and summation orders.
+ *
+ * The element type sets how a value is widened to binary32 (exactly) and how
+ * the binary32 total is rounded back (round to nearest, ties to even; binary32
+ * totals are stored as they are).  The order sets the shape of the fold over
+ * the P widened values of one element:
+ *   ORC_ORDER_LINEAR: ((x0 + x1) + x2) + ... + x_{P-1};
+ *   ORC_ORDER_TREE:   fold(x[lo..hi)) = x[lo] for one value, otherwise
+ *                     fold(x[lo..lo+m)) + fold(x[lo+m..hi)) with m the largest
+ *                     power of two below hi - lo (pairs of neighbouring ranks,
+ *                     then pairs of pairs, the last odd group added last).
+ * Every add is one binary32 add, round to nearest even.  Page:
+ * [PR491], author's replies: the backend is named "cuda_ipc_fixed_tree" (a
+ * fixed tree is named; its shape is not given, and the one above is the
+ * reading used). */
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2 };
+enum { ORC_ORDER_LINEAR = 0, ORC_ORDER_TREE = 1 };
+
+/* IEEE binary16 bit pattern -> binary32, exact. */
+float orc_f16_to_f32(uint16_t h);
+/* binary32 -> IEEE binary16, round to nearest, ties to even; NaN -> quiet NaN
+ * (0x7E00) with the input's sign. */
+uint16_t orc_f32_to_f16_rne(float f);
+int orc_f32_to_f16_rne_array(const float *in, uint16_t *out, size_t n);
+
+/* all_reduce / reduce_scatter of element type `dtype` (element size 2 for
+ * BF16 and F16, 4 for F32) in summation order `order`; same layouts and
+ * aliasing rules as the BF16 functions above. */
+int orc_all_reduce(const void *const *in, void *const *out, int P, size_t count, int dtype,
+                   int order);
+int orc_reduce_scatter(const void *const *in, void *const *out, int P, size_t C, int dtype,
+                       int order);
+
 /* 1 if binary32 subnormals survive arithmetic on this host (no FTZ/DAZ),
  * 0 otherwise.  The oracle is only meaningful when this returns 1. */
 int orc_subnormals_preserved(void);

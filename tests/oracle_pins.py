@@ -320,3 +320,199 @@ ALL_CHECKS = [
     check_reduce_scatter_shards,
     check_reduce_scatter_worked_example,
 ]
+
+
+# ------------------------------------------- other element types and orders ---
+
+def load_typed_examples():
+    rows = []
+    with open(os.path.join(GOLDEN, "typed_reduction_worked_examples.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, dtype, order, ins, exp, _why = [c.strip() for c in line.split("|", 5)]
+            rows.append((name, dtype, order, [int(h, 16) for h in ins.split()], int(exp, 16)))
+    return rows
+
+
+_NP = {"bf16": np.uint16, "f16": np.uint16, "f32": np.uint32}
+
+
+def _bits(arr, dtype):
+    return np.ascontiguousarray(arr).view(_NP[dtype])
+
+
+def check_typed_worked_examples(orc):
+    for name, dtype, order, inputs, expected in load_typed_examples():
+        cols = [np.array([h], dtype=_NP[dtype]) for h in inputs]
+        got = int(_bits(orc.all_reduce(cols, dtype, order), dtype)[0])
+        assert got == expected, (name, hex(got), hex(expected))
+        # every rank's output, and several copies of the column (no interaction)
+        cols = [np.full(9, h, dtype=_NP[dtype]) for h in inputs]
+        for out in orc.all_reduce_all_outputs(cols, dtype, order):
+            assert (_bits(out, dtype) == expected).all(), (name, "all outputs")
+
+
+def check_f16_rounding_matches_torch_cast(orc):
+    """Library routine: torch's float32 -> float16 cast (round to nearest
+    even)."""
+    import torch
+
+    u = _rounding_probe_values()
+    # also the binary16 neighbourhoods: ties on the 13 dropped bits
+    rng = np.random.default_rng(11)
+    hi = rng.integers(0, 1 << 19, 4000, dtype=np.uint64)
+    ties = ((hi << np.uint64(13)) | np.uint64(0x1000)).astype(np.uint32)
+    u = np.concatenate([u, ties, ties - 1, ties + 1,
+                        np.array([0x477FF000, 0x477FEFFF, 0x38800000, 0x387FFFFF, 0x33800000,
+                                  0x33000000, 0x33000001, 0x337FFFFF, 0x00000001], dtype=np.uint32)])
+    got = orc.f32_to_f16_rne_array(u)
+    ref = torch.from_numpy(u.view(np.float32).copy()).to(torch.float16).view(torch.int16)
+    ref = ref.numpy().view(np.uint16)
+    nan = np.isnan(u.view(np.float32))
+    assert np.array_equal(got[~nan], ref[~nan]), "binary16 rounding differs from torch's cast"
+    assert all(((h & 0x7C00) == 0x7C00 and (h & 0x3FF)) for h in got[nan].tolist())
+
+
+def check_f16_rounding_matches_exact(orc, seed=12):
+    rng = np.random.default_rng(seed)
+    u = np.concatenate([
+        rng.integers(0, 1 << 32, 2000, dtype=np.uint64).astype(np.uint32),
+        # values inside the binary16 range, where the rounding does work
+        (rng.integers(0x33000000, 0x477FFFFF, 3000, dtype=np.uint64)).astype(np.uint32),
+        np.array([0x477FF000, 0x477FEFFF, 0x38800000, 0x387FFFFF, 0x33000000, 0x33000001],
+                 dtype=np.uint32),
+    ])
+    got = orc.f32_to_f16_rne_array(u)
+    for ui, gi in zip(u.tolist(), got.tolist()):
+        if (ui & 0x7F800000) == 0x7F800000:
+            continue
+        assert gi == ex.f32_to_f16_exact(ui), (hex(ui), hex(gi))
+
+
+def check_f16_widening_exhaustive(orc):
+    """Every binary16 pattern widens to the value torch's float16 -> float32
+    cast gives (NaN by class)."""
+    import torch
+
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(h.view(np.int16).copy()).view(torch.float16).float().numpy()
+    got = np.array([orc.f16_to_f32(int(x)) for x in range(0, 65536, 1)], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def _typed_column(rng, P, dtype, wide):
+    out = []
+    for _ in range(P):
+        s = int(rng.integers(0, 2))
+        if dtype == "bf16":
+            e = int(rng.integers(1, 255)) if wide else int(rng.integers(120, 131))
+            out.append((s << 15) | (e << 7) | int(rng.integers(0, 128)))
+        elif dtype == "f16":
+            e = int(rng.integers(0, 31)) if wide else int(rng.integers(12, 18))
+            out.append((s << 15) | (e << 10) | int(rng.integers(0, 1024)))
+        else:
+            e = int(rng.integers(1, 255)) if wide else int(rng.integers(120, 131))
+            out.append((s << 31) | (e << 23) | int(rng.integers(0, 1 << 23)))
+    return out
+
+
+def check_typed_folds_match_exact(orc, seed=13, n_cols=120):
+    """Exact rational fold (every binary32 add and the final rounding from
+    their definitions) for every element type, both orders, several P."""
+    rng = np.random.default_rng(seed)
+    for dtype in ("bf16", "f16", "f32"):
+        for order in ("linear", "tree"):
+            for P in (1, 2, 3, 4, 5, 6, 7, 8, 13):
+                cols = []
+                for k in range(n_cols):
+                    while True:
+                        c = _typed_column(rng, P, dtype, wide=(k % 3 == 0))
+                        try:
+                            cols.append((c, ex.fold_exact(c, dtype, order)))
+                            break
+                        except ValueError:
+                            continue
+                inputs = [np.array([c[r] for c, _ in cols], dtype=_NP[dtype]) for r in range(P)]
+                got = _bits(orc.all_reduce(inputs, dtype, order), dtype)
+                for k, (c, e) in enumerate(cols):
+                    assert int(got[k]) == e, (dtype, order, P, [hex(h) for h in c], hex(int(got[k])), hex(e))
+
+
+def check_typed_linear_matches_torch_cpu(orc, seed=14):
+    """Library routine: torch CPU binary32 adds in rank order, then torch's
+    cast back, for float16 and float32 (and the bfloat16 path again)."""
+    import torch
+
+    rng = np.random.default_rng(seed)
+    for dtype, tdt in (("f16", torch.float16), ("f32", torch.float32), ("bf16", torch.bfloat16)):
+        for P in (2, 3, 8):
+            xs = [_bits(np.array(_typed_column(rng, 4000, dtype, wide=False)), dtype) for _ in range(1)]
+            cols = [np.array(_typed_column(rng, 4000, dtype, wide=False), dtype=_NP[dtype]) for _ in range(P)]
+            t = [torch.from_numpy(c.view(np.int16 if dtype != "f32" else np.int32).copy()).view(tdt) for c in cols]
+            acc = t[0].float()
+            for q in range(1, P):
+                acc = acc + t[q].float()
+            ref = acc.to(tdt).view(torch.int16 if dtype != "f32" else torch.int32).numpy().view(_NP[dtype])
+            got = _bits(orc.all_reduce(cols, dtype, "linear"), dtype)
+            assert np.array_equal(got, ref), (dtype, P)
+            del xs
+
+
+def check_tree_order_bruteforce(orc):
+    """Every rank permutation of order-sensitive columns in the tree order:
+    the oracle equals the exact tree fold in that rank order, and the tree
+    and linear orders disagree on some of them."""
+    small = [0x3F80, 0xBF80, 0x3B80, 0xBB80, 0x3C00, 0xBC00, 0x4000, 0x4B80]
+    rng = random.Random(15)
+    differs = total = 0
+    for P in (4, 5, 6):
+        for _ in range(6):
+            big = rng.choice([0x4B80, 0xCB80])
+            col = [big, big ^ 0x8000] + [rng.choice(small) for _ in range(P - 2)]
+            perms = sorted(set(itertools.permutations(col)))[:400]
+            inputs = [np.array([p[r] for p in perms], dtype=np.uint16) for r in range(P)]
+            got = orc.all_reduce(inputs, "bf16", "tree")
+            lin = orc.all_reduce(inputs, "bf16", "linear")
+            exact = [ex.fold_exact(list(p), "bf16", "tree") for p in perms]
+            assert [int(g) for g in got] == exact, (P, col)
+            total += 1
+            differs += int(not np.array_equal(got, lin))
+    assert differs >= total // 2, (differs, total)
+
+
+def check_typed_reduce_scatter_shards(orc, seed=16):
+    rng = np.random.default_rng(seed)
+    for dtype in ("bf16", "f16", "f32"):
+        for order in ("linear", "tree"):
+            P, C = int(rng.integers(1, 9)), int(rng.integers(1, 200))
+            xs = [np.array(_typed_column(rng, P * C, dtype, wide=False), dtype=_NP[dtype]) for _ in range(P)]
+            full = _bits(orc.all_reduce(xs, dtype, order), dtype)
+            shards = orc.reduce_scatter(xs, dtype, order)
+            for r in range(P):
+                assert np.array_equal(_bits(shards[r], dtype), full[r * C:(r + 1) * C]), (dtype, order, r)
+
+
+def check_bf16_entry_points_agree(orc, seed=17):
+    """The BF16 functions and the typed functions with bf16 / linear are the
+    same fold."""
+    rng = np.random.default_rng(seed)
+    xs = [rng.integers(0, 65536, 3000, dtype=np.uint16) for _ in range(5)]
+    assert np.array_equal(orc.all_reduce_bf16(xs).view(np.uint8),
+                          orc.all_reduce(xs, "bf16", "linear").view(np.uint8))
+
+
+ALL_CHECKS += [
+    check_typed_worked_examples,
+    check_f16_rounding_matches_torch_cast,
+    check_f16_rounding_matches_exact,
+    check_f16_widening_exhaustive,
+    check_typed_folds_match_exact,
+    check_typed_linear_matches_torch_cpu,
+    check_tree_order_bruteforce,
+    check_typed_reduce_scatter_shards,
+    check_bf16_entry_points_agree,
+]

@@ -25,7 +25,10 @@ MUTANTS = {
     "zero_initial_accumulator": ("float acc = orc_bf16_to_f32(in[0][i]);\n    for (int q = 1;",
                                  "float acc = 0.0f;\n    for (int q = 0;"),
     # the last rank is dropped
-    "drop_last_rank": ("for (int q = 1; q < P; ++q)", "for (int q = 1; q < P - 1; ++q)"),
+    "drop_last_rank": ("for (int q = 1; q < P; ++q) {", "for (int q = 1; q < P - 1; ++q) {"),
+    # typed linear fold: the last rank dropped
+    "typed_drop_last_rank": ("for (int q = 1; q < P; ++q)\n        acc = acc + x[q];",
+                             "for (int q = 1; q < P - 1; ++q)\n        acc = acc + x[q];"),
     # BF16 rounding after every add instead of binary32 accumulation
     "bf16_accumulation": ("acc = acc + x;",
                           "acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + x));"),
@@ -48,6 +51,22 @@ MUTANTS = {
                                    "fold_ranks(in, P, j * (size_t)P + (size_t)r)"),
     # all_reduce only fills rank 0's output
     "all_reduce_one_output": ("out[r][i] = y;", "out[0][i] = y;"),
+    # binary16: truncation instead of round to nearest even
+    "f16_truncate": ("uint32_t r = a + 0x0FFFu + ((a >> 13) & 1u);", "uint32_t r = a;"),
+    # binary16: only infinity saturates; large finite values overflow the exponent
+    "f16_no_overflow_check": ("if (a >= 0x477FF000u)", "if (a >= 0x7F800000u)"),
+    # binary16 subnormals: off-by-one scale
+    "f16_subnormal_scale": ("int sh = -(e + 1);", "int sh = -e;"),
+    # binary16 widening: wrong exponent bias
+    "f16_widen_bias": ("u = sign | ((e - 15u + 127u) << 23) | (f << 13);",
+                       "u = sign | ((e - 15u + 128u) << 23) | (f << 13);"),
+    # tree order: halves instead of the largest power of two below the count
+    "tree_half_split": ("int m = 1;\n    while (m * 2 < n)\n        m *= 2;", "int m = n / 2;"),
+    # tree order ignored
+    "tree_is_linear": ("if (order == ORC_ORDER_TREE)", "if (0)"),
+    # binary16 payloads widened as BF16
+    "f16_read_as_bf16": ("return dtype == ORC_F16 ? orc_f16_to_f32(h) : orc_bf16_to_f32(h);",
+                         "return orc_bf16_to_f32(h);"),
 }
 
 
