@@ -311,6 +311,7 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     rows.append({"op": "reduce_scatter_bf16", "P": c["P"], "count": n, "shape": "16384x8192",
                  "us": us, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     del ins, outs
+    rows.extend(typed_rows(torch, dc, device, stream, flush, peak))
     P = W.CONFIG5_MANY_P
     tens = [[W.random_bytes_device(W.seed_for(5, 1), r, B, device, tensor=t) for r in range(P)]
             for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
@@ -319,6 +320,45 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     nbytes = 2 * P * sum(W.CONFIG5_MANY_SIZES)
     rows.append({"op": "all_gather_many", "P": P, "count": len(W.CONFIG5_MANY_SIZES),
                  "shape": "{3 B, 4 KiB, 100000 B, 1 MiB, 7 MiB+5 B, 32 MiB}", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    return rows
+
+
+def typed_rows(torch, dc, device, stream, flush, peak):
+    """FP16 / FP32 and tree-order all_reduce at full size, and the batched
+    all_reduce_many / reduce_scatter_many over the five per-rank sizes of the
+    all_reduce workload (P=8), each timed like the sweep."""
+    rows = []
+    P = W.CONFIG4_P
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+    for dt, order, shape in (("bf16", "tree", "16384x8192"), ("f16", "tree", "8627x8192"),
+                             ("f32", "linear", "8627x8192")):
+        n = W.CONFIG4_COUNTS[shape]
+        ins = [W.normal_device(W.seed_for(4, 9900), r, n, device, tdt[dt]) for r in range(P)]
+        outs = [torch.empty_like(x) for x in ins]
+        us = statistics.median(timed_calls(
+            torch, stream, flush, [lambda: dc.all_reduce(ins, outs, order=order)], 5)[0])
+        nbytes = 2 * P * n * ins[0].element_size()
+        rows.append({"op": f"all_reduce_{dt}_{order}", "P": P, "count": n, "shape": shape, "us": us,
+                     "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+        del ins, outs
+    counts = list(W.CONFIG4_COUNTS.values())
+    ins = [[W.normal_bf16_device(W.seed_for(4, 9910), r, n, device, tensor=t) for r in range(P)]
+           for t, n in enumerate(counts)]
+    outs = [[torch.empty_like(x) for x in t] for t in ins]
+    us = statistics.median(timed_calls(
+        torch, stream, flush, [lambda: dc.all_reduce_many(ins, outs)], 5)[0])
+    nbytes = 4 * P * sum(counts)
+    rows.append({"op": "all_reduce_many_bf16_linear", "P": P, "count": len(counts),
+                 "shape": "{" + ", ".join(W.CONFIG4_COUNTS) + "}", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    outs = [[torch.empty(n // P, dtype=torch.bfloat16, device=device) for _ in range(P)]
+            for n in counts]
+    us = statistics.median(timed_calls(
+        torch, stream, flush, [lambda: dc.reduce_scatter_many(ins, outs, order="tree")], 5)[0])
+    nbytes = 2 * P * sum(counts) + 2 * sum(counts)
+    rows.append({"op": "reduce_scatter_many_bf16_tree", "P": P, "count": len(counts),
+                 "shape": "{" + ", ".join(W.CONFIG4_COUNTS) + "}", "us": us,
                  "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     return rows
 

@@ -51,9 +51,15 @@ typedef enum {
     DC_ERR_TIMEOUT = 6   /* reserved for bounded device waits; no current kernel waits */
 } dc_status_t;
 
+/* Element types and summation orders of the reductions. */
+typedef enum { DC_BF16 = 0, DC_F16 = 1, DC_F32 = 2 } dc_dtype_t;
+typedef enum { DC_ORDER_LINEAR = 0, DC_ORDER_TREE = 1 } dc_order_t;
+
 #define DC_MAX_RANKS 64          /* P <= 64 */
 #define DC_MANY_MAX_TENSORS 256  /* all_gather_many: T <= 256 */
 #define DC_MANY_MAX_SEGMENTS 1024 /* all_gather_many: T * P <= 1024 */
+#define DC_MANY_MAX_REDUCE_JOBS 256  /* reductions: T (all_reduce) or T * P (reduce_scatter) <= 256 */
+#define DC_MANY_MAX_REDUCE_PTRS 1024 /* reductions: 2 * T * P <= 1024 */
 
 /*
  * dc_all_gather -- rank-ordered all-gather ([PR491] section "What",
@@ -125,6 +131,44 @@ dc_status_t dc_all_reduce_bf16(const void *const *in_ptrs, void *const *out_ptrs
  */
 dc_status_t dc_reduce_scatter_bf16(const void *const *in_ptrs, void *const *out_ptrs, int P,
                                    size_t count_per_shard, dc_stream_t stream);
+
+/*
+ * dc_all_reduce / dc_reduce_scatter -- the same operations for any element
+ * type and either summation order.  Every element is widened exactly to
+ * binary32, the P values of an element are added one binary32 add (round to
+ * nearest even) at a time in `order`, and the total is rounded once to
+ * `dtype` (round to nearest even; DC_F32 totals are stored as they are):
+ *   DC_ORDER_LINEAR: ((x0 + x1) + x2) + ... + x_{P-1};
+ *   DC_ORDER_TREE:   fold(x[lo..hi)) = fold(x[lo..lo+m)) + fold(x[lo+m..hi)),
+ *                    m the largest power of two below hi - lo.
+ * [PR491] names a fixed-tree backend ("cuda_ipc_fixed_tree", author's
+ * replies) without its shape; DC_ORDER_TREE is the plainest reading, and
+ * DC_ORDER_LINEAR the default of the BF16 entry points above.  Pointers must
+ * be aligned to the element size (2 or 4 bytes); aliasing rules as above.
+ */
+dc_status_t dc_all_reduce(const void *const *in_ptrs, void *const *out_ptrs, int P, size_t count,
+                          dc_dtype_t dtype, dc_order_t order, dc_stream_t stream);
+dc_status_t dc_reduce_scatter(const void *const *in_ptrs, void *const *out_ptrs, int P,
+                              size_t count_per_shard, dc_dtype_t dtype, dc_order_t order,
+                              dc_stream_t stream);
+
+/*
+ * dc_all_reduce_many / dc_reduce_scatter_many -- T independent reductions of
+ * the same P, type and order in one launch ([PR491] "Tests":
+ * reduce_scatter_many(..., outs=) with caller-given outputs).
+ * in_ptrs, out_ptrs: host arrays of T*P device pointers, tensor-major
+ *                    (tensor t, rank r at index t*P + r).
+ * counts / counts_per_shard: host array of T element counts (zero allowed).
+ * Limits: DC_MANY_MAX_REDUCE_JOBS jobs (T for all_reduce, T*P for
+ * reduce_scatter) and 2*T*P <= DC_MANY_MAX_REDUCE_PTRS (DC_ERR_TOO_MANY).
+ * Outputs may alias only their own tensor's inputs, as in the single forms.
+ */
+dc_status_t dc_all_reduce_many(const void *const *in_ptrs, void *const *out_ptrs,
+                               const size_t *counts, int T, int P, dc_dtype_t dtype,
+                               dc_order_t order, dc_stream_t stream);
+dc_status_t dc_reduce_scatter_many(const void *const *in_ptrs, void *const *out_ptrs,
+                                   const size_t *counts_per_shard, int T, int P, dc_dtype_t dtype,
+                                   dc_order_t order, dc_stream_t stream);
 
 /* Message describing the last failed call on this thread ("" if none). */
 const char *dc_last_error(void);

@@ -24,8 +24,8 @@ from typing import Sequence
 
 __all__ = [
     "DCError", "LibraryMissing", "all_gather", "all_gather_many", "all_reduce",
-    "reduce_scatter", "set_option", "get_option", "launch_count", "last_error",
-    "options", "lib", "LIB_PATH", "STATUS",
+    "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "set_option", "get_option",
+    "launch_count", "last_error", "options", "lib", "LIB_PATH", "STATUS", "DTYPES", "ORDERS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +37,11 @@ STATUS = {0: "DC_OK", 1: "DC_ERR_INVALID", 2: "DC_ERR_ALIGN", 3: "DC_ERR_OVERLAP
 MAX_RANKS = 64
 MANY_MAX_TENSORS = 256
 MANY_MAX_SEGMENTS = 1024
+MANY_MAX_REDUCE_JOBS = 256
+MANY_MAX_REDUCE_PTRS = 1024
+
+DTYPES = {"bf16": 0, "f16": 1, "f32": 2}      # dc_dtype_t
+ORDERS = {"linear": 0, "tree": 1}             # dc_order_t
 
 
 class LibraryMissing(RuntimeError):
@@ -72,8 +77,16 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_size_t, _VP]
         L.dc_reduce_scatter_bf16.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP),
                                              ctypes.c_int, ctypes.c_size_t, _VP]
+        L.dc_all_reduce.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP), ctypes.c_int,
+                                    ctypes.c_size_t, ctypes.c_int, ctypes.c_int, _VP]
+        L.dc_reduce_scatter.argtypes = L.dc_all_reduce.argtypes
+        L.dc_all_reduce_many.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP),
+                                         ctypes.POINTER(ctypes.c_size_t), ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, _VP]
+        L.dc_reduce_scatter_many.argtypes = L.dc_all_reduce_many.argtypes
         for f in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
-                  "dc_reduce_scatter_bf16"):
+                  "dc_reduce_scatter_bf16", "dc_all_reduce", "dc_reduce_scatter",
+                  "dc_all_reduce_many", "dc_reduce_scatter_many"):
             getattr(L, f).restype = ctypes.c_int
         L.dc_last_error.argtypes = []
         L.dc_last_error.restype = ctypes.c_char_p
@@ -125,6 +138,35 @@ def dc_reduce_scatter_bf16(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: i
                            count_per_shard: int, stream: int = 0) -> int:
     return lib().dc_reduce_scatter_bf16(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P,
                                         count_per_shard, stream)
+
+
+def dc_all_reduce(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int, count: int,
+                  dtype: int = 0, order: int = 0, stream: int = 0) -> int:
+    return lib().dc_all_reduce(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P, count, dtype, order,
+                               stream)
+
+
+def dc_reduce_scatter(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int,
+                      count_per_shard: int, dtype: int = 0, order: int = 0, stream: int = 0) -> int:
+    return lib().dc_reduce_scatter(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P, count_per_shard,
+                                   dtype, order, stream)
+
+
+def _sizes(xs: Sequence[int]):
+    return (ctypes.c_size_t * max(1, len(xs)))(*[int(x) for x in xs])
+
+
+def dc_all_reduce_many(in_ptrs: Sequence[int], out_ptrs: Sequence[int], counts: Sequence[int],
+                       T: int, P: int, dtype: int = 0, order: int = 0, stream: int = 0) -> int:
+    return lib().dc_all_reduce_many(_ptr_array(in_ptrs), _ptr_array(out_ptrs), _sizes(counts), T, P,
+                                    dtype, order, stream)
+
+
+def dc_reduce_scatter_many(in_ptrs: Sequence[int], out_ptrs: Sequence[int],
+                           counts_per_shard: Sequence[int], T: int, P: int, dtype: int = 0,
+                           order: int = 0, stream: int = 0) -> int:
+    return lib().dc_reduce_scatter_many(_ptr_array(in_ptrs), _ptr_array(out_ptrs),
+                                        _sizes(counts_per_shard), T, P, dtype, order, stream)
 
 
 # ---------------------------------------------------------- tensor API ---
@@ -199,37 +241,53 @@ def all_gather_many(peers_per_tensor: Sequence[Sequence], outs: Sequence, stream
     return outs
 
 
-def _bf16_tensors(ts: Sequence, what: str, count: int | None):
+def _dtype_code(t) -> int:
     import torch
 
+    codes = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+    if t.dtype not in codes:
+        raise ValueError(f"reductions take bfloat16, float16 or float32 tensors (got {t.dtype})")
+    return codes[t.dtype]
+
+
+def _reduce_tensors(ts: Sequence, what: str, count: int | None, dtype):
     for i, t in enumerate(ts):
         _device_tensor(t, f"{what}[{i}]")
-        if t.dtype != torch.bfloat16:
-            raise ValueError(f"{what}[{i}] must be torch.bfloat16 (got {t.dtype})")
+        if t.dtype != dtype:
+            raise ValueError(f"{what}[{i}] has dtype {t.dtype}, expected {dtype}")
         if count is not None and t.numel() != count:
             raise ValueError(f"{what}[{i}] has {t.numel()} elements, expected {count}")
 
 
-def all_reduce(inputs: Sequence, outputs: Sequence, stream=None):
-    """Deterministic BF16 all_reduce: every ``outputs[r]`` receives the sum of
-    ``inputs[0..P-1]``, folded in rank order in binary32 and rounded once to
-    BF16.  ``outputs[r]`` may be one of the inputs (in place).  Returns
-    outputs."""
+def _order_code(order: str) -> int:
+    if order not in ORDERS:
+        raise ValueError(f"order must be one of {sorted(ORDERS)} (got {order!r})")
+    return ORDERS[order]
+
+
+def all_reduce(inputs: Sequence, outputs: Sequence, order: str = "linear", stream=None):
+    """Deterministic all_reduce: every ``outputs[r]`` receives the sum of
+    ``inputs[0..P-1]`` (bfloat16, float16 or float32), each element widened to
+    binary32, added in a fixed order (``"linear"``: rank 0, 1, 2, ...;
+    ``"tree"``: pairs of neighbouring ranks, then pairs of pairs) and rounded
+    once to the element type.  ``outputs[r]`` may be one of the inputs (in
+    place).  Returns outputs."""
     P = len(inputs)
     if P == 0 or len(outputs) != P:
         raise ValueError("need P >= 1 inputs and P outputs")
     n = inputs[0].numel()
-    _bf16_tensors(inputs, "inputs", n)
-    _bf16_tensors(outputs, "outputs", n)
-    _check(dc_all_reduce_bf16([t.data_ptr() for t in inputs], [t.data_ptr() for t in outputs],
-                              P, n, _stream_handle(stream)))
+    dt = inputs[0].dtype
+    _reduce_tensors(inputs, "inputs", n, dt)
+    _reduce_tensors(outputs, "outputs", n, dt)
+    _check(dc_all_reduce([t.data_ptr() for t in inputs], [t.data_ptr() for t in outputs], P, n,
+                         _dtype_code(inputs[0]), _order_code(order), _stream_handle(stream)))
     return outputs
 
 
-def reduce_scatter(inputs: Sequence, outputs: Sequence, stream=None):
-    """Deterministic BF16 reduce_scatter (input = world x output): each input
-    holds P*C elements; ``outputs[r]`` (C elements) receives the rank-order
-    fold of shard r of every input.  Returns outputs."""
+def reduce_scatter(inputs: Sequence, outputs: Sequence, order: str = "linear", stream=None):
+    """Deterministic reduce_scatter (input = world x output): each input holds
+    P*C elements; ``outputs[r]`` (C elements) receives the fixed-order fold of
+    shard r of every input.  Returns outputs."""
     P = len(inputs)
     if P == 0 or len(outputs) != P:
         raise ValueError("need P >= 1 inputs and P outputs")
@@ -237,11 +295,58 @@ def reduce_scatter(inputs: Sequence, outputs: Sequence, stream=None):
     if n % P:
         raise ValueError(f"input length {n} is not divisible by P = {P}")
     C = n // P
-    _bf16_tensors(inputs, "inputs", n)
-    _bf16_tensors(outputs, "outputs", C)
-    _check(dc_reduce_scatter_bf16([t.data_ptr() for t in inputs], [t.data_ptr() for t in outputs],
-                                  P, C, _stream_handle(stream)))
+    dt = inputs[0].dtype
+    _reduce_tensors(inputs, "inputs", n, dt)
+    _reduce_tensors(outputs, "outputs", C, dt)
+    _check(dc_reduce_scatter([t.data_ptr() for t in inputs], [t.data_ptr() for t in outputs], P, C,
+                             _dtype_code(inputs[0]), _order_code(order), _stream_handle(stream)))
     return outputs
+
+
+def _many(inputs_per_tensor, outputs_per_tensor, scatter: bool):
+    T = len(inputs_per_tensor)
+    if len(outputs_per_tensor) != T:
+        raise ValueError("need one output list per tensor")
+    if T == 0:
+        return [], [], [], 0, 0
+    P = len(inputs_per_tensor[0])
+    dt = inputs_per_tensor[0][0].dtype
+    ins, outs, counts = [], [], []
+    for t, (it, ot) in enumerate(zip(inputs_per_tensor, outputs_per_tensor)):
+        if len(it) != P or len(ot) != P:
+            raise ValueError("every tensor needs P inputs and P outputs")
+        n = it[0].numel()
+        if scatter and n % P:
+            raise ValueError(f"tensor {t}: input length {n} is not divisible by P = {P}")
+        c = n // P if scatter else n
+        _reduce_tensors(it, f"inputs[{t}]", n, dt)
+        _reduce_tensors(ot, f"outputs[{t}]", c, dt)
+        ins.extend(x.data_ptr() for x in it)
+        outs.extend(x.data_ptr() for x in ot)
+        counts.append(c)
+    return ins, outs, counts, T, P
+
+
+def all_reduce_many(inputs_per_tensor: Sequence[Sequence], outputs_per_tensor: Sequence[Sequence],
+                    order: str = "linear", stream=None):
+    """T independent all_reduces (same P, element type and order) in one
+    launch.  Returns outputs_per_tensor."""
+    ins, outs, counts, T, P = _many(inputs_per_tensor, outputs_per_tensor, False)
+    if T:
+        _check(dc_all_reduce_many(ins, outs, counts, T, P, _dtype_code(inputs_per_tensor[0][0]),
+                                  _order_code(order), _stream_handle(stream)))
+    return outputs_per_tensor
+
+
+def reduce_scatter_many(inputs_per_tensor: Sequence[Sequence],
+                        outputs_per_tensor: Sequence[Sequence], order: str = "linear", stream=None):
+    """T independent reduce_scatters in one launch, into caller-given
+    outputs.  Returns outputs_per_tensor."""
+    ins, outs, counts, T, P = _many(inputs_per_tensor, outputs_per_tensor, True)
+    if T:
+        _check(dc_reduce_scatter_many(ins, outs, counts, T, P, _dtype_code(inputs_per_tensor[0][0]),
+                                      _order_code(order), _stream_handle(stream)))
+    return outputs_per_tensor
 
 
 # ------------------------------------------------------------- options ---

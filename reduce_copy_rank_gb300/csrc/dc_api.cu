@@ -21,6 +21,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "dc.h"
 #include "dc_internal.h"
@@ -101,7 +102,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 24;
+constexpr int kFamilies = 48;
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -233,38 +234,100 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
 }
 
 // --------------------------------------------------------------- reduce ---
-template <class Params>
-void set_reduce_job(Params& prm, int j, uint64_t in_off, uint64_t count, uint32_t out0,
-                    uint32_t nout, const uint64_t* in, const uint64_t* out_ptrs, int P,
-                    uint64_t* units) {
-  ReduceJob& J = prm.job[j];
-  J.in_off = in_off;
-  J.count = count;
-  J.out0 = out0;
-  J.nout = nout;
-  const uint32_t o = static_cast<uint32_t>((in[0] + 2 * in_off) & 15u);
-  bool vec = true;
-  for (int q = 0; q < P; ++q) vec = vec && ((in[q] + 2 * in_off) & 15u) == o;
-  for (uint32_t m = 0; m < nout; ++m) vec = vec && (out_ptrs[out0 + m] & 15u) == o;
-  if (vec) {
-    uint64_t head = ((16u - o) & 15u) / 2;
-    if (head > count) head = count;
-    const uint64_t rest = count - head;
-    J.head = static_cast<uint32_t>(head);
-    J.flags = kJobVec;
-    J.nunits = (head ? 1 : 0) + rest / 8 + ((rest & 7u) ? 1 : 0);
-  } else {
-    J.head = 0;
-    J.flags = 0;
-    J.nunits = count;
+int esize_of(int dtype) { return dtype == kF32 ? 4 : 2; }
+int epv_of(int dtype) { return dtype == kF32 ? 4 : 8; }  // elements per 16-byte vector
+
+const char* dtype_name(int dtype) {
+  return dtype == kF16 ? "FP16" : dtype == kF32 ? "FP32" : "BF16";
+}
+
+// A byte range of one tensor's input or output of rank `rank`.
+struct Range {
+  uint64_t lo, hi;
+  int tensor, rank;
+  bool out;
+};
+
+// Reject any overlap between an output and another output, and between an
+// output and an input unless it is the exact in-place alias of that output:
+// all_reduce out_r == in_q (same tensor); reduce_scatter out_r == in_q +
+// r * shard bytes (same tensor).  Inputs may overlap inputs.
+dc_status_t check_reduce_overlaps(std::vector<Range>& v, bool scatter, const uint64_t* shard_bytes) {
+  std::sort(v.begin(), v.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+  for (size_t i = 0; i < v.size(); ++i) {
+    for (size_t k = i + 1; k < v.size() && v[k].lo < v[i].hi; ++k) {
+      const Range& a = v[i];
+      const Range& b = v[k];
+      if (!a.out && !b.out) continue;
+      if (a.out && b.out)
+        return fail(DC_ERR_OVERLAP, "outputs of tensor %d rank %d and tensor %d rank %d overlap",
+                    a.tensor, a.rank, b.tensor, b.rank);
+      const Range& o = a.out ? a : b;
+      const Range& in = a.out ? b : a;
+      const uint64_t alias = in.lo + (scatter ? static_cast<uint64_t>(o.rank) * shard_bytes[o.tensor] : 0);
+      if (o.tensor == in.tensor && o.lo == alias) continue;  // exact in-place alias
+      return fail(DC_ERR_OVERLAP,
+                  "output of tensor %d rank %d overlaps input %d of tensor %d without being %s",
+                  o.tensor, o.rank, in.rank, in.tensor,
+                  scatter ? "its own shard of it" : "the same buffer");
+    }
   }
-  J.ufirst = *units;
-  *units += J.nunits;
+  return DC_OK;
 }
 
 template <class Params>
-dc_status_t launch_reduce_plan(Params& prm, int family, uint64_t in_bytes_per_rank,
-                               cudaStream_t stream, const char* what) {
+void fill_reduce(Params& prm, int P, int dtype, bool scatter, const std::vector<int>& live,
+                 const void* const* in_ptrs, void* const* out_ptrs, const size_t* counts) {
+  const int nz = static_cast<int>(live.size());
+  const int es = esize_of(dtype), epv = epv_of(dtype);
+  prm.P = P;
+  for (int k = 0; k < nz; ++k) {
+    const int t = live[k];
+    for (int q = 0; q < P; ++q) {
+      prm.ptr[k * P + q] = reinterpret_cast<uint64_t>(in_ptrs[static_cast<size_t>(t) * P + q]);
+      prm.ptr[nz * P + k * P + q] = reinterpret_cast<uint64_t>(out_ptrs[static_cast<size_t>(t) * P + q]);
+    }
+  }
+  uint64_t units = 0;
+  int nj = 0;
+  for (int k = 0; k < nz; ++k) {
+    const uint64_t n = counts[live[k]];
+    const int nparts = scatter ? P : 1;
+    for (int r = 0; r < nparts; ++r) {
+      ReduceJob& J = prm.job[nj++];
+      J.in0 = static_cast<uint16_t>(k * P);
+      J.out0 = static_cast<uint16_t>(nz * P + k * P + (scatter ? r : 0));
+      J.nout = static_cast<uint16_t>(scatter ? 1 : P);
+      J.in_off = scatter ? static_cast<uint64_t>(r) * n : 0;
+      J.count = n;
+      const uint64_t off = J.in_off * es;
+      const uint32_t o = static_cast<uint32_t>((prm.ptr[J.in0] + off) & 15u);
+      bool vec = true;
+      for (int q = 0; q < P; ++q) vec = vec && ((prm.ptr[J.in0 + q] + off) & 15u) == o;
+      for (int m = 0; m < J.nout; ++m) vec = vec && (prm.ptr[J.out0 + m] & 15u) == o;
+      if (vec) {
+        uint64_t head = ((16u - o) & 15u) / es;
+        if (head > n) head = n;
+        const uint64_t rest = n - head;
+        J.head = static_cast<uint8_t>(head);
+        J.flags = kJobVec;
+        J.nunits = (head ? 1 : 0) + rest / epv + ((rest % epv) ? 1 : 0);
+      } else {
+        J.head = 0;
+        J.flags = 0;
+        J.nunits = n;
+      }
+      J.ufirst = units;
+      units += J.nunits;
+    }
+  }
+  prm.njobs = nj;
+  prm.total_units = units;
+}
+
+template <class Params>
+dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
+                               uint64_t in_bytes_per_rank, cudaStream_t stream, const char* what) {
   if (g_opt.test_fail_launch.load())
     return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
   int dev = 0, sms = 0;
@@ -276,26 +339,82 @@ dc_status_t launch_reduce_plan(Params& prm, int family, uint64_t in_bytes_per_ra
   int grid = 1;
   if (!single) {
     const int P = prm.P;
-    const bool scatter = family >= 20;
-    const int occ = occupancy(dev, family, [P, scatter] { return reduce_ctas_per_sm(P, scatter); });
+    const int fam = 12 + (((dtype * 3 + variant) * 2 + order) * 2 + (P == 8 ? 1 : 0));
+    const int occ = occupancy(dev, fam, [dtype, variant, order, P] {
+      return reduce_ctas_per_sm(dtype, variant, order, P);
+    });
     const uint64_t tile = static_cast<uint64_t>(kReduceBlock) * kReduceUnroll;
     grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
   }
-  return check_launch(launch_reduce(prm, grid, single, g_opt.pdl.load() != 0, stream), what);
+  return check_launch(launch_reduce(prm, dtype, order, grid, single, g_opt.pdl.load() != 0, stream),
+                      what);
 }
 
-int reduce_family(int P, bool scatter) {  // occupancy cache slots 16..23 (gather uses 0..11)
-  const int pt = P == 8 ? 0 : P == 4 ? 1 : P == 2 ? 2 : 3;
-  return (scatter ? 20 : 16) + pt;
-}
-
-dc_status_t check_bf16_ptrs(const void* const* ptrs, int P, const char* name) {
-  for (int r = 0; r < P; ++r) {
-    if (!ptrs[r]) return fail(DC_ERR_INVALID, "%s[%d] is NULL", name, r);
-    if (reinterpret_cast<uint64_t>(ptrs[r]) & 1u)
-      return fail(DC_ERR_ALIGN, "%s[%d] = %p is not 2-byte aligned (BF16)", name, r, ptrs[r]);
+// Every reduction entry point: T tensors of P ranks; counts[t] is the
+// element count per rank (all_reduce) or per shard (reduce_scatter).
+dc_status_t reduce_entry(const void* const* in_ptrs, void* const* out_ptrs, const size_t* counts,
+                         int T, int P, int dtype, int order, bool scatter, cudaStream_t stream,
+                         const char* what) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (dtype < kBF16 || dtype > kF32) return fail(DC_ERR_INVALID, "unknown element type %d", dtype);
+  if (order != kOrderLinear && order != kOrderTree)
+    return fail(DC_ERR_INVALID, "unknown summation order %d", order);
+  if (T < 0) return fail(DC_ERR_INVALID, "T = %d is negative", T);
+  const long long jobs = static_cast<long long>(T) * (scatter ? P : 1);
+  if (jobs > kManyMaxReduceJobs || 2LL * T * P > kManyMaxReducePtrs)
+    return fail(DC_ERR_TOO_MANY, "%d tensors x %d ranks exceed the %d jobs / %d pointers of one launch",
+                T, P, kManyMaxReduceJobs, kManyMaxReducePtrs);
+  if (T > 0 && !counts) return fail(DC_ERR_INVALID, "counts is NULL");
+  std::vector<int> live;
+  for (int t = 0; t < T; ++t)
+    if (counts[t]) live.push_back(t);
+  if (live.empty()) return ok();
+  if (!in_ptrs || !out_ptrs) return fail(DC_ERR_INVALID, "in_ptrs and out_ptrs must not be NULL");
+  const uint64_t es = static_cast<uint64_t>(esize_of(dtype));
+  std::vector<Range> ranges;
+  std::vector<uint64_t> shard_bytes(T, 0);
+  uint64_t in_bytes_per_rank = 0;
+  for (int t : live) {
+    const uint64_t n = counts[t];
+    if (n > UINT64_MAX / es / static_cast<uint64_t>(P))
+      return fail(DC_ERR_INVALID, "count of tensor %d overflows", t);
+    const uint64_t out_b = n * es, in_b = out_b * (scatter ? static_cast<uint64_t>(P) : 1);
+    shard_bytes[t] = out_b;
+    in_bytes_per_rank += in_b;
+    for (int q = 0; q < P; ++q) {
+      const void* pin = in_ptrs[static_cast<size_t>(t) * P + q];
+      const void* pout = out_ptrs[static_cast<size_t>(t) * P + q];
+      if (!pin || !pout)
+        return fail(DC_ERR_INVALID, "pointer of tensor %d rank %d is NULL", t, q);
+      const uint64_t i = reinterpret_cast<uint64_t>(pin), o = reinterpret_cast<uint64_t>(pout);
+      if ((i | o) & (es - 1))
+        return fail(DC_ERR_ALIGN, "tensor %d rank %d: %s pointers must be %d-byte aligned", t, q,
+                    dtype_name(dtype), static_cast<int>(es));
+      if (i + in_b < i || o + out_b < o)
+        return fail(DC_ERR_INVALID, "buffer of tensor %d rank %d wraps around", t, q);
+      ranges.push_back(Range{i, i + in_b, t, q, false});
+      ranges.push_back(Range{o, o + out_b, t, q, true});
+    }
   }
-  return DC_OK;
+  dc_status_t st = check_reduce_overlaps(ranges, scatter, shard_bytes.data());
+  if (st != DC_OK) return st;
+  const int nz = static_cast<int>(live.size());
+  const int njobs = nz * (scatter ? P : 1), nptr = 2 * nz * P;
+  if (njobs == 1 && nptr <= 2 * kMaxRanks) {
+    ReduceParams1 prm{};
+    fill_reduce(prm, P, dtype, scatter, live, in_ptrs, out_ptrs, counts);
+    return launch_reduce_plan(prm, 0, dtype, order, in_bytes_per_rank, stream, what);
+  }
+  if (njobs <= kMaxRanks && nptr <= 4 * kMaxRanks) {
+    ReduceParamsS prm{};
+    fill_reduce(prm, P, dtype, scatter, live, in_ptrs, out_ptrs, counts);
+    return launch_reduce_plan(prm, 1, dtype, order, in_bytes_per_rank, stream, what);
+  }
+  static thread_local ReduceParamsL prm;  // 18 KB: keep it off the stack
+  std::memset(&prm, 0, sizeof prm);
+  fill_reduce(prm, P, dtype, scatter, live, in_ptrs, out_ptrs, counts);
+  return launch_reduce_plan(prm, 2, dtype, order, in_bytes_per_rank, stream, what);
 }
 
 }  // namespace
@@ -395,92 +514,44 @@ dc_status_t dc_all_gather_many(const void* const* peer_ptrs, const size_t* bytes
 
 dc_status_t dc_all_reduce_bf16(const void* const* in_ptrs, void* const* out_ptrs, int P,
                                size_t count, dc_stream_t stream) {
-  read_env_once();
-  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
-  if (count == 0) return ok();
-  if (!in_ptrs || !out_ptrs) return fail(DC_ERR_INVALID, "in_ptrs and out_ptrs must not be NULL");
-  if (count > UINT64_MAX / 2) return fail(DC_ERR_INVALID, "count overflows");
-  dc_status_t st = check_bf16_ptrs(in_ptrs, P, "in_ptrs");
-  if (st != DC_OK) return st;
-  st = check_bf16_ptrs(const_cast<const void* const*>(out_ptrs), P, "out_ptrs");
-  if (st != DC_OK) return st;
-  const uint64_t nb = 2 * static_cast<uint64_t>(count);
-  uint64_t in[kMaxRanks], out[kMaxRanks];
-  for (int r = 0; r < P; ++r) {
-    in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
-    out[r] = reinterpret_cast<uint64_t>(out_ptrs[r]);
-    if (in[r] + nb < in[r] || out[r] + nb < out[r])
-      return fail(DC_ERR_INVALID, "buffer of rank %d wraps around", r);
-  }
-  for (int r = 0; r < P; ++r) {
-    for (int u = r + 1; u < P; ++u)
-      if (overlaps(out[r], nb, out[u], nb))
-        return fail(DC_ERR_OVERLAP, "outputs of ranks %d and %d overlap", r, u);
-    for (int q = 0; q < P; ++q)
-      if (out[r] != in[q] && overlaps(out[r], nb, in[q], nb))
-        return fail(DC_ERR_OVERLAP,
-                    "output of rank %d overlaps input %d without being the same buffer", r, q);
-  }
-  ReduceParams1 prm{};
-  prm.P = P;
-  prm.njobs = 1;
-  for (int r = 0; r < P; ++r) {
-    prm.in[r] = in[r];
-    prm.out[r] = out[r];
-  }
-  uint64_t units = 0;
-  set_reduce_job(prm, 0, 0, count, 0, static_cast<uint32_t>(P), in, out, P, &units);
-  prm.total_units = units;
-  return launch_reduce_plan(prm, reduce_family(P, false), nb, static_cast<cudaStream_t>(stream),
-                            "all_reduce");
+  return reduce_entry(in_ptrs, out_ptrs, &count, 1, P, kBF16, kOrderLinear, false,
+                      static_cast<cudaStream_t>(stream), "all_reduce");
 }
 
 dc_status_t dc_reduce_scatter_bf16(const void* const* in_ptrs, void* const* out_ptrs, int P,
                                    size_t count_per_shard, dc_stream_t stream) {
-  read_env_once();
-  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
-  if (count_per_shard == 0) return ok();
-  if (!in_ptrs || !out_ptrs) return fail(DC_ERR_INVALID, "in_ptrs and out_ptrs must not be NULL");
-  const uint64_t C = count_per_shard;
-  if (C > UINT64_MAX / 2 / static_cast<uint64_t>(P))
-    return fail(DC_ERR_INVALID, "P * count_per_shard overflows");
-  dc_status_t st = check_bf16_ptrs(in_ptrs, P, "in_ptrs");
-  if (st != DC_OK) return st;
-  st = check_bf16_ptrs(const_cast<const void* const*>(out_ptrs), P, "out_ptrs");
-  if (st != DC_OK) return st;
-  const uint64_t nb_out = 2 * C, nb_in = nb_out * static_cast<uint64_t>(P);
-  uint64_t in[kMaxRanks], out[kMaxRanks];
-  for (int r = 0; r < P; ++r) {
-    in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
-    out[r] = reinterpret_cast<uint64_t>(out_ptrs[r]);
-    if (in[r] + nb_in < in[r] || out[r] + nb_out < out[r])
-      return fail(DC_ERR_INVALID, "buffer of rank %d wraps around", r);
-  }
-  for (int r = 0; r < P; ++r) {
-    for (int u = r + 1; u < P; ++u)
-      if (overlaps(out[r], nb_out, out[u], nb_out))
-        return fail(DC_ERR_OVERLAP, "outputs of ranks %d and %d overlap", r, u);
-    for (int q = 0; q < P; ++q) {
-      if (out[r] == in[q] + static_cast<uint64_t>(r) * nb_out) continue;  // in place: shard r
-      if (overlaps(out[r], nb_out, in[q], nb_in))
-        return fail(DC_ERR_OVERLAP,
-                    "output of rank %d overlaps input %d outside that input's shard %d", r, q, r);
-    }
-  }
-  ReduceParamsP prm{};
-  prm.P = P;
-  prm.njobs = P;
-  for (int r = 0; r < P; ++r) {
-    prm.in[r] = in[r];
-    prm.out[r] = out[r];
-  }
-  uint64_t units = 0;
-  for (int r = 0; r < P; ++r)
-    set_reduce_job(prm, r, static_cast<uint64_t>(r) * C, C, static_cast<uint32_t>(r), 1, in, out, P,
-                   &units);
-  prm.total_units = units;
-  return launch_reduce_plan(prm, reduce_family(P, true), nb_in, static_cast<cudaStream_t>(stream),
-                            "reduce_scatter");
+  return reduce_entry(in_ptrs, out_ptrs, &count_per_shard, 1, P, kBF16, kOrderLinear, true,
+                      static_cast<cudaStream_t>(stream), "reduce_scatter");
+}
+
+dc_status_t dc_all_reduce(const void* const* in_ptrs, void* const* out_ptrs, int P, size_t count,
+                          dc_dtype_t dtype, dc_order_t order, dc_stream_t stream) {
+  return reduce_entry(in_ptrs, out_ptrs, &count, 1, P, static_cast<int>(dtype),
+                      static_cast<int>(order), false, static_cast<cudaStream_t>(stream), "all_reduce");
+}
+
+dc_status_t dc_reduce_scatter(const void* const* in_ptrs, void* const* out_ptrs, int P,
+                              size_t count_per_shard, dc_dtype_t dtype, dc_order_t order,
+                              dc_stream_t stream) {
+  return reduce_entry(in_ptrs, out_ptrs, &count_per_shard, 1, P, static_cast<int>(dtype),
+                      static_cast<int>(order), true, static_cast<cudaStream_t>(stream),
+                      "reduce_scatter");
+}
+
+dc_status_t dc_all_reduce_many(const void* const* in_ptrs, void* const* out_ptrs,
+                               const size_t* counts, int T, int P, dc_dtype_t dtype,
+                               dc_order_t order, dc_stream_t stream) {
+  return reduce_entry(in_ptrs, out_ptrs, counts, T, P, static_cast<int>(dtype),
+                      static_cast<int>(order), false, static_cast<cudaStream_t>(stream),
+                      "all_reduce_many");
+}
+
+dc_status_t dc_reduce_scatter_many(const void* const* in_ptrs, void* const* out_ptrs,
+                                   const size_t* counts_per_shard, int T, int P, dc_dtype_t dtype,
+                                   dc_order_t order, dc_stream_t stream) {
+  return reduce_entry(in_ptrs, out_ptrs, counts_per_shard, T, P, static_cast<int>(dtype),
+                      static_cast<int>(order), true, static_cast<cudaStream_t>(stream),
+                      "reduce_scatter_many");
 }
 
 const char* dc_last_error(void) { return g_err; }

@@ -112,6 +112,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return r;
 }
 
+// binary16 <-> binary32 (cvt: the widening is exact; the narrowing rounds to
+// nearest even and keeps binary16 subnormals).
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+  float r;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(h));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));

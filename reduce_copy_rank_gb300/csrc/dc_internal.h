@@ -73,38 +73,47 @@ using GatherParamsS = GatherParams<kManySmallTensors, kManySmallSegments>;
 using GatherParamsL = GatherParams<kManyMaxTensors, kManyMaxSegments>;
 
 // ---------------------------------------------------------- reduction ---
+enum : int { kBF16 = 0, kF16 = 1, kF32 = 2 };              // element types
+enum : int { kOrderLinear = 0, kOrderTree = 1 };           // summation orders
 enum : uint32_t {
   kJobVec = 1u,    // every pointer of the job has the same address mod 16
 };
 
-// One fixed-order reduction over `count` elements: element i reads
-// in[q][in_off + i] for q = 0..P-1 and writes out[out0 + m][i] for
-// m = 0..nout-1.  Work units: an optional scalar head (elements before the
-// first 16-byte boundary), 8-element groups, and an optional scalar tail;
-// for a job without kJobVec every unit is one element.
+// Batched reductions: at most kManyMaxReduceJobs jobs and kManyMaxReducePtrs
+// pointers (inputs and outputs) per launch.
+constexpr int kManyMaxReduceJobs = 256;
+constexpr int kManyMaxReducePtrs = 1024;
+
+// One fixed-order reduction over `count` elements of one tensor: element i
+// reads input q at element in_off + i (input q's pointer is ptr[in0 + q],
+// q < P) and writes output m at element i (pointer ptr[out0 + m],
+// m < nout).  Work units: an optional scalar head (elements before the first
+// 16-byte boundary), 16-byte vectors, and an optional scalar tail; for a job
+// without kJobVec every unit is one element.
 struct ReduceJob {
   uint64_t in_off;
   uint64_t count;
   uint64_t ufirst;
   uint64_t nunits;
-  uint32_t out0;
-  uint32_t nout;
-  uint32_t head;
-  uint32_t flags;
+  uint16_t in0;
+  uint16_t out0;
+  uint16_t nout;
+  uint8_t head;
+  uint8_t flags;
 };
 
-template <int MAXJ>
+template <int MAXJ, int MAXPTR>
 struct ReduceParams {
   uint64_t total_units;
   int32_t njobs;
   int32_t P;
-  uint64_t in[kMaxRanks];
-  uint64_t out[kMaxRanks];
+  uint64_t ptr[MAXPTR];
   ReduceJob job[MAXJ];
 };
 
-using ReduceParams1 = ReduceParams<1>;          // all_reduce
-using ReduceParamsP = ReduceParams<kMaxRanks>;  // reduce_scatter: one job per rank
+using ReduceParams1 = ReduceParams<1, 2 * kMaxRanks>;                        // one all_reduce
+using ReduceParamsS = ReduceParams<kMaxRanks, 4 * kMaxRanks>;                // reduce_scatter, small batches
+using ReduceParamsL = ReduceParams<kManyMaxReduceJobs, kManyMaxReducePtrs>;  // large batches
 
 // ------------------------------------------------- launch entry points ---
 // Each returns the error of the launch itself.  pdl: launch with
@@ -113,8 +122,37 @@ using ReduceParamsP = ReduceParams<kMaxRanks>;  // reduce_scatter: one job per r
 cudaError_t launch_gather(const GatherParams1& p, int grid, bool single, bool pdl, cudaStream_t s);
 cudaError_t launch_gather(const GatherParamsS& p, int grid, bool single, bool pdl, cudaStream_t s);
 cudaError_t launch_gather(const GatherParamsL& p, int grid, bool single, bool pdl, cudaStream_t s);
-cudaError_t launch_reduce(const ReduceParams1& p, int grid, bool single, bool pdl, cudaStream_t s);
-cudaError_t launch_reduce(const ReduceParamsP& p, int grid, bool single, bool pdl, cudaStream_t s);
+#define DC_DECLARE_REDUCE(NAME)                                                                  \
+  cudaError_t launch_reduce_##NAME(const ReduceParams1& p, int order, int grid, bool single,     \
+                                   bool pdl, cudaStream_t s);                                    \
+  cudaError_t launch_reduce_##NAME(const ReduceParamsS& p, int order, int grid, bool single,     \
+                                   bool pdl, cudaStream_t s);                                    \
+  cudaError_t launch_reduce_##NAME(const ReduceParamsL& p, int order, int grid, bool single,     \
+                                   bool pdl, cudaStream_t s);                                    \
+  int reduce_ctas_per_sm_##NAME(int variant, int order, int P);
+DC_DECLARE_REDUCE(bf16)
+DC_DECLARE_REDUCE(f16)
+DC_DECLARE_REDUCE(f32)
+#undef DC_DECLARE_REDUCE
+
+template <class Params>
+cudaError_t launch_reduce(const Params& p, int dtype, int order, int grid, bool single, bool pdl,
+                          cudaStream_t s) {
+  switch (dtype) {
+    case kF16: return launch_reduce_f16(p, order, grid, single, pdl, s);
+    case kF32: return launch_reduce_f32(p, order, grid, single, pdl, s);
+    default: return launch_reduce_bf16(p, order, grid, single, pdl, s);
+  }
+}
+
+// variant: 0 ReduceParams1, 1 ReduceParamsS, 2 ReduceParamsL.
+inline int reduce_ctas_per_sm(int dtype, int variant, int order, int P) {
+  switch (dtype) {
+    case kF16: return reduce_ctas_per_sm_f16(variant, order, P);
+    case kF32: return reduce_ctas_per_sm_f32(variant, order, P);
+    default: return reduce_ctas_per_sm_bf16(variant, order, P);
+  }
+}
 
 // cudaLaunchKernelEx with an optional programmatic-serialization attribute.
 template <typename Kernel, typename Params>
@@ -140,6 +178,5 @@ int gather_ctas_per_sm(int which, int mode);  // which: 0 one job, 1 small many,
 int gather_mode_of(const GatherParams1& p);
 int gather_mode_of(const GatherParamsS& p);
 int gather_mode_of(const GatherParamsL& p);
-int reduce_ctas_per_sm(int P, bool scatter);
 
 }  // namespace dc

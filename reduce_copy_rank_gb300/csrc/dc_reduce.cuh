@@ -1,0 +1,395 @@
+// dc_reduce.cuh -- the deterministic fixed-order reductions (all_reduce,
+// reduce_scatter and their batched forms) for BF16, FP16 and FP32, in the
+// linear or the tree summation order.  Included by one .cu file per element
+// type, which instantiates the kernels for that type.
+//
+// "perf(cuda): vectorize the deterministic all-gather copy and right-size its
+// single-block path" (RL-Kernel PR 491) names the deterministic all_reduce
+// and reduce_scatter (sections "What" and "Not in this PR": their single-block
+// paths grow linearly with size), their batched form (reduce_scatter_many,
+// whose outs= argument upstream rejected), the reduce_scatter shape (author's
+// reply: input = world x output) and a backend called "cuda_ipc_fixed_tree".
+// The page never prints the arithmetic.  The reading implemented here: every
+// element of every rank is widened exactly to binary32; the P values of one
+// element are added in a fixed order, one binary32 add (round to nearest
+// even) at a time:
+//   linear: ((x0 + x1) + x2) + ... + x_{P-1};
+//   tree:   fold(x[lo..hi)) = fold(x[lo..lo+m)) + fold(x[lo+m..hi)), m the
+//           largest power of two below hi - lo (pairs of neighbouring ranks,
+//           then pairs of pairs; a trailing odd group is added last);
+// and the binary32 total is rounded once to the element type (round to
+// nearest even; FP32 totals are stored as they are).  No reassociation and no
+// cross-thread combine: each thread folds its own elements, so the bits do
+// not depend on grid, block or vector width.  Subnormals are kept.
+//
+// Work: a job is one contiguous element range of one tensor with one input
+// offset (all_reduce: one job per tensor, writing P outputs; reduce_scatter:
+// one job per tensor and rank r, reading elements [r*C, (r+1)*C) of the
+// tensor's inputs and writing output r).  When every pointer of a job has the
+// same address mod 16, the job is a scalar head up to the first 16-byte
+// boundary, a body of 16-byte vectors (one load per rank, one store per
+// output) and a scalar tail; otherwise it is folded element by element.
+// Units are taken in tiles round robin by the CTAs.
+#pragma once
+
+#include "dc_device.cuh"
+#include "dc_internal.h"
+
+namespace dc {
+namespace red {
+
+// ------------------------------------------------------- element types ---
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<kBF16> {
+  static constexpr int kSize = 2, kPerVec = 8;
+  using Raw = uint16_t;
+  __device__ static __forceinline__ float widen1(Raw h) { return __uint_as_float(uint32_t{h} << 16); }
+  __device__ static __forceinline__ Raw narrow1(float x) { return f32_to_bf16_rn(x); }
+  __device__ static __forceinline__ void widen(const uint4& v, float (&a)[kPerVec]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a[2 * i] = bf16lo_to_f32(w[i]);
+      a[2 * i + 1] = bf16hi_to_f32(w[i]);
+    }
+  }
+  __device__ static __forceinline__ uint4 narrow(const float (&a)[kPerVec]) {
+    return make_uint4(pack_bf16x2_rn(a[0], a[1]), pack_bf16x2_rn(a[2], a[3]),
+                      pack_bf16x2_rn(a[4], a[5]), pack_bf16x2_rn(a[6], a[7]));
+  }
+};
+
+template <>
+struct Elem<kF16> {
+  static constexpr int kSize = 2, kPerVec = 8;
+  using Raw = uint16_t;
+  __device__ static __forceinline__ float widen1(Raw h) { return f16_to_f32(h); }
+  __device__ static __forceinline__ Raw narrow1(float x) { return f32_to_f16_rn(x); }
+  __device__ static __forceinline__ void widen(const uint4& v, float (&a)[kPerVec]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a[2 * i] = f16_to_f32(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      a[2 * i + 1] = f16_to_f32(static_cast<uint16_t>(w[i] >> 16));
+    }
+  }
+  __device__ static __forceinline__ uint4 narrow(const float (&a)[kPerVec]) {
+    return make_uint4(pack_f16x2_rn(a[0], a[1]), pack_f16x2_rn(a[2], a[3]),
+                      pack_f16x2_rn(a[4], a[5]), pack_f16x2_rn(a[6], a[7]));
+  }
+};
+
+template <>
+struct Elem<kF32> {
+  static constexpr int kSize = 4, kPerVec = 4;
+  using Raw = uint32_t;
+  __device__ static __forceinline__ float widen1(Raw u) { return __uint_as_float(u); }
+  __device__ static __forceinline__ Raw narrow1(float x) { return __float_as_uint(x); }
+  __device__ static __forceinline__ void widen(const uint4& v, float (&a)[kPerVec]) {
+    a[0] = __uint_as_float(v.x);
+    a[1] = __uint_as_float(v.y);
+    a[2] = __uint_as_float(v.z);
+    a[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint4 narrow(const float (&a)[kPerVec]) {
+    return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                      __float_as_uint(a[3]));
+  }
+};
+
+// -------------------------------------------------------------- folds ---
+template <int E>
+__device__ __forceinline__ void add_into(float (&acc)[E], const float (&x)[E]) {  // acc = acc + x
+#pragma unroll
+  for (int i = 0; i < E; ++i) acc[i] = __fadd_rn(acc[i], x[i]);
+}
+
+template <int E>
+__device__ __forceinline__ void add_left(const float (&left)[E], float (&acc)[E]) {  // acc = left + acc
+#pragma unroll
+  for (int i = 0; i < E; ++i) acc[i] = __fadd_rn(left[i], acc[i]);
+}
+
+// Tree fold with a stack of partial sums: rank q enters as a leaf of level 0;
+// while the top of the stack has the same level, the two merge (older on the
+// left) into one of the next level; at the end the stack is folded from the
+// top down, each entry added on the left.  This builds exactly
+// fold(lo..hi) = fold(lo..lo+m) + fold(lo+m..hi) with m the largest power of
+// two below hi - lo.
+template <int E>
+struct TreeStack {
+  static constexpr int kDepth = 7;  // P <= 64
+  float s[kDepth][E];
+  int level[kDepth];
+  int n = 0;
+  __device__ __forceinline__ void push(float (&x)[E]) {
+    int l = 0;
+    while (n > 0 && level[n - 1] == l) {
+      add_left(s[n - 1], x);  // x = s[top] + x
+      --n;
+      ++l;
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) s[n][i] = x[i];
+    level[n] = l;
+    ++n;
+  }
+  __device__ __forceinline__ void finish(float (&acc)[E]) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] = s[n - 1][i];
+    for (int k = n - 2; k >= 0; --k) add_left(s[k], acc);
+  }
+};
+
+// ------------------------------------------------------------- params ---
+template <int MAXJ, int MAXPTR>
+__device__ __forceinline__ const uint8_t* in_ptr(const ReduceParams<MAXJ, MAXPTR>& p,
+                                                 const ReduceJob& J, int q) {
+  return reinterpret_cast<const uint8_t*>(p.ptr[J.in0 + q]);
+}
+template <int MAXJ, int MAXPTR>
+__device__ __forceinline__ uint8_t* out_ptr(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J,
+                                            int m) {
+  return reinterpret_cast<uint8_t*>(p.ptr[J.out0 + m]);
+}
+
+// Elements [e0, e1) (step `step`) of job J, one at a time.
+template <int DT, int ORDER, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void fold_scalar(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J,
+                                            uint64_t e0, uint64_t e1, uint64_t step) {
+  using T = Elem<DT>;
+  using Raw = typename T::Raw;
+  for (uint64_t i = e0; i < e1; i += step) {
+    const uint64_t off = (J.in_off + i) * T::kSize;
+    float acc[1];
+    if (ORDER == kOrderTree) {
+      TreeStack<1> st;
+      for (int q = 0; q < p.P; ++q) {
+        float x[1] = {T::widen1(*reinterpret_cast<const Raw*>(in_ptr(p, J, q) + off))};
+        st.push(x);
+      }
+      st.finish(acc);
+    } else {
+      acc[0] = T::widen1(*reinterpret_cast<const Raw*>(in_ptr(p, J, 0) + off));
+      for (int q = 1; q < p.P; ++q)
+        acc[0] = __fadd_rn(acc[0], T::widen1(*reinterpret_cast<const Raw*>(in_ptr(p, J, q) + off)));
+    }
+    const Raw y = T::narrow1(acc[0]);
+    for (uint32_t m = 0; m < J.nout; ++m)
+      *reinterpret_cast<Raw*>(out_ptr(p, J, m) + i * T::kSize) = y;
+  }
+}
+
+// The fold of one 16-byte vector of every rank at byte offset `off` of each
+// input.  PT > 0: P = PT known at compile time, all loads issued first by the
+// caller (`v`).  PT == 0: ranks in batches of 8 loads.
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void fold_vector(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J,
+                                            uint64_t off, const uint4 (&v)[PT > 0 ? PT : 1],
+                                            float (&acc)[Elem<DT>::kPerVec]) {
+  using T = Elem<DT>;
+  constexpr int E = T::kPerVec;
+  if constexpr (PT > 0) {
+    float x[PT][E];
+#pragma unroll
+    for (int q = 0; q < PT; ++q) T::widen(v[q], x[q]);
+    if constexpr (ORDER == kOrderTree) {
+      // levels of a complete binary tree over PT = 2^k leaves, left + right
+#pragma unroll
+      for (int width = 1; width < PT; width *= 2)
+#pragma unroll
+        for (int q = 0; q + width < PT; q += 2 * width) add_into(x[q], x[q + width]);
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[i] = x[0][i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[i] = x[0][i];
+#pragma unroll
+      for (int q = 1; q < PT; ++q) add_into(acc, x[q]);
+    }
+  } else {
+    TreeStack<E> st;
+    for (int q0 = 0; q0 < p.P; q0 += 8) {
+      uint4 w[8];
+      const int nb = min(8, p.P - q0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < nb) w[k] = ld_stream(reinterpret_cast<const uint4*>(in_ptr(p, J, q0 + k) + off));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < nb) {
+          float x[E];
+          T::widen(w[k], x);
+          if constexpr (ORDER == kOrderTree) {
+            st.push(x);
+          } else if (q0 + k == 0) {
+#pragma unroll
+            for (int i = 0; i < E; ++i) acc[i] = x[i];
+          } else {
+            add_into(acc, x);
+          }
+        }
+      }
+    }
+    if constexpr (ORDER == kOrderTree) st.finish(acc);
+  }
+}
+
+template <int DT, int ORDER, int BLOCK, int UNROLL, int PT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>& p,
+                                               const ReduceJob& J, uint64_t a, uint64_t b) {
+  using T = Elem<DT>;
+  constexpr int E = T::kPerVec;
+  const uint64_t hu = J.head ? 1 : 0;
+  const uint64_t nbody = (J.count - J.head) / E;
+  const uint64_t tail_unit = hu + nbody;
+  const bool has_tail = ((J.count - J.head) % E) != 0;
+  if (hu && a == 0 && threadIdx.x == 0) fold_scalar<DT, ORDER>(p, J, 0, J.head, 1);
+  if (has_tail && a <= tail_unit && tail_unit < b && threadIdx.x == BLOCK - 1)
+    fold_scalar<DT, ORDER>(p, J, J.head + E * nbody, J.count, 1);
+  const uint64_t ba = max(a, hu), bb = min(b, tail_unit);
+  for (uint64_t u0 = ba + threadIdx.x; u0 < bb; u0 += BLOCK * UNROLL) {
+    uint4 v[UNROLL][PT > 0 ? PT : 1];
+    if constexpr (PT > 0) {
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const uint64_t u = u0 + k * BLOCK;
+        if (u < bb) {
+          const uint64_t off = (J.in_off + J.head + E * (u - hu)) * T::kSize;
+#pragma unroll
+          for (int q = 0; q < PT; ++q)
+            v[k][q] = ld_stream(reinterpret_cast<const uint4*>(in_ptr(p, J, q) + off));
+        }
+      }
+    }
+    float acc[UNROLL][E];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint64_t u = u0 + k * BLOCK;
+      if (u < bb)
+        fold_vector<DT, ORDER, PT>(p, J, (J.in_off + J.head + E * (u - hu)) * T::kSize, v[k], acc[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint64_t u = u0 + k * BLOCK;
+      if (u < bb) {
+        const uint4 y = T::narrow(acc[k]);
+        const uint64_t byte_off = (J.head + E * (u - hu)) * T::kSize;
+        for (uint32_t m = 0; m < J.nout; ++m)
+          st16(reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off), y);
+      }
+    }
+  }
+}
+
+// Tile t covers global units [t*TILE, (t+1)*TILE), TILE = BLOCK*UNROLL; a
+// CTA takes tiles first, first + step, ... so that all CTAs sweep the buffers
+// together.  A tile's job is found by walking the job table forward.
+template <int DT, int ORDER, int BLOCK, int UNROLL, int PT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t first,
+                                             uint64_t step) {
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
+  const uint64_t ntiles = (p.total_units + kTile - 1) / kTile;
+  int j = 0;
+  for (uint64_t t = first; t < ntiles; t += step) {
+    const uint64_t g0 = t * kTile, g1 = min(g0 + kTile, p.total_units);
+    while (j + 1 < p.njobs && p.job[j].ufirst + p.job[j].nunits <= g0) ++j;
+    for (int jj = j; jj < p.njobs && p.job[jj].ufirst < g1; ++jj) {
+      const ReduceJob& J = p.job[jj];
+      const uint64_t a = max(g0, J.ufirst) - J.ufirst;
+      const uint64_t b = min(g1, J.ufirst + J.nunits) - J.ufirst;
+      if (a >= b) continue;
+      if (J.flags & kJobVec)
+        reduce_job_vec<DT, ORDER, BLOCK, UNROLL, PT>(p, J, a, b);
+      else
+        fold_scalar<DT, ORDER>(p, J, a + threadIdx.x, b, BLOCK);
+    }
+  }
+}
+
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+__global__ void __launch_bounds__(kReduceBlock)
+    dc_reduce_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
+  pdl_enter();
+  reduce_tiles<DT, ORDER, kReduceBlock, kReduceUnroll, PT>(p, blockIdx.x, gridDim.x);
+}
+
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+__global__ void __launch_bounds__(kReduceSingleBlock)
+    dc_reduce_single_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
+  pdl_enter();
+  reduce_tiles<DT, ORDER, kReduceSingleBlock, kReduceUnroll, PT>(p, 0, 1);
+}
+
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+cudaError_t launch_pt(const ReduceParams<MAXJ, MAXPTR>& p, int grid, bool single, bool pdl,
+                      cudaStream_t s) {
+  if (single)
+    return launch_ex(dc_reduce_single_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, 1, kReduceSingleBlock, pdl,
+                     s, p);
+  return launch_ex(dc_reduce_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, grid, kReduceBlock, pdl, s, p);
+}
+
+template <int DT, int ORDER, int MAXJ, int MAXPTR>
+cudaError_t launch_order(const ReduceParams<MAXJ, MAXPTR>& p, int grid, bool single, bool pdl,
+                         cudaStream_t s) {
+  return p.P == 8 ? launch_pt<DT, ORDER, 8>(p, grid, single, pdl, s)
+                  : launch_pt<DT, ORDER, 0>(p, grid, single, pdl, s);
+}
+
+template <int DT, int MAXJ, int MAXPTR>
+cudaError_t launch_dtype(const ReduceParams<MAXJ, MAXPTR>& p, int order, int grid, bool single,
+                         bool pdl, cudaStream_t s) {
+  return order == kOrderTree ? launch_order<DT, kOrderTree>(p, grid, single, pdl, s)
+                             : launch_order<DT, kOrderLinear>(p, grid, single, pdl, s);
+}
+
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+int occupancy_pt() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, dc_reduce_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, kReduceBlock, 0) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+template <int DT, int MAXJ, int MAXPTR>
+int occupancy_dtype(int order, int P) {
+  if (order == kOrderTree)
+    return P == 8 ? occupancy_pt<DT, kOrderTree, 8, MAXJ, MAXPTR>()
+                  : occupancy_pt<DT, kOrderTree, 0, MAXJ, MAXPTR>();
+  return P == 8 ? occupancy_pt<DT, kOrderLinear, 8, MAXJ, MAXPTR>()
+                : occupancy_pt<DT, kOrderLinear, 0, MAXJ, MAXPTR>();
+}
+
+}  // namespace red
+}  // namespace dc
+
+// Instantiates the launch and occupancy entry points of one element type.
+#define DC_REDUCE_INSTANTIATE(DT, NAME)                                                            \
+  namespace dc {                                                                                   \
+  cudaError_t launch_reduce_##NAME(const ReduceParams1& p, int order, int grid, bool single,       \
+                                   bool pdl, cudaStream_t s) {                                     \
+    return red::launch_dtype<DT>(p, order, grid, single, pdl, s);                                  \
+  }                                                                                                \
+  cudaError_t launch_reduce_##NAME(const ReduceParamsS& p, int order, int grid, bool single,       \
+                                   bool pdl, cudaStream_t s) {                                     \
+    return red::launch_dtype<DT>(p, order, grid, single, pdl, s);                                  \
+  }                                                                                                \
+  cudaError_t launch_reduce_##NAME(const ReduceParamsL& p, int order, int grid, bool single,       \
+                                   bool pdl, cudaStream_t s) {                                     \
+    return red::launch_dtype<DT>(p, order, grid, single, pdl, s);                                  \
+  }                                                                                                \
+  int reduce_ctas_per_sm_##NAME(int variant, int order, int P) {                                   \
+    switch (variant) {                                                                             \
+      case 0: return red::occupancy_dtype<DT, 1, 2 * kMaxRanks>(order, P);                        \
+      case 1: return red::occupancy_dtype<DT, kMaxRanks, 4 * kMaxRanks>(order, P);                \
+      default: return red::occupancy_dtype<DT, kManyMaxReduceJobs, kManyMaxReducePtrs>(order, P); \
+    }                                                                                              \
+  }                                                                                                \
+  }  // namespace dc

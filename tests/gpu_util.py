@@ -87,3 +87,45 @@ def assert_bf16_equal(got: np.ndarray, want: np.ndarray, what: str = "") -> None
         i = int(bad[0])
         raise AssertionError(f"{what}: {bad.size} elements differ, first at {i}: "
                              f"got {got[i]:#06x} want {want[i]:#06x}")
+
+
+NP_OF = {"bf16": np.uint16, "f16": np.uint16, "f32": np.uint32}
+
+
+def torch_dtype(dtype: str):
+    torch = _torch()
+    return {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+
+
+def typed_tensor(bits: np.ndarray, dtype: str, device="cuda"):
+    """A device tensor of element type `dtype` holding the given bit patterns."""
+    torch = _torch()
+    as_int = np.ascontiguousarray(bits).view(np.int16 if dtype != "f32" else np.int32)
+    return torch.from_numpy(as_int).to(device).view(torch_dtype(dtype))
+
+
+def typed_bits(t, dtype: str) -> np.ndarray:
+    torch = _torch()
+    iv = torch.int16 if dtype != "f32" else torch.int32
+    return t.view(iv).cpu().numpy().view(NP_OF[dtype])
+
+
+def is_nan_typed(h: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return is_nan_bits(h)
+    if dtype == "f16":
+        return ((h & 0x7C00) == 0x7C00) & ((h & 0x03FF) != 0)
+    return ((h & 0x7F800000) == 0x7F800000) & ((h & 0x007FFFFF) != 0)
+
+
+def assert_typed_equal(got: np.ndarray, want: np.ndarray, dtype: str, what: str = "") -> None:
+    """Bit-exact equality except NaN, compared by class."""
+    gn, wn = is_nan_typed(got, dtype), is_nan_typed(want, dtype)
+    if not np.array_equal(gn, wn):
+        i = int(np.flatnonzero(gn != wn)[0])
+        raise AssertionError(f"{what}: NaN class differs at {i}: got {int(got[i]):#x} want {int(want[i]):#x}")
+    bad = np.flatnonzero((got != want) & ~wn)
+    if bad.size:
+        i = int(bad[0])
+        raise AssertionError(f"{what}: {bad.size} elements differ, first at {i}: "
+                             f"got {int(got[i]):#x} want {int(want[i]):#x}")

@@ -227,3 +227,58 @@ def test_tensor_api_requires_cuda_tensors():
     x = torch.zeros(16, dtype=torch.uint8)
     with pytest.raises(ValueError):
         dc.all_gather([x], torch.zeros(16, dtype=torch.uint8))
+
+
+# ------------------------------------------------- typed and batched reductions ---
+
+def test_typed_reduce_rejects_bad_type_and_order():
+    ins = [BASE, BASE + 4096]
+    outs = [BASE + 8192, BASE + 12288]
+    assert dc.dc_all_reduce(ins, outs, 2, 8, 3, 0) == INVALID
+    assert dc.dc_all_reduce(ins, outs, 2, 8, 0, 2) == INVALID
+    assert dc.dc_reduce_scatter(ins, outs, 2, 8, -1, 0) == INVALID
+
+
+def test_f32_needs_4_byte_alignment(no_launch):
+    ins = [BASE, BASE + 4096 + 2]
+    outs = [BASE + 8192, BASE + 12288]
+    assert dc.dc_all_reduce(ins, outs, 2, 8, 2, 0) == ALIGN
+    assert dc.dc_all_reduce(ins, outs, 2, 8, 1, 0) == CUDA  # 2-byte aligned is enough for FP16
+
+
+def test_batched_reduce_limits():
+    P = 8
+    assert dc.dc_all_reduce_many([BASE] * (257 * 1), [BASE] * 257, [4] * 257, 257, 1) == TOO_MANY
+    T = 65  # 2 * 65 * 8 = 1040 pointers
+    assert dc.dc_all_reduce_many([BASE] * (T * P), [BASE] * (T * P), [4] * T, T, P) == TOO_MANY
+    T = 33  # 264 reduce_scatter jobs
+    assert dc.dc_reduce_scatter_many([BASE] * (T * P), [BASE] * (T * P), [4] * T, T, P) == TOO_MANY
+    assert dc.dc_all_reduce_many([], [], [], 0, P) == OK
+
+
+def test_batched_reduce_aliasing(no_launch):
+    P, n = 2, 64
+    ins = [BASE + i * 4096 for i in range(2 * P)]        # tensor 0: 0,1  tensor 1: 2,3
+    outs = [BASE + 65536 + i * 4096 for i in range(2 * P)]
+    assert dc.dc_all_reduce_many(ins, outs, [n, n], 2, P) == CUDA
+    outs_inplace = [ins[0], ins[1], ins[2], ins[3]]     # each tensor in place
+    assert dc.dc_all_reduce_many(ins, outs_inplace, [n, n], 2, P) == CUDA
+    outs_cross = [outs[0], outs[1], ins[0], outs[3]]    # tensor 1 writes over tensor 0's input
+    assert dc.dc_all_reduce_many(ins, outs_cross, [n, n], 2, P) == OVERLAP
+    assert "tensor 1" in dc.last_error()
+
+
+def test_batched_reduce_scatter_inplace_shards(no_launch):
+    P, C = 4, 32
+    ins = [BASE + i * 8192 for i in range(2 * P)]
+    outs = [ins[t * P + r] + 2 * r * C for t in range(2) for r in range(P)]
+    assert dc.dc_reduce_scatter_many(ins, outs, [C, C], 2, P) == CUDA
+    outs[5] = ins[0] + 2 * 1 * C  # tensor 1 rank 1 writes into tensor 0's input
+    assert dc.dc_reduce_scatter_many(ins, outs, [C, C], 2, P) == OVERLAP
+
+
+def test_batched_zero_counts_launch_nothing():
+    before = dc.launch_count()
+    assert dc.dc_all_reduce_many([0] * 6, [0] * 6, [0, 0, 0], 3, 2) == OK
+    assert dc.dc_reduce_scatter_many([0] * 6, [0] * 6, [0, 0, 0], 3, 2) == OK
+    assert dc.launch_count() == before

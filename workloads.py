@@ -143,6 +143,17 @@ def normal_bf16_device(seed: int, rank: int, count: int, device, tensor: int = 0
     return torch.randn(count, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
+def normal_device(seed: int, rank: int, count: int, device, dtype, tensor: int = 0):
+    """N(0,1) drawn on ``device`` in FP32 and cast by torch to ``dtype``
+    (torch.bfloat16, torch.float16 or torch.float32); same stream as
+    normal_bf16_device for the same seed, rank and tensor."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(device_seed(seed, rank, tensor))
+    return torch.randn(count, generator=g, device=device, dtype=torch.float32).to(dtype)
+
+
 def random_bytes_device(seed: int, rank: int, nbytes: int, device, tensor: int = 0):
     """Uniform random bytes drawn on ``device`` with a seeded torch generator."""
     import torch
