@@ -65,9 +65,23 @@ def parse_args(argv=None):
     ap.add_argument("--no-reductions", action="store_true",
                     help="skip the all_reduce / reduce_scatter / all_gather_many block")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparators", action="store_true",
+                    help="skip the torch comparators and the warm back-to-back latency graphs")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--crossover", action="store_true", help="run the single/multi-CTA sweep")
+    ap.add_argument("--skew", action="store_true",
+                    help="rank-skew calibration of all_reduce on simulated ranks (one JSON line "
+                         "per mode, P, shape and requested delay)")
+    ap.add_argument("--skew-shapes", nargs="+", default=["8x8192", "8627x8192", "16384x8192"])
+    ap.add_argument("--skew-delays-us", nargs="+", type=float, default=[0.0, 50.0, 250.0, 1000.0])
+    ap.add_argument("--skew-ranks", nargs="+", type=int, default=[2, 4],
+                    help="simulated rank counts P")
+    ap.add_argument("--skew-rank", type=int, default=None,
+                    help="the delayed rank (default: the last one)")
+    ap.add_argument("--skew-modes", nargs="+", choices=["graph", "eager"], default=["graph", "eager"])
+    ap.add_argument("--skew-trials", type=int, default=50)
+    ap.add_argument("--skew-warmup", type=int, default=10)
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
     ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
                     help="profiling helper: run one call REPS times and exit, e.g. "
@@ -203,6 +217,40 @@ def cpu_oracle_sample(seconds: float):
     return {"value": step_bytes * passes / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{passes} full passes of the 14-gather sweep ({step_bytes} algorithmic bytes "
                       f"each) through the single-threaded C oracle, {el:.1f} s"}
+
+
+def cpu_oracle_threaded(seconds: float):
+    """The same oracle sweep run by one thread per host core, each thread
+    doing whole passes (the C calls release the GIL), for `seconds`."""
+    import threading
+
+    import oracle
+
+    cases = sweep_cases()
+    host = [[W.random_bf16_patterns(seed, r, B // 2).view(np.uint8) for r in range(P)]
+            for (P, B, seed) in cases]
+    step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
+    oracle.all_gather(host[0])
+    nthreads = len(os.sched_getaffinity(0))
+    done = [0] * nthreads
+    t0 = time.perf_counter()
+
+    def work(i):
+        while time.perf_counter() - t0 < seconds:
+            for peers in host:
+                oracle.all_gather(peers)
+            done[i] += 1
+
+    th = [threading.Thread(target=work, args=(i,)) for i in range(nthreads)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    el = time.perf_counter() - t0
+    return {"value": step_bytes * sum(done) / el / 1e9, "unit": UNIT, "cores": nthreads,
+            "kind": "oracle, one thread per core",
+            "sample": f"{sum(done)} full passes of the 14-gather sweep over {nthreads} threads, "
+                      f"{el:.1f} s"}
 
 
 def run_reference(args) -> int:
@@ -360,6 +408,103 @@ def typed_rows(torch, dc, device, stream, flush, peak):
     rows.append({"op": "reduce_scatter_many_bf16_tree", "P": P, "count": len(counts),
                  "shape": "{" + ", ".join(W.CONFIG4_COUNTS) + "}", "us": us,
                  "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    return rows
+
+
+def alternating(torch, stream, flush, fns, reps):
+    """Time the callables of `fns` after a flush each, alternating which one
+    goes first from sample to sample (as the page's benchmark does);
+    returns per-callable medians in microseconds."""
+    samples = [[] for _ in fns]
+    for i in range(reps):
+        order = list(range(len(fns)))
+        if i % 2:
+            order.reverse()
+        got = timed_calls(torch, stream, flush, [fns[j] for j in order], 1)
+        for k, j in enumerate(order):
+            samples[j].extend(got[k])
+    return [statistics.median(x) for x in samples]
+
+
+def comparators_block(torch, dc, device, stream, flush, reps=10):
+    """torch comparators beside this library, same inputs, alternating
+    order per sample: torch.cat(peers, out=out) for every gather of the
+    sweep, and a torch loop (acc = x0.float(); acc = acc + xq.float() for
+    q = 1..P-1; one cast to BF16, copied to the P outputs) for the all_reduce
+    sizes.  Bits of both are compared, for the record."""
+    gathers = []
+    for (P, B, seed) in sweep_cases():
+        peers = [torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)).to(device)
+                 for r in range(P)]
+        out_dc = torch.empty(P * B, dtype=torch.uint8, device=device)
+        out_t = torch.empty_like(out_dc)
+        ours, theirs = alternating(torch, stream, flush,
+                                   [lambda: dc.all_gather(peers, out_dc),
+                                    lambda: torch.cat(peers, out=out_t)], reps)
+        gathers.append({"P": P, "bytes_per_rank": B, "us": ours, "torch_cat_us": theirs,
+                        "speedup": theirs / ours, "bits_equal": bool(torch.equal(out_dc, out_t))})
+    reduces = []
+    P = W.CONFIG4_P
+    for name, n in W.CONFIG4_COUNTS.items():
+        ins = [W.normal_bf16_device(W.seed_for(4, list(W.CONFIG4_COUNTS).index(name)), r, n, device)
+               for r in range(P)]
+        outs = [torch.empty_like(x) for x in ins]
+        touts = [torch.empty_like(x) for x in ins]
+
+        def torch_loop():
+            acc = ins[0].float()
+            for q in range(1, P):
+                acc = acc + ins[q].float()
+            y = acc.bfloat16()
+            for o in touts:
+                o.copy_(y)
+
+        ours, theirs = alternating(torch, stream, flush,
+                                   [lambda: dc.all_reduce(ins, outs), torch_loop], reps)
+        reduces.append({"P": P, "shape": name, "count": n, "us": ours, "torch_loop_us": theirs,
+                        "speedup": theirs / ours,
+                        "bits_equal": bool(torch.equal(outs[0].view(torch.int16),
+                                                       touts[0].view(torch.int16)))})
+        del ins, outs, touts
+    return {"all_gather_vs_torch_cat": gathers, "all_reduce_bf16_vs_torch_loop": reduces}
+
+
+def warm_latency_block(torch, dc, device, calls_per_graph=1000, replays=3):
+    """Per-call latency of back-to-back calls with warm caches: for each
+    gather of the sweep whose inputs and output fit in a quarter of L2, one
+    CUDA graph of `calls_per_graph` identical calls, timed by events around
+    its replay (median of `replays`), for this library and torch.cat."""
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20)
+    rows = []
+    for (P, B, seed) in sweep_cases():
+        if 2 * P * B > l2 // 4:
+            continue
+        peers = [torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)).to(device)
+                 for r in range(P)]
+        out = torch.empty(P * B, dtype=torch.uint8, device=device)
+        row = {"P": P, "bytes_per_rank": B}
+        for label, fn in (("us", lambda: dc.all_gather(peers, out)),
+                          ("torch_cat_us", lambda: torch.cat(peers, out=out))):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(calls_per_graph):
+                    fn()
+            torch.cuda.synchronize()
+            g.replay()
+            t = []
+            for _ in range(replays):
+                s = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                s.record()
+                g.replay()
+                e.record()
+                torch.cuda.synchronize()
+                t.append(s.elapsed_time(e) * 1e3 / calls_per_graph)
+            row[label] = statistics.median(t)
+            del g
+        rows.append(row)
     return rows
 
 
@@ -529,6 +674,10 @@ def run_dc(args) -> int:
     extra = None
     if not args.no_reductions:
         extra = reductions_block(torch, dc, device, stream, flush, peak)
+    comparators = latency = None
+    if not args.no_comparators:
+        comparators = comparators_block(torch, dc, device, stream, flush)
+        latency = warm_latency_block(torch, dc, device)
     e2e = e2e_measure(torch, dc, device, stream, cases, min(args.steps, 20))
     e2e["value"] = job_throughput(world, step_bytes, rank_max(e2e["ms_per_step"], dist, device))
 
@@ -560,8 +709,12 @@ def run_dc(args) -> int:
     }
     if extra is not None:
         line["other_ops"] = extra
+    if comparators is not None:
+        line["comparators"] = comparators
+        line["warm_latency_graph_1000_calls"] = latency
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(args.cpu_seconds)
+        line["cpu_oracle_all_cores"] = cpu_oracle_threaded(args.cpu_seconds)
     if rank == 0:
         emit(line, args)
     if dist:
@@ -618,6 +771,41 @@ def run_crossover(args) -> int:
     return 0
 
 
+def run_skew(args) -> int:
+    """Rank-skew calibration (the page "[Benchmark] Add all-reduce rank-skew
+    calibration", section "Test Plan"): BF16 all_reduce of each shape per
+    rank on P simulated ranks, one rank delayed on the GPU by each requested
+    delay, eager and CUDA-graph mode; one JSON line of medians per point."""
+    import torch
+
+    import reduce_copy_rank_gb300 as dc
+    from reduce_copy_rank_gb300.skew import SkewTrial
+
+    device = torch.device("cuda", 0)
+    lines = []
+    for P in args.skew_ranks:
+        inj = P - 1 if args.skew_rank is None else args.skew_rank
+        for shape in args.skew_shapes:
+            n = W.CONFIG4_COUNTS[shape]
+            ins = [W.normal_bf16_device(W.seed_for(4, 9990), r, n, device) for r in range(P)]
+            outs = [torch.empty_like(x) for x in ins]
+            for mode in args.skew_modes:
+                cal = SkewTrial(P=P, collective=lambda st: dc.all_reduce(ins, outs, stream=st),
+                                injected_rank=inj, mode=mode)
+                for d in args.skew_delays_us:
+                    res = cal.run(d, trials=args.skew_trials, warmup=args.skew_warmup)
+                    res.pop("trials_detail")
+                    res.update({"op": "all_reduce_bf16", "shape": shape, "count": n})
+                    print(json.dumps(res), flush=True)
+                    lines.append(res)
+            del ins, outs
+    if args.out:
+        with open(args.out, "w") as fh:
+            for ln in lines:
+                fh.write(json.dumps(ln) + "\n")
+    return 0
+
+
 def run_case(args) -> int:
     """Run one operation a few times with nothing else on the GPU (for ncu)."""
     import torch
@@ -664,6 +852,8 @@ def main(argv=None) -> int:
         return run_crossover(args)
     if args.case:
         return run_case(args)
+    if args.skew:
+        return run_skew(args)
     return run_dc(args)
 
 

@@ -170,6 +170,24 @@ dc_status_t dc_reduce_scatter_many(const void *const *in_ptrs, void *const *out_
                                    const size_t *counts_per_shard, int T, int P, dc_dtype_t dtype,
                                    dc_order_t order, dc_stream_t stream);
 
+/*
+ * dc_inject_delay_ns -- keeps one GPU thread busy for `ns` nanoseconds of
+ * the GPU's global timer, in stream order.  The rank-skew calibration
+ * ("[Benchmark] Add all-reduce rank-skew calibration", vLLM pull request
+ * 57037, section "Purpose") puts it on one simulated rank's stream before
+ * that rank arrives at the collective.
+ *
+ * ns:     0..DC_MAX_DELAY_NS (DC_ERR_INVALID above); 0 launches a kernel
+ *         that returns at once.
+ * stream: the stream to delay.
+ * The kernel reads no memory and writes none.  It stops when the timer has
+ * advanced by ns, or, should the timer stall, after 4*ns + 2^20 SM cycles.
+ * The requested delay is a lower bound on the kernel's duration; time it
+ * with events to get the measured delay.
+ */
+#define DC_MAX_DELAY_NS 1000000000ull
+dc_status_t dc_inject_delay_ns(unsigned long long ns, dc_stream_t stream);
+
 /* Message describing the last failed call on this thread ("" if none). */
 const char *dc_last_error(void);
 

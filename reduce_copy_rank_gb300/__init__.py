@@ -24,7 +24,8 @@ from typing import Sequence
 
 __all__ = [
     "DCError", "LibraryMissing", "all_gather", "all_gather_many", "all_reduce",
-    "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "set_option", "get_option",
+    "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "inject_delay", "set_option",
+    "get_option",
     "launch_count", "last_error", "options", "lib", "LIB_PATH", "STATUS", "DTYPES", "ORDERS",
 ]
 
@@ -39,6 +40,7 @@ MANY_MAX_TENSORS = 256
 MANY_MAX_SEGMENTS = 1024
 MANY_MAX_REDUCE_JOBS = 256
 MANY_MAX_REDUCE_PTRS = 1024
+MAX_DELAY_NS = 1_000_000_000
 
 DTYPES = {"bf16": 0, "f16": 1, "f32": 2}      # dc_dtype_t
 ORDERS = {"linear": 0, "tree": 1}             # dc_order_t
@@ -84,9 +86,10 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_size_t), ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, _VP]
         L.dc_reduce_scatter_many.argtypes = L.dc_all_reduce_many.argtypes
+        L.dc_inject_delay_ns.argtypes = [ctypes.c_ulonglong, _VP]
         for f in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
                   "dc_reduce_scatter_bf16", "dc_all_reduce", "dc_reduce_scatter",
-                  "dc_all_reduce_many", "dc_reduce_scatter_many"):
+                  "dc_all_reduce_many", "dc_reduce_scatter_many", "dc_inject_delay_ns"):
             getattr(L, f).restype = ctypes.c_int
         L.dc_last_error.argtypes = []
         L.dc_last_error.restype = ctypes.c_char_p
@@ -167,6 +170,10 @@ def dc_reduce_scatter_many(in_ptrs: Sequence[int], out_ptrs: Sequence[int],
                            order: int = 0, stream: int = 0) -> int:
     return lib().dc_reduce_scatter_many(_ptr_array(in_ptrs), _ptr_array(out_ptrs),
                                         _sizes(counts_per_shard), T, P, dtype, order, stream)
+
+
+def dc_inject_delay_ns(ns: int, stream: int = 0) -> int:
+    return lib().dc_inject_delay_ns(int(ns), stream)
 
 
 # ---------------------------------------------------------- tensor API ---
@@ -347,6 +354,12 @@ def reduce_scatter_many(inputs_per_tensor: Sequence[Sequence],
         _check(dc_reduce_scatter_many(ins, outs, counts, T, P, _dtype_code(inputs_per_tensor[0][0]),
                                       _order_code(order), _stream_handle(stream)))
     return outputs_per_tensor
+
+
+def inject_delay(ns: int, stream=None) -> None:
+    """Delay `stream` (default: the current torch stream) by `ns` nanoseconds
+    of the GPU's global timer (one-thread kernel; rank-skew calibration)."""
+    _check(dc_inject_delay_ns(ns, _stream_handle(stream)))
 
 
 # ------------------------------------------------------------- options ---

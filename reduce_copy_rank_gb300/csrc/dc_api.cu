@@ -554,6 +554,16 @@ dc_status_t dc_reduce_scatter_many(const void* const* in_ptrs, void* const* out_
                       "reduce_scatter_many");
 }
 
+dc_status_t dc_inject_delay_ns(unsigned long long ns, dc_stream_t stream) {
+  read_env_once();
+  if (ns > DC_MAX_DELAY_NS)
+    return fail(DC_ERR_INVALID, "delay %llu ns is above the %llu ns limit", ns,
+                static_cast<unsigned long long>(DC_MAX_DELAY_NS));
+  if (g_opt.test_fail_launch.load())
+    return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
+  return check_launch(launch_delay(ns, static_cast<cudaStream_t>(stream)), "delay");
+}
+
 const char* dc_last_error(void) { return g_err; }
 
 const char* dc_status_name(int status) {

@@ -145,6 +145,10 @@ cudaError_t launch_reduce(const Params& p, int dtype, int order, int grid, bool 
   }
 }
 
+// One-thread delay of `ns` nanoseconds of the global timer (rank-skew
+// calibration); defined in dc_delay.cu.
+cudaError_t launch_delay(unsigned long long ns, cudaStream_t s);
+
 // variant: 0 ReduceParams1, 1 ReduceParamsS, 2 ReduceParamsL.
 inline int reduce_ctas_per_sm(int dtype, int variant, int order, int P) {
   switch (dtype) {

@@ -282,3 +282,11 @@ def test_batched_zero_counts_launch_nothing():
     assert dc.dc_all_reduce_many([0] * 6, [0] * 6, [0, 0, 0], 3, 2) == OK
     assert dc.dc_reduce_scatter_many([0] * 6, [0] * 6, [0, 0, 0], 3, 2) == OK
     assert dc.launch_count() == before
+
+
+def test_delay_limit_checked_before_cuda(no_launch):
+    assert dc.dc_inject_delay_ns(dc.MAX_DELAY_NS + 1, 0) == 1  # DC_ERR_INVALID
+    assert "limit" in dc.last_error()
+    # a valid request reaches the (refused) launch
+    assert dc.dc_inject_delay_ns(0, 0) == 5
+    assert dc.dc_inject_delay_ns(dc.MAX_DELAY_NS, 0) == 5
