@@ -199,8 +199,10 @@ const char *dc_status_name(int status);
  *   "force_path"              0 = automatic, 1 = single CTA, 2 = multi CTA
  *   "force_generic"           1 = never use the flat aligned gather path
  *   "gather_single_max_bytes" single-CTA gather up to this many output bytes
+ *                             (default 16384, measured)
  *   "reduce_single_max_bytes" single-CTA reductions up to this many input
- *                             bytes per rank
+ *                             bytes per rank (default 0: the grid was never
+ *                             slower on GB300)
  *   "grid_ctas"               0 = automatic, else the multi-CTA grid size
  *   "pdl"                     1 (default) = launch with programmatic stream
  *                             serialization, so a kernel's launch overlaps the

@@ -17,6 +17,7 @@ per process.
 """
 from __future__ import annotations
 
+import array
 import contextlib
 import ctypes
 import os
@@ -72,19 +73,14 @@ def lib() -> ctypes.CDLL:
                 f"{LIB_PATH} is missing: build it with `python -m reduce_copy_rank_gb300._build` "
                 "(or __graft_entry__.build()); there is no fallback path")
         L = ctypes.CDLL(LIB_PATH)
-        L.dc_all_gather.argtypes = [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_size_t, _VP, _VP]
-        L.dc_all_gather_many.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(ctypes.c_size_t),
-                                         ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int, _VP]
-        L.dc_all_reduce_bf16.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP), ctypes.c_int,
-                                         ctypes.c_size_t, _VP]
-        L.dc_reduce_scatter_bf16.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP),
-                                             ctypes.c_int, ctypes.c_size_t, _VP]
-        L.dc_all_reduce.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP), ctypes.c_int,
-                                    ctypes.c_size_t, ctypes.c_int, ctypes.c_int, _VP]
+        A, I, Z = _VP, ctypes.c_int, ctypes.c_size_t  # A: address of a host array
+        L.dc_all_gather.argtypes = [A, I, Z, _VP, _VP]
+        L.dc_all_gather_many.argtypes = [A, A, A, I, I, _VP]
+        L.dc_all_reduce_bf16.argtypes = [A, A, I, Z, _VP]
+        L.dc_reduce_scatter_bf16.argtypes = [A, A, I, Z, _VP]
+        L.dc_all_reduce.argtypes = [A, A, I, Z, I, I, _VP]
         L.dc_reduce_scatter.argtypes = L.dc_all_reduce.argtypes
-        L.dc_all_reduce_many.argtypes = [ctypes.POINTER(_VP), ctypes.POINTER(_VP),
-                                         ctypes.POINTER(ctypes.c_size_t), ctypes.c_int, ctypes.c_int,
-                                         ctypes.c_int, ctypes.c_int, _VP]
+        L.dc_all_reduce_many.argtypes = [A, A, A, I, I, I, I, _VP]
         L.dc_reduce_scatter_many.argtypes = L.dc_all_reduce_many.argtypes
         L.dc_inject_delay_ns.argtypes = [ctypes.c_ulonglong, _VP]
         for f in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
@@ -112,8 +108,19 @@ def _check(status: int) -> None:
         raise DCError(status, lib().dc_last_error().decode(errors="replace"))
 
 
-def _ptr_array(ptrs: Sequence[int]):
-    return (_VP * max(1, len(ptrs)))(*[int(p) for p in ptrs])
+# Host arrays of pointers and sizes are built as array("Q") (64-bit values;
+# size_t and pointers are 64 bits on the supported platforms) and passed by
+# address; the caller keeps the array object alive for the call.
+assert ctypes.sizeof(ctypes.c_size_t) == 8 and ctypes.sizeof(ctypes.c_void_p) == 8
+assert array.array("Q").itemsize == 8
+
+
+def _u64(xs: Sequence[int]) -> array.array:
+    return array.array("Q", xs) if len(xs) else array.array("Q", (0,))
+
+
+def _addr(a: array.array) -> int:
+    return a.buffer_info()[0]
 
 
 # ------------------------------------------------------------ raw (C ABI) ---
@@ -123,53 +130,51 @@ def _ptr_array(ptrs: Sequence[int]):
 
 def dc_all_gather(peer_ptrs: Sequence[int], P: int, bytes_per_rank: int, out: int,
                   stream: int = 0) -> int:
-    return lib().dc_all_gather(_ptr_array(peer_ptrs), P, bytes_per_rank, out, stream)
+    a = _u64(peer_ptrs)
+    return lib().dc_all_gather(_addr(a), P, bytes_per_rank, out, stream)
 
 
 def dc_all_gather_many(peer_ptrs: Sequence[int], bytes_per_rank: Sequence[int],
                        outs: Sequence[int], T: int, P: int, stream: int = 0) -> int:
-    sizes = (ctypes.c_size_t * max(1, len(bytes_per_rank)))(*[int(b) for b in bytes_per_rank])
-    return lib().dc_all_gather_many(_ptr_array(peer_ptrs), sizes, _ptr_array(outs), T, P, stream)
+    a, b, c = _u64(peer_ptrs), _u64(bytes_per_rank), _u64(outs)
+    return lib().dc_all_gather_many(_addr(a), _addr(b), _addr(c), T, P, stream)
 
 
 def dc_all_reduce_bf16(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int, count: int,
                        stream: int = 0) -> int:
-    return lib().dc_all_reduce_bf16(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P, count, stream)
+    a, b = _u64(in_ptrs), _u64(out_ptrs)
+    return lib().dc_all_reduce_bf16(_addr(a), _addr(b), P, count, stream)
 
 
 def dc_reduce_scatter_bf16(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int,
                            count_per_shard: int, stream: int = 0) -> int:
-    return lib().dc_reduce_scatter_bf16(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P,
-                                        count_per_shard, stream)
+    a, b = _u64(in_ptrs), _u64(out_ptrs)
+    return lib().dc_reduce_scatter_bf16(_addr(a), _addr(b), P, count_per_shard, stream)
 
 
 def dc_all_reduce(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int, count: int,
                   dtype: int = 0, order: int = 0, stream: int = 0) -> int:
-    return lib().dc_all_reduce(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P, count, dtype, order,
-                               stream)
+    a, b = _u64(in_ptrs), _u64(out_ptrs)
+    return lib().dc_all_reduce(_addr(a), _addr(b), P, count, dtype, order, stream)
 
 
 def dc_reduce_scatter(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int,
                       count_per_shard: int, dtype: int = 0, order: int = 0, stream: int = 0) -> int:
-    return lib().dc_reduce_scatter(_ptr_array(in_ptrs), _ptr_array(out_ptrs), P, count_per_shard,
-                                   dtype, order, stream)
-
-
-def _sizes(xs: Sequence[int]):
-    return (ctypes.c_size_t * max(1, len(xs)))(*[int(x) for x in xs])
+    a, b = _u64(in_ptrs), _u64(out_ptrs)
+    return lib().dc_reduce_scatter(_addr(a), _addr(b), P, count_per_shard, dtype, order, stream)
 
 
 def dc_all_reduce_many(in_ptrs: Sequence[int], out_ptrs: Sequence[int], counts: Sequence[int],
                        T: int, P: int, dtype: int = 0, order: int = 0, stream: int = 0) -> int:
-    return lib().dc_all_reduce_many(_ptr_array(in_ptrs), _ptr_array(out_ptrs), _sizes(counts), T, P,
-                                    dtype, order, stream)
+    a, b, c = _u64(in_ptrs), _u64(out_ptrs), _u64(counts)
+    return lib().dc_all_reduce_many(_addr(a), _addr(b), _addr(c), T, P, dtype, order, stream)
 
 
 def dc_reduce_scatter_many(in_ptrs: Sequence[int], out_ptrs: Sequence[int],
                            counts_per_shard: Sequence[int], T: int, P: int, dtype: int = 0,
                            order: int = 0, stream: int = 0) -> int:
-    return lib().dc_reduce_scatter_many(_ptr_array(in_ptrs), _ptr_array(out_ptrs),
-                                        _sizes(counts_per_shard), T, P, dtype, order, stream)
+    a, b, c = _u64(in_ptrs), _u64(out_ptrs), _u64(counts_per_shard)
+    return lib().dc_reduce_scatter_many(_addr(a), _addr(b), _addr(c), T, P, dtype, order, stream)
 
 
 def dc_inject_delay_ns(ns: int, stream: int = 0) -> int:
@@ -178,11 +183,21 @@ def dc_inject_delay_ns(ns: int, stream: int = 0) -> int:
 
 # ---------------------------------------------------------- tensor API ---
 
-def _stream_handle(stream) -> int:
-    import torch
+_raw_stream = None
 
+
+def _stream_handle(stream) -> int:
+    """cudaStream_t of `stream` (None: torch's current stream on the current
+    device), read through torch's raw-stream accessor when it has one."""
+    global _raw_stream
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        import torch
+
+        if _raw_stream is None:
+            f = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            _raw_stream = (lambda: f(torch.cuda.current_device())) if f is not None else \
+                (lambda: torch.cuda.current_stream().cuda_stream)
+        return _raw_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -207,17 +222,25 @@ def all_gather(peers: Sequence, out, stream=None):
     P = len(peers)
     if P == 0:
         raise ValueError("need at least one peer")
+    B = peers[0].nbytes
+    ptrs = []
+    for p in peers:
+        if not p.is_cuda or p.nbytes != B or not p.is_contiguous():
+            _explain_peers(peers)
+        ptrs.append(p.data_ptr())
+    if not out.is_cuda or not out.is_contiguous():
+        _device_tensor(out, "out")
+    if out.nbytes != P * B:
+        raise ValueError(f"out holds {out.nbytes} bytes, expected P * {B} = {P * B}")
+    a = array.array("Q", ptrs)
+    _check(lib().dc_all_gather(_addr(a), P, B, out.data_ptr(), _stream_handle(stream)))
+    return out
+
+
+def _explain_peers(peers) -> None:
     for r, p in enumerate(peers):
         _device_tensor(p, f"peers[{r}]")
-    _device_tensor(out, "out")
-    B = _nbytes(peers[0])
-    if any(_nbytes(p) != B for p in peers):
-        raise ValueError("all peers must have the same number of bytes")
-    if _nbytes(out) != P * B:
-        raise ValueError(f"out holds {_nbytes(out)} bytes, expected P * {B} = {P * B}")
-    _check(dc_all_gather([p.data_ptr() for p in peers], P, B, out.data_ptr(),
-                         _stream_handle(stream)))
-    return out
+    raise ValueError("all peers must have the same number of bytes")
 
 
 def all_gather_many(peers_per_tensor: Sequence[Sequence], outs: Sequence, stream=None):
@@ -248,13 +271,30 @@ def all_gather_many(peers_per_tensor: Sequence[Sequence], outs: Sequence, stream
     return outs
 
 
-def _dtype_code(t) -> int:
-    import torch
+_dtype_codes = None
 
-    codes = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
-    if t.dtype not in codes:
+
+def _dtype_code(t) -> int:
+    global _dtype_codes
+    if _dtype_codes is None:
+        import torch
+
+        _dtype_codes = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+    c = _dtype_codes.get(t.dtype)
+    if c is None:
         raise ValueError(f"reductions take bfloat16, float16 or float32 tensors (got {t.dtype})")
-    return codes[t.dtype]
+    return c
+
+
+def _reduce_ptrs(ts: Sequence, what: str, count: int, dtype) -> list:
+    """Data pointers of `ts` after the checks of _reduce_tensors (which runs
+    only to name the offending tensor)."""
+    ptrs = []
+    for t in ts:
+        if not t.is_cuda or t.dtype != dtype or t.numel() != count or not t.is_contiguous():
+            _reduce_tensors(ts, what, count, dtype)
+        ptrs.append(t.data_ptr())
+    return ptrs
 
 
 def _reduce_tensors(ts: Sequence, what: str, count: int | None, dtype):
@@ -284,10 +324,10 @@ def all_reduce(inputs: Sequence, outputs: Sequence, order: str = "linear", strea
         raise ValueError("need P >= 1 inputs and P outputs")
     n = inputs[0].numel()
     dt = inputs[0].dtype
-    _reduce_tensors(inputs, "inputs", n, dt)
-    _reduce_tensors(outputs, "outputs", n, dt)
-    _check(dc_all_reduce([t.data_ptr() for t in inputs], [t.data_ptr() for t in outputs], P, n,
-                         _dtype_code(inputs[0]), _order_code(order), _stream_handle(stream)))
+    a = array.array("Q", _reduce_ptrs(inputs, "inputs", n, dt))
+    b = array.array("Q", _reduce_ptrs(outputs, "outputs", n, dt))
+    _check(lib().dc_all_reduce(_addr(a), _addr(b), P, n, _dtype_code(inputs[0]), _order_code(order),
+                               _stream_handle(stream)))
     return outputs
 
 
@@ -303,10 +343,10 @@ def reduce_scatter(inputs: Sequence, outputs: Sequence, order: str = "linear", s
         raise ValueError(f"input length {n} is not divisible by P = {P}")
     C = n // P
     dt = inputs[0].dtype
-    _reduce_tensors(inputs, "inputs", n, dt)
-    _reduce_tensors(outputs, "outputs", C, dt)
-    _check(dc_reduce_scatter([t.data_ptr() for t in inputs], [t.data_ptr() for t in outputs], P, C,
-                             _dtype_code(inputs[0]), _order_code(order), _stream_handle(stream)))
+    a = array.array("Q", _reduce_ptrs(inputs, "inputs", n, dt))
+    b = array.array("Q", _reduce_ptrs(outputs, "outputs", C, dt))
+    _check(lib().dc_reduce_scatter(_addr(a), _addr(b), P, C, _dtype_code(inputs[0]),
+                                   _order_code(order), _stream_handle(stream)))
     return outputs
 
 
@@ -326,10 +366,8 @@ def _many(inputs_per_tensor, outputs_per_tensor, scatter: bool):
         if scatter and n % P:
             raise ValueError(f"tensor {t}: input length {n} is not divisible by P = {P}")
         c = n // P if scatter else n
-        _reduce_tensors(it, f"inputs[{t}]", n, dt)
-        _reduce_tensors(ot, f"outputs[{t}]", c, dt)
-        ins.extend(x.data_ptr() for x in it)
-        outs.extend(x.data_ptr() for x in ot)
+        ins.extend(_reduce_ptrs(it, f"inputs[{t}]", n, dt))
+        outs.extend(_reduce_ptrs(ot, f"outputs[{t}]", c, dt))
         counts.append(c)
     return ins, outs, counts, T, P
 

@@ -33,13 +33,16 @@ using namespace dc;
 thread_local char g_err[512] = "";
 std::atomic<unsigned long long> g_launches{0};
 
-// Single-CTA thresholds measured on GB300 (bench.py --crossover, CUDA events,
-// L2 flushed before every call): one CTA is as fast as the multi-CTA grid up
-// to 64 KiB of gathered output (P = 2 and P = 8) and slower from 128 KiB; for
-// the P = 8 all_reduce it is as fast up to 8 KiB of input per rank and slower
-// from 32 KiB.  Above these sizes every extra CTA adds bandwidth.
-constexpr long long kDefaultGatherSingleMax = 64 * 1024;
-constexpr long long kDefaultReduceSingleMax = 8 * 1024;
+// Single-CTA thresholds measured on GB300 (bench.py --crossover: per-call
+// time of 200 back-to-back calls in a CUDA graph, where differences of 0.1 us
+// show; a call timed alone after an L2 flush reads within one 2 us tick of
+// the event clock for both paths at these sizes).  Gather: one CTA is faster
+// up to 16 KiB of output (P = 2 and P = 8: 1.34 vs 1.39-1.45 us) and slower
+// from 32 KiB (1.77 vs 1.64 us; 2.5 vs 1.6 us at 64 KiB).  All_reduce (P = 8):
+// the grid is never slower, from 1 KiB per rank (1.86 vs 1.93 us) up, so the
+// single-CTA reduction is used only when forced.
+constexpr long long kDefaultGatherSingleMax = 16 * 1024;
+constexpr long long kDefaultReduceSingleMax = 0;
 
 struct Options {
   std::atomic<long long> force_path{0};
