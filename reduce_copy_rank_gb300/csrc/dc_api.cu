@@ -53,6 +53,7 @@ struct Options {
   std::atomic<long long> test_fail_launch{0};
   std::atomic<long long> pdl{1};
   std::atomic<long long> gather_staged{1};
+  std::atomic<long long> split_cost_pct{250};  // see plan_split
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -71,6 +72,7 @@ const OptionKey kKeys[] = {
     {"test_fail_launch", nullptr, &g_opt.test_fail_launch},
     {"pdl", "DC_PDL", &g_opt.pdl},
     {"gather_staged", "DC_GATHER_STAGED", &g_opt.gather_staged},
+    {"gather_split_cost_pct", "DC_GATHER_SPLIT_COST_PCT", &g_opt.split_cost_pct},
 };
 
 void read_env_once() {
@@ -105,7 +107,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 48;
+constexpr int kFamilies = 64;  // gather: family * 5 + mode (< 15); reductions: 16 + ...
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -183,34 +185,81 @@ struct GatherTensor {
   const void* const* peers;  // P pointers
 };
 
-// Fill jobs and sources of a gather parameter block from T tensors.
+bool tensor_aligned(const GatherTensor& g, int P, bool allow_flat) {
+  bool aligned = allow_flat && (g.out & 15u) == 0 && (g.bytes & 15u) == 0;
+  for (int r = 0; r < P && aligned; ++r)
+    aligned = (reinterpret_cast<uint64_t>(g.peers[r]) & 15u) == 0;
+  return aligned;
+}
+
+// Fill jobs and sources of a gather parameter block from T tensors.  The
+// aligned jobs come first (their vectors are [0, flat_vec)), then the rest;
+// each keeps its own output, so the order changes no result.
 template <class Params>
 void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_flat) {
   uint64_t v = 0;
   int nj = 0;
-  for (int t = 0; t < T; ++t) {
-    const GatherTensor& g = ts[t];
-    if (g.bytes == 0) continue;
-    GatherJob& J = prm.job[nj];
-    J.out = g.out;
-    J.bytes = g.bytes;
-    J.src0 = static_cast<uint32_t>(nj * P);
-    bool aligned = allow_flat && (g.out & 15u) == 0 && (g.bytes & 15u) == 0;
-    for (int r = 0; r < P; ++r) {
-      const uint64_t s = reinterpret_cast<uint64_t>(g.peers[r]);
-      prm.src[nj * P + r] = s;
-      aligned = aligned && (s & 15u) == 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int t = 0; t < T; ++t) {
+      const GatherTensor& g = ts[t];
+      if (g.bytes == 0) continue;
+      const bool aligned = tensor_aligned(g, P, allow_flat);
+      if (aligned != (pass == 0)) continue;
+      GatherJob& J = prm.job[nj];
+      J.out = g.out;
+      J.bytes = g.bytes;
+      J.src0 = static_cast<uint32_t>(nj * P);
+      for (int r = 0; r < P; ++r) prm.src[nj * P + r] = reinterpret_cast<uint64_t>(g.peers[r]);
+      J.flags = aligned ? kJobFlat : (g.bytes < kGatherSmallBytes ? kJobSmall : 0u);
+      const uint64_t end = g.out + static_cast<uint64_t>(P) * g.bytes;
+      J.nvec = ((end - 1) >> 4) - (g.out >> 4) + 1;
+      J.vfirst = v;
+      v += J.nvec;
+      ++nj;
     }
-    J.flags = aligned ? kJobFlat : (g.bytes < kGatherSmallBytes ? kJobSmall : 0u);
-    const uint64_t end = g.out + static_cast<uint64_t>(P) * g.bytes;
-    J.nvec = ((end - 1) >> 4) - (g.out >> 4) + 1;
-    J.vfirst = v;
-    v += J.nvec;
-    ++nj;
+    if (pass == 0) prm.flat_vec = v;
   }
   prm.njobs = nj;
   prm.P = P;
   prm.total_vec = v;
+}
+
+// Split of a launch's CTAs (at most `cap`) between the aligned jobs (tiles of
+// kSplitVectors vectors per thread) and the rest (tiles of
+// kGatherUnrollGeneral), in proportion to their work: a realigned 16-byte
+// vector counts gather_split_cost_pct / 100 staged ones, so both parts
+// finish together.  Measured on GB300 with the six mixed tensors of the
+// all_gather_many workload (P = 8): 100 % -> 141 us, 175 % -> 117 us,
+// 250 % -> 108.5 us, 300 % -> 112 us; one launch without the split: 139 us.  Each part gets the fewest
+// CTAs that finish its tiles in the same number of rounds.  Returns the total grid, 0 if no split
+// is possible (fewer than two CTAs for two parts).
+template <class Params>
+int plan_split(Params& prm, uint64_t cap) {
+  const uint64_t fv = prm.flat_vec, gv = prm.total_vec - prm.flat_vec;
+  const uint64_t ftile = static_cast<uint64_t>(kGatherBlock) * kSplitVectors;
+  const uint64_t gtile = static_cast<uint64_t>(kGatherBlock) * kGatherUnrollGeneral;
+  const uint64_t ft = (fv + ftile - 1) / ftile, gt = (gv + gtile - 1) / gtile;
+  uint64_t gf, gg;
+  if (gt == 0) {
+    gf = std::min(cap, ft);
+    gg = 0;
+  } else {
+    if (cap < 2) return 0;
+    const double cost = static_cast<double>(std::max(1LL, g_opt.split_cost_pct.load())) / 100.0;
+    const double wf = static_cast<double>(fv), wg = cost * static_cast<double>(gv);
+    gf = static_cast<uint64_t>(static_cast<double>(cap) * wf / (wf + wg) + 0.5);
+    gf = std::min(std::max<uint64_t>(gf, 1), cap - 1);
+    gg = cap - gf;
+  }
+  auto trim = [](uint64_t tiles, uint64_t g) {
+    if (g == 0) return g;
+    const uint64_t rounds = (tiles + g - 1) / g;
+    return (tiles + rounds - 1) / rounds;
+  };
+  gf = trim(ft, std::min(gf, ft));
+  gg = trim(gt, std::min(gg, gt));
+  prm.flat_ctas = static_cast<int32_t>(gf);
+  return static_cast<int>(gf + gg);
 }
 
 template <class Params>
@@ -224,14 +273,30 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   if (st != DC_OK) return st;
   const bool single = use_single(out_bytes, g_opt.gather_single_max.load());
   prm.staged = g_opt.gather_staged.load() ? 1 : 0;
+  prm.flat_ctas = 0;
   int grid = 1;
   if (!single) {
-    const int mode = gather_mode_of(prm);
-    const int fam = family * 4 + mode;
-    const int occ = occupancy(dev, fam, [family, mode] { return gather_ctas_per_sm(family, mode); });
-    const int unroll = mode == 0 ? kGatherUnrollGeneral : mode == 3 ? kStagedVectors : kGatherUnroll;
-    const uint64_t tile = static_cast<uint64_t>(kGatherBlock) * unroll;
-    grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
+    int mode = gather_mode_of(prm);
+    if (mode == kGatherModeSplit) {
+      const int occ = occupancy(dev, family * 5 + mode,
+                                [family, mode] { return gather_ctas_per_sm(family, mode); });
+      const long long forced = g_opt.grid_ctas.load();
+      const uint64_t cap = forced > 0 ? static_cast<uint64_t>(forced)
+                                      : static_cast<uint64_t>(sms) * static_cast<uint64_t>(occ);
+      grid = plan_split(prm, std::min<uint64_t>(cap, 0x7FFFFFFFull));
+      if (grid == 0) {  // one CTA cannot hold both parts: every CTA takes the realigning path
+        prm.staged = 0;
+        prm.flat_ctas = 0;
+        mode = gather_mode_of(prm);
+      }
+    }
+    if (mode != kGatherModeSplit) {
+      const int fam = family * 5 + mode;
+      const int occ = occupancy(dev, fam, [family, mode] { return gather_ctas_per_sm(family, mode); });
+      const int unroll = mode == 0 ? kGatherUnrollGeneral : mode == 3 ? kStagedVectors : kGatherUnroll;
+      const uint64_t tile = static_cast<uint64_t>(kGatherBlock) * unroll;
+      grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
+    }
   }
   return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather");
 }
@@ -342,7 +407,7 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
   int grid = 1;
   if (!single) {
     const int P = prm.P;
-    const int fam = 12 + (((dtype * 3 + variant) * 2 + order) * 2 + (P == 8 ? 1 : 0));
+    const int fam = 16 + (((dtype * 3 + variant) * 2 + order) * 2 + (P == 8 ? 1 : 0));
     const int occ = occupancy(dev, fam, [dtype, variant, order, P] {
       return reduce_ctas_per_sm(dtype, variant, order, P);
     });

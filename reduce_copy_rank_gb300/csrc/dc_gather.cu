@@ -29,6 +29,8 @@
 //    vectors that straddle two ranks or stick out of the output (at most P+1
 //    per job) are written byte by byte.
 //  * Jobs with fewer than kGatherSmallBytes per rank are copied byte by byte.
+#include <atomic>
+
 #include "dc_device.cuh"
 #include "dc_internal.h"
 
@@ -243,14 +245,71 @@ __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>&
   cp_async_wait<0>();
 }
 
+// The aligned jobs of a split launch (global vectors [0, flat_vec), jobs
+// ordered aligned first), staged like gather_tiles_staged but over a job
+// table: the issuing side walks jobs and ranks forward with a Cursor, the
+// draining side walks jobs only (it needs each vector's output address).
+template <int BLOCK, int V, int S, int MAXJ, int MAXS>
+__device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ, MAXS>& p,
+                                                         uint64_t first, uint64_t step) {
+  extern __shared__ uint4 stage_buf[];  // [S][V][BLOCK]
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
+  const uint64_t total = p.flat_vec;
+  const uint64_t ntiles = (total + kTile - 1) / kTile;
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
+  Cursor c{0, p.job[0].vfirst, p.job[0].vfirst + p.job[0].nvec, true, 0, 0, 0};
+  int jd = 0;
+  uint64_t dbeg = p.job[0].vfirst, dend = dbeg + p.job[0].nvec;
+  auto issue = [&](uint32_t slot, uint64_t t) {
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint64_t k = t * kTile + static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
+      if (t < ntiles && k < total) {
+        cursor_to_job(p, c, k);
+        cp_async16(sbase + 16u * BLOCK * (slot * V + u), flat_source(p, c, p.job[c.j], k - c.jbeg));
+      }
+    }
+    cp_async_commit();
+  };
+  uint64_t t_issue = first;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    issue(s, t_issue);
+    t_issue += step;
+  }
+  uint32_t slot = 0;
+  for (uint64_t t = first; t < ntiles; t += step) {
+    cp_async_wait<S - 1>();
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint64_t k = t * kTile + static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
+      if (k < total) {
+        while (k >= dend) {
+          ++jd;
+          dbeg = p.job[jd].vfirst;
+          dend = dbeg + p.job[jd].nvec;
+        }
+        st16(reinterpret_cast<uint4*>(p.job[jd].out) + (k - dbeg),
+             ld_shared16(sbase + 16u * BLOCK * (slot * V + u)));
+      }
+    }
+    issue(slot, t_issue);
+    t_issue += step;
+    slot = (slot + 1 == S) ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// voff: the tiles cover global vectors [voff, total_vec) (a split launch
+// gives the vectors below voff to other CTAs).
 template <int BLOCK, int UNROLL, bool FLAT, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
-                                             uint64_t step) {
+                                             uint64_t step, uint64_t voff = 0) {
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
-  const uint64_t ntiles = (p.total_vec + kTile - 1) / kTile;
+  const uint64_t ntiles = (p.total_vec - voff + kTile - 1) / kTile;
   Cursor c{0, p.job[0].vfirst, p.job[0].vfirst + p.job[0].nvec, true, 0, 0, 0};
   for (uint64_t t = first; t < ntiles; t += step) {
-    const uint64_t base = t * kTile + threadIdx.x;
+    const uint64_t base = voff + t * kTile + threadIdx.x;
     uint4 lo[UNROLL], hi[UNROLL];
     uint64_t dst[UNROLL];
     uint32_t meta[UNROLL];  // FLAT: unused; else shift | kind << 8 | rank << 16
@@ -316,8 +375,11 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
 }
 
 // Kernel modes: kGeneral (any jobs), kFlat (all jobs 16-byte aligned),
-// kFlat1 (one aligned job with fewer than 2^31 output vectors).
-enum Mode : int { kGeneral = 0, kFlat = 1, kFlat1 = 2, kFlat1Staged = 3 };
+// kFlat1 (one aligned job with fewer than 2^31 output vectors), kFlat1Staged
+// (the same through shared memory), kManySplit (several jobs, some aligned:
+// the first flat_ctas CTAs stage the aligned jobs, the others realign the
+// rest).
+enum Mode : int { kGeneral = 0, kFlat = 1, kFlat1 = 2, kFlat1Staged = 3, kManySplit = 4 };
 
 template <int BLOCK, int UNROLL, int MODE, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
@@ -328,7 +390,13 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
   else if constexpr (MODE == kFlat1Staged && MAXJ == 1)
     gather_tiles_staged<BLOCK, kStagedVectors, kStagedStages>(p, static_cast<uint32_t>(first),
                                                               static_cast<uint32_t>(step));
-  else
+  else if constexpr (MODE == kManySplit) {
+    const uint64_t fc = static_cast<uint64_t>(p.flat_ctas);
+    if (first < fc)
+      gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, first, fc);
+    else
+      gather_tiles<BLOCK, kGatherUnrollGeneral, false>(p, first - fc, step - fc, p.flat_vec);
+  } else
     gather_tiles<BLOCK, UNROLL, MODE != kGeneral>(p, first, step);
 }
 
@@ -350,10 +418,13 @@ __global__ void __launch_bounds__(MODE == kGeneral ? kGatherSingleBlockGeneral :
   gather_mode<kBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(p, 0, 1);
 }
 
+// The mode of a launch.  Jobs are ordered aligned first, so job 0 tells
+// whether any job is aligned and flat_vec == total_vec whether all are.
 template <int MAXJ, int MAXS>
 int mode_of(const GatherParams<MAXJ, MAXS>& p) {
-  for (int j = 0; j < p.njobs; ++j)
-    if (!(p.job[j].flags & kJobFlat)) return kGeneral;
+  const bool all_flat = p.flat_vec == p.total_vec;
+  if (MAXJ > 1 && p.staged && p.flat_vec > 0) return kManySplit;
+  if (!all_flat) return kGeneral;
   if (MAXJ == 1 && p.total_vec < (1ull << 31)) return p.staged ? kFlat1Staged : kFlat1;
   return kFlat;
 }
@@ -362,24 +433,65 @@ constexpr size_t staged_smem(int block) {
   return static_cast<size_t>(kStagedStages) * kStagedVectors * block * 16;
 }
 
+constexpr size_t split_smem(int block) {
+  return static_cast<size_t>(kSplitStages) * kSplitVectors * block * 16;
+}
+
+template <int MODE>
+constexpr size_t mode_smem() {
+  return MODE == kFlat1Staged ? staged_smem(kGatherBlock)
+                              : MODE == kManySplit ? split_smem(kGatherBlock) : 0;
+}
+
+// Kernels that ask for more than 48 KB of dynamic shared memory must say so
+// once per device (cudaFuncAttributeMaxDynamicSharedMemorySize).
+template <int MAXJ, int MAXS, int MODE>
+cudaError_t allow_smem() {
+  constexpr size_t smem = mode_smem<MODE>();
+  if constexpr (smem <= 48 * 1024) {
+    return cudaSuccess;
+  } else {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(dc_gather_kernel<MAXJ, MAXS, MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+}
+
 template <int MAXJ, int MAXS, int MODE>
 cudaError_t launch_mode(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, bool pdl,
                         cudaStream_t s) {
+  if (!single) {
+    const cudaError_t e = allow_smem<MAXJ, MAXS, MODE>();
+    if (e != cudaSuccess) return e;
+  }
   if (single) {  // small outputs: staging buys nothing, use the register path
-    constexpr int kMode = MODE == kFlat1Staged ? kFlat1 : MODE;
+    constexpr int kMode = MODE == kFlat1Staged ? kFlat1 : MODE == kManySplit ? kGeneral : MODE;
     constexpr int block = kMode == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock;
     return launch_ex(dc_gather_single_kernel<MAXJ, MAXS, kMode>, 1, block, pdl, s, p);
   }
   return launch_ex(dc_gather_kernel<MAXJ, MAXS, MODE>, grid, kGatherBlock, pdl, s, p,
-                   MODE == kFlat1Staged ? staged_smem(kGatherBlock) : 0);
+                   mode_smem<MODE>());
 }
 
 template <int MAXJ, int MAXS>
 cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, bool pdl,
                         cudaStream_t s) {
-  switch (mode_of(p)) {
+  int mode = mode_of(p);
+  if (mode == kManySplit && (single || p.flat_ctas < 1 || p.flat_ctas > grid))
+    mode = p.flat_vec == p.total_vec ? kFlat : kGeneral;  // no split: one path for every CTA
+  switch (mode) {
     case kGeneral: return launch_mode<MAXJ, MAXS, kGeneral>(p, grid, single, pdl, s);
     case kFlat: return launch_mode<MAXJ, MAXS, kFlat>(p, grid, single, pdl, s);
+    case kManySplit:
+      if constexpr (MAXJ > 1) return launch_mode<MAXJ, MAXS, kManySplit>(p, grid, single, pdl, s);
+      return cudaErrorInvalidValue;
     case kFlat1:
       if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
@@ -396,9 +508,16 @@ int occupancy_impl(int mode) {
   if (mode == kGeneral)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kGeneral>,
                                                       kGatherBlock, 0);
-  else if (mode == kFlat || MAXJ != 1)
+  else if (mode == kFlat || (MAXJ != 1 && mode != kManySplit))
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kFlat>,
                                                       kGatherBlock, 0);
+  else if (mode == kManySplit && MAXJ > 1) {
+    constexpr int kM = MAXJ == 1 ? kFlat : kManySplit;
+    e = allow_smem<MAXJ, MAXS, kM>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kM>,
+                                                        kGatherBlock, mode_smem<kM>());
+  }
   else if (mode == kFlat1)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &n, dc_gather_kernel<MAXJ, MAXS, MAXJ == 1 ? kFlat1 : kFlat>, kGatherBlock, 0);

@@ -28,6 +28,11 @@ constexpr int kGatherUnrollGeneral = 2;  // realigned vectors (up to two loads e
 // CTA, four CTAs = 192 KB in flight per SM, no registers held).
 constexpr int kStagedStages = 2;
 constexpr int kStagedVectors = 3;
+// all_gather_many with 16-byte aligned jobs: the aligned jobs are copied by
+// the first part of the grid through a deeper ring (the kernel also carries
+// the realigning path, so two CTAs fit per SM: 2 x 96 KB in flight).
+constexpr int kSplitStages = 3;
+constexpr int kSplitVectors = 4;
 constexpr int kReduceBlock = 256;
 constexpr int kReduceSingleBlock = 512;
 constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread
@@ -60,10 +65,11 @@ struct GatherJob {
 template <int MAXJ, int MAXS>
 struct GatherParams {
   uint64_t total_vec;   // sum of nvec over the jobs
+  uint64_t flat_vec;    // jobs are ordered aligned (kJobFlat) first: their vectors are [0, flat_vec)
   int32_t njobs;
   int32_t P;
-  int32_t staged;       // aligned single job: stage through shared memory with cp.async
-  int32_t pad;
+  int32_t staged;       // stage aligned copies through shared memory with cp.async
+  int32_t flat_ctas;    // split launch: CTAs [0, flat_ctas) copy the aligned jobs
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
 };
@@ -178,7 +184,9 @@ cudaError_t launch_ex(Kernel kernel, int grid, int block, bool pdl, cudaStream_t
 // Resident CTAs per SM of the multi-CTA kernels (occupancy API, per device).
 int gather_ctas_per_sm(int which, int mode);  // which: 0 one job, 1 small many, 2 large many
 // Kernel mode a launch will use: 0 general, 1 aligned jobs, 2 one aligned job,
-// 3 one aligned job staged through shared memory.
+// 3 one aligned job staged through shared memory, 4 (kGatherModeSplit) several
+// jobs, the aligned ones staged by the first flat_ctas CTAs.
+constexpr int kGatherModeSplit = 4;
 int gather_mode_of(const GatherParams1& p);
 int gather_mode_of(const GatherParamsS& p);
 int gather_mode_of(const GatherParamsL& p);

@@ -77,6 +77,40 @@ def test_many_random_layouts():
         assert guards
 
 
+@pytest.mark.parametrize("opts", [{}, {"grid_ctas": 1}, {"grid_ctas": 2}, {"grid_ctas": 3},
+                                  {"grid_ctas": 7}, {"grid_ctas": 5000}, {"gather_staged": 0},
+                                  {"force_path": 2, "grid_ctas": 2}],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "default")
+def test_many_split_aligned_and_unaligned(opts):
+    """Aligned and unaligned tensors interleaved: the aligned ones are staged
+    by the first part of the grid, the others realigned by the rest; every
+    grid size (one CTA falls back to one path) gives the same bytes."""
+    rng = np.random.default_rng(W.seed_for(5, 9002))
+    P = 8
+    sizes = [4096, 100003, 65536, 7, 1 << 20, 33, 300000 + 16, 129]
+    tensors = [[rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)] for B in sizes]
+    in_offs = [[0] * P if B % 16 == 0 else [int(x) for x in rng.integers(0, 16, P)] for B in sizes]
+    out_offs = [0 if B % 16 == 0 else int(rng.integers(1, 16)) for B in sizes]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, in_offs, out_offs, **opts)
+    for t in range(len(sizes)):
+        assert np.array_equal(got[t], want[t]), (t, opts)
+    assert guards
+
+
+@pytest.mark.parametrize("grid", [0, 1, 2, 5, 5000])
+def test_many_all_aligned(grid):
+    rng = np.random.default_rng(W.seed_for(5, 9003))
+    P = 4
+    sizes = [16, 4096, 1 << 20, 48, 262144 + 32]
+    tensors = [[rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)] for B in sizes]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, [[0] * P] * len(sizes), [0] * len(sizes), grid_ctas=grid)
+    for t in range(len(sizes)):
+        assert np.array_equal(got[t], want[t]), (t, grid)
+    assert guards
+
+
 def test_many_large_table():
     """More tensors than the small parameter block holds (T=100, P=8)."""
     rng = np.random.default_rng(W.seed_for(5, 9001))
