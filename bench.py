@@ -85,7 +85,8 @@ def parse_args(argv=None):
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
     ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
                     help="profiling helper: run one call REPS times and exit, e.g. "
-                         "gather:8:4194304:3 or allreduce:8:268435456:2 (BYTES per rank)")
+                         "gather:8:4194304:3, allreduce:8:268435456:2 (BYTES per rank) or "
+                         "many:8:0:3 (the all_gather_many workload)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps must be >= 1 and --warmup >= 0")
@@ -890,6 +891,11 @@ def run_case(args) -> int:
         ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
         outs = [torch.empty_like(x) for x in ins]
         fn = lambda: dc.all_reduce(ins, outs)  # noqa: E731
+    elif op == "many":  # the all_gather_many workload (six mixed tensors); BYTES unused
+        tens = [[W.random_bytes_device(W.seed_for(5, 1), r, B, device, tensor=t) for r in range(P)]
+                for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
+        outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in W.CONFIG5_MANY_SIZES]
+        fn = lambda: dc.all_gather_many(tens, outs)  # noqa: E731
     elif op == "reducescatter":
         ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
         outs = [torch.empty(nbytes // 2 // P, dtype=torch.bfloat16, device=device) for _ in range(P)]
