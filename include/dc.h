@@ -214,11 +214,15 @@ const char *dc_status_name(int status);
  *                             tensors: cost of a realigned 16-byte vector in
  *                             percent of a staged aligned one, for splitting
  *                             the grid between the two (default 250, measured)
+ *   "prefetch"                tiles per CTA whose inputs are prefetched into
+ *                             L2 before the kernel waits for the previous
+ *                             kernel in the stream (single aligned gathers and
+ *                             reductions; 0 = off; default 1)
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
  * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
- * DC_GATHER_STAGED and DC_GATHER_SPLIT_COST_PCT set the initial values (read
- * once, at the first call).
+ * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT and DC_PREFETCH set the initial
+ * values (read once, at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.
  */

@@ -54,6 +54,7 @@ struct Options {
   std::atomic<long long> pdl{1};
   std::atomic<long long> gather_staged{1};
   std::atomic<long long> split_cost_pct{250};  // see plan_split
+  std::atomic<long long> prefetch{1};
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -73,6 +74,7 @@ const OptionKey kKeys[] = {
     {"pdl", "DC_PDL", &g_opt.pdl},
     {"gather_staged", "DC_GATHER_STAGED", &g_opt.gather_staged},
     {"gather_split_cost_pct", "DC_GATHER_SPLIT_COST_PCT", &g_opt.split_cost_pct},
+    {"prefetch", "DC_PREFETCH", &g_opt.prefetch},
 };
 
 void read_env_once() {
@@ -273,6 +275,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   if (st != DC_OK) return st;
   const bool single = use_single(out_bytes, g_opt.gather_single_max.load());
   prm.staged = g_opt.gather_staged.load() ? 1 : 0;
+  prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.flat_ctas = 0;
   int grid = 1;
   if (!single) {
@@ -404,6 +407,7 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
   st = sm_count(dev, &sms);
   if (st != DC_OK) return st;
   const bool single = use_single(in_bytes_per_rank, g_opt.reduce_single_max.load());
+  prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   int grid = 1;
   if (!single) {
     const int P = prm.P;

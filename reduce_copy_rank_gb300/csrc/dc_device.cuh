@@ -20,6 +20,20 @@ __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The two halves of pdl_enter, for kernels that do something before the wait.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Bulk prefetch of [p, p + bytes) from HBM into L2 (p 16-byte aligned, bytes a
+// multiple of 16).  It moves data between HBM and L2 only; L2 is where every
+// SM's loads and stores meet, so a later load still sees any store made in
+// between, and the prefetch may be issued before griddepcontrol.wait.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Streaming 16-byte load through the read-only path without allocating in
 // L1: each source byte of an aligned copy is read exactly once.  Only for
 // data that no thread writes during the launch (gather sources).

@@ -400,11 +400,43 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     gather_tiles<BLOCK, UNROLL, MODE != kGeneral>(p, first, step);
 }
 
+// One aligned job: the source bytes of output vectors [k, kend) (one
+// segment per rank they cross) prefetched into L2.  Issued before the PDL
+// wait, the HBM latency of the first tile overlaps the end of the previous
+// kernel in the stream.
+template <int MAXS>
+__device__ __forceinline__ void prefetch_vectors(const GatherParams<1, MAXS>& p, uint64_t k,
+                                                 uint64_t kend) {
+  constexpr uint64_t kMaxVec = 2048;  // at most 32 KiB per prefetch instruction
+  const uint64_t vp = p.job[0].bytes >> 4;
+  kend = kend < p.total_vec ? kend : p.total_vec;
+  while (k < kend) {
+    const uint64_t r = k / vp;
+    uint64_t seg = (r + 1) * vp < kend ? (r + 1) * vp : kend;
+    seg = seg - k > kMaxVec ? k + kMaxVec : seg;
+    prefetch_l2(reinterpret_cast<const uint4*>(p.src[r]) + (k - r * vp),
+                static_cast<uint32_t>((seg - k) * 16));
+    k = seg;
+  }
+}
+
 // Multi-CTA gather: CTA c copies tiles c, c + gridDim.x, ...
 template <int MAXJ, int MAXS, int MODE>
 __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat1Staged) ? 4 : 2)
     dc_gather_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
-  pdl_enter();
+  if constexpr (MAXJ == 1 && (MODE == kFlat1 || MODE == kFlat1Staged)) {
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {  // the CTA's first p.prefetch tiles
+      constexpr uint64_t kTile = static_cast<uint64_t>(kGatherBlock) *
+                                 (MODE == kFlat1Staged ? kStagedVectors : kGatherUnroll);
+      uint64_t t = blockIdx.x;
+      for (int i = 0; i < p.prefetch && t * kTile < p.total_vec; ++i, t += gridDim.x)
+        prefetch_vectors(p, t * kTile, (t + 1) * kTile);
+    }
+    pdl_wait();
+  } else {
+    pdl_enter();
+  }
   gather_mode<kGatherBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(
       p, blockIdx.x, gridDim.x);
 }
@@ -414,7 +446,18 @@ template <int MAXJ, int MAXS, int MODE>
 __global__ void __launch_bounds__(MODE == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock)
     dc_gather_single_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
   constexpr int kBlock = MODE == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock;
-  pdl_enter();
+  if constexpr (MAXJ == 1 && MODE == kFlat1) {
+    pdl_launch_dependents();
+    if (p.prefetch && threadIdx.x < static_cast<unsigned>(p.P)) {
+      // thread r: the start of rank r's payload (all of it below 32 KiB)
+      const uint64_t vp = p.job[0].bytes >> 4;
+      const uint64_t k = threadIdx.x * vp;
+      prefetch_vectors(p, k, k + (vp < 2048 ? vp : 2048));
+    }
+    pdl_wait();
+  } else {
+    pdl_enter();
+  }
   gather_mode<kBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(p, 0, 1);
 }
 

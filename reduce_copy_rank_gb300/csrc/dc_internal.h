@@ -70,6 +70,8 @@ struct GatherParams {
   int32_t P;
   int32_t staged;       // stage aligned copies through shared memory with cp.async
   int32_t flat_ctas;    // split launch: CTAs [0, flat_ctas) copy the aligned jobs
+  int32_t prefetch;     // one aligned job: tiles per CTA prefetched into L2 before the PDL wait
+  int32_t pad;
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
 };
@@ -113,6 +115,8 @@ struct ReduceParams {
   uint64_t total_units;
   int32_t njobs;
   int32_t P;
+  int32_t prefetch;     // tiles per CTA whose inputs are prefetched into L2 before the PDL wait
+  int32_t pad;
   uint64_t ptr[MAXPTR];
   ReduceJob job[MAXJ];
 };

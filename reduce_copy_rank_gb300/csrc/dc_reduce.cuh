@@ -310,17 +310,52 @@ __device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ, MAXPTR>& p
   }
 }
 
+// The 16-byte input vectors of tile t prefetched into L2, thread q < P
+// taking rank q (one bulk prefetch per job the tile overlaps; scalar heads
+// and tails are left out).  Issued before the PDL wait, so the HBM latency
+// of the first tiles overlaps the end of the previous kernel in the stream.
+template <int DT, int BLOCK, int UNROLL, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MAXPTR>& p,
+                                                     uint64_t t) {
+  using T = Elem<DT>;
+  constexpr int E = T::kPerVec;
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
+  const uint64_t g0 = t * kTile;
+  if (g0 >= p.total_units || threadIdx.x >= static_cast<unsigned>(p.P)) return;
+  const uint64_t g1 = min(g0 + kTile, p.total_units);
+  for (int jj = 0; jj < p.njobs && p.job[jj].ufirst < g1; ++jj) {
+    const ReduceJob& J = p.job[jj];
+    if (J.ufirst + J.nunits <= g0 || !(J.flags & kJobVec)) continue;
+    const uint64_t hu = J.head ? 1 : 0;
+    const uint64_t body_end = hu + (J.count - J.head) / E;
+    const uint64_t a = max(max(g0, J.ufirst) - J.ufirst, hu);
+    const uint64_t b = min(min(g1, J.ufirst + J.nunits) - J.ufirst, body_end);
+    if (a >= b) continue;
+    prefetch_l2(in_ptr(p, J, threadIdx.x) + (J.in_off + J.head + E * (a - hu)) * T::kSize,
+                static_cast<uint32_t>((b - a) * 16));
+  }
+}
+
+template <int DT, int BLOCK, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void reduce_enter(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t first,
+                                             uint64_t step) {
+  pdl_launch_dependents();
+  for (int i = 0; i < p.prefetch; ++i)
+    reduce_prefetch_tile<DT, BLOCK, kReduceUnroll>(p, first + static_cast<uint64_t>(i) * step);
+  pdl_wait();
+}
+
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceBlock)
     dc_reduce_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
-  pdl_enter();
+  reduce_enter<DT, kReduceBlock>(p, blockIdx.x, gridDim.x);
   reduce_tiles<DT, ORDER, kReduceBlock, kReduceUnroll, PT>(p, blockIdx.x, gridDim.x);
 }
 
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceSingleBlock)
     dc_reduce_single_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
-  pdl_enter();
+  reduce_enter<DT, kReduceSingleBlock>(p, 0, 1);
   reduce_tiles<DT, ORDER, kReduceSingleBlock, kReduceUnroll, PT>(p, 0, 1);
 }
 
