@@ -85,7 +85,8 @@ def parse_args(argv=None):
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
     ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
                     help="profiling helper: run one call REPS times and exit, e.g. "
-                         "gather:8:4194304:3, allreduce:8:268435456:2 (BYTES per rank) or "
+                         "gather:8:4194304:3, ugather:8:4194305:3 (unaligned), "
+                         "allreduce:8:268435456:2 (BYTES per rank) or "
                          "many:8:0:3 (the all_gather_many workload)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
@@ -886,6 +887,11 @@ def run_case(args) -> int:
     if op == "gather":
         peers = [torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=device) for _ in range(P)]
         out = torch.empty(P * nbytes, dtype=torch.uint8, device=device)
+        fn = lambda: dc.all_gather(peers, out)  # noqa: E731
+    elif op == "ugather":  # unaligned: every payload starts 1 byte, the output 3 bytes past 16
+        peers = [torch.randint(0, 256, (nbytes + 1,), dtype=torch.uint8, device=device)[1:]
+                 for _ in range(P)]
+        out = torch.empty(P * nbytes + 3, dtype=torch.uint8, device=device)[3:]
         fn = lambda: dc.all_gather(peers, out)  # noqa: E731
     elif op == "allreduce":
         ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]

@@ -109,7 +109,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 64;  // gather: family * 5 + mode (< 15); reductions: 16 + ...
+constexpr int kFamilies = 64;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + ...
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -281,7 +281,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   if (!single) {
     int mode = gather_mode_of(prm);
     if (mode == kGatherModeSplit) {
-      const int occ = occupancy(dev, family * 5 + mode,
+      const int occ = occupancy(dev, family * kGatherModes + mode,
                                 [family, mode] { return gather_ctas_per_sm(family, mode); });
       const long long forced = g_opt.grid_ctas.load();
       const uint64_t cap = forced > 0 ? static_cast<uint64_t>(forced)
@@ -294,9 +294,12 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       }
     }
     if (mode != kGatherModeSplit) {
-      const int fam = family * 5 + mode;
+      const int fam = family * kGatherModes + mode;
       const int occ = occupancy(dev, fam, [family, mode] { return gather_ctas_per_sm(family, mode); });
-      const int unroll = mode == 0 ? kGatherUnrollGeneral : mode == 3 ? kStagedVectors : kGatherUnroll;
+      const int unroll = mode == 0   ? kGatherUnrollGeneral
+                         : mode == 3 ? kStagedVectors
+                         : mode == 5 ? kRealignVectors
+                                     : kGatherUnroll;
       const uint64_t tile = static_cast<uint64_t>(kGatherBlock) * unroll;
       grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
     }
@@ -411,7 +414,7 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
   int grid = 1;
   if (!single) {
     const int P = prm.P;
-    const int fam = 16 + (((dtype * 3 + variant) * 2 + order) * 2 + (P == 8 ? 1 : 0));
+    const int fam = 24 + (((dtype * 3 + variant) * 2 + order) * 2 + (P == 8 ? 1 : 0));
     const int occ = occupancy(dev, fam, [dtype, variant, order, P] {
       return reduce_ctas_per_sm(dtype, variant, order, P);
     });

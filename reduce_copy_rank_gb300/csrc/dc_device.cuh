@@ -100,6 +100,11 @@ __device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uin
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
 }
+// The same through L1 (.ca): a block that neighbouring threads both copy is
+// fetched from L2 once.
+__device__ __forceinline__ void cp_async16_ca(uint32_t smem_addr, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

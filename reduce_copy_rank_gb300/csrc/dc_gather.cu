@@ -300,6 +300,164 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
   cp_async_wait<0>();
 }
 
+// A vector at a rank boundary of a job of at least kGatherSmallBytes per rank
+// (x 16-byte aligned, r the rank of byte x; x may lie before the output or
+// the vector stick out of its end).  Its bytes come from the end of rank r's
+// payload and the start of rank r+1's: all 16 byte loads are issued before
+// the first store, so the vector costs one memory latency instead of one per
+// byte, and a vector inside the output is written with one 16-byte store.
+template <int MAXS>
+__device__ __forceinline__ void copy_boundary(const GatherParams<1, MAXS>& p, const GatherJob& J,
+                                              uint64_t x, uint32_t r) {
+  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
+  const uint64_t d = J.out + static_cast<uint64_t>(r) * J.bytes;  // first output byte of rank r
+  const uint8_t* s0 = reinterpret_cast<const uint8_t*>(p.src[r]);
+  const uint8_t* s1 = r + 1 < static_cast<uint32_t>(p.P) ? reinterpret_cast<const uint8_t*>(p.src[r + 1]) : s0;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (uint32_t i = 0; i < 16; ++i) {
+    const uint64_t y = x + i;
+    if (y < J.out || y >= out_end) continue;
+    const uint32_t b = y < d + J.bytes ? __ldg(s0 + (y - d)) : __ldg(s1 + (y - d - J.bytes));
+    w[i >> 2] |= b << (8u * (i & 3u));
+  }
+  if (x >= J.out && x + 16 <= out_end) {
+    st16(reinterpret_cast<uint4*>(x), make_uint4(w[0], w[1], w[2], w[3]));
+    return;
+  }
+#pragma unroll
+  for (uint32_t i = 0; i < 16; ++i) {
+    const uint64_t y = x + i;
+    if (y >= J.out && y < out_end)
+      *reinterpret_cast<uint8_t*>(y) = static_cast<uint8_t>(w[i >> 2] >> (8u * (i & 3u)));
+  }
+}
+
+// Forward walk over the ranks of one unaligned job, in output-vector units.
+// Output vector k is x(k) = xbase + 16k, xbase = out rounded down to 16.
+// Rank r owns output bytes [d, d + B), d = out + r*B; the vectors wholly
+// inside it are k in [klo, khi), klo = ceil((d - xbase)/16), khi =
+// floor((d + B - xbase)/16).  For those the source start is src_r + x(k) -
+// d, whose offset in its 16-byte block, s = (src_r + xbase - d) mod 16, is
+// the same for every k, and whose block is base + k with base = (src_r +
+// xbase - d - s) / 16: all of it computed once per rank.  The vectors in
+// between (k < klo, or k >= khi in the last rank) straddle two ranks or an
+// end of the output.
+template <typename Idx>
+struct RankWalk {
+  uint32_t r;
+  uint32_t s;
+  Idx klo, khi;
+  uint64_t base;  // block address of vector k: base + 16k, formed only for k in [klo, khi)
+  bool fresh;
+};
+
+template <typename Idx, int MAXS>
+__device__ __forceinline__ void rank_enter(RankWalk<Idx>& w, const GatherParams<1, MAXS>& p,
+                                           const GatherJob& J, uint64_t xbase) {
+  const uint64_t d = J.out + static_cast<uint64_t>(w.r) * J.bytes;
+  w.klo = static_cast<Idx>((d - xbase + 15) >> 4);
+  w.khi = static_cast<Idx>((d + J.bytes - xbase) >> 4);
+  const uint64_t a = p.src[w.r] + xbase - d;  // source address that x(0) would map to
+  w.s = static_cast<uint32_t>(a & 15u);
+  w.base = a - w.s;  // modulo 2^64: it may lie outside every allocation
+}
+
+// Idx is uint32_t when the whole output (from out rounded down to 16) is
+// under 4 GiB, so that 16k and every rank size fit 32 bits.
+template <typename Idx, int MAXS>
+__device__ __forceinline__ void walk_to(RankWalk<Idx>& w, const GatherParams<1, MAXS>& p,
+                                        const GatherJob& J, uint64_t xbase, Idx k) {
+  if (w.fresh) {
+    const Idx lead = static_cast<Idx>(J.out - xbase);  // output bytes before out in vector 0
+    const Idx x = static_cast<Idx>(16) * k;            // relative to xbase
+    w.r = static_cast<uint32_t>((x > lead ? x - lead : Idx(0)) / static_cast<Idx>(J.bytes));
+    rank_enter(w, p, J, xbase);
+    w.fresh = false;
+  }
+  while (k >= w.khi && w.r + 1 < static_cast<uint32_t>(p.P)) {
+    ++w.r;
+    rank_enter(w, p, J, xbase);
+  }
+}
+
+// One unaligned job (at least kGatherSmallBytes per rank), staged through
+// shared memory.  Issuing side (rank walk above): vector k inside rank r
+// copies block base + k and, if s != 0, the next one (both hold source bytes
+// of the vector, so both lie in the source allocation) with cp.async into
+// the thread's ring slot, and notes s and "inside one rank" in 5 bits of a
+// register (S*V*5 <= 32 bits).  Draining side: the funnel shift of the two
+// blocks by s gives the 16 output bytes, one 16-byte store; a vector at a
+// rank boundary or an output end finds its rank by one division (at most
+// P+1 such vectors per job) and goes through copy_boundary.  No barrier:
+// each thread reads back only the slots it filled.
+template <int BLOCK, int V, int S, typename Idx, int MAXS>
+__device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1, MAXS>& p,
+                                                            Idx first, Idx step) {
+  static_assert(S * V * 5 <= 32, "ring notes must fit one register");
+  extern __shared__ uint4 stage_buf[];  // [S][V][2][BLOCK]
+  const GatherJob& J = p.job[0];
+  constexpr Idx kTile = static_cast<Idx>(BLOCK) * V;
+  const Idx total = static_cast<Idx>(p.total_vec);
+  const Idx ntiles = (total + kTile - 1) / kTile;
+  const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
+  uint4* const out = reinterpret_cast<uint4*>(xbase);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
+  RankWalk<Idx> w{0, 0, 0, 0, 0, true};
+  uint32_t notes = 0;  // 5 bits per ring vector: s | inside << 4
+  auto slot_addr = [&](uint32_t slot, int u, int h) {
+    return sbase + 16u * BLOCK * static_cast<uint32_t>((slot * V + u) * 2 + h);
+  };
+  auto issue = [&](uint32_t slot, Idx t) {
+    notes &= ~(((1u << (5 * V)) - 1u) << (5 * V * slot));
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const Idx k = t * kTile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
+      if (t < ntiles && k < total) {
+        walk_to(w, p, J, xbase, k);
+        if (k >= w.klo && k < w.khi) {
+          const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * static_cast<uint64_t>(k));
+          cp_async16_ca(slot_addr(slot, u, 0), blk);  // block k+1 of a thread is
+          if (w.s) cp_async16_ca(slot_addr(slot, u, 1), blk + 1);  // block k of its neighbour
+          notes |= (w.s | 16u) << (5 * (slot * V + u));
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  Idx t_issue = first;
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    issue(i, t_issue);
+    t_issue += step;
+  }
+  uint32_t slot = 0;
+  for (Idx t = first; t < ntiles; t += step) {
+    cp_async_wait<S - 1>();
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const Idx k = t * kTile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
+      if (k < total) {
+        const uint32_t m = (notes >> (5 * (slot * V + u))) & 31u;
+        if (m & 16u) {
+          const uint32_t sh = m & 15u;
+          const uint4 lo = ld_shared16(slot_addr(slot, u, 0));
+          const uint4 hi = sh ? ld_shared16(slot_addr(slot, u, 1)) : lo;
+          st16(out + k, realign16(lo, hi, sh));
+        } else {
+          const uint64_t x = xbase + 16 * static_cast<uint64_t>(k);
+          const uint32_t r = x < J.out ? 0u : static_cast<uint32_t>((x - J.out) / J.bytes);
+          copy_boundary(p, J, x, r);
+        }
+      }
+    }
+    issue(slot, t_issue);
+    t_issue += step;
+    slot = (slot + 1 == S) ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
 // voff: the tiles cover global vectors [voff, total_vec) (a split launch
 // gives the vectors below voff to other CTAs).
 template <int BLOCK, int UNROLL, bool FLAT, int MAXJ, int MAXS>
@@ -379,7 +537,14 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
 // (the same through shared memory), kManySplit (several jobs, some aligned:
 // the first flat_ctas CTAs stage the aligned jobs, the others realign the
 // rest).
-enum Mode : int { kGeneral = 0, kFlat = 1, kFlat1 = 2, kFlat1Staged = 3, kManySplit = 4 };
+enum Mode : int {
+  kGeneral = 0,
+  kFlat = 1,
+  kFlat1 = 2,
+  kFlat1Staged = 3,
+  kManySplit = 4,
+  kGeneral1Staged = 5,  // one unaligned job (>= kGatherSmallBytes per rank) through shared memory
+};
 
 template <int BLOCK, int UNROLL, int MODE, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
@@ -390,6 +555,14 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
   else if constexpr (MODE == kFlat1Staged && MAXJ == 1)
     gather_tiles_staged<BLOCK, kStagedVectors, kStagedStages>(p, static_cast<uint32_t>(first),
                                                               static_cast<uint32_t>(step));
+  else if constexpr (MODE == kGeneral1Staged && MAXJ == 1) {
+    const uint64_t span = p.total_vec * 16;  // output bytes from out rounded down to 16
+    if (span < (1ull << 32) && p.job[0].bytes < (1ull << 32))
+      gather_tiles_staged_realign<BLOCK, kRealignVectors, kRealignStages, uint32_t>(
+          p, static_cast<uint32_t>(first), static_cast<uint32_t>(step));
+    else
+      gather_tiles_staged_realign<BLOCK, kRealignVectors, kRealignStages, uint64_t>(p, first, step);
+  }
   else if constexpr (MODE == kManySplit) {
     const uint64_t fc = static_cast<uint64_t>(p.flat_ctas);
     if (first < fc)
@@ -422,7 +595,9 @@ __device__ __forceinline__ void prefetch_vectors(const GatherParams<1, MAXS>& p,
 
 // Multi-CTA gather: CTA c copies tiles c, c + gridDim.x, ...
 template <int MAXJ, int MAXS, int MODE>
-__global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat1Staged) ? 4 : 2)
+__global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat1Staged) ? 4
+                                                : MODE == kGeneral1Staged             ? 3
+                                                                                      : 2)
     dc_gather_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
   if constexpr (MAXJ == 1 && (MODE == kFlat1 || MODE == kFlat1Staged)) {
     pdl_launch_dependents();
@@ -467,7 +642,8 @@ template <int MAXJ, int MAXS>
 int mode_of(const GatherParams<MAXJ, MAXS>& p) {
   const bool all_flat = p.flat_vec == p.total_vec;
   if (MAXJ > 1 && p.staged && p.flat_vec > 0) return kManySplit;
-  if (!all_flat) return kGeneral;
+  if (!all_flat)
+    return MAXJ == 1 && p.staged && !(p.job[0].flags & kJobSmall) ? kGeneral1Staged : kGeneral;
   if (MAXJ == 1 && p.total_vec < (1ull << 31)) return p.staged ? kFlat1Staged : kFlat1;
   return kFlat;
 }
@@ -480,10 +656,16 @@ constexpr size_t split_smem(int block) {
   return static_cast<size_t>(kSplitStages) * kSplitVectors * block * 16;
 }
 
+constexpr size_t realign_smem(int block) {
+  return static_cast<size_t>(kRealignStages) * kRealignVectors * 2 * block * 16;
+}
+
 template <int MODE>
 constexpr size_t mode_smem() {
-  return MODE == kFlat1Staged ? staged_smem(kGatherBlock)
-                              : MODE == kManySplit ? split_smem(kGatherBlock) : 0;
+  return MODE == kFlat1Staged      ? staged_smem(kGatherBlock)
+         : MODE == kManySplit      ? split_smem(kGatherBlock)
+         : MODE == kGeneral1Staged ? realign_smem(kGatherBlock)
+                                   : 0;
 }
 
 // Kernels that ask for more than 48 KB of dynamic shared memory must say so
@@ -515,7 +697,9 @@ cudaError_t launch_mode(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
     if (e != cudaSuccess) return e;
   }
   if (single) {  // small outputs: staging buys nothing, use the register path
-    constexpr int kMode = MODE == kFlat1Staged ? kFlat1 : MODE == kManySplit ? kGeneral : MODE;
+    constexpr int kMode = MODE == kFlat1Staged ? kFlat1
+                          : (MODE == kManySplit || MODE == kGeneral1Staged) ? kGeneral
+                                                                            : MODE;
     constexpr int block = kMode == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock;
     return launch_ex(dc_gather_single_kernel<MAXJ, MAXS, kMode>, 1, block, pdl, s, p);
   }
@@ -535,6 +719,9 @@ cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
     case kManySplit:
       if constexpr (MAXJ > 1) return launch_mode<MAXJ, MAXS, kManySplit>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
+    case kGeneral1Staged:
+      if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kGeneral1Staged>(p, grid, single, pdl, s);
+      return cudaErrorInvalidValue;
     case kFlat1:
       if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
@@ -551,10 +738,16 @@ int occupancy_impl(int mode) {
   if (mode == kGeneral)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kGeneral>,
                                                       kGatherBlock, 0);
-  else if (mode == kFlat || (MAXJ != 1 && mode != kManySplit))
+  else if (mode == kFlat || (MAXJ != 1 && mode != kManySplit) || (MAXJ != 1 && mode == kGeneral1Staged))
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kFlat>,
                                                       kGatherBlock, 0);
-  else if (mode == kManySplit && MAXJ > 1) {
+  else if (mode == kGeneral1Staged && MAXJ == 1) {
+    constexpr int kM = MAXJ == 1 ? kGeneral1Staged : kGeneral;
+    e = allow_smem<MAXJ, MAXS, kM>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kM>,
+                                                        kGatherBlock, mode_smem<kM>());
+  } else if (mode == kManySplit && MAXJ > 1) {
     constexpr int kM = MAXJ == 1 ? kFlat : kManySplit;
     e = allow_smem<MAXJ, MAXS, kM>();
     if (e == cudaSuccess)

@@ -33,6 +33,12 @@ constexpr int kStagedVectors = 3;
 // the realigning path, so two CTAs fit per SM: 2 x 96 KB in flight).
 constexpr int kSplitStages = 3;
 constexpr int kSplitVectors = 4;
+// One unaligned job staged through shared memory: per thread kRealignStages
+// slots of kRealignVectors output vectors, each with the two aligned source
+// blocks it is cut from (2 x 2 x 2 x 512 x 16 B = 64 KB per CTA, three CTAs
+// per SM).
+constexpr int kRealignStages = 2;
+constexpr int kRealignVectors = 2;
 constexpr int kReduceBlock = 256;
 constexpr int kReduceSingleBlock = 512;
 constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread
@@ -189,8 +195,10 @@ cudaError_t launch_ex(Kernel kernel, int grid, int block, bool pdl, cudaStream_t
 int gather_ctas_per_sm(int which, int mode);  // which: 0 one job, 1 small many, 2 large many
 // Kernel mode a launch will use: 0 general, 1 aligned jobs, 2 one aligned job,
 // 3 one aligned job staged through shared memory, 4 (kGatherModeSplit) several
-// jobs, the aligned ones staged by the first flat_ctas CTAs.
+// jobs, the aligned ones staged by the first flat_ctas CTAs, 5 one unaligned
+// job staged through shared memory.
 constexpr int kGatherModeSplit = 4;
+constexpr int kGatherModes = 6;
 int gather_mode_of(const GatherParams1& p);
 int gather_mode_of(const GatherParamsS& p);
 int gather_mode_of(const GatherParamsL& p);

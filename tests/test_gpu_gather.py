@@ -153,14 +153,16 @@ def test_independent_per_rank_offsets():
     {"force_generic": 1, "force_path": 1},
     {"gather_staged": 1}, {"gather_staged": 1, "force_path": 2, "grid_ctas": 3},
     {"gather_staged": 1, "force_path": 2, "grid_ctas": 7000}, {"gather_staged": 1, "force_path": 1},
-    {"pdl": 0},
+    {"pdl": 0}, {"gather_staged": 0}, {"gather_staged": 0, "force_path": 2, "grid_ctas": 3},
+    {"prefetch": 0}, {"prefetch": 4, "force_path": 2, "grid_ctas": 2},
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_path_and_grid_independence(opts):
     """The bytes never depend on the path, the grid or the flat/generic
     choice (aligned and unaligned layouts)."""
     rng = np.random.default_rng(W.seed_for(2, 9003))
     for (P, B, io, oo) in [(8, 64 * 1024, 0, 0), (2, 200000, 0, 0), (3, 65537, 1, 8),
-                           (8, 4096 + 5, 15, 0), (5, 1 << 20, 8, 8)]:
+                           (8, 4096 + 5, 15, 0), (5, 1 << 20, 8, 8), (4, 300000 + 3, 7, 9),
+                           (2, 128, 3, 5), (64, 129, 1, 0)]:
         peers = [rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)]
         want = oracle.all_gather(peers)
         got, guards = run_gather(peers, [io] * P, oo, **opts)
