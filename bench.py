@@ -340,7 +340,9 @@ def build_gather_calls(torch, dc, device, cases):
 def reductions_block(torch, dc, device, stream, flush, peak):
     """The other paths, each measured like the sweep (flush, CUDA events,
     median of 5): all_reduce at the five per-rank sizes, reduce_scatter
-    16384x8192 per rank, all_gather_many of the six mixed tensors (P=8)."""
+    16384x8192 per rank, the typed, tree and batched reductions, unaligned
+    gathers of 4 MiB+1 B and 32 MiB+1 B per rank, all_gather_many of the six
+    mixed tensors (P=8)."""
     rows = []
     P = W.CONFIG4_P
     for name, n in W.CONFIG4_COUNTS.items():
@@ -362,6 +364,15 @@ def reductions_block(torch, dc, device, stream, flush, peak):
                  "us": us, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     del ins, outs
     rows.extend(typed_rows(torch, dc, device, stream, flush, peak))
+    for B in (4 * 1024 * 1024 + 1, 32 * 1024 * 1024 + 1):  # unaligned: payloads +1, output +3
+        peers = [W.random_bytes_device(W.seed_for(3, 9000), r, B + 1, device)[1:] for r in range(8)]
+        out = torch.empty(8 * B + 3, dtype=torch.uint8, device=device)[3:]
+        us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather(peers, out)], 5)[0])
+        nbytes = 2 * 8 * B
+        rows.append({"op": "all_gather_unaligned", "P": 8, "count": B,
+                     "shape": f"{B} B per rank, payloads at +1 B, output at +3 B", "us": us,
+                     "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+        del peers, out
     P = W.CONFIG5_MANY_P
     tens = [[W.random_bytes_device(W.seed_for(5, 1), r, B, device, tensor=t) for r in range(P)]
             for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
