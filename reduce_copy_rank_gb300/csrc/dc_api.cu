@@ -228,23 +228,27 @@ void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_f
 
 // Split of a launch's CTAs (at most `cap`) between the aligned jobs (tiles of
 // kSplitVectors vectors per thread) and the rest (tiles of
-// kGatherUnrollGeneral), in proportion to their work: a realigned 16-byte
+// kSplitRealignVectors), in proportion to their work: a realigned 16-byte
 // vector counts gather_split_cost_pct / 100 staged ones, so both parts
 // finish together.  Measured on GB300 with the six mixed tensors of the
-// all_gather_many workload (P = 8): 100 % -> 141 us, 175 % -> 117 us,
-// 250 % -> 108.5 us, 300 % -> 112 us; one launch without the split: 139 us.  Each part gets the fewest
+// all_gather_many workload (P = 8), both parts staged: 100 % -> 115 us,
+// 150 % -> 108.5 us, 200 % -> 108 us, 250 % -> 100.6 us, 300 % -> 104 us;
+// every CTA on the register realigning path instead: 141 us.  Each part gets the fewest
 // CTAs that finish its tiles in the same number of rounds.  Returns the total grid, 0 if no split
 // is possible (fewer than two CTAs for two parts).
 template <class Params>
 int plan_split(Params& prm, uint64_t cap) {
   const uint64_t fv = prm.flat_vec, gv = prm.total_vec - prm.flat_vec;
   const uint64_t ftile = static_cast<uint64_t>(kGatherBlock) * kSplitVectors;
-  const uint64_t gtile = static_cast<uint64_t>(kGatherBlock) * kGatherUnrollGeneral;
+  const uint64_t gtile = static_cast<uint64_t>(kGatherBlock) * kSplitRealignVectors;
   const uint64_t ft = (fv + ftile - 1) / ftile, gt = (gv + gtile - 1) / gtile;
   uint64_t gf, gg;
   if (gt == 0) {
     gf = std::min(cap, ft);
     gg = 0;
+  } else if (ft == 0) {
+    gf = 0;
+    gg = std::min(cap, gt);
   } else {
     if (cap < 2) return 0;
     const double cost = static_cast<double>(std::max(1LL, g_opt.split_cost_pct.load())) / 100.0;

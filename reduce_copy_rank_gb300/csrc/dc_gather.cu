@@ -306,13 +306,14 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
 // payload and the start of rank r+1's: all 16 byte loads are issued before
 // the first store, so the vector costs one memory latency instead of one per
 // byte, and a vector inside the output is written with one 16-byte store.
-template <int MAXS>
-__device__ __forceinline__ void copy_boundary(const GatherParams<1, MAXS>& p, const GatherJob& J,
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ void copy_boundary(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
                                               uint64_t x, uint32_t r) {
   const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
   const uint64_t d = J.out + static_cast<uint64_t>(r) * J.bytes;  // first output byte of rank r
-  const uint8_t* s0 = reinterpret_cast<const uint8_t*>(p.src[r]);
-  const uint8_t* s1 = r + 1 < static_cast<uint32_t>(p.P) ? reinterpret_cast<const uint8_t*>(p.src[r + 1]) : s0;
+  const uint8_t* s0 = reinterpret_cast<const uint8_t*>(p.src[J.src0 + r]);
+  const uint8_t* s1 = r + 1 < static_cast<uint32_t>(p.P)
+                          ? reinterpret_cast<const uint8_t*>(p.src[J.src0 + r + 1]) : s0;
   uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (uint32_t i = 0; i < 16; ++i) {
@@ -352,21 +353,21 @@ struct RankWalk {
   bool fresh;
 };
 
-template <typename Idx, int MAXS>
-__device__ __forceinline__ void rank_enter(RankWalk<Idx>& w, const GatherParams<1, MAXS>& p,
+template <typename Idx, int MAXJ, int MAXS>
+__device__ __forceinline__ void rank_enter(RankWalk<Idx>& w, const GatherParams<MAXJ, MAXS>& p,
                                            const GatherJob& J, uint64_t xbase) {
   const uint64_t d = J.out + static_cast<uint64_t>(w.r) * J.bytes;
   w.klo = static_cast<Idx>((d - xbase + 15) >> 4);
   w.khi = static_cast<Idx>((d + J.bytes - xbase) >> 4);
-  const uint64_t a = p.src[w.r] + xbase - d;  // source address that x(0) would map to
+  const uint64_t a = p.src[J.src0 + w.r] + xbase - d;  // source address that x(0) would map to
   w.s = static_cast<uint32_t>(a & 15u);
   w.base = a - w.s;  // modulo 2^64: it may lie outside every allocation
 }
 
 // Idx is uint32_t when the whole output (from out rounded down to 16) is
 // under 4 GiB, so that 16k and every rank size fit 32 bits.
-template <typename Idx, int MAXS>
-__device__ __forceinline__ void walk_to(RankWalk<Idx>& w, const GatherParams<1, MAXS>& p,
+template <typename Idx, int MAXJ, int MAXS>
+__device__ __forceinline__ void walk_to(RankWalk<Idx>& w, const GatherParams<MAXJ, MAXS>& p,
                                         const GatherJob& J, uint64_t xbase, Idx k) {
   if (w.fresh) {
     const Idx lead = static_cast<Idx>(J.out - xbase);  // output bytes before out in vector 0
@@ -458,6 +459,105 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
   cp_async_wait<0>();
 }
 
+// The unaligned jobs of a split launch (global vectors [voff, total_vec),
+// after the aligned jobs), through the same kind of shared-memory ring as
+// gather_tiles_staged_realign.  The issuing side walks jobs forward and,
+// inside a job of at least kGatherSmallBytes per rank, its ranks (RankWalk
+// in job-local vector units); the draining side walks jobs only, for each
+// vector's output address, and reads the vector's shift and kind from the
+// register notes.  Vectors of smaller jobs and vectors at rank boundaries or
+// output ends are copied byte by byte.
+template <int BLOCK, int V, int S, int MAXJ, int MAXS>
+__device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherParams<MAXJ, MAXS>& p,
+                                                                 uint64_t first, uint64_t step,
+                                                                 uint64_t voff) {
+  static_assert(S * V * 5 <= 32, "ring notes must fit one register");
+  extern __shared__ uint4 stage_buf[];  // [S][V][2][BLOCK]
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
+  const uint64_t total = p.total_vec;
+  const uint64_t ntiles = (total - voff + kTile - 1) / kTile;
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
+  // issuing side: job j (vectors [jbeg, jend)), its ranks
+  int j = 0;
+  uint64_t jbeg = p.job[0].vfirst, jend = jbeg + p.job[0].nvec;
+  RankWalk<uint64_t> w{0, 0, 0, 0, 0, true};
+  // draining side: job jd (vectors [dbeg, dend))
+  int jd = 0;
+  uint64_t dbeg = jbeg, dend = jend;
+  uint32_t notes = 0;  // 5 bits per ring vector: s | inside << 4
+  auto slot_addr = [&](uint32_t slot, int u, int h) {
+    return sbase + 16u * BLOCK * static_cast<uint32_t>((slot * V + u) * 2 + h);
+  };
+  auto issue = [&](uint32_t slot, uint64_t t) {
+    notes &= ~(((1u << (5 * V)) - 1u) << (5 * V * slot));
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint64_t k = voff + t * kTile + static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
+      if (t < ntiles && k < total) {
+        while (k >= jend) {
+          ++j;
+          jbeg = p.job[j].vfirst;
+          jend = jbeg + p.job[j].nvec;
+          w.fresh = true;
+        }
+        const GatherJob& J = p.job[j];
+        if (!(J.flags & kJobSmall)) {
+          const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
+          const uint64_t kl = k - jbeg;
+          walk_to(w, p, J, xbase, kl);
+          if (kl >= w.klo && kl < w.khi) {
+            const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * kl);
+            cp_async16_ca(slot_addr(slot, u, 0), blk);
+            if (w.s) cp_async16_ca(slot_addr(slot, u, 1), blk + 1);
+            notes |= (w.s | 16u) << (5 * (slot * V + u));
+          }
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  uint64_t t_issue = first;
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    issue(i, t_issue);
+    t_issue += step;
+  }
+  uint32_t slot = 0;
+  for (uint64_t t = first; t < ntiles; t += step) {
+    cp_async_wait<S - 1>();
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint64_t k = voff + t * kTile + static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
+      if (k < total) {
+        while (k >= dend) {
+          ++jd;
+          dbeg = p.job[jd].vfirst;
+          dend = dbeg + p.job[jd].nvec;
+        }
+        const GatherJob& J = p.job[jd];
+        const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
+        const uint64_t kl = k - dbeg;
+        const uint32_t m = (notes >> (5 * (slot * V + u))) & 31u;
+        if (m & 16u) {
+          const uint32_t sh = m & 15u;
+          const uint4 lo = ld_shared16(slot_addr(slot, u, 0));
+          const uint4 hi = sh ? ld_shared16(slot_addr(slot, u, 1)) : lo;
+          st16(reinterpret_cast<uint4*>(xbase) + kl, realign16(lo, hi, sh));
+        } else {
+          const uint64_t x = xbase + 16 * kl;
+          const bool small = (J.flags & kJobSmall) != 0;
+          const uint32_t r = small || x < J.out ? 0u : static_cast<uint32_t>((x - J.out) / J.bytes);
+          copy_bytes(p, J, x, r, small);
+        }
+      }
+    }
+    issue(slot, t_issue);
+    t_issue += step;
+    slot = (slot + 1 == S) ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
 // voff: the tiles cover global vectors [voff, total_vec) (a split launch
 // gives the vectors below voff to other CTAs).
 template <int BLOCK, int UNROLL, bool FLAT, int MAXJ, int MAXS>
@@ -534,8 +634,8 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
 
 // Kernel modes: kGeneral (any jobs), kFlat (all jobs 16-byte aligned),
 // kFlat1 (one aligned job with fewer than 2^31 output vectors), kFlat1Staged
-// (the same through shared memory), kManySplit (several jobs, some aligned:
-// the first flat_ctas CTAs stage the aligned jobs, the others realign the
+// (the same through shared memory), kManySplit (several jobs: the first
+// flat_ctas CTAs stage the aligned jobs, the others stage and realign the
 // rest).
 enum Mode : int {
   kGeneral = 0,
@@ -568,7 +668,8 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     if (first < fc)
       gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, first, fc);
     else
-      gather_tiles<BLOCK, kGatherUnrollGeneral, false>(p, first - fc, step - fc, p.flat_vec);
+      gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
+          p, first - fc, step - fc, p.flat_vec);
   } else
     gather_tiles<BLOCK, UNROLL, MODE != kGeneral>(p, first, step);
 }
@@ -641,7 +742,7 @@ __global__ void __launch_bounds__(MODE == kGeneral ? kGatherSingleBlockGeneral :
 template <int MAXJ, int MAXS>
 int mode_of(const GatherParams<MAXJ, MAXS>& p) {
   const bool all_flat = p.flat_vec == p.total_vec;
-  if (MAXJ > 1 && p.staged && p.flat_vec > 0) return kManySplit;
+  if (MAXJ > 1 && p.staged) return kManySplit;
   if (!all_flat)
     return MAXJ == 1 && p.staged && !(p.job[0].flags & kJobSmall) ? kGeneral1Staged : kGeneral;
   if (MAXJ == 1 && p.total_vec < (1ull << 31)) return p.staged ? kFlat1Staged : kFlat1;
@@ -711,8 +812,11 @@ template <int MAXJ, int MAXS>
 cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single, bool pdl,
                         cudaStream_t s) {
   int mode = mode_of(p);
-  if (mode == kManySplit && (single || p.flat_ctas < 1 || p.flat_ctas > grid))
-    mode = p.flat_vec == p.total_vec ? kFlat : kGeneral;  // no split: one path for every CTA
+  // A split needs CTAs for each part that has work; otherwise one path for every CTA.
+  if (mode == kManySplit &&
+      (single || p.flat_ctas > grid || (p.flat_vec > 0 && p.flat_ctas < 1) ||
+       (p.flat_vec < p.total_vec && p.flat_ctas >= grid)))
+    mode = p.flat_vec == p.total_vec ? kFlat : kGeneral;
   switch (mode) {
     case kGeneral: return launch_mode<MAXJ, MAXS, kGeneral>(p, grid, single, pdl, s);
     case kFlat: return launch_mode<MAXJ, MAXS, kFlat>(p, grid, single, pdl, s);

@@ -33,6 +33,10 @@ constexpr int kStagedVectors = 3;
 // the realigning path, so two CTAs fit per SM: 2 x 96 KB in flight).
 constexpr int kSplitStages = 3;
 constexpr int kSplitVectors = 4;
+// ... and the unaligned jobs by the rest of the grid through a ring of the
+// same size: 3 slots x 2 vectors x 2 source blocks.
+constexpr int kSplitRealignStages = 3;
+constexpr int kSplitRealignVectors = 2;
 // One unaligned job staged through shared memory: per thread kRealignStages
 // slots of kRealignVectors output vectors, each with the two aligned source
 // blocks it is cut from (2 x 2 x 2 x 512 x 16 B = 64 KB per CTA, three CTAs

@@ -111,6 +111,23 @@ def test_many_all_aligned(grid):
     assert guards
 
 
+@pytest.mark.parametrize("grid", [0, 1, 2, 7, 5000])
+def test_many_all_unaligned(grid):
+    """No aligned tensor: every CTA stages and realigns; small jobs (under
+    128 B per rank) and rank boundaries go byte by byte."""
+    rng = np.random.default_rng(W.seed_for(5, 9004))
+    P = 5
+    sizes = [3, 127, 128, 129, 4097, 100001, 300007]
+    tensors = [[rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)] for B in sizes]
+    in_offs = [[int(x) for x in rng.integers(1, 16, P)] for _ in sizes]
+    out_offs = [int(x) for x in rng.integers(1, 16, len(sizes))]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, in_offs, out_offs, grid_ctas=grid)
+    for t in range(len(sizes)):
+        assert np.array_equal(got[t], want[t]), (t, grid)
+    assert guards
+
+
 def test_many_large_table():
     """More tensors than the small parameter block holds (T=100, P=8)."""
     rng = np.random.default_rng(W.seed_for(5, 9001))
