@@ -109,7 +109,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 64;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + ...
+constexpr int kFamilies = 128;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + (< 72)
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -418,11 +418,12 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
   int grid = 1;
   if (!single) {
     const int P = prm.P;
-    const int fam = 24 + (((dtype * 3 + variant) * 2 + order) * 2 + (P == 8 ? 1 : 0));
+    const int pt = reduce_pt(P);
+    const int fam = 24 + (((dtype * 3 + variant) * 2 + order) * 4 + (pt == 2 ? 1 : pt == 4 ? 2 : pt == 8 ? 3 : 0));
     const int occ = occupancy(dev, fam, [dtype, variant, order, P] {
       return reduce_ctas_per_sm(dtype, variant, order, P);
     });
-    const uint64_t tile = static_cast<uint64_t>(kReduceBlock) * kReduceUnroll;
+    const uint64_t tile = static_cast<uint64_t>(kReduceBlock) * reduce_unroll(pt);
     grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
   }
   return check_launch(launch_reduce(prm, dtype, order, grid, single, g_opt.pdl.load() != 0, stream),

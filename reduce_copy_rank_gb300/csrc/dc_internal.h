@@ -45,7 +45,14 @@ constexpr int kRealignStages = 2;
 constexpr int kRealignVectors = 2;
 constexpr int kReduceBlock = 256;
 constexpr int kReduceSingleBlock = 512;
-constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread
+constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread (P = 8 or any P)
+// Groups in flight per thread of the kernel compiled for P = pt (0: any P):
+// 16 rank loads in flight for P = 2, 4 and 8.
+__host__ __device__ constexpr int reduce_unroll(int pt) {
+  return pt == 2 ? 8 : pt == 4 ? 4 : kReduceUnroll;
+}
+// The compile-time rank counts of the reduction kernels (0 = any P).
+__host__ __device__ constexpr int reduce_pt(int P) { return P == 2 || P == 4 || P == 8 ? P : 0; }
 
 // Below this many bytes per rank a gather job is copied byte by byte: each
 // rank then spans at most a handful of 16-byte output vectors, the total is

@@ -265,18 +265,15 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>&
         }
       }
     }
-    float acc[UNROLL][E];
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const uint64_t u = u0 + k * BLOCK;
-      if (u < bb)
-        fold_vector<DT, ORDER, PT>(p, J, (J.in_off + J.head + E * (u - hu)) * T::kSize, v[k], acc[k]);
-    }
+    // group by group: one accumulator live at a time, however many groups
+    // are in flight
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       const uint64_t u = u0 + k * BLOCK;
       if (u < bb) {
-        const uint4 y = T::narrow(acc[k]);
+        float acc[E];
+        fold_vector<DT, ORDER, PT>(p, J, (J.in_off + J.head + E * (u - hu)) * T::kSize, v[k], acc);
+        const uint4 y = T::narrow(acc);
         const uint64_t byte_off = (J.head + E * (u - hu)) * T::kSize;
         for (uint32_t m = 0; m < J.nout; ++m)
           st16(reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off), y);
@@ -336,27 +333,29 @@ __device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MA
   }
 }
 
-template <int DT, int BLOCK, int MAXJ, int MAXPTR>
+template <int DT, int BLOCK, int UNROLL, int MAXJ, int MAXPTR>
 __device__ __forceinline__ void reduce_enter(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t first,
                                              uint64_t step) {
   pdl_launch_dependents();
   for (int i = 0; i < p.prefetch; ++i)
-    reduce_prefetch_tile<DT, BLOCK, kReduceUnroll>(p, first + static_cast<uint64_t>(i) * step);
+    reduce_prefetch_tile<DT, BLOCK, UNROLL>(p, first + static_cast<uint64_t>(i) * step);
   pdl_wait();
 }
 
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceBlock)
     dc_reduce_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
-  reduce_enter<DT, kReduceBlock>(p, blockIdx.x, gridDim.x);
-  reduce_tiles<DT, ORDER, kReduceBlock, kReduceUnroll, PT>(p, blockIdx.x, gridDim.x);
+  constexpr int kUnroll = reduce_unroll(PT);
+  reduce_enter<DT, kReduceBlock, kUnroll>(p, blockIdx.x, gridDim.x);
+  reduce_tiles<DT, ORDER, kReduceBlock, kUnroll, PT>(p, blockIdx.x, gridDim.x);
 }
 
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceSingleBlock)
     dc_reduce_single_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
-  reduce_enter<DT, kReduceSingleBlock>(p, 0, 1);
-  reduce_tiles<DT, ORDER, kReduceSingleBlock, kReduceUnroll, PT>(p, 0, 1);
+  constexpr int kUnroll = reduce_unroll(PT);
+  reduce_enter<DT, kReduceSingleBlock, kUnroll>(p, 0, 1);
+  reduce_tiles<DT, ORDER, kReduceSingleBlock, kUnroll, PT>(p, 0, 1);
 }
 
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
@@ -371,8 +370,12 @@ cudaError_t launch_pt(const ReduceParams<MAXJ, MAXPTR>& p, int grid, bool single
 template <int DT, int ORDER, int MAXJ, int MAXPTR>
 cudaError_t launch_order(const ReduceParams<MAXJ, MAXPTR>& p, int grid, bool single, bool pdl,
                          cudaStream_t s) {
-  return p.P == 8 ? launch_pt<DT, ORDER, 8>(p, grid, single, pdl, s)
-                  : launch_pt<DT, ORDER, 0>(p, grid, single, pdl, s);
+  switch (reduce_pt(p.P)) {
+    case 2: return launch_pt<DT, ORDER, 2>(p, grid, single, pdl, s);
+    case 4: return launch_pt<DT, ORDER, 4>(p, grid, single, pdl, s);
+    case 8: return launch_pt<DT, ORDER, 8>(p, grid, single, pdl, s);
+    default: return launch_pt<DT, ORDER, 0>(p, grid, single, pdl, s);
+  }
 }
 
 template <int DT, int MAXJ, int MAXPTR>
@@ -393,13 +396,20 @@ int occupancy_pt() {
   return n > 0 ? n : 1;
 }
 
+template <int DT, int ORDER, int MAXJ, int MAXPTR>
+int occupancy_order(int P) {
+  switch (reduce_pt(P)) {
+    case 2: return occupancy_pt<DT, ORDER, 2, MAXJ, MAXPTR>();
+    case 4: return occupancy_pt<DT, ORDER, 4, MAXJ, MAXPTR>();
+    case 8: return occupancy_pt<DT, ORDER, 8, MAXJ, MAXPTR>();
+    default: return occupancy_pt<DT, ORDER, 0, MAXJ, MAXPTR>();
+  }
+}
+
 template <int DT, int MAXJ, int MAXPTR>
 int occupancy_dtype(int order, int P) {
-  if (order == kOrderTree)
-    return P == 8 ? occupancy_pt<DT, kOrderTree, 8, MAXJ, MAXPTR>()
-                  : occupancy_pt<DT, kOrderTree, 0, MAXJ, MAXPTR>();
-  return P == 8 ? occupancy_pt<DT, kOrderLinear, 8, MAXJ, MAXPTR>()
-                : occupancy_pt<DT, kOrderLinear, 0, MAXJ, MAXPTR>();
+  return order == kOrderTree ? occupancy_order<DT, kOrderTree, MAXJ, MAXPTR>(P)
+                             : occupancy_order<DT, kOrderLinear, MAXJ, MAXPTR>(P);
 }
 
 }  // namespace red
