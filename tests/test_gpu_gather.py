@@ -213,3 +213,37 @@ def test_every_call_is_one_launch():
     for _ in range(10):
         dc.all_gather(peers, out)
     assert dc.launch_count() - before == 10
+
+
+def _free_bytes():
+    free, _total = torch.cuda.mem_get_info()
+    return free
+
+
+@pytest.mark.parametrize("P,B,in_off,out_off,path", [
+    (2, (9 << 28) + 1, 1, 3, "unaligned, 4.5 GiB output: 64-bit staged realign indices"),
+    (2, (16 << 30) + 16, 0, 0, "aligned, 32 GiB output: more than 2^31 vectors, 64-bit flat path"),
+])
+def test_huge_outputs_take_64_bit_paths(P, B, in_off, out_off, path):
+    """Outputs past 4 GiB (unaligned) and past 2^31 16-byte vectors (aligned)
+    switch the kernels to 64-bit indices.  At these sizes the oracle is the
+    definition itself, checked on the device: slice r of the output equals
+    payload r byte for byte (and the guard bytes around it are untouched)."""
+    need = 2 * P * B + (1 << 30)
+    if _free_bytes() < need:
+        pytest.skip(f"needs {need >> 30} GiB of free device memory")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(W.device_seed(W.seed_for(3, 9200), 0))
+    store = [torch.empty(B + 16, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    peers = []
+    for s in store:
+        v = s[in_off:in_off + B]
+        v.random_(0, 256, generator=g)
+        peers.append(v)
+    out_store = torch.full((P * B + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = out_store[out_off:out_off + P * B]
+    dc.all_gather(peers, out)
+    torch.cuda.synchronize()
+    for r in range(P):
+        assert torch.equal(out[r * B:(r + 1) * B], peers[r]), (path, r)
+    assert bool((out_store[:out_off] == 0xA5).all()) and bool((out_store[out_off + P * B:] == 0xA5).all())
