@@ -122,3 +122,72 @@ def test_replica_aggregation_world_size_2_gloo(tmp_path):
 
 def test_rank_max_without_process_group():
     assert bench.rank_max(7.5) == 7.5
+
+
+class _FakeClock:
+    """A scripted device clock for the timing helpers: events read `now`
+    when recorded; calls and flushes advance it."""
+
+    def __init__(self):
+        self.now = 0.0  # ms
+        self.log = []
+
+    def torch(self):
+        clock = self
+
+        class Event:
+            def __init__(self, enable_timing=False, external=False):
+                self.t = None
+
+            def record(self, stream=None):
+                self.t = clock.now
+
+            def elapsed_time(self, other):
+                return other.t - self.t
+
+        class _Cuda:
+            pass
+
+        cuda = _Cuda()
+        cuda.Event = Event
+        cuda.synchronize = lambda *a, **k: None
+        ns = type("FakeTorch", (), {})()
+        ns.cuda = cuda
+        return ns
+
+    def call(self, name, ms):
+        def fn():
+            self.log.append(name)
+            self.now += ms
+        return fn
+
+
+def test_timed_calls_attribute_each_call_and_exclude_the_flush():
+    clk = _FakeClock()
+
+    def flush():
+        clk.log.append("flush")
+        clk.now += 50.0  # never inside a call's events
+
+    out = bench.timed_calls(clk.torch(), None, flush, [clk.call("a", 0.002), clk.call("b", 0.010)], 3)
+    assert [round(x, 6) for x in out[0]] == [2.0] * 3  # microseconds
+    assert [round(x, 6) for x in out[1]] == [10.0] * 3
+    assert clk.log == ["flush", "a", "flush", "b"] * 3
+
+
+def test_alternating_swaps_order_and_takes_medians():
+    clk = _FakeClock()
+    durations = {"a": [0.001, 0.003, 0.002, 0.100], "b": [0.005, 0.004, 0.006, 0.005]}
+    counters = {"a": 0, "b": 0}
+
+    def make(name):
+        def fn():
+            clk.log.append(name)
+            clk.now += durations[name][counters[name]]
+            counters[name] += 1
+        return fn
+
+    med = bench.alternating(clk.torch(), None, lambda: None, [make("a"), make("b")], 4)
+    assert clk.log == ["a", "b", "b", "a", "a", "b", "b", "a"]
+    assert round(med[0], 6) == 2.5  # median of 1, 3, 2, 100 us
+    assert round(med[1], 6) == 5.0

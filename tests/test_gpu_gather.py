@@ -146,6 +146,21 @@ def test_independent_per_rank_offsets():
     _batched_cases(cases, lambda P, B: [rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)])
 
 
+def test_page_size_list_all_offsets():
+    """The sizes the page's distributed test uses to straddle the single-block
+    threshold (4095 B, 32 KiB+3 B, 96 KiB, 1 MiB, and 1 MiB+5 B, its largest
+    per-rank case), for P = 2 and 8, every payload and the output at each of
+    the offsets {0, 1, 8, 15} (16 pairs), against the oracle."""
+    rng = np.random.default_rng(W.seed_for(3, 9300))
+    cases = []
+    for P in (2, 8):
+        for B in (4095, 32 * 1024 + 3, 96 * 1024, 1024 * 1024, 1024 * 1024 + 5):
+            for io in (0, 1, 8, 15):
+                for oo in (0, 1, 8, 15):
+                    cases.append((P, B, [io] * P, oo))
+    _batched_cases(cases, lambda P, B: [rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)])
+
+
 @pytest.mark.parametrize("opts", [
     {"force_path": 1}, {"force_path": 2}, {"force_generic": 1},
     {"force_path": 2, "grid_ctas": 1}, {"force_path": 2, "grid_ctas": 3},
