@@ -378,17 +378,20 @@ void fill_reduce(Params& prm, int P, int dtype, bool scatter, const std::vector<
       J.nout = static_cast<uint16_t>(scatter ? 1 : P);
       J.in_off = scatter ? static_cast<uint64_t>(r) * n : 0;
       J.count = n;
+      // 16-byte units are anchored at the outputs: they need every output at
+      // the same address mod 16; inputs at that offset too load whole
+      // vectors, inputs at other offsets are realigned.
       const uint64_t off = J.in_off * es;
-      const uint32_t o = static_cast<uint32_t>((prm.ptr[J.in0] + off) & 15u);
-      bool vec = true;
-      for (int q = 0; q < P; ++q) vec = vec && ((prm.ptr[J.in0 + q] + off) & 15u) == o;
-      for (int m = 0; m < J.nout; ++m) vec = vec && (prm.ptr[J.out0 + m] & 15u) == o;
-      if (vec) {
+      const uint32_t o = static_cast<uint32_t>(prm.ptr[J.out0] & 15u);
+      bool outs_agree = true, ins_agree = true;
+      for (int m = 0; m < J.nout; ++m) outs_agree = outs_agree && (prm.ptr[J.out0 + m] & 15u) == o;
+      for (int q = 0; q < P; ++q) ins_agree = ins_agree && ((prm.ptr[J.in0 + q] + off) & 15u) == o;
+      if (outs_agree) {
         uint64_t head = ((16u - o) & 15u) / es;
         if (head > n) head = n;
         const uint64_t rest = n - head;
         J.head = static_cast<uint8_t>(head);
-        J.flags = kJobVec;
+        J.flags = ins_agree ? kJobVec : (kJobVec | kJobRealign);
         J.nunits = (head ? 1 : 0) + rest / epv + ((rest % epv) ? 1 : 0);
       } else {
         J.head = 0;

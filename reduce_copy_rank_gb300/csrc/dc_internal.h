@@ -101,7 +101,8 @@ using GatherParamsL = GatherParams<kManyMaxTensors, kManyMaxSegments>;
 enum : int { kBF16 = 0, kF16 = 1, kF32 = 2 };              // element types
 enum : int { kOrderLinear = 0, kOrderTree = 1 };           // summation orders
 enum : uint32_t {
-  kJobVec = 1u,    // every pointer of the job has the same address mod 16
+  kJobVec = 1u,      // 16-byte units: every output has the same address mod 16 ...
+  kJobRealign = 2u,  // ... and the inputs do not share it: their units are realigned
 };
 
 // Batched reductions: at most kManyMaxReduceJobs jobs and kManyMaxReducePtrs
@@ -112,9 +113,9 @@ constexpr int kManyMaxReducePtrs = 1024;
 // One fixed-order reduction over `count` elements of one tensor: element i
 // reads input q at element in_off + i (input q's pointer is ptr[in0 + q],
 // q < P) and writes output m at element i (pointer ptr[out0 + m],
-// m < nout).  Work units: an optional scalar head (elements before the first
-// 16-byte boundary), 16-byte vectors, and an optional scalar tail; for a job
-// without kJobVec every unit is one element.
+// m < nout).  Work units: an optional scalar head (elements before the
+// outputs' first 16-byte boundary), 16-byte vectors, and an optional scalar
+// tail; for a job without kJobVec every unit is one element.
 struct ReduceJob {
   uint64_t in_off;
   uint64_t count;

@@ -156,6 +156,25 @@ __device__ __forceinline__ uint8_t* out_ptr(const ReduceParams<MAXJ, MAXPTR>& p,
   return reinterpret_cast<uint8_t*>(p.ptr[J.out0 + m]);
 }
 
+// The 16 input bytes at `a`.  A job whose inputs all share the outputs'
+// address mod 16 loads them with one aligned load; a realigning job (inputs
+// at other offsets) loads the aligned block holding `a` and, if `a` is not
+// 16-byte aligned, the next one, and funnel-shifts them.  Both blocks hold
+// bytes of [a, a + 16), so they lie in the input buffer; a thread's second
+// block is its neighbour's first (cached load).
+template <bool REALIGN>
+__device__ __forceinline__ uint4 ld_input(const uint8_t* a) {
+  if constexpr (!REALIGN) {
+    return ld_stream(reinterpret_cast<const uint4*>(a));
+  } else {
+    const uint32_t s = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a) & 15u);
+    const uint4* blk = reinterpret_cast<const uint4*>(a - s);
+    const uint4 lo = ld_nc_cached(blk);
+    const uint4 hi = s ? ld_nc_cached(blk + 1) : lo;
+    return realign16(lo, hi, s);
+  }
+}
+
 // Elements [e0, e1) (step `step`) of job J, one at a time.
 template <int DT, int ORDER, int MAXJ, int MAXPTR>
 __device__ __forceinline__ void fold_scalar(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J,
@@ -186,7 +205,7 @@ __device__ __forceinline__ void fold_scalar(const ReduceParams<MAXJ, MAXPTR>& p,
 // The fold of one 16-byte vector of every rank at byte offset `off` of each
 // input.  PT > 0: P = PT known at compile time, all loads issued first by the
 // caller (`v`).  PT == 0: ranks in batches of 8 loads.
-template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+template <int DT, int ORDER, int PT, bool REALIGN, int MAXJ, int MAXPTR>
 __device__ __forceinline__ void fold_vector(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J,
                                             uint64_t off, const uint4 (&v)[PT > 0 ? PT : 1],
                                             float (&acc)[Elem<DT>::kPerVec]) {
@@ -217,7 +236,7 @@ __device__ __forceinline__ void fold_vector(const ReduceParams<MAXJ, MAXPTR>& p,
       const int nb = min(8, p.P - q0);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (k < nb) w[k] = ld_stream(reinterpret_cast<const uint4*>(in_ptr(p, J, q0 + k) + off));
+        if (k < nb) w[k] = ld_input<REALIGN>(in_ptr(p, J, q0 + k) + off);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (k < nb) {
@@ -238,7 +257,7 @@ __device__ __forceinline__ void fold_vector(const ReduceParams<MAXJ, MAXPTR>& p,
   }
 }
 
-template <int DT, int ORDER, int BLOCK, int UNROLL, int PT, int MAXJ, int MAXPTR>
+template <int DT, int ORDER, int BLOCK, int UNROLL, int PT, bool REALIGN, int MAXJ, int MAXPTR>
 __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>& p,
                                                const ReduceJob& J, uint64_t a, uint64_t b) {
   using T = Elem<DT>;
@@ -261,7 +280,7 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>&
           const uint64_t off = (J.in_off + J.head + E * (u - hu)) * T::kSize;
 #pragma unroll
           for (int q = 0; q < PT; ++q)
-            v[k][q] = ld_stream(reinterpret_cast<const uint4*>(in_ptr(p, J, q) + off));
+            v[k][q] = ld_input<REALIGN>(in_ptr(p, J, q) + off);
         }
       }
     }
@@ -272,7 +291,8 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>&
       const uint64_t u = u0 + k * BLOCK;
       if (u < bb) {
         float acc[E];
-        fold_vector<DT, ORDER, PT>(p, J, (J.in_off + J.head + E * (u - hu)) * T::kSize, v[k], acc);
+        fold_vector<DT, ORDER, PT, REALIGN>(p, J, (J.in_off + J.head + E * (u - hu)) * T::kSize, v[k],
+                                            acc);
         const uint4 y = T::narrow(acc);
         const uint64_t byte_off = (J.head + E * (u - hu)) * T::kSize;
         for (uint32_t m = 0; m < J.nout; ++m)
@@ -299,8 +319,10 @@ __device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ, MAXPTR>& p
       const uint64_t a = max(g0, J.ufirst) - J.ufirst;
       const uint64_t b = min(g1, J.ufirst + J.nunits) - J.ufirst;
       if (a >= b) continue;
-      if (J.flags & kJobVec)
-        reduce_job_vec<DT, ORDER, BLOCK, UNROLL, PT>(p, J, a, b);
+      if ((J.flags & (kJobVec | kJobRealign)) == kJobVec)
+        reduce_job_vec<DT, ORDER, BLOCK, UNROLL, PT, false>(p, J, a, b);
+      else if (J.flags & kJobVec)  // realigned inputs: two loads each, half as many groups in flight
+        reduce_job_vec<DT, ORDER, BLOCK, (UNROLL > 1 ? UNROLL / 2 : 1), PT, true>(p, J, a, b);
       else
         fold_scalar<DT, ORDER>(p, J, a + threadIdx.x, b, BLOCK);
     }
@@ -322,7 +344,7 @@ __device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MA
   const uint64_t g1 = min(g0 + kTile, p.total_units);
   for (int jj = 0; jj < p.njobs && p.job[jj].ufirst < g1; ++jj) {
     const ReduceJob& J = p.job[jj];
-    if (J.ufirst + J.nunits <= g0 || !(J.flags & kJobVec)) continue;
+    if (J.ufirst + J.nunits <= g0 || (J.flags & (kJobVec | kJobRealign)) != kJobVec) continue;
     const uint64_t hu = J.head ? 1 : 0;
     const uint64_t body_end = hu + (J.count - J.head) / E;
     const uint64_t a = max(max(g0, J.ufirst) - J.ufirst, hu);

@@ -223,3 +223,73 @@ def test_tree_and_linear_differ_on_gpu():
     assert_typed_equal(ga, lin, "bf16", "linear")
     assert_typed_equal(gb, tree, "bf16", "tree")
     assert (ga[differ] != gb[differ]).all()
+
+
+def _at_offsets(cols, dtype, offs):
+    """Device copies of `cols`, rank r's starting `offs[r]` elements past a
+    16-byte boundary."""
+    es = 4 if dtype == "f32" else 2
+    out = []
+    for c, o in zip(cols, offs):
+        n = c.size
+        store = torch.empty(n * es + 64, dtype=torch.uint8, device="cuda")
+        start = ((-store.data_ptr()) % 16) + o * es
+        v = store[start:start + n * es].view(torch_dtype(dtype))
+        v.copy_(typed_tensor(c, dtype))
+        out.append(v)
+    return out
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("order", ORDERS)
+def test_realigned_inputs(dtype, order):
+    """Inputs at different offsets from 16 bytes, outputs aligned: 16-byte
+    units anchored at the outputs, every input realigned (all_reduce and
+    reduce_scatter, compile-time and runtime P)."""
+    epv = 4 if dtype == "f32" else 8
+    rng = np.random.default_rng(W.seed_for(4, 9990))
+    for P in (2, 3, 4, 8, 13):
+        for C in (1, 9, 1000, 65536 + 3):
+            offs = [int(x) for x in rng.integers(0, epv, P)]
+            offs[0] = (offs[0] + 1) % epv if len(set(offs)) == 1 else offs[0]  # not all equal
+            cols = [random_bits(W.seed_for(4, 9991 + P), r, P * C, dtype) for r in range(P)]
+            ins = _at_offsets(cols, dtype, offs)
+            outs = [torch.empty(P * C, dtype=torch_dtype(dtype), device="cuda") for _ in range(P)]
+            dc.all_reduce(ins, outs, order=order)
+            shards = [torch.empty(C, dtype=torch_dtype(dtype), device="cuda") for _ in range(P)]
+            dc.reduce_scatter(ins, shards, order=order)
+            torch.cuda.synchronize()
+            want = np.asarray(oracle.all_reduce(cols, dtype, order)).view(NP_OF[dtype])
+            for r in range(P):
+                assert_typed_equal(typed_bits(outs[r], dtype), want, dtype,
+                                   f"all_reduce {dtype} {order} P={P} C={C} offs={offs} rank {r}")
+            want_rs = oracle.reduce_scatter(cols, dtype, order)
+            for r in range(P):
+                assert_typed_equal(typed_bits(shards[r], dtype), want_rs[r].view(NP_OF[dtype]), dtype,
+                                   f"reduce_scatter {dtype} {order} P={P} C={C} offs={offs} shard {r}")
+
+
+def test_in_place_at_disagreeing_offsets():
+    """In-place all_reduce with each rank's buffer at its own offset: the
+    outputs disagree mod 16, so the job runs element by element."""
+    P, n = 4, 10007
+    cols = [random_bits(W.seed_for(4, 9995), r, n, "bf16") for r in range(P)]
+    want = np.asarray(oracle.all_reduce(cols, "bf16", "linear")).view(np.uint16)
+    bufs = _at_offsets(cols, "bf16", [0, 1, 2, 5])
+    dc.all_reduce(bufs, bufs)
+    torch.cuda.synchronize()
+    for r in range(P):
+        assert_typed_equal(typed_bits(bufs[r], "bf16"), want, "bf16", f"rank {r}")
+
+
+def test_full_size_realigned_all_reduce():
+    """8627x8192 per rank, P = 8, rank 1's input one element off: bit exact
+    at full size on the realigning path."""
+    P, n = 8, W.CONFIG4_COUNTS["8627x8192"]
+    store = [normal_bits(W.seed_for(4, 9996), r, n + 8, "bf16") for r in range(P)]
+    ins = [store[r][(1 if r == 1 else 0):(1 if r == 1 else 0) + n] for r in range(P)]
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dc.all_reduce(ins, outs)
+    torch.cuda.synchronize()
+    want = oracle.all_reduce([typed_bits(x, "bf16") for x in ins], "bf16", "linear")
+    assert_typed_equal(typed_bits(outs[5], "bf16"), np.asarray(want), "bf16", "rank 5")
