@@ -12,23 +12,30 @@
 // Design on one GB300:
 //  * The unit of work is a 16-byte-aligned OUTPUT vector.  A launch covers
 //    the output vectors of one or more jobs (all_gather_many packs several
-//    gathers into one launch), numbered by a prefix over the jobs.  Each CTA
-//    owns one contiguous run of them and finds its first job once.
-//  * Inside a run, thread t takes vectors t, t+BLOCK, t+2*BLOCK, ..., UNROLL
-//    of them at a time with all loads issued before the first store, across
-//    rank boundaries: the flat loop of the page.  (The page's first version
-//    copied rank by rank, leaving threads idle and serialising the ranks'
-//    reads; a per-rank walk inside a CTA has the same defect.)  A thread's
-//    vector index only grows, so it finds its rank by walking forward from
-//    the rank of the run's first vector: comparisons, never a division per
-//    element.
-//  * Aligned job (flat): plain LDG.128 / STG.128.
+//    gathers into one launch), numbered by a prefix over the jobs.  Vectors
+//    are grouped in tiles of BLOCK x V; CTA c takes tiles c, c + G, c + 2G,
+//    ... (G CTAs), so that all CTAs sweep the buffers together.
+//  * Inside a tile, thread t takes vectors t, t + BLOCK, ..., across rank
+//    boundaries: the flat loop of the page.  (The page's first version copied
+//    rank by rank, leaving threads idle and serialising the ranks' reads.)  A
+//    thread's vector index only grows, so it finds its rank (and job) by
+//    walking forward: comparisons, one division when it enters a job, never
+//    one per element.
+//  * Aligned job (flat): 16-byte loads and stores, either held in registers
+//    (mode 2) or staged through a per-thread cp.async ring in shared memory
+//    (mode 3, the default: more bytes in flight without registers).
 //  * Unaligned job: each output vector that lies inside one rank's bytes is
 //    built from the two aligned source blocks that cover it with a funnel
-//    shift, so loads and stores stay 16 bytes wide and aligned; the few
-//    vectors that straddle two ranks or stick out of the output (at most P+1
-//    per job) are written byte by byte.
+//    shift, so loads and stores stay 16 bytes wide and aligned (registers,
+//    mode 0; staged through a cp.async ring with per-rank affine state,
+//    mode 5); the few vectors that straddle two ranks or stick out of the
+//    output (at most P+1 per job) are written byte by byte.
+//  * all_gather_many (mode 4): the aligned jobs come first and are staged by
+//    the first part of the grid, the unaligned ones by the rest.
 //  * Jobs with fewer than kGatherSmallBytes per rank are copied byte by byte.
+//  * Every kernel triggers the next kernel of the stream at entry; the
+//    aligned single-job kernels prefetch their first tile into L2 before they
+//    wait for the previous kernel (programmatic dependent launch).
 #include <atomic>
 
 #include "dc_device.cuh"

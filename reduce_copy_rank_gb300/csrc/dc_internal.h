@@ -1,5 +1,6 @@
 // dc_internal.h -- definitions shared by the host planner (dc_api.cu) and the
-// kernels (dc_gather.cu, dc_reduce.cu).  Not part of the public C ABI.
+// kernels (dc_gather.cu, dc_reduce.cuh and its per-type units, dc_delay.cu).
+// Not part of the public C ABI.
 //
 // Everything a kernel needs travels by value in one parameter block, so a
 // launch allocates nothing, reads no host memory after it is enqueued and can
