@@ -86,7 +86,8 @@ def parse_args(argv=None):
     ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
                     help="profiling helper: run one call REPS times and exit, e.g. "
                          "gather:8:4194304:3, ugather:8:4194305:3 (unaligned), "
-                         "allreduce:8:268435456:2 (BYTES per rank) or "
+                         "allreduce:8:268435456:2, allreduce_mis:8:67108864:2 (rank 1 one "
+                         "element off; BYTES per rank) or "
                          "many:8:0:3 (the all_gather_many workload)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
@@ -913,6 +914,11 @@ def run_case(args) -> int:
                 for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
         outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in W.CONFIG5_MANY_SIZES]
         fn = lambda: dc.all_gather_many(tens, outs)  # noqa: E731
+    elif op == "allreduce_mis":  # rank 1's input one element past the others' alignment
+        store = [torch.randn(nbytes // 2 + 8, device=device).to(torch.bfloat16) for _ in range(P)]
+        ins = [store[r][(1 if r == 1 else 0):(1 if r == 1 else 0) + nbytes // 2] for r in range(P)]
+        outs = [torch.empty(nbytes // 2, dtype=torch.bfloat16, device=device) for _ in range(P)]
+        fn = lambda: dc.all_reduce(ins, outs)  # noqa: E731
     elif op == "reducescatter":
         ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
         outs = [torch.empty(nbytes // 2 // P, dtype=torch.bfloat16, device=device) for _ in range(P)]
