@@ -290,3 +290,14 @@ def test_delay_limit_checked_before_cuda(no_launch):
     # a valid request reaches the (refused) launch
     assert dc.dc_inject_delay_ns(0, 0) == 5
     assert dc.dc_inject_delay_ns(dc.MAX_DELAY_NS, 0) == 5
+
+
+def test_every_documented_option_exists_and_round_trips():
+    keys = re.findall(r'\*   "([a-z_]+)"', open(HEADER).read())
+    assert {"gather_single_max_bytes", "reduce_single_max_bytes", "prefetch",
+            "gather_split_cost_pct", "gather_staged", "pdl"} <= set(keys)
+    for k in keys:
+        v = dc.get_option(k)
+        assert v >= 0, k
+        with dc.options(**{k: v}):
+            assert dc.get_option(k) == v
