@@ -67,6 +67,17 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
+// Coherent 16-byte load that allocates in L1: the realigning reductions read
+// every aligned input block twice (the high half of one unit, the low half
+// of the next) and may run in place.
+__device__ __forceinline__ uint4 ld_cached(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void st16(uint4* p, const uint4& v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                :

@@ -161,7 +161,8 @@ __device__ __forceinline__ uint8_t* out_ptr(const ReduceParams<MAXJ, MAXPTR>& p,
 // at other offsets) loads the aligned block holding `a` and, if `a` is not
 // 16-byte aligned, the next one, and funnel-shifts them.  Both blocks hold
 // bytes of [a, a + 16), so they lie in the input buffer; a thread's second
-// block is its neighbour's first (cached load).
+// block is its neighbour's first (coherent, L1-allocating load: a job may
+// run in place).
 template <bool REALIGN>
 __device__ __forceinline__ uint4 ld_input(const uint8_t* a) {
   if constexpr (!REALIGN) {
@@ -169,8 +170,8 @@ __device__ __forceinline__ uint4 ld_input(const uint8_t* a) {
   } else {
     const uint32_t s = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a) & 15u);
     const uint4* blk = reinterpret_cast<const uint4*>(a - s);
-    const uint4 lo = ld_nc_cached(blk);
-    const uint4 hi = s ? ld_nc_cached(blk + 1) : lo;
+    const uint4 lo = ld_cached(blk);
+    const uint4 hi = s ? ld_cached(blk + 1) : lo;
     return realign16(lo, hi, s);
   }
 }
