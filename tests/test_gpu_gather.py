@@ -231,6 +231,7 @@ def test_every_call_is_one_launch():
 
 
 def _free_bytes():
+    torch.cuda.empty_cache()  # memory cached for earlier tests counts as used
     free, _total = torch.cuda.mem_get_info()
     return free
 
