@@ -483,6 +483,32 @@ def comparators_block(torch, dc, device, stream, flush, reps=10):
     return {"all_gather_vs_torch_cat": gathers, "all_reduce_bf16_vs_torch_loop": reduces}
 
 
+def back_to_back_block(torch, dc, device, flush, per_size=8, replays=10):
+    """Per-call time of each sweep size in the back-to-back regime: one CUDA
+    graph of `per_size` calls of that size on distinct buffers (so every
+    call reads inputs no kernel has touched since the L2 flush that opens
+    the graph), timed by events around the calls; median over replays."""
+    rows = []
+    for (P, B, seed) in sweep_cases():
+        bufs = []
+        for i in range(per_size):
+            peers = [torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2, tensor=i).view(np.uint8))
+                     .to(device) for r in range(P)]
+            bufs.append((peers, torch.empty(P * B, dtype=torch.uint8, device=device)))
+        calls = [lambda p=p, o=o: dc.all_gather(p, o) for (p, o) in bufs]
+        g, evs = build_step_graph(torch, flush, calls)
+        t = []
+        for _ in range(replays):
+            g.replay()
+            torch.cuda.synchronize()
+            t.append(evs[0].elapsed_time(evs[1]) * 1e3 / per_size)
+        us = statistics.median(t)
+        rows.append({"P": P, "bytes_per_rank": B, "us": us,
+                     "gbs": algorithmic_bytes(P, B) / us / 1e3})
+        del g, bufs
+    return rows
+
+
 def warm_latency_block(torch, dc, device, calls_per_graph=1000, replays=3):
     """Per-call latency of back-to-back calls with warm caches: for each
     gather of the sweep whose inputs and output fit in a quarter of L2, one
@@ -716,6 +742,7 @@ def run_dc(args) -> int:
     if not args.no_comparators:
         comparators = comparators_block(torch, dc, device, stream, flush)
         latency = warm_latency_block(torch, dc, device)
+    back_to_back = back_to_back_block(torch, dc, device, flush)
     e2e = e2e_measure(torch, dc, device, stream, cases, min(args.steps, 20))
     e2e["value"] = job_throughput(world, step_bytes, rank_max(e2e["ms_per_step"], dist, device))
 
@@ -746,6 +773,7 @@ def run_dc(args) -> int:
                                   "share": kern_time[dom] / sum(kern_time.values())}},
         "headline_4MiB_P8": {"us": big["us_mean"], "gbs": big["gbs"], "frac": big["frac"]},
         "per_call": table,
+        "per_call_back_to_back": back_to_back,
         "gpu_launches": kernels_per_step * args.steps + eager_launches,
         "wall_s_timed_region": t_wall,
         "clocks": clocks,
