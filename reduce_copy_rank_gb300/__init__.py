@@ -207,6 +207,19 @@ def _nbytes(t) -> int:
     return t.numel() * t.element_size()
 
 
+def _cur_dev() -> int:
+    """The current CUDA device: the library launches there, so every tensor
+    must live there (a pointer of another device would fault the kernel)."""
+    import torch
+
+    return torch.cuda.current_device()
+
+
+def _wrong_device(what: str, t, dev: int):
+    raise ValueError(f"{what} is on {t.device}, but the current device is cuda:{dev}; "
+                     "make it current (torch.cuda.set_device) or move the tensor")
+
+
 def _device_tensor(t, what: str):
     if not t.is_cuda:
         raise ValueError(f"{what} must be a CUDA tensor (got device {t.device})")
@@ -223,13 +236,20 @@ def all_gather(peers: Sequence, out, stream=None):
     if P == 0:
         raise ValueError("need at least one peer")
     B = peers[0].nbytes
+    if not peers[0].is_cuda:
+        _explain_peers(peers)
+    dev = _cur_dev()
     ptrs = []
-    for p in peers:
+    for r, p in enumerate(peers):
         if not p.is_cuda or p.nbytes != B or not p.is_contiguous():
             _explain_peers(peers)
+        if p.get_device() != dev:
+            _wrong_device(f"peers[{r}]", p, dev)
         ptrs.append(p.data_ptr())
     if not out.is_cuda or not out.is_contiguous():
         _device_tensor(out, "out")
+    if out.get_device() != dev:
+        _wrong_device("out", out, dev)
     if out.nbytes != P * B:
         raise ValueError(f"out holds {out.nbytes} bytes, expected P * {B} = {P * B}")
     a = array.array("Q", ptrs)
@@ -252,6 +272,7 @@ def all_gather_many(peers_per_tensor: Sequence[Sequence], outs: Sequence, stream
     if T == 0:
         return outs
     P = len(peers_per_tensor[0])
+    dev = None
     ptrs, sizes = [], []
     for t, peers in enumerate(peers_per_tensor):
         if len(peers) != P:
@@ -261,7 +282,15 @@ def all_gather_many(peers_per_tensor: Sequence[Sequence], outs: Sequence, stream
             _device_tensor(p, f"peers_per_tensor[{t}][{r}]")
             if _nbytes(p) != B:
                 raise ValueError(f"tensor {t}: all peers must have the same number of bytes")
+            if dev is None:
+                dev = _cur_dev()
+            if p.get_device() != dev:
+                _wrong_device(f"peers_per_tensor[{t}][{r}]", p, dev)
         _device_tensor(outs[t], f"outs[{t}]")
+        if dev is None:
+            dev = _cur_dev()
+        if outs[t].get_device() != dev:
+            _wrong_device(f"outs[{t}]", outs[t], dev)
         if _nbytes(outs[t]) != P * B:
             raise ValueError(f"outs[{t}] holds {_nbytes(outs[t])} bytes, expected {P * B}")
         ptrs.extend(p.data_ptr() for p in peers)
@@ -289,10 +318,15 @@ def _dtype_code(t) -> int:
 def _reduce_ptrs(ts: Sequence, what: str, count: int, dtype) -> list:
     """Data pointers of `ts` after the checks of _reduce_tensors (which runs
     only to name the offending tensor)."""
+    dev = None
     ptrs = []
-    for t in ts:
+    for i, t in enumerate(ts):
         if not t.is_cuda or t.dtype != dtype or t.numel() != count or not t.is_contiguous():
             _reduce_tensors(ts, what, count, dtype)
+        if dev is None:
+            dev = _cur_dev()
+        if t.get_device() != dev:
+            _wrong_device(f"{what}[{i}]", t, dev)
         ptrs.append(t.data_ptr())
     return ptrs
 

@@ -301,3 +301,47 @@ def test_every_documented_option_exists_and_round_trips():
         assert v >= 0, k
         with dc.options(**{k: v}):
             assert dc.get_option(k) == v
+
+
+class _FakeCudaTensor:
+    """Just enough of a CUDA tensor for the binding's checks (never launched)."""
+
+    def __init__(self, nbytes, device_index, dtype=None):
+        import torch
+
+        self.is_cuda = True
+        self.nbytes = nbytes
+        self.dtype = dtype if dtype is not None else torch.uint8
+        self._dev = device_index
+        self.device = f"cuda:{device_index}"
+
+    def is_contiguous(self):
+        return True
+
+    def get_device(self):
+        return self._dev
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+    def data_ptr(self):
+        return 0x10000 * (self._dev + 1)
+
+
+def test_tensors_on_another_device_are_rejected(monkeypatch):
+    """The library launches on the current device; a tensor elsewhere must be
+    refused before the call, not fault the kernel."""
+    monkeypatch.setattr(dc, "_cur_dev", lambda: 0)
+    peers = [_FakeCudaTensor(64, 0), _FakeCudaTensor(64, 1)]
+    with pytest.raises(ValueError, match="current device"):
+        dc.all_gather(peers, _FakeCudaTensor(128, 0))
+    with pytest.raises(ValueError, match="current device"):
+        dc.all_gather([_FakeCudaTensor(64, 0)], _FakeCudaTensor(64, 1))
+    with pytest.raises(ValueError, match="current device"):
+        dc.all_gather_many([[_FakeCudaTensor(64, 0)]], [_FakeCudaTensor(64, 2)])
+    with pytest.raises(ValueError, match="current device"):
+        dc.all_reduce([_FakeCudaTensor(64, 0), _FakeCudaTensor(64, 0)],
+                      [_FakeCudaTensor(64, 0), _FakeCudaTensor(64, 3)])
