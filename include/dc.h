@@ -222,11 +222,15 @@ const char *dc_status_name(int status);
  *                             L2 before the kernel waits for the previous
  *                             kernel in the stream (single aligned gathers and
  *                             reductions; 0 = off; default 1)
+ *   "gather_tile_min"         staged aligned gathers: the smallest tile (in
+ *                             16-byte vectors) that an output too small for a
+ *                             full tile per CTA is cut into, so that it is
+ *                             spread evenly over the SMs (default 512, measured)
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
  * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
- * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT and DC_PREFETCH set the initial
- * values (read once, at the first call).
+ * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH and
+ * DC_GATHER_TILE_MIN set the initial values (read once, at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.
  */

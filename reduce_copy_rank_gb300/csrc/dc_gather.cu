@@ -201,9 +201,9 @@ template <int BLOCK, int V, int S, int MAXS>
 __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>& p, uint32_t first,
                                                     uint32_t step) {
   extern __shared__ uint4 stage_buf[];  // [S][V][BLOCK]
-  constexpr uint32_t kTile = static_cast<uint32_t>(BLOCK) * V;
+  const uint32_t tile = static_cast<uint32_t>(p.tile_vec);  // <= BLOCK*V
   const uint32_t total = static_cast<uint32_t>(p.total_vec);
-  const uint32_t ntiles = (total + kTile - 1) / kTile;
+  const uint32_t ntiles = (total + tile - 1) / tile;
   const uint32_t vp = static_cast<uint32_t>(p.job[0].bytes >> 4);
   uint4* out = reinterpret_cast<uint4*>(p.job[0].out);
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
@@ -212,8 +212,8 @@ __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>&
   auto issue = [&](uint32_t slot, uint32_t t) {
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-      const uint32_t k = t * kTile + u * BLOCK + threadIdx.x;
-      if (t < ntiles && k < total) {
+      const uint32_t i = u * BLOCK + threadIdx.x, k = t * tile + i;
+      if (t < ntiles && i < tile && k < total) {
         if (fresh) {
           r = k / vp;
           rlo = r * vp;
@@ -242,8 +242,8 @@ __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>&
     cp_async_wait<S - 1>();  // the oldest group: tile t
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-      const uint32_t k = t * kTile + u * BLOCK + threadIdx.x;
-      if (k < total) st16(out + k, ld_shared16(sbase + 16u * BLOCK * (slot * V + u)));
+      const uint32_t i = u * BLOCK + threadIdx.x, k = t * tile + i;
+      if (i < tile && k < total) st16(out + k, ld_shared16(sbase + 16u * BLOCK * (slot * V + u)));
     }
     issue(slot, t_issue);  // refill the slot just drained
     t_issue += step;
@@ -710,11 +710,12 @@ __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat
   if constexpr (MAXJ == 1 && (MODE == kFlat1 || MODE == kFlat1Staged)) {
     pdl_launch_dependents();
     if (threadIdx.x == 0) {  // the CTA's first p.prefetch tiles
-      constexpr uint64_t kTile = static_cast<uint64_t>(kGatherBlock) *
-                                 (MODE == kFlat1Staged ? kStagedVectors : kGatherUnroll);
+      const uint64_t tile = MODE == kFlat1Staged
+                                ? static_cast<uint64_t>(p.tile_vec)
+                                : static_cast<uint64_t>(kGatherBlock) * kGatherUnroll;
       uint64_t t = blockIdx.x;
-      for (int i = 0; i < p.prefetch && t * kTile < p.total_vec; ++i, t += gridDim.x)
-        prefetch_vectors(p, t * kTile, (t + 1) * kTile);
+      for (int i = 0; i < p.prefetch && t * tile < p.total_vec; ++i, t += gridDim.x)
+        prefetch_vectors(p, t * tile, (t + 1) * tile);
     }
     pdl_wait();
   } else {
@@ -837,7 +838,11 @@ cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
       if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
     default:
-      if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1Staged>(p, grid, single, pdl, s);
+      if constexpr (MAXJ == 1) {
+        if (!single && (p.tile_vec < 1 || p.tile_vec > kGatherBlock * kStagedVectors))
+          return cudaErrorInvalidValue;
+        return launch_mode<MAXJ, MAXS, kFlat1Staged>(p, grid, single, pdl, s);
+      }
       return cudaErrorInvalidValue;
   }
 }

@@ -89,7 +89,7 @@ struct GatherParams {
   int32_t staged;       // stage aligned copies through shared memory with cp.async
   int32_t flat_ctas;    // split launch: CTAs [0, flat_ctas) copy the aligned jobs
   int32_t prefetch;     // one aligned job: tiles per CTA prefetched into L2 before the PDL wait
-  int32_t pad;
+  int32_t tile_vec;     // one aligned job, staged: vectors per tile (BLOCK*V, fewer for small outputs)
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
 };

@@ -170,6 +170,8 @@ def test_page_size_list_all_offsets():
     {"gather_staged": 1, "force_path": 2, "grid_ctas": 7000}, {"gather_staged": 1, "force_path": 1},
     {"pdl": 0}, {"gather_staged": 0}, {"gather_staged": 0, "force_path": 2, "grid_ctas": 3},
     {"prefetch": 0}, {"prefetch": 4, "force_path": 2, "grid_ctas": 2},
+    {"gather_tile_min": 32}, {"gather_tile_min": 33}, {"gather_tile_min": 1 << 20},
+    {"gather_tile_min": 33, "force_path": 2, "grid_ctas": 5}, {"gather_tile_min": 33, "prefetch": 3},
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_path_and_grid_independence(opts):
     """The bytes never depend on the path, the grid or the flat/generic
