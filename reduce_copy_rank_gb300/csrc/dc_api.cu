@@ -56,6 +56,7 @@ struct Options {
   std::atomic<long long> split_cost_pct{250};  // see plan_split
   std::atomic<long long> prefetch{1};
   std::atomic<long long> tile_min{512};  // see staged_tile
+  std::atomic<long long> reduce_tile_min{64};  // see launch_reduce_plan
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -77,6 +78,7 @@ const OptionKey kKeys[] = {
     {"gather_split_cost_pct", "DC_GATHER_SPLIT_COST_PCT", &g_opt.split_cost_pct},
     {"prefetch", "DC_PREFETCH", &g_opt.prefetch},
     {"gather_tile_min", "DC_GATHER_TILE_MIN", &g_opt.tile_min},
+    {"reduce_tile_min", "DC_REDUCE_TILE_MIN", &g_opt.reduce_tile_min},
 };
 
 void read_env_once() {
@@ -270,32 +272,26 @@ int plan_split(Params& prm, uint64_t cap) {
   return static_cast<int>(gf + gg);
 }
 
-// Vectors per tile of the staged single-job gather, chosen so that every SM
-// gets the same share of the output: a CTA moves its tile through one SM's
-// load and store ports, and a call is over when its busiest SM is.  An
-// output larger than one full tile (kGatherBlock * kStagedVectors vectors)
-// per resident CTA takes R = ceil(total / (resident * full)) rounds of
-// tiles of total / (resident * R) vectors, rounded up to 32.  A smaller one
-// is cut into tiles of about total / (sms * k) vectors, rounded up to 32,
-// with k the most CTAs per SM (up to the resident count) that keep a tile at
-// gather_tile_min vectors or more.  Measured on GB300 (14 calls back to back after an
-// L2 flush, per call): 8 x 8 KiB 2.15 -> 1.73 us, 8 x 128 KiB 2.17 -> 2.0 us,
-// 2 x 1 MiB 2.44 -> 2.17 us, 8 x 1 MiB 3.92 -> 3.47 us; whereas 256 tiles of
-// 512 vectors for 2 MiB of output (uneven over 152 SMs) took 2.46 us and tiles
-// under 512 vectors were slower for outputs of 512 KiB to 2 MiB.
-uint64_t staged_tile(uint64_t total_vec, int sms, int occ) {
-  const uint64_t full = static_cast<uint64_t>(kGatherBlock) * kStagedVectors;
-  const uint64_t lo = std::min<uint64_t>(full, static_cast<uint64_t>(std::max(32LL, g_opt.tile_min.load())));
+// Work units per tile, chosen so that every SM gets the same share of a
+// launch's units: a CTA moves its tiles through one SM's load and store ports,
+// and a call is over when its busiest SM is.  A launch of more than one full
+// tile per resident CTA (sms * occ of them) takes R = ceil(total / (sms * occ
+// * full)) rounds of tiles of total / (sms * occ * R) units, rounded up to
+// 32.  A smaller one is cut into tiles of about total / (sms * k) units,
+// rounded up to 32, with k the most CTAs per SM (up to occ) that keep a tile
+// at `min_tile` units or more.
+uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long min_tile) {
+  const uint64_t lo = std::min<uint64_t>(full, static_cast<uint64_t>(std::max(32LL, min_tile)));
   const uint64_t nsm = static_cast<uint64_t>(std::max(sms, 1));
   const uint64_t slots = nsm * static_cast<uint64_t>(std::max(occ, 1));
-  if (total_vec > slots * full) {  // several rounds: every CTA the same number of equal tiles
-    const uint64_t rounds = (total_vec + slots * full - 1) / (slots * full);
+  if (total > slots * full) {  // several rounds: every CTA the same number of equal tiles
+    const uint64_t rounds = (total + slots * full - 1) / (slots * full);
     const uint64_t per = slots * rounds;
-    return std::min(full, ((total_vec + per - 1) / per + 31) / 32 * 32);
+    return std::min(full, ((total + per - 1) / per + 31) / 32 * 32);
   }
   for (int k = std::max(occ, 1); k >= 1; --k) {
     const uint64_t per = nsm * static_cast<uint64_t>(k);
-    const uint64_t t = ((total_vec + per - 1) / per + 31) / 32 * 32;
+    const uint64_t t = ((total + per - 1) / per + 31) / 32 * 32;
     if (t >= lo) return std::min(full, t);
   }
   return lo;
@@ -339,10 +335,24 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
                          : mode == 5 ? kRealignVectors
                                      : kGatherUnroll;
       uint64_t tile = static_cast<uint64_t>(kGatherBlock) * unroll;
-      if (mode == 3) {
-        tile = staged_tile(prm.total_vec, sms, occ);
-        prm.tile_vec = static_cast<int32_t>(tile);
-      }
+      // The staged single-job kernels take even tiles: the aligned one (mode
+      // 3) of at least gather_tile_min vectors, the realigning one (mode 5)
+      // only when it has several rounds of full tiles.  Measured on GB300 (14
+      // calls back to back after an L2 flush, per call; fixed full tiles ->
+      // even tiles), aligned: 8 x 8 KiB 2.01 -> 1.74 us, 2 x 1 MiB 2.32 ->
+      // 2.16 us, 8 x 1 MiB 3.78 -> 3.48 us, 8 x 2 MiB 6.56 -> 5.83 us, 8 x 4
+      // MiB 11.2 -> 10.8 us; 256 tiles of 512 vectors for 2 MiB of output
+      // (uneven over 152 SMs) took 2.46 us, and tiles under 512 vectors were
+      // slower for outputs of 512 KiB to 2 MiB.  Realigning (payloads at +1 B,
+      // output at +3 B, 12 calls): 8 x (1 MiB+1) 7.17 -> 6.63 us, 8 x (2
+      // MiB+1) 9.44 -> 8.67 us, 8 x (4 MiB+1) 13.7 -> 13.05 us, whereas
+      // smaller tiles in a single round made 8 x (256 KiB+1) and 3 x (1
+      // MiB+1) 3-6 % slower.  Mode 5 with 64-bit indices keeps full tiles.
+      const bool wide = mode == 5 && (prm.total_vec * 16 >= (1ull << 32) || prm.job[0].bytes >= (1ull << 32));
+      if ((mode == 3 || mode == 5) && !wide)
+        tile = even_tile(prm.total_vec, sms, occ, tile,
+                         mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load());
+      if (mode == 3 || mode == 5) prm.tile_vec = static_cast<int32_t>(tile);
       grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
     }
   }
@@ -456,6 +466,7 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
   if (st != DC_OK) return st;
   const bool single = use_single(in_bytes_per_rank, g_opt.reduce_single_max.load());
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
+  prm.tile_units = kReduceBlock * reduce_unroll(reduce_pt(prm.P));
   int grid = 1;
   if (!single) {
     const int P = prm.P;
@@ -464,7 +475,22 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
     const int occ = occupancy(dev, fam, [dtype, variant, order, P] {
       return reduce_ctas_per_sm(dtype, variant, order, P);
     });
-    const uint64_t tile = static_cast<uint64_t>(kReduceBlock) * reduce_unroll(pt);
+    // One job (an all_reduce of one tensor): tiles spread evenly over the
+    // SMs.  Several jobs (reduce_scatter, batches): full tiles, which do not
+    // cut a job of a multiple of 512 units; a tile that straddles two jobs
+    // runs their parts one after the other, and for 8 shards of 64 Ki BF16
+    // elements even tiles were slower (3.70 -> 4.04 us back to back).
+    // Measured on GB300 for one all_reduce (BF16, 12 calls back to back after
+    // an L2 flush, per call; full tiles -> even tiles of >= 64 units): P = 8
+    // x 8 KiB 3.36 -> 2.53 us, 8 x 256 KiB 3.56 -> 2.70 us, 8 x 512 KiB 4.21
+    // -> 3.01 us, 8 x 2 MiB 6.64 -> 6.11 us, 8 x 8 MiB unchanged; P = 2 x 512
+    // KiB 3.97 -> 2.51 us; P = 4 x 2 MiB 5.09 -> 3.88 us.  A 32-unit minimum
+    // was no better, 128 and 256 were slower for 128-512 KiB per rank.
+    const uint64_t full = static_cast<uint64_t>(kReduceBlock) * reduce_unroll(pt);
+    const uint64_t tile = prm.njobs == 1
+                              ? even_tile(prm.total_units, sms, occ, full, g_opt.reduce_tile_min.load())
+                              : full;
+    prm.tile_units = static_cast<int32_t>(tile);
     grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
   }
   return check_launch(launch_reduce(prm, dtype, order, grid, single, g_opt.pdl.load() != 0, stream),

@@ -405,9 +405,13 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
   static_assert(S * V * 5 <= 32, "ring notes must fit one register");
   extern __shared__ uint4 stage_buf[];  // [S][V][2][BLOCK]
   const GatherJob& J = p.job[0];
-  constexpr Idx kTile = static_cast<Idx>(BLOCK) * V;
+  // <= BLOCK*V; outputs of 4 GiB or more (64-bit indices) always take full
+  // tiles, which keeps that instance of the loop within its registers
+  const Idx tile = sizeof(Idx) == 4 ? static_cast<Idx>(p.tile_vec) : static_cast<Idx>(BLOCK) * V;
   const Idx total = static_cast<Idx>(p.total_vec);
-  const Idx ntiles = (total + kTile - 1) / kTile;
+  const Idx ntiles = (total + tile - 1) / tile;
+  // this thread's vectors of a tile: u*BLOCK + threadIdx.x < tile for u < nv
+  const int nv = threadIdx.x < tile ? static_cast<int>((tile - threadIdx.x + BLOCK - 1) / BLOCK) : 0;
   const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
   uint4* const out = reinterpret_cast<uint4*>(xbase);
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
@@ -420,8 +424,8 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
     notes &= ~(((1u << (5 * V)) - 1u) << (5 * V * slot));
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-      const Idx k = t * kTile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
-      if (t < ntiles && k < total) {
+      const Idx k = t * tile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
+      if (t < ntiles && u < nv && k < total) {
         walk_to(w, p, J, xbase, k);
         if (k >= w.klo && k < w.khi) {
           const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * static_cast<uint64_t>(k));
@@ -444,8 +448,8 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
     cp_async_wait<S - 1>();
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-      const Idx k = t * kTile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
-      if (k < total) {
+      const Idx k = t * tile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
+      if (u < nv && k < total) {
         const uint32_t m = (notes >> (5 * (slot * V + u))) & 31u;
         if (m & 16u) {
           const uint32_t sh = m & 15u;
@@ -832,7 +836,11 @@ cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
       if constexpr (MAXJ > 1) return launch_mode<MAXJ, MAXS, kManySplit>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
     case kGeneral1Staged:
-      if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kGeneral1Staged>(p, grid, single, pdl, s);
+      if constexpr (MAXJ == 1) {
+        if (!single && (p.tile_vec < 1 || p.tile_vec > kGatherBlock * kRealignVectors))
+          return cudaErrorInvalidValue;
+        return launch_mode<MAXJ, MAXS, kGeneral1Staged>(p, grid, single, pdl, s);
+      }
       return cudaErrorInvalidValue;
     case kFlat1:
       if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);

@@ -89,7 +89,7 @@ struct GatherParams {
   int32_t staged;       // stage aligned copies through shared memory with cp.async
   int32_t flat_ctas;    // split launch: CTAs [0, flat_ctas) copy the aligned jobs
   int32_t prefetch;     // one aligned job: tiles per CTA prefetched into L2 before the PDL wait
-  int32_t tile_vec;     // one aligned job, staged: vectors per tile (BLOCK*V, fewer for small outputs)
+  int32_t tile_vec;     // one job, staged (modes 3, 5): vectors per tile (at most BLOCK*V)
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
 };
@@ -135,7 +135,7 @@ struct ReduceParams {
   int32_t njobs;
   int32_t P;
   int32_t prefetch;     // tiles per CTA whose inputs are prefetched into L2 before the PDL wait
-  int32_t pad;
+  int32_t tile_units;   // multi-CTA kernel: units per tile (kReduceBlock*unroll, fewer for small launches)
   uint64_t ptr[MAXPTR];
   ReduceJob job[MAXJ];
 };

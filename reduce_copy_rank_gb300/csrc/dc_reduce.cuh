@@ -303,17 +303,17 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>&
   }
 }
 
-// Tile t covers global units [t*TILE, (t+1)*TILE), TILE = BLOCK*UNROLL; a
-// CTA takes tiles first, first + step, ... so that all CTAs sweep the buffers
-// together.  A tile's job is found by walking the job table forward.
+// Tile t covers global units [t*tile, (t+1)*tile) (tile = BLOCK*UNROLL, or
+// fewer units so that a small launch reaches every SM); a CTA takes tiles
+// first, first + step, ... so that all CTAs sweep the buffers together.  A
+// tile's job is found by walking the job table forward.
 template <int DT, int ORDER, int BLOCK, int UNROLL, int PT, int MAXJ, int MAXPTR>
-__device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t first,
-                                             uint64_t step) {
-  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
-  const uint64_t ntiles = (p.total_units + kTile - 1) / kTile;
+__device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t tile,
+                                             uint64_t first, uint64_t step) {
+  const uint64_t ntiles = (p.total_units + tile - 1) / tile;
   int j = 0;
   for (uint64_t t = first; t < ntiles; t += step) {
-    const uint64_t g0 = t * kTile, g1 = min(g0 + kTile, p.total_units);
+    const uint64_t g0 = t * tile, g1 = min(g0 + tile, p.total_units);
     while (j + 1 < p.njobs && p.job[j].ufirst + p.job[j].nunits <= g0) ++j;
     for (int jj = j; jj < p.njobs && p.job[jj].ufirst < g1; ++jj) {
       const ReduceJob& J = p.job[jj];
@@ -334,15 +334,14 @@ __device__ __forceinline__ void reduce_tiles(const ReduceParams<MAXJ, MAXPTR>& p
 // taking rank q (one bulk prefetch per job the tile overlaps; scalar heads
 // and tails are left out).  Issued before the PDL wait, so the HBM latency
 // of the first tiles overlaps the end of the previous kernel in the stream.
-template <int DT, int BLOCK, int UNROLL, int MAXJ, int MAXPTR>
+template <int DT, int MAXJ, int MAXPTR>
 __device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MAXPTR>& p,
-                                                     uint64_t t) {
+                                                     uint64_t tile, uint64_t t) {
   using T = Elem<DT>;
   constexpr int E = T::kPerVec;
-  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
-  const uint64_t g0 = t * kTile;
+  const uint64_t g0 = t * tile;
   if (g0 >= p.total_units || threadIdx.x >= static_cast<unsigned>(p.P)) return;
-  const uint64_t g1 = min(g0 + kTile, p.total_units);
+  const uint64_t g1 = min(g0 + tile, p.total_units);
   for (int jj = 0; jj < p.njobs && p.job[jj].ufirst < g1; ++jj) {
     const ReduceJob& J = p.job[jj];
     if (J.ufirst + J.nunits <= g0 || (J.flags & (kJobVec | kJobRealign)) != kJobVec) continue;
@@ -356,12 +355,12 @@ __device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MA
   }
 }
 
-template <int DT, int BLOCK, int UNROLL, int MAXJ, int MAXPTR>
-__device__ __forceinline__ void reduce_enter(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t first,
-                                             uint64_t step) {
+template <int DT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void reduce_enter(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t tile,
+                                             uint64_t first, uint64_t step) {
   pdl_launch_dependents();
   for (int i = 0; i < p.prefetch; ++i)
-    reduce_prefetch_tile<DT, BLOCK, UNROLL>(p, first + static_cast<uint64_t>(i) * step);
+    reduce_prefetch_tile<DT>(p, tile, first + static_cast<uint64_t>(i) * step);
   pdl_wait();
 }
 
@@ -369,16 +368,18 @@ template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceBlock)
     dc_reduce_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
   constexpr int kUnroll = reduce_unroll(PT);
-  reduce_enter<DT, kReduceBlock, kUnroll>(p, blockIdx.x, gridDim.x);
-  reduce_tiles<DT, ORDER, kReduceBlock, kUnroll, PT>(p, blockIdx.x, gridDim.x);
+  const uint64_t tile = static_cast<uint64_t>(p.tile_units);
+  reduce_enter<DT>(p, tile, blockIdx.x, gridDim.x);
+  reduce_tiles<DT, ORDER, kReduceBlock, kUnroll, PT>(p, tile, blockIdx.x, gridDim.x);
 }
 
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceSingleBlock)
     dc_reduce_single_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
   constexpr int kUnroll = reduce_unroll(PT);
-  reduce_enter<DT, kReduceSingleBlock, kUnroll>(p, 0, 1);
-  reduce_tiles<DT, ORDER, kReduceSingleBlock, kUnroll, PT>(p, 0, 1);
+  constexpr uint64_t kTile = static_cast<uint64_t>(kReduceSingleBlock) * kUnroll;
+  reduce_enter<DT>(p, kTile, 0, 1);
+  reduce_tiles<DT, ORDER, kReduceSingleBlock, kUnroll, PT>(p, kTile, 0, 1);
 }
 
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
@@ -387,6 +388,7 @@ cudaError_t launch_pt(const ReduceParams<MAXJ, MAXPTR>& p, int grid, bool single
   if (single)
     return launch_ex(dc_reduce_single_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, 1, kReduceSingleBlock, pdl,
                      s, p);
+  if (p.tile_units < 1) return cudaErrorInvalidValue;
   return launch_ex(dc_reduce_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, grid, kReduceBlock, pdl, s, p);
 }
 

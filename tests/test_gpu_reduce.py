@@ -198,6 +198,8 @@ def test_reduce_scatter_in_place_and_ragged():
 @pytest.mark.parametrize("opts", [
     {"force_path": 1}, {"force_path": 2}, {"force_path": 2, "grid_ctas": 1},
     {"force_path": 2, "grid_ctas": 7}, {"force_path": 2, "grid_ctas": 4000},
+    {"reduce_tile_min": 32}, {"reduce_tile_min": 33}, {"reduce_tile_min": 1 << 20},
+    {"reduce_tile_min": 33, "force_path": 2, "grid_ctas": 9}, {"reduce_tile_min": 33, "prefetch": 3},
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_path_and_grid_independence(opts):
     P = 8
@@ -231,8 +233,8 @@ def test_repeatable_bits():
     ins = [W.normal_bf16_device(W.seed_for(4, 9700), r, n, "cuda") for r in range(P)]
     outs = [torch.empty_like(x) for x in ins]
     digests = set()
-    for grid in (0, 0, 0, 17, 1000):
-        with dc.options(grid_ctas=grid):
+    for grid, tmin in ((0, 64), (0, 64), (0, 64), (17, 64), (1000, 64), (0, 33), (0, 1 << 20)):
+        with dc.options(grid_ctas=grid, reduce_tile_min=tmin):
             dc.all_reduce(ins, outs)
         torch.cuda.synchronize()
         digests.add(hashlib.sha256(bits_of(outs[0]).tobytes()).hexdigest())
