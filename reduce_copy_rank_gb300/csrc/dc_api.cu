@@ -152,11 +152,12 @@ int occupancy(int dev, int family, F query) {
 }
 
 // Multi-CTA grid for `tiles` tiles of work taken round robin: at most the
-// CTAs that fit on the GPU at once, and the fewest CTAs that still finish in
-// the same number of rounds (so every CTA does the same number of tiles,
-// give or take one).
-int plan_grid(uint64_t tiles, int sms, int ctas_per_sm) {
-  const uint64_t cap = std::max<uint64_t>(1, static_cast<uint64_t>(sms) * ctas_per_sm);
+// CTAs that fit on the GPU at once (less `reserve` kept for other CTAs of the
+// launch), and the fewest CTAs that still finish in the same number of rounds
+// (so every CTA does the same number of tiles, give or take one).
+int plan_grid(uint64_t tiles, int sms, int ctas_per_sm, int reserve = 0) {
+  const uint64_t all = static_cast<uint64_t>(sms) * static_cast<uint64_t>(ctas_per_sm);
+  const uint64_t cap = std::max<uint64_t>(1, all > static_cast<uint64_t>(reserve) ? all - reserve : 1);
   uint64_t g;
   const long long forced = g_opt.grid_ctas.load();
   if (forced > 0) {
@@ -279,18 +280,20 @@ int plan_split(Params& prm, uint64_t cap) {
 // * full)) rounds of tiles of total / (sms * occ * R) units, rounded up to
 // 32.  A smaller one is cut into tiles of about total / (sms * k) units,
 // rounded up to 32, with k the most CTAs per SM (up to occ) that keep a tile
-// at `min_tile` units or more.
-uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long min_tile) {
+// at `min_tile` units or more.  `reserve` CTA slots are kept for other CTAs
+// of the launch.
+uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long min_tile, int reserve = 0) {
   const uint64_t lo = std::min<uint64_t>(full, static_cast<uint64_t>(std::max(32LL, min_tile)));
   const uint64_t nsm = static_cast<uint64_t>(std::max(sms, 1));
-  const uint64_t slots = nsm * static_cast<uint64_t>(std::max(occ, 1));
+  const uint64_t all = nsm * static_cast<uint64_t>(std::max(occ, 1));
+  const uint64_t slots = all > static_cast<uint64_t>(reserve) ? all - reserve : 1;
   if (total > slots * full) {  // several rounds: every CTA the same number of equal tiles
     const uint64_t rounds = (total + slots * full - 1) / (slots * full);
     const uint64_t per = slots * rounds;
     return std::min(full, ((total + per - 1) / per + 31) / 32 * 32);
   }
   for (int k = std::max(occ, 1); k >= 1; --k) {
-    const uint64_t per = nsm * static_cast<uint64_t>(k);
+    const uint64_t per = std::min(slots, nsm * static_cast<uint64_t>(k));
     const uint64_t t = ((total + per - 1) / per + 31) / 32 * 32;
     if (t >= lo) return std::min(full, t);
   }
@@ -348,12 +351,15 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       // MiB+1) 9.44 -> 8.67 us, 8 x (4 MiB+1) 13.7 -> 13.05 us, whereas
       // smaller tiles in a single round made 8 x (256 KiB+1) and 3 x (1
       // MiB+1) 3-6 % slower.  Mode 5 with 64-bit indices keeps full tiles.
+      // Mode 5 adds one CTA for the rank-boundary vectors (copy_boundaries),
+      // and keeps a slot free for it.
+      const int reserve = mode == 5 ? 1 : 0;
       const bool wide = mode == 5 && (prm.total_vec * 16 >= (1ull << 32) || prm.job[0].bytes >= (1ull << 32));
       if ((mode == 3 || mode == 5) && !wide)
         tile = even_tile(prm.total_vec, sms, occ, tile,
-                         mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load());
+                         mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load(), reserve);
       if (mode == 3 || mode == 5) prm.tile_vec = static_cast<int32_t>(tile);
-      grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ);
+      grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ, reserve) + reserve;
     }
   }
   return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather");

@@ -307,37 +307,66 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
   cp_async_wait<0>();
 }
 
+// The 16 source bytes starting at `a`, of which the first `len` (1..16) are
+// wanted: the aligned blocks holding the first and the last wanted byte (the
+// same block when the span does not cross a 16-byte boundary) funnel-shifted
+// by a mod 16.  Both blocks hold wanted bytes, so both lie in the source
+// allocation; bytes past `len` are whatever follows in those blocks.
+__device__ __forceinline__ uint4 load_span(const uint8_t* a, uint64_t len) {
+  const uintptr_t ia = reinterpret_cast<uintptr_t>(a);
+  const uint4 lo = ld_nc_stream(reinterpret_cast<const uint4*>(ia & ~static_cast<uintptr_t>(15)));
+  const uint4 hi = ld_nc_stream(reinterpret_cast<const uint4*>((ia + len - 1) & ~static_cast<uintptr_t>(15)));
+  return realign16(lo, hi, static_cast<uint32_t>(ia & 15u));
+}
+
+// v's bytes moved up by n (0..15) places (byte i -> i + n; little-endian).
+__device__ __forceinline__ void shift_up_bytes(uint64_t& lo, uint64_t& hi, uint32_t n) {
+  if (n >= 8) {
+    hi = lo << (8u * (n - 8u));
+    lo = 0;
+  } else if (n > 0) {
+    hi = (hi << (8u * n)) | (lo >> (64u - 8u * n));
+    lo <<= 8u * n;
+  }
+}
+
 // A vector at a rank boundary of a job of at least kGatherSmallBytes per rank
 // (x 16-byte aligned, r the rank of byte x; x may lie before the output or
-// the vector stick out of its end).  Its bytes come from the end of rank r's
-// payload and the start of rank r+1's: all 16 byte loads are issued before
-// the first store, so the vector costs one memory latency instead of one per
-// byte, and a vector inside the output is written with one 16-byte store.
+// the vector stick out of its end).  Its output bytes [y0, y1) are the end of
+// rank r's payload, [y0, z), and the start of rank r+1's, [z, y1): each part
+// is one span of at most 16 source bytes, loaded as one or two aligned
+// 16-byte blocks (all four loads issued together), shifted into place and
+// merged; a vector inside the output is written with one 16-byte store, the
+// first and last vector of the output byte by byte.
 template <int MAXJ, int MAXS>
 __device__ __forceinline__ void copy_boundary(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
                                               uint64_t x, uint32_t r) {
   const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
   const uint64_t d = J.out + static_cast<uint64_t>(r) * J.bytes;  // first output byte of rank r
+  const uint64_t y0 = max(x, J.out), y1 = min(x + 16, out_end);
+  const uint64_t z = min(d + J.bytes, y1);  // first output byte of rank r+1, or y1
   const uint8_t* s0 = reinterpret_cast<const uint8_t*>(p.src[J.src0 + r]);
   const uint8_t* s1 = r + 1 < static_cast<uint32_t>(p.P)
                           ? reinterpret_cast<const uint8_t*>(p.src[J.src0 + r + 1]) : s0;
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (uint32_t i = 0; i < 16; ++i) {
-    const uint64_t y = x + i;
-    if (y < J.out || y >= out_end) continue;
-    const uint32_t b = y < d + J.bytes ? __ldg(s0 + (y - d)) : __ldg(s1 + (y - d - J.bytes));
-    w[i >> 2] |= b << (8u * (i & 3u));
-  }
-  if (x >= J.out && x + 16 <= out_end) {
-    st16(reinterpret_cast<uint4*>(x), make_uint4(w[0], w[1], w[2], w[3]));
+  const uint4 va = load_span(s0 + (y0 - d), z - y0);
+  const uint4 vb = z < y1 ? load_span(s1, y1 - z) : va;
+  uint64_t alo = va.x | (static_cast<uint64_t>(va.y) << 32), ahi = va.z | (static_cast<uint64_t>(va.w) << 32);
+  uint64_t blo = vb.x | (static_cast<uint64_t>(vb.y) << 32), bhi = vb.z | (static_cast<uint64_t>(vb.w) << 32);
+  const uint32_t na = static_cast<uint32_t>(y0 - x), nb = static_cast<uint32_t>(z - x);
+  shift_up_bytes(alo, ahi, na);
+  shift_up_bytes(blo, bhi, nb & 15u);
+  // bytes [0, nb) from rank r, [nb, 16) from rank r+1
+  const uint64_t mlo = nb >= 8 ? ~0ull : (1ull << (8u * nb)) - 1u;
+  const uint64_t mhi = nb >= 16 ? ~0ull : nb <= 8 ? 0ull : (1ull << (8u * (nb - 8u))) - 1u;
+  const uint64_t lo = (alo & mlo) | (blo & ~mlo), hi = (ahi & mhi) | (bhi & ~mhi);
+  if (y0 == x && y1 == x + 16) {
+    st16(reinterpret_cast<uint4*>(x), make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                                                  static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32)));
     return;
   }
-#pragma unroll
-  for (uint32_t i = 0; i < 16; ++i) {
-    const uint64_t y = x + i;
-    if (y >= J.out && y < out_end)
-      *reinterpret_cast<uint8_t*>(y) = static_cast<uint8_t>(w[i >> 2] >> (8u * (i & 3u)));
+  for (uint64_t y = y0; y < y1; ++y) {
+    const uint32_t i = static_cast<uint32_t>(y - x);
+    *reinterpret_cast<uint8_t*>(y) = static_cast<uint8_t>((i < 8 ? lo >> (8u * i) : hi >> (8u * (i - 8u))) & 0xFFu);
   }
 }
 
@@ -395,10 +424,12 @@ __device__ __forceinline__ void walk_to(RankWalk<Idx>& w, const GatherParams<MAX
 // of the vector, so both lie in the source allocation) with cp.async into
 // the thread's ring slot, and notes s and "inside one rank" in 5 bits of a
 // register (S*V*5 <= 32 bits).  Draining side: the funnel shift of the two
-// blocks by s gives the 16 output bytes, one 16-byte store; a vector at a
-// rank boundary or an output end finds its rank by one division (at most
-// P+1 such vectors per job) and goes through copy_boundary.  No barrier:
-// each thread reads back only the slots it filled.
+// blocks by s gives the 16 output bytes, one 16-byte store.  No barrier:
+// each thread reads back only the slots it filled.  The vectors that are not
+// inside one rank (the ones holding d_b = out + b*B, b in [0, P], with d_b
+// not 16-byte aligned; B >= 16) are skipped here: the launch's last CTA
+// copies them (copy_boundaries), so their memory round trip runs beside the
+// ring instead of after a ring thread's last tile.
 template <int BLOCK, int V, int S, typename Idx, int MAXS>
 __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1, MAXS>& p,
                                                             Idx first, Idx step) {
@@ -451,15 +482,11 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
       const Idx k = t * tile + static_cast<Idx>(u) * BLOCK + threadIdx.x;
       if (u < nv && k < total) {
         const uint32_t m = (notes >> (5 * (slot * V + u))) & 31u;
-        if (m & 16u) {
+        if (m & 16u) {  // inside one rank (the others: copy_boundaries)
           const uint32_t sh = m & 15u;
           const uint4 lo = ld_shared16(slot_addr(slot, u, 0));
           const uint4 hi = sh ? ld_shared16(slot_addr(slot, u, 1)) : lo;
           st16(out + k, realign16(lo, hi, sh));
-        } else {
-          const uint64_t x = xbase + 16 * static_cast<uint64_t>(k);
-          const uint32_t r = x < J.out ? 0u : static_cast<uint32_t>((x - J.out) / J.bytes);
-          copy_boundary(p, J, x, r);
         }
       }
     }
@@ -468,6 +495,19 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
     slot = (slot + 1 == S) ? 0 : slot + 1;
   }
   cp_async_wait<0>();
+}
+
+// The rank-boundary vectors of one unaligned job (at least
+// kGatherSmallBytes per rank): thread b copies the vector holding d_b = out +
+// b*B, b in [0, P], if d_b is not 16-byte aligned (the byte before d_b is
+// rank b-1's, or lies before the output for b = 0).
+template <int BLOCK, int MAXS>
+__device__ __forceinline__ void copy_boundaries(const GatherParams<1, MAXS>& p) {
+  const GatherJob& J = p.job[0];
+  for (uint32_t b = threadIdx.x; b <= static_cast<uint32_t>(p.P); b += BLOCK) {
+    const uint64_t d = J.out + static_cast<uint64_t>(b) * J.bytes;
+    if (d & 15u) copy_boundary(p, J, d & ~static_cast<uint64_t>(15), b == 0 ? 0u : b - 1);
+  }
 }
 
 // The unaligned jobs of a split launch (global vectors [voff, total_vec),
@@ -667,6 +707,12 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     gather_tiles_staged<BLOCK, kStagedVectors, kStagedStages>(p, static_cast<uint32_t>(first),
                                                               static_cast<uint32_t>(step));
   else if constexpr (MODE == kGeneral1Staged && MAXJ == 1) {
+    // the last CTA copies the rank-boundary vectors, the others the rest
+    if (first + 1 == step) {
+      copy_boundaries<BLOCK>(p);
+      return;
+    }
+    --step;
     const uint64_t span = p.total_vec * 16;  // output bytes from out rounded down to 16
     if (span < (1ull << 32) && p.job[0].bytes < (1ull << 32))
       gather_tiles_staged_realign<BLOCK, kRealignVectors, kRealignStages, uint32_t>(
@@ -836,8 +882,8 @@ cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
       if constexpr (MAXJ > 1) return launch_mode<MAXJ, MAXS, kManySplit>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
     case kGeneral1Staged:
-      if constexpr (MAXJ == 1) {
-        if (!single && (p.tile_vec < 1 || p.tile_vec > kGatherBlock * kRealignVectors))
+      if constexpr (MAXJ == 1) {  // grid: at least one tile CTA and the boundary CTA
+        if (!single && (grid < 2 || p.tile_vec < 1 || p.tile_vec > kGatherBlock * kRealignVectors))
           return cudaErrorInvalidValue;
         return launch_mode<MAXJ, MAXS, kGeneral1Staged>(p, grid, single, pdl, s);
       }
