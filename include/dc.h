@@ -220,7 +220,8 @@ const char *dc_status_name(int status);
  *                             the grid between the two (default 250, measured)
  *   "prefetch"                tiles per CTA whose inputs are prefetched into
  *                             L2 before the kernel waits for the previous
- *                             kernel in the stream (single aligned gathers and
+ *                             kernel in the stream (dc_all_gather on its
+ *                             aligned and staged realigning paths, and the
  *                             reductions; 0 = off; default 1)
  *   "gather_tile_min"         staged aligned gathers: the smallest tile (in
  *                             16-byte vectors) that an output too small for a

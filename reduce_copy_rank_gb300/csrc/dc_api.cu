@@ -277,11 +277,14 @@ int plan_split(Params& prm, uint64_t cap) {
 // launch's units: a CTA moves its tiles through one SM's load and store ports,
 // and a call is over when its busiest SM is.  A launch of more than one full
 // tile per resident CTA (sms * occ of them) takes R = ceil(total / (sms * occ
-// * full)) rounds of tiles of total / (sms * occ * R) units, rounded up to
-// 32.  A smaller one is cut into tiles of about total / (sms * k) units,
-// rounded up to 32, with k the most CTAs per SM (up to occ) that keep a tile
-// at `min_tile` units or more.  `reserve` CTA slots are kept for other CTAs
-// of the launch.
+// * full)) rounds of tiles of total / (sms * occ * R) units.  A smaller one
+// is cut into tiles of about total / (sms * k) units, with k the most CTAs
+// per SM (up to occ) that keep a tile at `min_tile` units or more.  Tiles are
+// rounded up to an even number of 16-byte units, so that a warp's 32
+// consecutive units start on a 32-byte sector; coarser rounding left CTA
+// slots empty (8 x (32 MiB+1) unaligned: 37 rounds of 1024-vector tiles on
+// 443 CTAs instead of 998-vector tiles on 455).  `reserve` CTA slots are kept
+// for other CTAs of the launch.
 uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long min_tile, int reserve = 0) {
   const uint64_t lo = std::min<uint64_t>(full, static_cast<uint64_t>(std::max(32LL, min_tile)));
   const uint64_t nsm = static_cast<uint64_t>(std::max(sms, 1));
@@ -290,11 +293,11 @@ uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long mi
   if (total > slots * full) {  // several rounds: every CTA the same number of equal tiles
     const uint64_t rounds = (total + slots * full - 1) / (slots * full);
     const uint64_t per = slots * rounds;
-    return std::min(full, ((total + per - 1) / per + 31) / 32 * 32);
+    return std::min(full, ((total + per - 1) / per + 1) / 2 * 2);
   }
   for (int k = std::max(occ, 1); k >= 1; --k) {
     const uint64_t per = std::min(slots, nsm * static_cast<uint64_t>(k));
-    const uint64_t t = ((total + per - 1) / per + 31) / 32 * 32;
+    const uint64_t t = ((total + per - 1) / per + 1) / 2 * 2;
     if (t >= lo) return std::min(full, t);
   }
   return lo;

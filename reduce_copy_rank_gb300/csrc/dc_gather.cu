@@ -751,6 +751,33 @@ __device__ __forceinline__ void prefetch_vectors(const GatherParams<1, MAXS>& p,
   }
 }
 
+// One unaligned job: the source bytes of output vectors [k0, k1) (one span
+// per rank they cross, widened to the 16-byte blocks holding its first and
+// last byte, at most 32 KiB per prefetch instruction) prefetched into L2.
+template <int MAXS>
+__device__ __forceinline__ void prefetch_unaligned(const GatherParams<1, MAXS>& p, uint64_t k0,
+                                                   uint64_t k1) {
+  const GatherJob& J = p.job[0];
+  const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
+  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
+  uint64_t y = max(xbase + 16 * k0, J.out);
+  const uint64_t yend = min(xbase + 16 * k1, out_end);
+  if (y >= yend) return;
+  uint64_t r = (y - J.out) / J.bytes;
+  while (y < yend && r < static_cast<uint64_t>(p.P)) {
+    const uint64_t d = J.out + r * J.bytes;
+    const uint64_t seg_end = min(yend, d + J.bytes);
+    const uint64_t src = p.src[J.src0 + r];
+    const uint64_t a0 = (src + (y - d)) & ~static_cast<uint64_t>(15);
+    const uint64_t a1 = (src + (seg_end - d) + 15) & ~static_cast<uint64_t>(15);
+    for (uint64_t c = a0; c < a1; c += 32768)
+      prefetch_l2(reinterpret_cast<const void*>(c),
+                  static_cast<uint32_t>(min(static_cast<uint64_t>(32768), a1 - c)));
+    y = seg_end;
+    ++r;
+  }
+}
+
 // Multi-CTA gather: CTA c copies tiles c, c + gridDim.x, ...
 template <int MAXJ, int MAXS, int MODE>
 __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat1Staged) ? 4
@@ -768,6 +795,19 @@ __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat
         prefetch_vectors(p, t * tile, (t + 1) * tile);
     }
     pdl_wait();
+  } else if constexpr (MAXJ == 1 && MODE == kGeneral1Staged) {
+    // the first p.prefetch tiles of each tile CTA (all but the last CTA)
+    // prefetched before the wait; dependents are let in after it (measured:
+    // 8 x (256 KiB+1) back to back 2.87 us, 3.21 us with the trigger first,
+    // 3.04 us without the prefetch)
+    if (threadIdx.x == 0 && blockIdx.x + 1 < gridDim.x) {
+      const uint64_t tile = static_cast<uint64_t>(p.tile_vec);
+      uint64_t t = blockIdx.x;
+      for (int i = 0; i < p.prefetch && t * tile < p.total_vec; ++i, t += gridDim.x - 1)
+        prefetch_unaligned(p, t * tile, min((t + 1) * tile, p.total_vec));
+    }
+    pdl_wait();
+    pdl_launch_dependents();
   } else {
     pdl_enter();
   }
