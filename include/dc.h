@@ -231,12 +231,17 @@ const char *dc_status_name(int status);
  *                             16-byte units) that a reduction too small for a
  *                             full tile per CTA is cut into (default 64,
  *                             measured)
+ *   "reduce_staged"           1 (default) = an all_reduce of one tensor whose
+ *                             inputs sit at other offsets (mod 16 bytes) than
+ *                             its outputs, P = 2, 4 or 8, stages its input
+ *                             blocks through shared memory; 0 = realign in
+ *                             registers
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
  * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
- * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN
- * and DC_REDUCE_TILE_MIN set the initial values (read once, at the first
- * call).
+ * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
+ * DC_REDUCE_TILE_MIN and DC_REDUCE_STAGED set the initial values (read once,
+ * at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.
  */

@@ -57,6 +57,7 @@ struct Options {
   std::atomic<long long> prefetch{1};
   std::atomic<long long> tile_min{512};  // see staged_tile
   std::atomic<long long> reduce_tile_min{64};  // see launch_reduce_plan
+  std::atomic<long long> reduce_staged{1};     // see launch_reduce_plan
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -79,6 +80,7 @@ const OptionKey kKeys[] = {
     {"prefetch", "DC_PREFETCH", &g_opt.prefetch},
     {"gather_tile_min", "DC_GATHER_TILE_MIN", &g_opt.tile_min},
     {"reduce_tile_min", "DC_REDUCE_TILE_MIN", &g_opt.reduce_tile_min},
+    {"reduce_staged", "DC_REDUCE_STAGED", &g_opt.reduce_staged},
 };
 
 void read_env_once() {
@@ -113,7 +115,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 128;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + (< 72)
+constexpr int kFamilies = 128;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + (< 72); staged realigning reduction: 96 + (< 24)
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -476,11 +478,25 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
   const bool single = use_single(in_bytes_per_rank, g_opt.reduce_single_max.load());
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.tile_units = kReduceBlock * reduce_unroll(reduce_pt(prm.P));
+  prm.staged = 0;
   int grid = 1;
-  if (!single) {
+  const int pt = reduce_pt(prm.P);
+  const int pti = pt == 2 ? 1 : pt == 4 ? 2 : pt == 8 ? 3 : 0;
+  // An all_reduce of one tensor whose inputs do not all share the outputs'
+  // offset mod 16, P = 2, 4 or 8: the staged realigning kernel, one unit per
+  // thread per tile (tiles of kReduceBlock body units).
+  if (!single && variant == 0 && pt > 0 && prm.njobs == 1 &&
+      prm.job[0].flags == (kJobVec | kJobRealign) && g_opt.reduce_staged.load()) {
     const int P = prm.P;
-    const int pt = reduce_pt(P);
-    const int fam = 24 + (((dtype * 3 + variant) * 2 + order) * 4 + (pt == 2 ? 1 : pt == 4 ? 2 : pt == 8 ? 3 : 0));
+    const int occ = occupancy(dev, 96 + (dtype * 2 + order) * 4 + pti,
+                              [dtype, order, P] { return reduce_ctas_per_sm(dtype, 3, order, P); });
+    const int epv = 16 / esize_of(dtype);
+    const uint64_t nbody = (prm.job[0].count - prm.job[0].head) / static_cast<uint64_t>(epv);
+    prm.staged = 1;
+    grid = plan_grid((nbody + kReduceBlock - 1) / kReduceBlock, sms, occ);
+  } else if (!single) {
+    const int P = prm.P;
+    const int fam = 24 + (((dtype * 3 + variant) * 2 + order) * 4 + pti);
     const int occ = occupancy(dev, fam, [dtype, variant, order, P] {
       return reduce_ctas_per_sm(dtype, variant, order, P);
     });

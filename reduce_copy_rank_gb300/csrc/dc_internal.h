@@ -52,6 +52,13 @@ constexpr int kReduceUnroll = 2;         // 8-element groups in flight per threa
 __host__ __device__ constexpr int reduce_unroll(int pt) {
   return pt == 2 ? 8 : pt == 4 ? 4 : kReduceUnroll;
 }
+// The staged realigning all_reduce (one job, P = 2, 4 or 8): ring stages,
+// and per stage, rank and warp of kReduceBlock threads 33 blocks of 16 bytes
+// (P = 8: 3 x 8 x 8 x 33 x 16 B = 99 KB per CTA, two CTAs per SM).
+constexpr int kRealignReduceStages = 3;
+__host__ __device__ constexpr size_t realign_reduce_smem(int pt) {
+  return static_cast<size_t>(kRealignReduceStages) * pt * (kReduceBlock / 32) * 33 * 16;
+}
 // The compile-time rank counts of the reduction kernels (0 = any P).
 __host__ __device__ constexpr int reduce_pt(int P) { return P == 2 || P == 4 || P == 8 ? P : 0; }
 
@@ -136,6 +143,8 @@ struct ReduceParams {
   int32_t P;
   int32_t prefetch;     // tiles per CTA whose inputs are prefetched into L2 before the PDL wait
   int32_t tile_units;   // multi-CTA kernel: units per tile (kReduceBlock*unroll, fewer for small launches)
+  int32_t staged;       // one realigning all_reduce job through shared memory (dc_reduce_realign_kernel)
+  int32_t pad;
   uint64_t ptr[MAXPTR];
   ReduceJob job[MAXJ];
 };
@@ -178,7 +187,8 @@ cudaError_t launch_reduce(const Params& p, int dtype, int order, int grid, bool 
 // calibration); defined in dc_delay.cu.
 cudaError_t launch_delay(unsigned long long ns, cudaStream_t s);
 
-// variant: 0 ReduceParams1, 1 ReduceParamsS, 2 ReduceParamsL.
+// variant: 0 ReduceParams1, 1 ReduceParamsS, 2 ReduceParamsL, 3 the staged
+// realigning kernel (ReduceParams1).
 inline int reduce_ctas_per_sm(int dtype, int variant, int order, int P) {
   switch (dtype) {
     case kF16: return reduce_ctas_per_sm_f16(variant, order, P);

@@ -32,6 +32,8 @@
 // Units are taken in tiles round robin by the CTAs.
 #pragma once
 
+#include <atomic>
+
 #include "dc_device.cuh"
 #include "dc_internal.h"
 
@@ -355,6 +357,113 @@ __device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MA
   }
 }
 
+// One all_reduce job (one tensor) whose inputs do not all share the outputs'
+// address mod 16 (kJobVec | kJobRealign), P = PT known at compile time.  The
+// register path loads two 16-byte blocks per realigned input and so keeps
+// half as many units in flight; here the input blocks go through shared
+// memory instead.  Tile t is body units [t*BLOCK, (t+1)*BLOCK); a CTA takes
+// tiles first, first + step, ... through a ring of S stages.  Per stage, rank
+// and warp the ring holds 33 blocks: lane l copies (cp.async, L2 only) the
+// aligned block holding its unit's first input byte into slot l; a realigned
+// rank's unit also needs the next block, which is lane l+1's, so only the
+// last active lane of the warp copies it, into slot l+1.  After its own
+// copies are in (cp.async.wait_group) a lane synchronises with its warp
+// (__syncwarp orders the lanes' shared-memory accesses), reads slots l and
+// l+1, funnel-shifts them (realign16) and folds the P vectors exactly as the
+// register path does (fold_vector), so the bits are the same; a second
+// __syncwarp keeps slot l from being refilled before lane l-1 has read it.
+// In place: an output may be exactly its rank's input; that rank then has the
+// outputs' offset (no second block), and its unit's block is copied in before
+// the same thread writes the unit.  The scalar head and tail (fewer than 16
+// bytes each) are folded by threads 0 and BLOCK-1 of the first CTA.
+template <int DT, int ORDER, int BLOCK, int PT, int S, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void reduce_realign_staged(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t first,
+                                                      uint64_t step) {
+  using T = Elem<DT>;
+  constexpr int E = T::kPerVec;
+  constexpr uint32_t kRow = 33;                                   // slots per warp, rank and stage
+  constexpr uint32_t kRank = 16u * kRow * (BLOCK / 32);           // bytes per rank and stage
+  extern __shared__ uint4 red_stage[];                            // [S][PT][BLOCK/32][kRow]
+  const ReduceJob& J = p.job[0];
+  const uint64_t nbody = (J.count - J.head) / E;
+  const uint64_t ntiles = (nbody + BLOCK - 1) / BLOCK;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(red_stage)) +
+                         16u * ((threadIdx.x >> 5) * kRow + lane);
+  // input byte address of body unit 0 of rank q (unit b starts 16*b later)
+  auto in0 = [&](int q) {
+    return reinterpret_cast<uint64_t>(in_ptr(p, J, q)) + (J.in_off + J.head) * T::kSize;
+  };
+  auto issue = [&](uint32_t slot, uint64_t t) {
+    const uint64_t b = t * BLOCK + threadIdx.x;
+    if (t < ntiles && b < nbody) {
+      const bool last = lane == 31u || b + 1 >= nbody;  // the warp's last active lane
+#pragma unroll
+      for (int q = 0; q < PT; ++q) {
+        const uint64_t a = in0(q) + 16 * b;
+        const uint64_t blk = a & ~static_cast<uint64_t>(15);
+        const uint32_t dst = sbase + kRank * (slot * PT + q);
+        cp_async16(dst, reinterpret_cast<const void*>(blk));
+        if ((a & 15u) && last) cp_async16(dst + 16u, reinterpret_cast<const void*>(blk + 16));
+      }
+    }
+    cp_async_commit();
+  };
+  uint64_t t_issue = first;
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    issue(static_cast<uint32_t>(i), t_issue);
+    t_issue += step;
+  }
+  if (first == 0) {  // scalar head and tail, while the ring fills
+    const uint64_t tail0 = J.head + static_cast<uint64_t>(E) * nbody;
+    if (J.head && threadIdx.x == 0) fold_scalar<DT, ORDER>(p, J, 0, J.head, 1);
+    if (tail0 < J.count && threadIdx.x == BLOCK - 1) fold_scalar<DT, ORDER>(p, J, tail0, J.count, 1);
+  }
+  uint32_t slot = 0;
+  for (uint64_t t = first; t < ntiles; t += step) {
+    cp_async_wait<S - 1>();
+    __syncwarp();
+    const uint64_t b = t * BLOCK + threadIdx.x;
+    if (b < nbody) {
+      uint4 v[PT];
+#pragma unroll
+      for (int q = 0; q < PT; ++q) {
+        const uint32_t sh = static_cast<uint32_t>(in0(q) & 15u);
+        const uint32_t src = sbase + kRank * (slot * PT + q);
+        const uint4 lo = ld_shared16(src);
+        v[q] = sh ? realign16(lo, ld_shared16(src + 16u), sh) : lo;
+      }
+      float acc[E];
+      fold_vector<DT, ORDER, PT, true>(p, J, 0, v, acc);
+      const uint4 y = T::narrow(acc);
+      const uint64_t byte_off = (J.head + static_cast<uint64_t>(E) * b) * T::kSize;
+      for (uint32_t m = 0; m < J.nout; ++m) st16(reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off), y);
+    }
+    __syncwarp();
+    issue(slot, t_issue);
+    t_issue += step;
+    slot = (slot + 1 == S) ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// The input blocks of body units [b0, b1) of the staged realigning job,
+// prefetched into L2 (thread q < P: rank q's span, widened to the 16-byte
+// blocks holding its first and last byte).
+template <int DT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ void realign_prefetch(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t b0,
+                                                 uint64_t b1) {
+  using T = Elem<DT>;
+  const ReduceJob& J = p.job[0];
+  if (b0 >= b1 || threadIdx.x >= static_cast<unsigned>(p.P)) return;
+  const uint64_t a = reinterpret_cast<uint64_t>(in_ptr(p, J, threadIdx.x)) + (J.in_off + J.head) * T::kSize;
+  const uint64_t lo = (a + 16 * b0) & ~static_cast<uint64_t>(15);
+  const uint64_t hi = (a + 16 * b1 + 15) & ~static_cast<uint64_t>(15);
+  for (uint64_t c = lo; c < hi; c += 32768)
+    prefetch_l2(reinterpret_cast<const void*>(c), static_cast<uint32_t>(min(static_cast<uint64_t>(32768), hi - c)));
+}
+
 template <int DT, int MAXJ, int MAXPTR>
 __device__ __forceinline__ void reduce_enter(const ReduceParams<MAXJ, MAXPTR>& p, uint64_t tile,
                                              uint64_t first, uint64_t step) {
@@ -373,6 +482,24 @@ __global__ void __launch_bounds__(kReduceBlock)
   reduce_tiles<DT, ORDER, kReduceBlock, kUnroll, PT>(p, tile, blockIdx.x, gridDim.x);
 }
 
+// All_reduce of one tensor with realigned inputs (reduce_realign_staged);
+// tiles of kReduceBlock body units.
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+__global__ void __launch_bounds__(kReduceBlock, 2)
+    dc_reduce_realign_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
+  pdl_launch_dependents();
+  {
+    using T = Elem<DT>;
+    const ReduceJob& J = p.job[0];
+    const uint64_t nbody = (J.count - J.head) / T::kPerVec;
+    uint64_t t = blockIdx.x;
+    for (int i = 0; i < p.prefetch; ++i, t += gridDim.x)
+      realign_prefetch<DT>(p, min(t * kReduceBlock, nbody), min((t + 1) * kReduceBlock, nbody));
+  }
+  pdl_wait();
+  reduce_realign_staged<DT, ORDER, kReduceBlock, PT, kRealignReduceStages>(p, blockIdx.x, gridDim.x);
+}
+
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 __global__ void __launch_bounds__(kReduceSingleBlock)
     dc_reduce_single_kernel(const __grid_constant__ ReduceParams<MAXJ, MAXPTR> p) {
@@ -382,9 +509,35 @@ __global__ void __launch_bounds__(kReduceSingleBlock)
   reduce_tiles<DT, ORDER, kReduceSingleBlock, kUnroll, PT>(p, kTile, 0, 1);
 }
 
+// Kernels that ask for more than 48 KB of dynamic shared memory must say so
+// once per device.
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+cudaError_t allow_realign_smem() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(dc_reduce_realign_kernel<DT, ORDER, PT, MAXJ, MAXPTR>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(realign_reduce_smem(PT)));
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
 cudaError_t launch_pt(const ReduceParams<MAXJ, MAXPTR>& p, int grid, bool single, bool pdl,
                       cudaStream_t s) {
+  if constexpr (PT > 0 && MAXJ == 1) {
+    if (!single && p.staged) {  // the planner checked: one job, kJobVec | kJobRealign
+      if (p.njobs != 1 || p.job[0].flags != (kJobVec | kJobRealign)) return cudaErrorInvalidValue;
+      const cudaError_t e = allow_realign_smem<DT, ORDER, PT, MAXJ, MAXPTR>();
+      if (e != cudaSuccess) return e;
+      return launch_ex(dc_reduce_realign_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, grid, kReduceBlock, pdl, s,
+                       p, realign_reduce_smem(PT));
+    }
+  }
   if (single)
     return launch_ex(dc_reduce_single_kernel<DT, ORDER, PT, MAXJ, MAXPTR>, 1, kReduceSingleBlock, pdl,
                      s, p);
@@ -419,6 +572,29 @@ int occupancy_pt() {
     n = 1;
   }
   return n > 0 ? n : 1;
+}
+
+template <int DT, int ORDER, int PT, int MAXJ, int MAXPTR>
+int occupancy_realign_pt() {
+  int n = 0;
+  cudaError_t e = allow_realign_smem<DT, ORDER, PT, MAXJ, MAXPTR>();
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_reduce_realign_kernel<DT, ORDER, PT, MAXJ, MAXPTR>,
+                                                      kReduceBlock, realign_reduce_smem(PT));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+template <int DT, int ORDER, int MAXJ, int MAXPTR>
+int occupancy_realign_order(int P) {
+  switch (reduce_pt(P)) {
+    case 2: return occupancy_realign_pt<DT, ORDER, 2, MAXJ, MAXPTR>();
+    case 4: return occupancy_realign_pt<DT, ORDER, 4, MAXJ, MAXPTR>();
+    default: return occupancy_realign_pt<DT, ORDER, 8, MAXJ, MAXPTR>();
+  }
 }
 
 template <int DT, int ORDER, int MAXJ, int MAXPTR>
@@ -459,6 +635,10 @@ int occupancy_dtype(int order, int P) {
     switch (variant) {                                                                             \
       case 0: return red::occupancy_dtype<DT, 1, 2 * kMaxRanks>(order, P);                        \
       case 1: return red::occupancy_dtype<DT, kMaxRanks, 4 * kMaxRanks>(order, P);                \
+      case 3:                                                                                      \
+        return order == kOrderTree                                                                 \
+                   ? red::occupancy_realign_order<DT, kOrderTree, 1, 2 * kMaxRanks>(P)             \
+                   : red::occupancy_realign_order<DT, kOrderLinear, 1, 2 * kMaxRanks>(P);          \
       default: return red::occupancy_dtype<DT, kManyMaxReduceJobs, kManyMaxReducePtrs>(order, P); \
     }                                                                                              \
   }                                                                                                \

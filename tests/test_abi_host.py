@@ -296,7 +296,7 @@ def test_every_documented_option_exists_and_round_trips():
     keys = re.findall(r'\*   "([a-z_]+)"', open(HEADER).read())
     assert {"gather_single_max_bytes", "reduce_single_max_bytes", "prefetch",
             "gather_split_cost_pct", "gather_staged", "pdl", "gather_tile_min",
-            "reduce_tile_min"} <= set(keys)
+            "reduce_tile_min", "reduce_staged"} <= set(keys)
     for k in keys:
         v = dc.get_option(k)
         assert v >= 0, k

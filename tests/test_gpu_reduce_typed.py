@@ -240,12 +240,15 @@ def _at_offsets(cols, dtype, offs):
     return out
 
 
+@pytest.mark.parametrize("staged", [1, 0])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("order", ORDERS)
-def test_realigned_inputs(dtype, order):
+def test_realigned_inputs(dtype, order, staged):
     """Inputs at different offsets from 16 bytes, outputs aligned: 16-byte
     units anchored at the outputs, every input realigned (all_reduce and
-    reduce_scatter, compile-time and runtime P)."""
+    reduce_scatter, compile-time and runtime P), with the all_reduce of one
+    tensor on the shared-memory staged kernel (P = 2, 4, 8) or on the
+    register path."""
     epv = 4 if dtype == "f32" else 8
     rng = np.random.default_rng(W.seed_for(4, 9990))
     for P in (2, 3, 4, 8, 13):
@@ -255,9 +258,10 @@ def test_realigned_inputs(dtype, order):
             cols = [random_bits(W.seed_for(4, 9991 + P), r, P * C, dtype) for r in range(P)]
             ins = _at_offsets(cols, dtype, offs)
             outs = [torch.empty(P * C, dtype=torch_dtype(dtype), device="cuda") for _ in range(P)]
-            dc.all_reduce(ins, outs, order=order)
             shards = [torch.empty(C, dtype=torch_dtype(dtype), device="cuda") for _ in range(P)]
-            dc.reduce_scatter(ins, shards, order=order)
+            with dc.options(reduce_staged=staged):
+                dc.all_reduce(ins, outs, order=order)
+                dc.reduce_scatter(ins, shards, order=order)
             torch.cuda.synchronize()
             want = np.asarray(oracle.all_reduce(cols, dtype, order)).view(NP_OF[dtype])
             for r in range(P):
@@ -280,6 +284,28 @@ def test_in_place_at_disagreeing_offsets():
     torch.cuda.synchronize()
     for r in range(P):
         assert_typed_equal(typed_bits(bufs[r], "bf16"), want, "bf16", f"rank {r}")
+
+
+@pytest.mark.parametrize("opts", [{}, {"grid_ctas": 1}, {"grid_ctas": 3}, {"grid_ctas": 5000},
+                                  {"prefetch": 0}, {"prefetch": 5}, {"pdl": 0}, {"force_path": 1}],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "default")
+def test_realigned_in_place_and_grids(opts):
+    """The staged realigning all_reduce with two ranks in place (their
+    outputs are exactly their inputs, at the outputs' offset) and two ranks'
+    inputs off by 1 and 3 elements; sizes around the tile and the ring (256
+    units per tile), odd grids and prefetch depths."""
+    P = 4
+    for n in (8 * 256 * 3 + 5, 8 * 256 * 7 + 8 * 3 + 1, 100003):
+        cols = [random_bits(W.seed_for(4, 9997), r, n, "bf16") for r in range(P)]
+        want = np.asarray(oracle.all_reduce(cols, "bf16", "tree")).view(np.uint16)
+        ins = _at_offsets(cols, "bf16", [0, 1, 0, 3])
+        outs = [ins[0], torch.empty(n, dtype=torch.bfloat16, device="cuda"), ins[2],
+                torch.empty(n, dtype=torch.bfloat16, device="cuda")]
+        with dc.options(**opts):
+            dc.all_reduce(ins, outs, order="tree")
+        torch.cuda.synchronize()
+        for r in range(P):
+            assert_typed_equal(typed_bits(outs[r], "bf16"), want, "bf16", f"n={n} {opts} rank {r}")
 
 
 def test_full_size_realigned_all_reduce():
