@@ -341,9 +341,9 @@ def build_gather_calls(torch, dc, device, cases):
 def reductions_block(torch, dc, device, stream, flush, peak):
     """The other paths, each measured like the sweep (flush, CUDA events,
     median of 5): all_reduce at the five per-rank sizes, reduce_scatter
-    16384x8192 per rank, the typed, tree and batched reductions, unaligned
-    gathers of 4 MiB+1 B and 32 MiB+1 B per rank, all_gather_many of the six
-    mixed tensors (P=8)."""
+    16384x8192 per rank, the typed, tree and batched reductions, an
+    all_reduce with one rank's input realigned, unaligned gathers of 4 MiB+1 B
+    and 32 MiB+1 B per rank, all_gather_many of the six mixed tensors (P=8)."""
     rows = []
     P = W.CONFIG4_P
     for name, n in W.CONFIG4_COUNTS.items():
@@ -365,6 +365,18 @@ def reductions_block(torch, dc, device, stream, flush, peak):
                  "us": us, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     del ins, outs
     rows.extend(typed_rows(torch, dc, device, stream, flush, peak))
+    # all_reduce with rank 1's input one element past the others' alignment
+    # (8627x8192 per rank, P=8): the realigning path
+    n = W.CONFIG4_COUNTS["8627x8192"]
+    store = [W.normal_bf16_device(W.seed_for(4, 9920), r, n + 8, device) for r in range(P)]
+    ins = [store[r][(1 if r == 1 else 0):(1 if r == 1 else 0) + n] for r in range(P)]
+    outs = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_reduce(ins, outs)], 5)[0])
+    nbytes = 4 * P * n
+    rows.append({"op": "all_reduce_bf16_realigned", "P": P, "count": n,
+                 "shape": "8627x8192, rank 1's input one element off 16 bytes", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    del store, ins, outs
     for B in (4 * 1024 * 1024 + 1, 32 * 1024 * 1024 + 1):  # unaligned: payloads +1, output +3
         peers = [W.random_bytes_device(W.seed_for(3, 9000), r, B + 1, device)[1:] for r in range(8)]
         out = torch.empty(8 * B + 3, dtype=torch.uint8, device=device)[3:]

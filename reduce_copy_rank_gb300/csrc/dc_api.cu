@@ -282,12 +282,15 @@ int plan_split(Params& prm, uint64_t cap) {
 // * full)) rounds of tiles of total / (sms * occ * R) units.  A smaller one
 // is cut into tiles of about total / (sms * k) units, with k the most CTAs
 // per SM (up to occ) that keep a tile at `min_tile` units or more.  Tiles are
-// rounded up to an even number of 16-byte units, so that a warp's 32
-// consecutive units start on a 32-byte sector; coarser rounding left CTA
-// slots empty (8 x (32 MiB+1) unaligned: 37 rounds of 1024-vector tiles on
-// 443 CTAs instead of 998-vector tiles on 455).  `reserve` CTA slots are kept
-// for other CTAs of the launch.
-uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long min_tile, int reserve = 0) {
+// rounded up to a multiple of `gran` units: 32 where every unit is a 16-byte
+// aligned load or store, so that each warp access covers whole 128-byte
+// lines (the 8627x8192 all_reduce took 7 % longer with tiles of 510 units
+// than of 512); 2 for the realigning gather, whose loads are not aligned
+// anyway and where rounding to 32 left CTA slots empty (8 x (32 MiB+1): 37
+// rounds of 1024-vector tiles on 443 CTAs instead of 998-vector tiles on
+// 455).  `reserve` CTA slots are kept for other CTAs of the launch.
+uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long min_tile, uint64_t gran,
+                   int reserve = 0) {
   const uint64_t lo = std::min<uint64_t>(full, static_cast<uint64_t>(std::max(32LL, min_tile)));
   const uint64_t nsm = static_cast<uint64_t>(std::max(sms, 1));
   const uint64_t all = nsm * static_cast<uint64_t>(std::max(occ, 1));
@@ -295,11 +298,11 @@ uint64_t even_tile(uint64_t total, int sms, int occ, uint64_t full, long long mi
   if (total > slots * full) {  // several rounds: every CTA the same number of equal tiles
     const uint64_t rounds = (total + slots * full - 1) / (slots * full);
     const uint64_t per = slots * rounds;
-    return std::min(full, ((total + per - 1) / per + 1) / 2 * 2);
+    return std::min(full, ((total + per - 1) / per + gran - 1) / gran * gran);
   }
   for (int k = std::max(occ, 1); k >= 1; --k) {
     const uint64_t per = std::min(slots, nsm * static_cast<uint64_t>(k));
-    const uint64_t t = ((total + per - 1) / per + 1) / 2 * 2;
+    const uint64_t t = ((total + per - 1) / per + gran - 1) / gran * gran;
     if (t >= lo) return std::min(full, t);
   }
   return lo;
@@ -362,7 +365,8 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       const bool wide = mode == 5 && (prm.total_vec * 16 >= (1ull << 32) || prm.job[0].bytes >= (1ull << 32));
       if ((mode == 3 || mode == 5) && !wide)
         tile = even_tile(prm.total_vec, sms, occ, tile,
-                         mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load(), reserve);
+                         mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load(), mode == 5 ? 2 : 32,
+                         reserve);
       if (mode == 3 || mode == 5) prm.tile_vec = static_cast<int32_t>(tile);
       grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ, reserve) + reserve;
     }
@@ -513,7 +517,7 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
     // was no better, 128 and 256 were slower for 128-512 KiB per rank.
     const uint64_t full = static_cast<uint64_t>(kReduceBlock) * reduce_unroll(pt);
     const uint64_t tile = prm.njobs == 1
-                              ? even_tile(prm.total_units, sms, occ, full, g_opt.reduce_tile_min.load())
+                              ? even_tile(prm.total_units, sms, occ, full, g_opt.reduce_tile_min.load(), 32)
                               : full;
     prm.tile_units = static_cast<int32_t>(tile);
     grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
