@@ -71,6 +71,30 @@ __device__ __forceinline__ void cursor_to_job(const GatherParams<MAXJ, MAXS>& p,
   }
 }
 
+// The job holding global vector k (k < total_vec): the last job whose first
+// vector is at or before k (jobs are numbered in vector order), found by
+// binary search, so that a thread whose first vector lies deep in a long job
+// table does not walk the table from its start.
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ int job_of(const GatherParams<MAXJ, MAXS>& p, uint64_t k) {
+  int lo = 0, hi = p.njobs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.job[mid].vfirst <= k)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// A cursor at the job holding global vector k (or at job 0 past the end).
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ Cursor cursor_at(const GatherParams<MAXJ, MAXS>& p, uint64_t k) {
+  const int j = k < p.total_vec ? job_of(p, k) : 0;
+  return Cursor{j, p.job[j].vfirst, p.job[j].vfirst + p.job[j].nvec, true, 0, 0, 0};
+}
+
 // Flat job: rank r owns job-local vectors [r*vp, (r+1)*vp), vp = B/16.
 template <int MAXJ, int MAXS>
 __device__ __forceinline__ const uint4* flat_source(const GatherParams<MAXJ, MAXS>& p, Cursor& c,
@@ -264,9 +288,9 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
   const uint64_t total = p.flat_vec;
   const uint64_t ntiles = (total + kTile - 1) / kTile;
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
-  Cursor c{0, p.job[0].vfirst, p.job[0].vfirst + p.job[0].nvec, true, 0, 0, 0};
-  int jd = 0;
-  uint64_t dbeg = p.job[0].vfirst, dend = dbeg + p.job[0].nvec;
+  Cursor c = cursor_at(p, first * kTile + threadIdx.x);
+  int jd = c.j;
+  uint64_t dbeg = c.jbeg, dend = c.jend;
   auto issue = [&](uint32_t slot, uint64_t t) {
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -510,14 +534,49 @@ __device__ __forceinline__ void copy_boundaries(const GatherParams<1, MAXS>& p) 
   }
 }
 
+// Bytes [x, x+16) of a job of fewer than kGatherSmallBytes per rank (the
+// whole job is under kMaxRanks*128 bytes, so 32-bit offsets): the rank of
+// the first byte by one division, then byte by byte forward; all 16 loads
+// are issued before the first store.
+template <int MAXJ, int MAXS>
+__device__ __forceinline__ void copy_small_vector(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J,
+                                                  uint64_t x) {
+  const uint64_t out_end = J.out + static_cast<uint64_t>(p.P) * J.bytes;
+  const uint32_t B = static_cast<uint32_t>(J.bytes);
+  const uint32_t lead = x < J.out ? static_cast<uint32_t>(J.out - x) : 0u;  // bytes before the output
+  const uint32_t o0 = static_cast<uint32_t>(x + lead - J.out);
+  uint32_t q = o0 / B, off = o0 - q * B;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (uint32_t i = 0; i < 16; ++i) {
+    if (i >= lead && x + i < out_end) {
+      const uint32_t b = __ldg(reinterpret_cast<const uint8_t*>(p.src[J.src0 + q]) + off);
+      w[i >> 2] |= b << (8u * (i & 3u));
+      if (++off == B) {
+        ++q;
+        off = 0;
+      }
+    }
+  }
+  if (lead == 0 && x + 16 <= out_end) {
+    st16(reinterpret_cast<uint4*>(x), make_uint4(w[0], w[1], w[2], w[3]));
+    return;
+  }
+#pragma unroll
+  for (uint32_t i = 0; i < 16; ++i)
+    if (i >= lead && x + i < out_end)
+      *reinterpret_cast<uint8_t*>(x + i) = static_cast<uint8_t>(w[i >> 2] >> (8u * (i & 3u)));
+}
+
 // The unaligned jobs of a split launch (global vectors [voff, total_vec),
 // after the aligned jobs), through the same kind of shared-memory ring as
 // gather_tiles_staged_realign.  The issuing side walks jobs forward and,
 // inside a job of at least kGatherSmallBytes per rank, its ranks (RankWalk
 // in job-local vector units); the draining side walks jobs only, for each
 // vector's output address, and reads the vector's shift and kind from the
-// register notes.  Vectors of smaller jobs and vectors at rank boundaries or
-// output ends are copied byte by byte.
+// register notes.  A vector of a smaller job (copy_small_vector) or at a
+// rank boundary or output end (copy_boundary) is copied with its loads
+// issued before its stores, so it costs one memory round trip.
 template <int BLOCK, int V, int S, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherParams<MAXJ, MAXS>& p,
                                                                  uint64_t first, uint64_t step,
@@ -529,11 +588,11 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
   const uint64_t ntiles = (total - voff + kTile - 1) / kTile;
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
   // issuing side: job j (vectors [jbeg, jend)), its ranks
-  int j = 0;
+  int j = 0;  // (a binary search here, as in the other job kernels, spilled registers)
   uint64_t jbeg = p.job[0].vfirst, jend = jbeg + p.job[0].nvec;
   RankWalk<uint64_t> w{0, 0, 0, 0, 0, true};
   // draining side: job jd (vectors [dbeg, dend))
-  int jd = 0;
+  int jd = j;
   uint64_t dbeg = jbeg, dend = jend;
   uint32_t notes = 0;  // 5 bits per ring vector: s | inside << 4
   auto slot_addr = [&](uint32_t slot, int u, int h) {
@@ -596,9 +655,10 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
           st16(reinterpret_cast<uint4*>(xbase) + kl, realign16(lo, hi, sh));
         } else {
           const uint64_t x = xbase + 16 * kl;
-          const bool small = (J.flags & kJobSmall) != 0;
-          const uint32_t r = small || x < J.out ? 0u : static_cast<uint32_t>((x - J.out) / J.bytes);
-          copy_bytes(p, J, x, r, small);
+          if (J.flags & kJobSmall)
+            copy_small_vector(p, J, x);
+          else
+            copy_boundary(p, J, x, x < J.out ? 0u : static_cast<uint32_t>((x - J.out) / J.bytes));
         }
       }
     }
@@ -616,7 +676,7 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
                                              uint64_t step, uint64_t voff = 0) {
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
   const uint64_t ntiles = (p.total_vec - voff + kTile - 1) / kTile;
-  Cursor c{0, p.job[0].vfirst, p.job[0].vfirst + p.job[0].nvec, true, 0, 0, 0};
+  Cursor c = cursor_at(p, voff + first * kTile + threadIdx.x);
   for (uint64_t t = first; t < ntiles; t += step) {
     const uint64_t base = voff + t * kTile + threadIdx.x;
     uint4 lo[UNROLL], hi[UNROLL];
