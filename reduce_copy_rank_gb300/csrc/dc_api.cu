@@ -321,7 +321,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   prm.staged = g_opt.gather_staged.load() ? 1 : 0;
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.flat_ctas = 0;
-  prm.tile_vec = kGatherBlock * kStagedVectors;
+  prm.tile_vec = 0;  // single-CTA launches: the kernel's own tile
   int grid = 1;
   if (!single) {
     int mode = gather_mode_of(prm);
@@ -363,11 +363,11 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       // and keeps a slot free for it.
       const int reserve = mode == 5 ? 1 : 0;
       const bool wide = mode == 5 && (prm.total_vec * 16 >= (1ull << 32) || prm.job[0].bytes >= (1ull << 32));
-      if ((mode == 3 || mode == 5) && !wide)
+      if ((mode == 2 || mode == 3 || mode == 5) && !wide)
         tile = even_tile(prm.total_vec, sms, occ, tile,
                          mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load(), mode == 5 ? 2 : 32,
                          reserve);
-      if (mode == 3 || mode == 5) prm.tile_vec = static_cast<int32_t>(tile);
+      if (mode == 2 || mode == 3 || mode == 5) prm.tile_vec = static_cast<int32_t>(tile);
       grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ, reserve) + reserve;
     }
   }

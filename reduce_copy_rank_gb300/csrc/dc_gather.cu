@@ -176,21 +176,24 @@ __device__ __forceinline__ void copy_bytes(const GatherParams<MAXJ, MAXS>& p, co
 template <int BLOCK, int UNROLL, typename Idx, int MAXS>
 __device__ __forceinline__ void gather_tiles_flat1(const GatherParams<1, MAXS>& p, Idx first,
                                                    Idx step) {
-  constexpr Idx kTile = static_cast<Idx>(BLOCK) * UNROLL;
+  // the launch's tile (multi-CTA launches), else a full BLOCK*UNROLL
+  const Idx tile = p.tile_vec > 0 && static_cast<Idx>(p.tile_vec) < static_cast<Idx>(BLOCK) * UNROLL
+                       ? static_cast<Idx>(p.tile_vec)
+                       : static_cast<Idx>(BLOCK) * UNROLL;
   const Idx total = static_cast<Idx>(p.total_vec);
-  const Idx ntiles = (total + kTile - 1) / kTile;
+  const Idx ntiles = (total + tile - 1) / tile;
   const Idx vp = static_cast<Idx>(p.job[0].bytes >> 4);
   uint4* out = reinterpret_cast<uint4*>(p.job[0].out);
   uint32_t r = 0;
   Idx rlo = 0, rhi = vp;
   bool fresh = true;
   for (Idx t = first; t < ntiles; t += step) {
-    const Idx base = t * kTile + threadIdx.x;
+    const Idx base = t * tile + threadIdx.x;
     uint4 v[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const Idx k = base + static_cast<Idx>(u) * BLOCK;
-      if (k < total) {
+      if (static_cast<Idx>(u) * BLOCK + threadIdx.x < tile && k < total) {
         if (fresh) {
           r = static_cast<uint32_t>(k / vp);
           rlo = static_cast<Idx>(r) * vp;
@@ -208,7 +211,7 @@ __device__ __forceinline__ void gather_tiles_flat1(const GatherParams<1, MAXS>& 
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const Idx k = base + static_cast<Idx>(u) * BLOCK;
-      if (k < total) st16(out + k, v[u]);
+      if (static_cast<Idx>(u) * BLOCK + threadIdx.x < tile && k < total) st16(out + k, v[u]);
     }
   }
 }
@@ -220,7 +223,11 @@ __device__ __forceinline__ void gather_tiles_flat1(const GatherParams<1, MAXS>& 
 // are already in flight, and in-flight data costs shared memory instead of
 // registers (192 KB per SM instead of 128 KB).  Each thread only reads back
 // the slots it filled itself, so no barrier is needed; the waits are
-// cp.async.wait_group, a hardware wait on the thread's own copies.
+// cp.async.wait_group, a hardware wait on the thread's own copies.  When
+// every CTA has one tile at most (outputs up to one full tile per resident
+// CTA, 14.9 MB), there is nothing to overlap, and the loads go straight to
+// registers: back to back, 8 x 128 KiB 2.02 -> 1.87 us per call, the same as
+// the register kernel (mode 2).
 template <int BLOCK, int V, int S, int MAXS>
 __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>& p, uint32_t first,
                                                     uint32_t step) {
@@ -233,6 +240,33 @@ __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>&
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
   uint32_t r = 0, rlo = 0, rhi = vp;
   bool fresh = true;
+  if (ntiles <= step) {  // one tile per CTA: no ring, the loads go straight to registers
+    uint4 v[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint32_t i = u * BLOCK + threadIdx.x, k = first * tile + i;
+      if (i < tile && k < total) {
+        if (fresh) {
+          r = k / vp;
+          rlo = r * vp;
+          rhi = rlo + vp;
+          fresh = false;
+        }
+        while (k >= rhi) {
+          ++r;
+          rlo = rhi;
+          rhi += vp;
+        }
+        v[u] = ld_nc_stream(reinterpret_cast<const uint4*>(p.src[r]) + (k - rlo));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint32_t i = u * BLOCK + threadIdx.x, k = first * tile + i;
+      if (i < tile && k < total) st16(out + k, v[u]);
+    }
+    return;
+  }
   auto issue = [&](uint32_t slot, uint32_t t) {
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -847,9 +881,7 @@ __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat
   if constexpr (MAXJ == 1 && (MODE == kFlat1 || MODE == kFlat1Staged)) {
     pdl_launch_dependents();
     if (threadIdx.x == 0) {  // the CTA's first p.prefetch tiles
-      const uint64_t tile = MODE == kFlat1Staged
-                                ? static_cast<uint64_t>(p.tile_vec)
-                                : static_cast<uint64_t>(kGatherBlock) * kGatherUnroll;
+      const uint64_t tile = static_cast<uint64_t>(p.tile_vec);
       uint64_t t = blockIdx.x;
       for (int i = 0; i < p.prefetch && t * tile < p.total_vec; ++i, t += gridDim.x)
         prefetch_vectors(p, t * tile, (t + 1) * tile);
