@@ -202,8 +202,13 @@ const char *dc_status_name(int status);
  * Process-wide tuning and test options.  Keys:
  *   "force_path"              0 = automatic, 1 = single CTA, 2 = multi CTA
  *   "force_generic"           1 = never use the flat aligned gather path
- *   "gather_single_max_bytes" single-CTA gather up to this many output bytes
- *                             (default 16384, measured)
+ *   "gather_single_max_bytes" dc_all_gather on one CTA up to this many output
+ *                             bytes (default 0: the grid was never slower on
+ *                             GB300; an unaligned gather of fewer than 128
+ *                             bytes per rank always runs on one CTA)
+ *   "gather_many_single_max_bytes"
+ *                             dc_all_gather_many on one CTA up to this many
+ *                             output bytes in all (default 16384, measured)
  *   "reduce_single_max_bytes" single-CTA reductions up to this many input
  *                             bytes per rank (default 0: the grid was never
  *                             slower on GB300)
@@ -238,7 +243,8 @@ const char *dc_status_name(int status);
  *                             registers
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
- * DC_GATHER_SINGLE_MAX_BYTES, DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
+ * DC_GATHER_SINGLE_MAX_BYTES, DC_GATHER_MANY_SINGLE_MAX_BYTES,
+ * DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
  * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
  * DC_REDUCE_TILE_MIN and DC_REDUCE_STAGED set the initial values (read once,
  * at the first call).

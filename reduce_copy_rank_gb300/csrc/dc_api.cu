@@ -33,21 +33,29 @@ using namespace dc;
 thread_local char g_err[512] = "";
 std::atomic<unsigned long long> g_launches{0};
 
-// Single-CTA thresholds measured on GB300 (bench.py --crossover: per-call
-// time of 200 back-to-back calls in a CUDA graph, where differences of 0.1 us
-// show; a call timed alone after an L2 flush reads within one 2 us tick of
-// the event clock for both paths at these sizes).  Gather: one CTA is faster
-// up to 16 KiB of output (P = 2 and P = 8: 1.34 vs 1.39-1.45 us) and slower
-// from 32 KiB (1.77 vs 1.64 us; 2.5 vs 1.6 us at 64 KiB).  All_reduce (P = 8):
-// the grid is never slower, from 1 KiB per rank (1.86 vs 1.93 us) up, so the
-// single-CTA reduction is used only when forced.
-constexpr long long kDefaultGatherSingleMax = 16 * 1024;
+// Single-CTA thresholds measured on GB300 (per-call time of back-to-back
+// calls in a CUDA graph: 14 calls on distinct buffers after an L2 flush, and
+// 200 identical calls with warm caches; a call timed alone after an L2 flush
+// reads within one 2 us tick of the event clock for both paths at these
+// sizes).  Gather: since the multi-CTA kernel spreads a small output evenly
+// over the SMs and loads a single round straight into registers, it is
+// faster at every size measured, 2 to 32 KiB of output (2 KiB: 1.42-1.56 vs
+// 1.56-1.76 us cold, 0.94-0.99 vs 1.12-1.18 us warm; 16 KiB: 1.56-1.68 vs
+// 1.75-1.90 us cold); before those two changes one CTA won up to 16 KiB.
+// All_reduce (P = 8): the grid is never slower, from 1 KiB per rank (1.86 vs
+// 1.93 us) up.  So the single-CTA kernels run only when forced.
+constexpr long long kDefaultGatherSingleMax = 0;
+// all_gather_many: one CTA up to 16 KiB of output (4 tensors of 512-2048 B x
+// 4 ranks: 2.44 vs 2.93 us cold, 1.73 vs 2.36 us warm; the split launch
+// costs more than it spreads).
+constexpr long long kDefaultGatherManySingleMax = 16 * 1024;
 constexpr long long kDefaultReduceSingleMax = 0;
 
 struct Options {
   std::atomic<long long> force_path{0};
   std::atomic<long long> force_generic{0};
   std::atomic<long long> gather_single_max{kDefaultGatherSingleMax};
+  std::atomic<long long> gather_many_single_max{kDefaultGatherManySingleMax};
   std::atomic<long long> reduce_single_max{kDefaultReduceSingleMax};
   std::atomic<long long> grid_ctas{0};
   std::atomic<long long> test_fail_launch{0};
@@ -71,6 +79,7 @@ const OptionKey kKeys[] = {
     {"force_path", "DC_FORCE_PATH", &g_opt.force_path},
     {"force_generic", "DC_FORCE_GENERIC", &g_opt.force_generic},
     {"gather_single_max_bytes", "DC_GATHER_SINGLE_MAX_BYTES", &g_opt.gather_single_max},
+    {"gather_many_single_max_bytes", "DC_GATHER_MANY_SINGLE_MAX_BYTES", &g_opt.gather_many_single_max},
     {"reduce_single_max_bytes", "DC_REDUCE_SINGLE_MAX_BYTES", &g_opt.reduce_single_max},
     {"grid_ctas", "DC_GRID_CTAS", &g_opt.grid_ctas},
     {"test_fail_launch", nullptr, &g_opt.test_fail_launch},
@@ -317,7 +326,16 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   if (st != DC_OK) return st;
   st = sm_count(dev, &sms);
   if (st != DC_OK) return st;
-  const bool single = use_single(out_bytes, g_opt.gather_single_max.load());
+  // One tensor: the grid, except a job under kGatherSmallBytes per rank (at
+  // most 8 KiB of output), whose vectors are all byte-assembled and which
+  // one CTA copies with each vector's loads issued first (P = 8 x 100 B at
+  // +1 B: 5.9 us on the multi-CTA kernel, whose byte path has no registers to
+  // spare).  Batches: one CTA up to gather_many_single_max_bytes of output.
+  const bool small_job = family == 0 && (prm.job[0].flags & kJobSmall) != 0;
+  const bool single =
+      use_single(out_bytes, small_job ? (1LL << 62)
+                                      : family == 0 ? g_opt.gather_single_max.load()
+                                                    : g_opt.gather_many_single_max.load());
   prm.staged = g_opt.gather_staged.load() ? 1 : 0;
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.flat_ctas = 0;

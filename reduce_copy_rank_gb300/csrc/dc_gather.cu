@@ -705,7 +705,7 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
 
 // voff: the tiles cover global vectors [voff, total_vec) (a split launch
 // gives the vectors below voff to other CTAs).
-template <int BLOCK, int UNROLL, bool FLAT, int MAXJ, int MAXS>
+template <int BLOCK, int UNROLL, bool FLAT, bool FAST_EDGES, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
                                              uint64_t step, uint64_t voff = 0) {
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * UNROLL;
@@ -771,8 +771,12 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
       const uint32_t kind = (meta[u] >> 8) & 0xFFu;
       if (kind == 0)
         st16(reinterpret_cast<uint4*>(dst[u]), realign16(lo[u], hi[u], meta[u] & 15u));
-      else
+      else if (!FAST_EDGES)  // (the multi-CTA kernel has no registers to spare)
         copy_bytes(p, p.job[job[u]], dst[u], meta[u] >> 16, kind == 2);
+      else if (kind == 2)
+        copy_small_vector(p, p.job[job[u]], dst[u]);
+      else
+        copy_boundary(p, p.job[job[u]], dst[u], meta[u] >> 16);
     }
   }
 }
@@ -791,7 +795,7 @@ enum Mode : int {
   kGeneral1Staged = 5,  // one unaligned job (>= kGatherSmallBytes per rank) through shared memory
 };
 
-template <int BLOCK, int UNROLL, int MODE, int MAXJ, int MAXS>
+template <int BLOCK, int UNROLL, int MODE, bool SINGLE = false, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, uint64_t first,
                                             uint64_t step) {
   if constexpr (MODE == kFlat1 && MAXJ == 1)
@@ -822,7 +826,7 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
       gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
           p, first - fc, step - fc, p.flat_vec);
   } else
-    gather_tiles<BLOCK, UNROLL, MODE != kGeneral>(p, first, step);
+    gather_tiles<BLOCK, UNROLL, MODE != kGeneral, SINGLE>(p, first, step);
 }
 
 // One aligned job: the source bytes of output vectors [k, kend) (one
@@ -924,7 +928,7 @@ __global__ void __launch_bounds__(MODE == kGeneral ? kGatherSingleBlockGeneral :
   } else {
     pdl_enter();
   }
-  gather_mode<kBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE>(p, 0, 1);
+  gather_mode<kBlock, MODE == kGeneral ? kGatherUnrollGeneral : kGatherUnroll, MODE, true>(p, 0, 1);
 }
 
 // The mode of a launch.  Jobs are ordered aligned first, so job 0 tells
