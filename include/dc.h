@@ -257,6 +257,10 @@ long long dc_get_option(const char *key);
 /* Kernels launched by this library since it was loaded (all threads). */
 unsigned long long dc_launch_count(void);
 
+/* CTAs in the grid of the calling thread's last successful launch (0 before
+ * the first): a diagnostic of the planner's grid choice. */
+int dc_last_grid(void);
+
 /* ABI version: 1. */
 int dc_version(void);
 

@@ -27,7 +27,7 @@ __all__ = [
     "DCError", "LibraryMissing", "all_gather", "all_gather_many", "all_reduce",
     "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "inject_delay", "set_option",
     "get_option",
-    "launch_count", "last_error", "options", "lib", "LIB_PATH", "STATUS", "DTYPES", "ORDERS",
+    "launch_count", "last_grid", "last_error", "options", "lib", "LIB_PATH", "STATUS", "DTYPES", "ORDERS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.dc_get_option.restype = ctypes.c_longlong
         L.dc_launch_count.argtypes = []
         L.dc_launch_count.restype = ctypes.c_ulonglong
+        L.dc_last_grid.argtypes = []
+        L.dc_last_grid.restype = ctypes.c_int
         L.dc_version.argtypes = []
         L.dc_version.restype = ctypes.c_int
         _lib = L
@@ -464,6 +466,11 @@ def options(**kw):
 def launch_count() -> int:
     """Kernels this process has launched through the library."""
     return int(lib().dc_launch_count())
+
+
+def last_grid() -> int:
+    """CTAs in the grid of this thread's last launch through the library."""
+    return int(lib().dc_last_grid())
 
 
 def last_error() -> str:

@@ -32,6 +32,7 @@ using namespace dc;
 
 thread_local char g_err[512] = "";
 std::atomic<unsigned long long> g_launches{0};
+thread_local int g_last_grid = 0;  // CTAs of this thread's last launch
 
 // Single-CTA thresholds measured on GB300 (per-call time of back-to-back
 // calls in a CUDA graph: 14 calls on distinct buffers after an L2 flush, and
@@ -169,6 +170,7 @@ int occupancy(int dev, int family, F query) {
 int plan_grid(uint64_t tiles, int sms, int ctas_per_sm, int reserve = 0) {
   const uint64_t all = static_cast<uint64_t>(sms) * static_cast<uint64_t>(ctas_per_sm);
   const uint64_t cap = std::max<uint64_t>(1, all > static_cast<uint64_t>(reserve) ? all - reserve : 1);
+  if (tiles == 0) return 1;  // (a launch with only scalar head and tail work)
   uint64_t g;
   const long long forced = g_opt.grid_ctas.load();
   if (forced > 0) {
@@ -187,12 +189,13 @@ bool use_single(uint64_t size_bytes, long long threshold) {
   return size_bytes <= static_cast<uint64_t>(threshold);
 }
 
-dc_status_t check_launch(cudaError_t e, const char* what) {
+dc_status_t check_launch(cudaError_t e, const char* what, int grid) {
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(DC_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
   }
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  g_last_grid = grid;
   return ok();
 }
 
@@ -389,7 +392,8 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ, reserve) + reserve;
     }
   }
-  return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather");
+  return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather",
+                      single ? 1 : grid);
 }
 
 // --------------------------------------------------------------- reduce ---
@@ -541,7 +545,7 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
     grid = plan_grid((prm.total_units + tile - 1) / tile, sms, occ);
   }
   return check_launch(launch_reduce(prm, dtype, order, grid, single, g_opt.pdl.load() != 0, stream),
-                      what);
+                      what, single ? 1 : grid);
 }
 
 // Every reduction entry point: T tensors of P ranks; counts[t] is the
@@ -755,7 +759,7 @@ dc_status_t dc_inject_delay_ns(unsigned long long ns, dc_stream_t stream) {
                 static_cast<unsigned long long>(DC_MAX_DELAY_NS));
   if (g_opt.test_fail_launch.load())
     return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
-  return check_launch(launch_delay(ns, static_cast<cudaStream_t>(stream)), "delay");
+  return check_launch(launch_delay(ns, static_cast<cudaStream_t>(stream)), "delay", 1);
 }
 
 const char* dc_last_error(void) { return g_err; }
@@ -793,6 +797,8 @@ long long dc_get_option(const char* key) {
 }
 
 unsigned long long dc_launch_count(void) { return g_launches.load(); }
+
+int dc_last_grid(void) { return g_last_grid; }
 
 int dc_version(void) { return 1; }
 
