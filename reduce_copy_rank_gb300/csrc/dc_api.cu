@@ -8,12 +8,16 @@
 //  * the single-block path only pays below a crossover on OUTPUT bytes for
 //    the gather (section "What", kAllGatherSingleBlockMaxBytes) and on INPUT
 //    bytes per rank for the reductions (author's reply:
-//    input_bytes <= kSingleBlockFastPathMaxBytes); both thresholds here are
-//    measured on GB300 and can be changed at run time;
+//    input_bytes <= kSingleBlockFastPathMaxBytes); on GB300 the measured
+//    crossovers are 0 for one-tensor gathers (but for unaligned jobs under
+//    128 B per rank) and reductions, and 16 KiB for all_gather_many; all
+//    can be changed at run time;
 //  * the multi-block grid is sized from the 16-byte vector (or 8-element
 //    group) count, not from bytes (review nitpick on
 //    DeterministicCollectiveState::all_gather: a byte-sized grid left 15 of
-//    16 blocks idle), and capped at the resident CTAs of the whole GPU.
+//    16 blocks idle), capped at the resident CTAs of the whole GPU, and the
+//    single-job kernels' tiles are sized so that every SM gets the same
+//    share (even_tile).
 #include <algorithm>
 #include <atomic>
 #include <cstdarg>

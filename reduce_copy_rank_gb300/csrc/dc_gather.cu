@@ -13,8 +13,10 @@
 //  * The unit of work is a 16-byte-aligned OUTPUT vector.  A launch covers
 //    the output vectors of one or more jobs (all_gather_many packs several
 //    gathers into one launch), numbered by a prefix over the jobs.  Vectors
-//    are grouped in tiles of BLOCK x V; CTA c takes tiles c, c + G, c + 2G,
-//    ... (G CTAs), so that all CTAs sweep the buffers together.
+//    are grouped in tiles of at most BLOCK x V; CTA c takes tiles c, c + G,
+//    c + 2G, ... (G CTAs), so that all CTAs sweep the buffers together.  The
+//    single-job kernels take their tile size from the launch, sized by the
+//    planner so that every SM gets the same share of the output.
 //  * Inside a tile, thread t takes vectors t, t + BLOCK, ..., across rank
 //    boundaries: the flat loop of the page.  (The page's first version copied
 //    rank by rank, leaving threads idle and serialising the ranks' reads.)  A
@@ -23,19 +25,22 @@
 //    one per element.
 //  * Aligned job (flat): 16-byte loads and stores, either held in registers
 //    (mode 2) or staged through a per-thread cp.async ring in shared memory
-//    (mode 3, the default: more bytes in flight without registers).
+//    (mode 3, the default: more bytes in flight without registers; a launch
+//    in which every CTA has one tile loads straight into registers).
 //  * Unaligned job: each output vector that lies inside one rank's bytes is
 //    built from the two aligned source blocks that cover it with a funnel
 //    shift, so loads and stores stay 16 bytes wide and aligned (registers,
 //    mode 0; staged through a cp.async ring with per-rank affine state,
 //    mode 5); the few vectors that straddle two ranks or stick out of the
-//    output (at most P+1 per job) are written byte by byte.
+//    output (at most P+1 per job) are assembled from each rank's part (one
+//    or two aligned blocks) or from bytes, with their loads issued before
+//    their stores; in mode 5 one extra CTA copies them beside the ring.
 //  * all_gather_many (mode 4): the aligned jobs come first and are staged by
 //    the first part of the grid, the unaligned ones by the rest.
-//  * Jobs with fewer than kGatherSmallBytes per rank are copied byte by byte.
-//  * Every kernel triggers the next kernel of the stream at entry; the
-//    aligned single-job kernels prefetch their first tile into L2 before they
-//    wait for the previous kernel (programmatic dependent launch).
+//  * Jobs with fewer than kGatherSmallBytes per rank are assembled from bytes.
+//  * Programmatic dependent launch: the single-job staged kernels prefetch
+//    their first tile into L2 before they wait for the previous kernel of
+//    the stream; the others trigger the next kernel and wait at entry.
 #include <atomic>
 
 #include "dc_device.cuh"
