@@ -25,11 +25,16 @@
 // Work: a job is one contiguous element range of one tensor with one input
 // offset (all_reduce: one job per tensor, writing P outputs; reduce_scatter:
 // one job per tensor and rank r, reading elements [r*C, (r+1)*C) of the
-// tensor's inputs and writing output r).  When every pointer of a job has the
-// same address mod 16, the job is a scalar head up to the first 16-byte
-// boundary, a body of 16-byte vectors (one load per rank, one store per
-// output) and a scalar tail; otherwise it is folded element by element.
-// Units are taken in tiles round robin by the CTAs.
+// tensor's inputs and writing output r).  When the outputs of a job share
+// one address mod 16, the job is a scalar head up to the outputs' first
+// 16-byte boundary, a body of 16-byte units (one store per output) and a
+// scalar tail; an input at the outputs' offset is read with one 16-byte load
+// per unit, an input at another offset as the two aligned blocks around the
+// unit, funnel-shifted (in registers, or for an all_reduce of one tensor with
+// P = 2, 4, 8 through shared memory: reduce_realign_staged).  When the
+// outputs disagree mod 16 the job is folded element by element.  Units are
+// taken in tiles round robin by the CTAs; a one-tensor all_reduce's tiles are
+// sized by the planner so that every SM gets the same share.
 #pragma once
 
 #include <atomic>
