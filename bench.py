@@ -119,13 +119,40 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string and
+    character literals kept as they are), so that the digest below follows
+    the code, not its commentary."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(ln.rstrip() for ln in "".join(out).splitlines() if ln.strip())
+
+
 def kernel_source_digest() -> str:
+    """Digest of the code (comments left out) of every file under
+    reduce_copy_rank_gb300/csrc."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "reduce_copy_rank_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -191,3 +191,14 @@ def test_alternating_swaps_order_and_takes_medians():
     assert clk.log == ["a", "b", "b", "a", "a", "b", "b", "a"]
     assert round(med[0], 6) == 2.5  # median of 1, 3, 2, 100 us
     assert round(med[1], 6) == 5.0
+
+
+def test_source_digest_follows_code_not_comments():
+    """The traffic record stays valid across comment edits of the kernel
+    sources, and goes stale on any change of the code."""
+    code = 'int f(int a) {  // one\n  /* two */ const char* s = "x // not a comment";\n  return a; }\n'
+    stripped = bench.strip_comments(code)
+    assert "one" not in stripped and "two" not in stripped
+    assert '"x // not a comment"' in stripped
+    assert bench.strip_comments(code.replace("// one", "// other words")) == stripped
+    assert bench.strip_comments(code.replace("return a;", "return a + 1;")) != stripped
