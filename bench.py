@@ -53,7 +53,15 @@ UNIT = "GB/s"
 WORKLOAD = ("all-gather sweep: P=8 and P=2 simulated ranks x {1, 8, 32, 64, 128 KiB, 1 MiB, "
             "4 MiB} per rank of BF16 bit patterns, 16-byte aligned; one step = the 14 gathers")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure: a second denominator beside the measured copy rate
 KIB = 1024
+MIB = 1024 * KIB
+
+
+def workload_config(world: int) -> dict:
+    """The `config` of the JSON line, the same dict for both arms."""
+    return {"workload": WORKLOAD, "P": [8, 2], "bytes_per_rank": W.CONFIG2_SIZES,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def parse_args(argv=None):
@@ -156,24 +164,28 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
-    was taken from the current kernel sources (else None)."""
+def load_traffic(kernel: str) -> dict:
+    """Per-launch figures of `kernel` from the committed ncu summary (DRAM
+    bytes, and the serialised cold-cache duration of ncu's launch list), if
+    they were taken from the current kernel sources (else {})."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         lines = open(path).read().splitlines()
     except OSError:
-        return None
+        return {}
     for ln in lines:
         if ln.startswith("#") or not ln.strip():
             continue
         parts = dict(kv.split("=", 1) for kv in ln.split() if "=" in kv)
         if parts.get("kernel") == kernel and parts.get("source") == kernel_source_digest():
-            try:
-                return float(parts["bytes_per_launch"])
-            except (KeyError, ValueError):
-                return None
-    return None
+            out = {}
+            for key in ("bytes_per_launch", "ncu_us_per_launch"):
+                try:
+                    out[key] = float(parts[key])
+                except (KeyError, ValueError):
+                    pass
+            return out
+    return {}
 
 
 class ClockSampler:
@@ -307,7 +319,8 @@ def run_reference(args) -> int:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded random BF16 bit patterns)",
-        "config": {"workload": WORKLOAD, "l2": "host oracle (no GPU)"},
+        "config": workload_config(int(os.environ.get("WORLD_SIZE", "1"))),
+        "timing": "host oracle on the host cores: whole passes of the sweep, wall clock",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} full passes of the 14-gather sweep through the "
                                    "single-threaded C oracle"},
@@ -370,7 +383,8 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     median of 5): all_reduce at the five per-rank sizes, reduce_scatter
     16384x8192 per rank, the typed, tree and batched reductions, an
     all_reduce with one rank's input realigned, unaligned gathers of 4 MiB+1 B
-    and 32 MiB+1 B per rank, all_gather_many of the six mixed tensors (P=8)."""
+    and 32 MiB+1 B per rank, all_gather_many of the six mixed tensors and of
+    120 tiny tensors (P=8), and the staged protocol over 8 ranks x 4 MiB."""
     rows = []
     P = W.CONFIG4_P
     for name, n in W.CONFIG4_COUNTS.items():
@@ -421,6 +435,38 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     nbytes = 2 * P * sum(W.CONFIG5_MANY_SIZES)
     rows.append({"op": "all_gather_many", "P": P, "count": len(W.CONFIG5_MANY_SIZES),
                  "shape": "{3 B, 4 KiB, 100000 B, 1 MiB, 7 MiB+5 B, 32 MiB}", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    del tens, outs
+    # many tiny tensors: 120 tensors x 8 ranks of 3..100 B at odd offsets
+    rng = np.random.default_rng(W.seed_for(5, 9005))
+    sizes = [int(x) for x in rng.integers(3, 101, 120)]
+    tens = [[W.random_bytes_device(W.seed_for(5, 2), r, B + 1, device, tensor=t)[1:] for r in range(8)]
+            for t, B in enumerate(sizes)]
+    outs = [torch.empty(8 * B, dtype=torch.uint8, device=device) for B in sizes]
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather_many(tens, outs)], 5)[0])
+    nbytes = 2 * 8 * sum(sizes)
+    rows.append({"op": "all_gather_many_tiny", "P": 8, "count": len(sizes),
+                 "shape": "120 tensors of 3..100 B per rank, payloads at +1 B", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    del tens, outs
+    # the staged protocol (stage -> gather -> complete), P = 8 ranks x 4 MiB:
+    # P*B read + P*B written to stage, P*P*B read + P*P*B written to gather
+    P, B = 8, 4 << 20
+    ins = [W.random_bytes_device(W.seed_for(2, 990), r, B, device) for r in range(P)]
+    stg = [torch.empty(B, dtype=torch.uint8, device=device) for _ in range(P)]
+    outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for _ in range(P)]
+    ws = dc.fused_workspace(P, device)
+    epoch = [0]
+
+    def fused():
+        epoch[0] += 1
+        dc.fused_all_gather(ins, stg, outs, ws, epoch[0])
+
+    us = statistics.median(timed_calls(torch, stream, flush, [fused], 5)[0])
+    dc.check_device()
+    nbytes = 2 * P * B + 2 * P * P * B
+    rows.append({"op": "fused_all_gather", "P": P, "count": B,
+                 "shape": "4 MiB per rank, every rank's own output (stage, gather, complete)", "us": us,
                  "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     return rows
 
@@ -545,6 +591,41 @@ def back_to_back_block(torch, dc, device, flush, per_size=8, replays=10):
         rows.append({"P": P, "bytes_per_rank": B, "us": us,
                      "gbs": algorithmic_bytes(P, B) / us / 1e3})
         del g, bufs
+    return rows
+
+
+def call_kernel(dc, P: int, B: int) -> str:
+    """The kernel that runs a 16-byte aligned gather of P x B bytes under the
+    library's current options (the planner's rule for one aligned tensor)."""
+    total = P * B
+    if total <= dc.get_option("gather_single_max_bytes"):
+        return "dc_gather_single_kernel<1,64,2>"
+    if dc.get_option("gather_bulk") and total >= dc.get_option("gather_bulk_min_bytes"):
+        return "dc_gather_bulk_kernel"
+    return "dc_gather_kernel<1,64,3>" if dc.get_option("gather_staged") else "dc_gather_kernel<1,64,2>"
+
+
+def by_size_rows(table, back_to_back, peak):
+    """The 4 MiB and 1 MiB per-rank gathers of the sweep (P = 8 and 2): the
+    call alone after a flush (median of the timed region's samples) and back
+    to back (per_call_back_to_back), each against the measured copy rate and
+    the nominal 8 TB/s."""
+    rows = []
+    for P in (8, 2):
+        for B in (4 * MIB, 1 * MIB):
+            iso = [r for r in table if r["P"] == P and r["bytes_per_rank"] == B]
+            b2b = [r for r in back_to_back if r["P"] == P and r["bytes_per_rank"] == B]
+            if not iso or not b2b:
+                continue
+            nbytes = algorithmic_bytes(P, B)
+            iso_us, b2b_us = iso[0]["us_median"], b2b[0]["us"]
+            rows.append({"P": P, "bytes_per_rank": B, "kernel": iso[0]["kernel"],
+                         "alone_us": iso_us, "alone_gbs": nbytes / iso_us / 1e3,
+                         "alone_frac_measured": nbytes / iso_us / 1e3 / peak,
+                         "alone_frac_nominal": nbytes / iso_us / 1e3 / NOMINAL_HBM_GBS,
+                         "back_to_back_us": b2b_us, "back_to_back_gbs": nbytes / b2b_us / 1e3,
+                         "back_to_back_frac_measured": nbytes / b2b_us / 1e3 / peak,
+                         "back_to_back_frac_nominal": nbytes / b2b_us / 1e3 / NOMINAL_HBM_GBS})
     return rows
 
 
@@ -697,7 +778,7 @@ def run_dc(args) -> int:
     cases = sweep_cases()
     calls, _keep = build_gather_calls(torch, dc, device, cases)
     single_max = dc.get_option("gather_single_max_bytes")
-    paths = ["single" if P * B <= single_max else "multi" for (P, B, _s) in cases]
+    paths = [call_kernel(dc, P, B) for (P, B, _s) in cases]
     step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
 
     launches0 = dc.launch_count()
@@ -706,7 +787,7 @@ def run_dc(args) -> int:
     # one more graph per kernel (path): that kernel's calls of the step back to
     # back after a flush, for its average launch duration in the roofline
     path_graphs = {}
-    for path in ("multi", "single"):
+    for path in sorted(set(paths)):
         idx = [i for i, p in enumerate(paths) if p == path]
         if idx:
             launches0 = dc.launch_count()
@@ -750,13 +831,13 @@ def run_dc(args) -> int:
     value = job_throughput(world, step_bytes, ms_per_step)  # GB/s over all ranks
 
     table = []
-    kern_time = {"multi": 0.0, "single": 0.0}
-    kern_bytes = {"multi": 0, "single": 0}
-    kern_launches = {"multi": 0, "single": 0}
+    kern_time = {path: 0.0 for path in paths}
+    kern_bytes = {path: 0 for path in paths}
+    kern_launches = {path: 0 for path in paths}
     for (P, B, _s), path, us_list in zip(cases, paths, per_call):
         nbytes = algorithmic_bytes(P, B)
         st = stats(us_list)
-        table.append({"P": P, "bytes_per_rank": B, "path": path, **st,
+        table.append({"P": P, "bytes_per_rank": B, "kernel": path, **st,
                       "gbs": nbytes / st["us_mean"] / 1e3, "frac": nbytes / st["us_mean"] / 1e3 / peak})
         kern_time[path] += sum(us_list)
         kern_bytes[path] += nbytes * len(us_list)
@@ -764,14 +845,13 @@ def run_dc(args) -> int:
     # the dominant kernel: the larger share of the per-path graphs' time
     graph_ms = {path: float(sum(v)) for path, v in path_ms.items()}
     dom = max(graph_ms, key=graph_ms.get)
-    kname = {"multi": "dc_gather_kernel<1,64,3>" if dc.get_option("gather_staged")
-             else "dc_gather_kernel<1,64,2>", "single": "dc_gather_single_kernel<1,64,2>"}[dom]
+    kname = dom
     dom_idx = path_graphs[dom][0]
     dom_bytes = sum(algorithmic_bytes(cases[i][0], cases[i][1]) for i in dom_idx)
     us_per_launch = graph_ms[dom] * 1e3 / (args.steps * len(dom_idx))
     achieved = dom_bytes / len(dom_idx) / us_per_launch / 1e3  # GB/s
     iso_achieved = kern_bytes[dom] / kern_time[dom] / 1e3
-    traffic = load_traffic(kname)
+    ncu = load_traffic(kname)
     big = [row for row in table if row["P"] == 8 and row["bytes_per_rank"] == 4 << 20][0]
 
     extra = None
@@ -782,6 +862,7 @@ def run_dc(args) -> int:
         comparators = comparators_block(torch, dc, device, stream, flush)
         latency = warm_latency_block(torch, dc, device)
     back_to_back = back_to_back_block(torch, dc, device, flush)
+    by_size = by_size_rows(table, back_to_back, peak)
     e2e = e2e_measure(torch, dc, device, stream, cases, min(args.steps, 20))
     e2e["value"] = job_throughput(world, step_bytes, rank_max(e2e["ms_per_step"], dist, device))
 
@@ -790,26 +871,38 @@ def run_dc(args) -> int:
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded random BF16 bit patterns, resident in HBM)",
-        "config": {"workload": WORKLOAD, "P": [8, 2], "bytes_per_rank": W.CONFIG2_SIZES,
-                   "timing": "value: one CUDA graph per step (L2 flush, event, the 14 calls back "
-                             "to back, event); roofline: per kernel one more graph per step with "
-                             "that kernel's calls of the step back to back (L2 flush, event, the "
-                             "calls, event); per_call and roofline.isolated: each call alone (L2 "
-                             "flush, event, the launch, event); all in the same timed region",
-                   "l2": "flushed before every step and before every separately timed call "
-                         "(write + read of 4x L2); each call's inputs are untouched since",
-                   "programmatic_dependent_launch": bool(dc.get_option("pdl")),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "gather_single_max_bytes": single_max},
+        "config": workload_config(world),
+        "timing": "value: one CUDA graph per step (L2 flush, event, the 14 calls back to back, "
+                  "event); roofline: per kernel one more graph per step with that kernel's calls "
+                  "of the step back to back (L2 flush, event, the calls, event); per_call and "
+                  "roofline.isolated: each call alone (L2 flush, event, the launch, event); all in "
+                  "the same timed region",
+        "l2": "flushed before every step and before every separately timed call (write + read of "
+              "4x L2); each call's inputs are untouched since",
+        "library": {"programmatic_dependent_launch": bool(dc.get_option("pdl")),
+                    "gather_single_max_bytes": single_max,
+                    "gather_bulk": dc.get_option("gather_bulk"),
+                    "gather_bulk_min_bytes": dc.get_option("gather_bulk_min_bytes"),
+                    "kernel_of_call": [{"P": P, "bytes_per_rank": B, "kernel": k}
+                                       for (P, B, _s), k in zip(cases, paths)]},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "launches": args.steps * len(dom_idx),
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": ncu.get("bytes_per_launch"), "launches": args.steps * len(dom_idx),
                      "us_per_launch": us_per_launch,
+                     "us_per_launch_regime": "back to back: that kernel's calls of the step in one "
+                                             "CUDA graph after an L2 flush, launched with "
+                                             "programmatic dependent launch (each launch overlaps "
+                                             "the previous one's tail); the average per launch",
+                     "ncu_us_per_launch": ncu.get("ncu_us_per_launch"),
+                     "ncu_regime": "ncu launch list of the bench command (gpu__time_duration, "
+                                   "--clock-control none): each launch serialised, caches flushed",
                      "share": graph_ms[dom] / sum(graph_ms.values()),
                      "algorithmic_bytes_per_launch": dom_bytes / len(dom_idx),
                      "isolated": {"achieved": iso_achieved, "frac": iso_achieved / peak,
                                   "us_per_launch": kern_time[dom] / max(kern_launches[dom], 1),
-                                  "share": kern_time[dom] / sum(kern_time.values())}},
+                                  "share": kern_time[dom] / sum(kern_time.values())},
+                     "by_size": by_size},
         "headline_4MiB_P8": {"us": big["us_mean"], "gbs": big["gbs"], "frac": big["frac"]},
         "per_call": table,
         "per_call_back_to_back": back_to_back,

@@ -48,7 +48,7 @@ typedef enum {
     DC_ERR_OVERLAP = 3,  /* an output range overlaps an input or another output */
     DC_ERR_TOO_MANY = 4, /* all_gather_many table larger than the limits below */
     DC_ERR_CUDA = 5,     /* the CUDA runtime refused the launch */
-    DC_ERR_TIMEOUT = 6   /* reserved for bounded device waits; no current kernel waits */
+    DC_ERR_TIMEOUT = 6   /* a bounded device wait ran out (reported by dc_check_device) */
 } dc_status_t;
 
 /* Element types and summation orders of the reductions. */
@@ -192,6 +192,70 @@ dc_status_t dc_reduce_scatter_many(const void *const *in_ptrs, void *const *out_
 #define DC_MAX_DELAY_NS 1000000000ull
 dc_status_t dc_inject_delay_ns(unsigned long long ns, dc_stream_t stream);
 
+/*
+ * dc_fused_all_gather -- the staged all-gather protocol of the collective's
+ * multi-rank deployment ([PR491] author's replies: the cuda_ipc_fixed_tree
+ * backend's CUDA-graph-safe fused protocol, stage -> gather -> complete;
+ * section "Not in this PR" and the review threads: a failed launch leaves the
+ * protocol pending with no abort path, and peers of a dead rank wait for the
+ * process-group timeout), run with the P ranks as CTA groups of one
+ * cooperative launch on one GPU, every wait bounded.
+ *
+ * Rank r stages in_ptrs[r] into staging[r], publishes it, gathers every
+ * rank's staging buffer into outs[r] in rank order, and completes once every
+ * rank has read its staging buffer.  Afterwards, for every r:
+ *
+ *   outs[r][q*bytes_per_rank + j] = in_ptrs[q][j]   (q < P, j < bytes_per_rank)
+ *
+ * and staging[r] holds a copy of in_ptrs[r].
+ *
+ * in_ptrs, staging, outs: host arrays of P device pointers (16-byte aligned);
+ *            each input and staging buffer holds bytes_per_rank bytes, each
+ *            output P*bytes_per_rank.  Staging buffers, outputs and the
+ *            workspace may overlap nothing; inputs may overlap inputs.
+ * bytes_per_rank: a multiple of 16 (DC_ERR_ALIGN otherwise); 0 is a no-op.
+ * workspace: device memory of dc_fused_workspace_bytes(P) bytes, 16-byte
+ *            aligned, owned by the caller and zero before its first use
+ *            (cudaMemset, or dc_fused_reset).  It holds the ranks' epoch flags.
+ * epoch:     1 for the first call after the workspace was cleared, then one
+ *            more for each call (never 0).  Calls on one workspace must not
+ *            overlap on the GPU: issue them on one stream.
+ * Every wait for a peer's flag is bounded by the "wait_limit_ns" option.  If
+ * one runs out (a rank that never arrives), the waiting CTAs record the fault
+ * and return, the outputs are incomplete, and dc_check_device returns
+ * DC_ERR_TIMEOUT naming the waiting and the awaited rank; clear the workspace
+ * with dc_fused_reset and start again at epoch 1.  P ranks need P*G CTAs
+ * resident at once (G chunks per rank, at least one): DC_ERR_INVALID if the
+ * GPU cannot hold P of them.
+ */
+size_t dc_fused_workspace_bytes(int P); /* 0 if P is outside 1..DC_MAX_RANKS */
+dc_status_t dc_fused_all_gather(const void *const *in_ptrs, void *const *staging, void *const *outs, int P,
+                                size_t bytes_per_rank, void *workspace, unsigned int epoch,
+                                dc_stream_t stream);
+/* Clears a fused workspace of P ranks on `stream` (cudaMemsetAsync); the next
+ * call on it uses epoch 1. */
+dc_status_t dc_fused_reset(void *workspace, int P, dc_stream_t stream);
+
+/*
+ * dc_check_device -- reports the faults that this library's kernels recorded
+ * on the current device since the last check, and clears them.
+ *
+ * The bulk-copy gather (the "gather_bulk" path of dc_all_gather) waits for
+ * its loads, and dc_fused_all_gather for its peers' flags, with a bound
+ * (option "wait_limit_ns", default one second of the GPU's global timer).  A
+ * wait that runs out does not hang the stream: the kernel records the fault
+ * in a device word, waits with the same bound for its own copies in flight
+ * and returns, leaving that call's output incomplete.  No correct bulk launch
+ * on a working GPU ever runs out; a fused launch runs out when a rank never
+ * arrives.
+ *
+ * Synchronous: it first waits for all work on the current device
+ * (cudaDeviceSynchronize), then reads and clears the fault word.
+ * Returns DC_OK if no wait ran out, DC_ERR_TIMEOUT if one did, DC_ERR_CUDA if
+ * the synchronisation or the read failed (the CUDA error in dc_last_error()).
+ */
+dc_status_t dc_check_device(void);
+
 /* Message describing the last failed call on this thread ("" if none). */
 const char *dc_last_error(void);
 
@@ -241,12 +305,37 @@ const char *dc_status_name(int status);
  *                             its outputs, P = 2, 4 or 8, stages its input
  *                             blocks through shared memory; 0 = realign in
  *                             registers
+ *   "gather_bulk"             1 (default) = a 16-byte aligned dc_all_gather
+ *                             (out, bytes_per_rank and every peer) of at least
+ *                             gather_bulk_min_bytes output bytes runs on the
+ *                             TMA engine: 1-D bulk copies global -> shared ->
+ *                             global through a ring of shared-memory stages
+ *   "gather_bulk_min_bytes"   see gather_bulk (default 0)
+ *   "bulk_chunk_bytes"        largest chunk one bulk stage moves (default 16384)
+ *   "bulk_chunk_min"          smallest chunk an output too small for one
+ *                             full chunk per CTA is cut into (default 2048)
+ *   "bulk_stages"             ring stages per CTA (default 6, at most 32)
+ *   "bulk_ctas_per_sm"        bulk CTAs per SM (default 2)
+ *   "bulk_prefetch"           bulk CTAs prefetch their sources into L2 this
+ *                             many chunks ahead of their loads (default 1; at
+ *                             most 64 MB ahead over the grid; 0 when
+ *                             "prefetch" is 0)
+ *   "wait_limit_ns"           bound of one device wait (default 1000000000;
+ *                             at least 1000)
+ *   "test_bulk_short_tx"      1 = every bulk CTA's first wait runs out (tests
+ *                             of dc_check_device)
+ *   "fused_chunk_min"         dc_fused_all_gather: smallest chunk per CTA
+ *                             (default 65536 bytes)
+ *   "test_fused_absent_ranks" bit r set: rank r of dc_fused_all_gather never
+ *                             arrives (tests of its bounded waits)
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
  * DC_GATHER_SINGLE_MAX_BYTES, DC_GATHER_MANY_SINGLE_MAX_BYTES,
  * DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
  * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
- * DC_REDUCE_TILE_MIN and DC_REDUCE_STAGED set the initial values (read once,
+ * DC_REDUCE_TILE_MIN, DC_REDUCE_STAGED, DC_GATHER_BULK, DC_GATHER_BULK_MIN_BYTES,
+ * DC_BULK_CHUNK_BYTES, DC_BULK_CHUNK_MIN, DC_BULK_STAGES, DC_BULK_CTAS_PER_SM,
+ * DC_BULK_PREFETCH, DC_FUSED_CHUNK_MIN and DC_WAIT_LIMIT_NS set the initial values (read once,
  * at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.

@@ -25,7 +25,9 @@ from typing import Sequence
 
 __all__ = [
     "DCError", "LibraryMissing", "all_gather", "all_gather_many", "all_reduce",
-    "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "inject_delay", "set_option",
+    "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "inject_delay", "check_device",
+    "fused_all_gather", "fused_workspace", "fused_reset",
+    "set_option",
     "get_option",
     "launch_count", "last_grid", "last_error", "options", "lib", "LIB_PATH", "STATUS", "DTYPES", "ORDERS",
 ]
@@ -83,9 +85,15 @@ def lib() -> ctypes.CDLL:
         L.dc_all_reduce_many.argtypes = [A, A, A, I, I, I, I, _VP]
         L.dc_reduce_scatter_many.argtypes = L.dc_all_reduce_many.argtypes
         L.dc_inject_delay_ns.argtypes = [ctypes.c_ulonglong, _VP]
+        L.dc_check_device.argtypes = []
+        L.dc_fused_workspace_bytes.argtypes = [I]
+        L.dc_fused_workspace_bytes.restype = Z
+        L.dc_fused_all_gather.argtypes = [A, A, A, I, Z, _VP, ctypes.c_uint, _VP]
+        L.dc_fused_reset.argtypes = [_VP, I, _VP]
         for f in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
                   "dc_reduce_scatter_bf16", "dc_all_reduce", "dc_reduce_scatter",
-                  "dc_all_reduce_many", "dc_reduce_scatter_many", "dc_inject_delay_ns"):
+                  "dc_all_reduce_many", "dc_reduce_scatter_many", "dc_inject_delay_ns",
+                  "dc_check_device", "dc_fused_all_gather", "dc_fused_reset"):
             getattr(L, f).restype = ctypes.c_int
         L.dc_last_error.argtypes = []
         L.dc_last_error.restype = ctypes.c_char_p
@@ -183,6 +191,25 @@ def dc_inject_delay_ns(ns: int, stream: int = 0) -> int:
     return lib().dc_inject_delay_ns(int(ns), stream)
 
 
+def dc_check_device() -> int:
+    return lib().dc_check_device()
+
+
+def dc_fused_workspace_bytes(P: int) -> int:
+    return int(lib().dc_fused_workspace_bytes(P))
+
+
+def dc_fused_all_gather(in_ptrs: Sequence[int], staging: Sequence[int], outs: Sequence[int], P: int,
+                        bytes_per_rank: int, workspace: int, epoch: int, stream: int = 0) -> int:
+    a, b, c = _u64(in_ptrs), _u64(staging), _u64(outs)
+    return lib().dc_fused_all_gather(_addr(a), _addr(b), _addr(c), P, bytes_per_rank, workspace, epoch,
+                                     stream)
+
+
+def dc_fused_reset(workspace: int, P: int, stream: int = 0) -> int:
+    return lib().dc_fused_reset(workspace, P, stream)
+
+
 # ---------------------------------------------------------- tensor API ---
 
 _raw_stream = None
@@ -257,6 +284,53 @@ def all_gather(peers: Sequence, out, stream=None):
     a = array.array("Q", ptrs)
     _check(lib().dc_all_gather(_addr(a), P, B, out.data_ptr(), _stream_handle(stream)))
     return out
+
+
+def fused_workspace(P: int, device=None):
+    """A zeroed workspace tensor for dc_fused_all_gather with P ranks
+    (allocated by torch; the library itself allocates nothing)."""
+    import torch
+
+    n = dc_fused_workspace_bytes(P)
+    if n == 0:
+        raise ValueError(f"P = {P} is outside 1..{MAX_RANKS}")
+    return torch.zeros(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def fused_all_gather(inputs: Sequence, staging: Sequence, outputs: Sequence, workspace, epoch: int,
+                     stream=None):
+    """The staged all-gather protocol (stage -> gather -> complete) over P
+    ranks on one GPU: afterwards every ``outputs[r]`` holds ``inputs[0]``,
+    ``inputs[1]``, ... in rank order and ``staging[r]`` a copy of
+    ``inputs[r]``.  ``epoch`` is 1 for the first call on a cleared
+    ``workspace`` (see :func:`fused_workspace`) and one more for each call.
+    A rank that never arrives shows up as DC_ERR_TIMEOUT from
+    :func:`check_device`.  Returns ``outputs``."""
+    P = len(inputs)
+    if P == 0 or len(staging) != P or len(outputs) != P:
+        raise ValueError("need the same number (>= 1) of inputs, staging buffers and outputs")
+    B = inputs[0].nbytes
+    dev = _cur_dev()
+    groups = (("inputs", inputs, B), ("staging", staging, B), ("outputs", outputs, P * B))
+    ptrs = {}
+    for name, ts, nbytes in groups:
+        for r, t in enumerate(ts):
+            if not t.is_cuda or not t.is_contiguous():
+                _device_tensor(t, f"{name}[{r}]")
+            if t.get_device() != dev:
+                _wrong_device(f"{name}[{r}]", t, dev)
+            if t.nbytes != nbytes:
+                raise ValueError(f"{name}[{r}] holds {t.nbytes} bytes, expected {nbytes}")
+        ptrs[name] = [t.data_ptr() for t in ts]
+    _device_tensor(workspace, "workspace")
+    _check(dc_fused_all_gather(ptrs["inputs"], ptrs["staging"], ptrs["outputs"], P, B,
+                               workspace.data_ptr(), int(epoch), _stream_handle(stream)))
+    return outputs
+
+
+def fused_reset(workspace, P: int, stream=None) -> None:
+    """Clear a fused workspace of P ranks (the next call uses epoch 1)."""
+    _check(dc_fused_reset(workspace.data_ptr(), P, _stream_handle(stream)))
 
 
 def _explain_peers(peers) -> None:
@@ -434,6 +508,13 @@ def inject_delay(ns: int, stream=None) -> None:
     """Delay `stream` (default: the current torch stream) by `ns` nanoseconds
     of the GPU's global timer (one-thread kernel; rank-skew calibration)."""
     _check(dc_inject_delay_ns(ns, _stream_handle(stream)))
+
+
+def check_device() -> None:
+    """Wait for the current device, then raise DCError(DC_ERR_TIMEOUT) if a
+    bounded wait in one of the library's kernels ran out since the last check
+    (the fault word is cleared)."""
+    _check(dc_check_device())
 
 
 # ------------------------------------------------------------- options ---

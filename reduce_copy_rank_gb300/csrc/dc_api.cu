@@ -71,6 +71,17 @@ struct Options {
   std::atomic<long long> tile_min{512};  // see staged_tile
   std::atomic<long long> reduce_tile_min{64};  // see launch_reduce_plan
   std::atomic<long long> reduce_staged{1};     // see launch_reduce_plan
+  std::atomic<long long> gather_bulk{0};       // see plan_bulk
+  std::atomic<long long> bulk_min_bytes{0};
+  std::atomic<long long> bulk_chunk_bytes{16384};
+  std::atomic<long long> bulk_chunk_min{2048};
+  std::atomic<long long> bulk_stages{6};
+  std::atomic<long long> bulk_ctas_per_sm{2};
+  std::atomic<long long> bulk_prefetch{2};
+  std::atomic<long long> fused_chunk_min{65536};
+  std::atomic<long long> test_fused_absent{0};
+  std::atomic<long long> wait_limit_ns{1000000000};
+  std::atomic<long long> test_bulk_short_tx{0};
 };
 Options g_opt;
 std::once_flag g_env_once;
@@ -95,6 +106,17 @@ const OptionKey kKeys[] = {
     {"gather_tile_min", "DC_GATHER_TILE_MIN", &g_opt.tile_min},
     {"reduce_tile_min", "DC_REDUCE_TILE_MIN", &g_opt.reduce_tile_min},
     {"reduce_staged", "DC_REDUCE_STAGED", &g_opt.reduce_staged},
+    {"gather_bulk", "DC_GATHER_BULK", &g_opt.gather_bulk},
+    {"gather_bulk_min_bytes", "DC_GATHER_BULK_MIN_BYTES", &g_opt.bulk_min_bytes},
+    {"bulk_chunk_bytes", "DC_BULK_CHUNK_BYTES", &g_opt.bulk_chunk_bytes},
+    {"bulk_chunk_min", "DC_BULK_CHUNK_MIN", &g_opt.bulk_chunk_min},
+    {"bulk_stages", "DC_BULK_STAGES", &g_opt.bulk_stages},
+    {"bulk_ctas_per_sm", "DC_BULK_CTAS_PER_SM", &g_opt.bulk_ctas_per_sm},
+    {"bulk_prefetch", "DC_BULK_PREFETCH", &g_opt.bulk_prefetch},
+    {"fused_chunk_min", "DC_FUSED_CHUNK_MIN", &g_opt.fused_chunk_min},
+    {"test_fused_absent_ranks", nullptr, &g_opt.test_fused_absent},
+    {"wait_limit_ns", "DC_WAIT_LIMIT_NS", &g_opt.wait_limit_ns},
+    {"test_bulk_short_tx", nullptr, &g_opt.test_bulk_short_tx},
 };
 
 void read_env_once() {
@@ -129,7 +151,7 @@ bool overlaps(uint64_t a, uint64_t na, uint64_t b, uint64_t nb) {
 
 // ---------------------------------------------------- device properties ---
 constexpr int kMaxDevices = 64;
-constexpr int kFamilies = 128;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + (< 72); staged realigning reduction: 96 + (< 24)
+constexpr int kFamilies = 128;  // gather: family * kGatherModes + mode (< 18); reductions: 24 + (< 72); staged realigning reduction: 96 + (< 24); fused all-gather: 127
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_occ[kMaxDevices][kFamilies];
 
@@ -217,19 +239,73 @@ bool tensor_aligned(const GatherTensor& g, int P, bool allow_flat) {
   return aligned;
 }
 
+// Rejects an output of a batch of gathers that overlaps another output or any
+// payload (payloads may overlap each other).  The T outputs and T*P payloads
+// are sorted by start and swept once, keeping per kind (output, payload) the
+// range that reaches furthest so far: since every earlier range starts at or
+// before the current one, the current range overlaps an earlier range of a
+// kind exactly when that kind's furthest end lies past its start.
+// O(n log n) for the n = T*(P+1) ranges of a call.
+dc_status_t check_gather_overlaps(const GatherTensor* ts, int T, int P) {
+  struct R {
+    uint64_t lo, hi;
+    int t, r;  // r < 0: the output of tensor t
+  };
+  std::vector<R> v;
+  v.reserve(static_cast<size_t>(T) * (P + 1));
+  for (int t = 0; t < T; ++t) {
+    const uint64_t B = ts[t].bytes;
+    if (B == 0) continue;
+    v.push_back(R{ts[t].out, ts[t].out + B * static_cast<uint64_t>(P), t, -1});
+    for (int r = 0; r < P; ++r) {
+      const uint64_t s = reinterpret_cast<uint64_t>(ts[t].peers[r]);
+      v.push_back(R{s, s + B, t, r});
+    }
+  }
+  std::sort(v.begin(), v.end(), [](const R& a, const R& b) { return a.lo < b.lo; });
+  const R* far_out = nullptr;  // the output reaching furthest so far
+  const R* far_in = nullptr;   // the payload reaching furthest so far
+  for (const R& x : v) {
+    if (x.r < 0) {
+      if (far_out && far_out->hi > x.lo)
+        return fail(DC_ERR_OVERLAP, "outputs of tensors %d and %d overlap", std::min(far_out->t, x.t),
+                    std::max(far_out->t, x.t));
+      if (far_in && far_in->hi > x.lo)
+        return fail(DC_ERR_OVERLAP, "output of tensor %d overlaps the payload of tensor %d rank %d", x.t,
+                    far_in->t, far_in->r);
+      if (!far_out || x.hi > far_out->hi) far_out = &x;
+    } else {
+      if (far_out && far_out->hi > x.lo)
+        return fail(DC_ERR_OVERLAP, "output of tensor %d overlaps the payload of tensor %d rank %d",
+                    far_out->t, x.t, x.r);
+      if (!far_in || x.hi > far_in->hi) far_in = &x;
+    }
+  }
+  return DC_OK;
+}
+
 // Fill jobs and sources of a gather parameter block from T tensors.  The
-// aligned jobs come first (their vectors are [0, flat_vec)), then the rest;
-// each keeps its own output, so the order changes no result.
+// aligned jobs come first (their vectors are [0, flat_vec)), then the other
+// jobs of at least kGatherSmallBytes per rank, then the smaller ones (vectors
+// [small_vec, total_vec)); each keeps its own output, so the order changes no
+// result.
 template <class Params>
 void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_flat) {
   uint64_t v = 0;
   int nj = 0;
-  for (int pass = 0; pass < 2; ++pass) {
+  prm.small_vec = 0;
+  prm.small_job0 = 0;
+  for (int pass = 0; pass < 3; ++pass) {
+    if (pass == 2) {
+      prm.small_vec = v;
+      prm.small_job0 = nj;
+    }
     for (int t = 0; t < T; ++t) {
       const GatherTensor& g = ts[t];
       if (g.bytes == 0) continue;
       const bool aligned = tensor_aligned(g, P, allow_flat);
-      if (aligned != (pass == 0)) continue;
+      const int kind = aligned ? 0 : g.bytes < kGatherSmallBytes ? 2 : 1;
+      if (kind != pass) continue;
       GatherJob& J = prm.job[nj];
       J.out = g.out;
       J.bytes = g.bytes;
@@ -249,19 +325,27 @@ void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_f
   prm.total_vec = v;
 }
 
-// Split of a launch's CTAs (at most `cap`) between the aligned jobs (tiles of
-// kSplitVectors vectors per thread) and the rest (tiles of
-// kSplitRealignVectors), in proportion to their work: a realigned 16-byte
-// vector counts gather_split_cost_pct / 100 staged ones, so both parts
-// finish together.  Measured on GB300 with the six mixed tensors of the
-// all_gather_many workload (P = 8), both parts staged: 100 % -> 115 us,
-// 150 % -> 108.5 us, 200 % -> 108 us, 250 % -> 100.6 us, 300 % -> 104 us;
-// every CTA on the register realigning path instead: 141 us.  Each part gets the fewest
-// CTAs that finish its tiles in the same number of rounds.  Returns the total grid, 0 if no split
-// is possible (fewer than two CTAs for two parts).
+// Split of a launch's CTAs (at most `cap`) between its three parts: the
+// jobs of fewer than kGatherSmallBytes per rank get one CTA per kGatherBlock
+// threads, kSmallSplit threads per output vector (so all their byte loads
+// are in flight at once), at the end of the grid; the rest goes to the
+// aligned jobs (tiles of kSplitVectors vectors per thread) and the other
+// unaligned jobs (tiles of kSplitRealignVectors), in proportion to their
+// work: a realigned 16-byte vector counts gather_split_cost_pct / 100 staged
+// ones, so both parts finish together.  Measured on GB300 with the six mixed
+// tensors of the all_gather_many workload (P = 8), both parts staged: 100 %
+// -> 115 us, 150 % -> 108.5 us, 200 % -> 108 us, 250 % -> 100.6 us, 300 %
+// -> 104 us; every CTA on the register realigning path instead: 141 us.
+// Each part gets the fewest CTAs that finish its tiles in the same number of
+// rounds.  Returns the total grid, 0 if no split is possible (fewer CTAs than
+// parts with work).
 template <class Params>
 int plan_split(Params& prm, uint64_t cap) {
-  const uint64_t fv = prm.flat_vec, gv = prm.total_vec - prm.flat_vec;
+  const uint64_t fv = prm.flat_vec, gv = prm.small_vec - prm.flat_vec, sv = prm.total_vec - prm.small_vec;
+  const uint64_t others = (fv > 0 ? 1 : 0) + (gv > 0 ? 1 : 0);
+  if (cap < others + (sv > 0 ? 1 : 0)) return 0;
+  const uint64_t sc = std::min((sv * kSmallSplit + kGatherBlock - 1) / kGatherBlock, cap - others);
+  cap -= sc;
   const uint64_t ftile = static_cast<uint64_t>(kGatherBlock) * kSplitVectors;
   const uint64_t gtile = static_cast<uint64_t>(kGatherBlock) * kSplitRealignVectors;
   const uint64_t ft = (fv + ftile - 1) / ftile, gt = (gv + gtile - 1) / gtile;
@@ -273,7 +357,6 @@ int plan_split(Params& prm, uint64_t cap) {
     gf = 0;
     gg = std::min(cap, gt);
   } else {
-    if (cap < 2) return 0;
     const double cost = static_cast<double>(std::max(1LL, g_opt.split_cost_pct.load())) / 100.0;
     const double wf = static_cast<double>(fv), wg = cost * static_cast<double>(gv);
     gf = static_cast<uint64_t>(static_cast<double>(cap) * wf / (wf + wg) + 0.5);
@@ -288,7 +371,8 @@ int plan_split(Params& prm, uint64_t cap) {
   gf = trim(ft, std::min(gf, ft));
   gg = trim(gt, std::min(gg, gt));
   prm.flat_ctas = static_cast<int32_t>(gf);
-  return static_cast<int>(gf + gg);
+  prm.small_ctas = static_cast<int32_t>(sc);
+  return static_cast<int>(gf + gg + sc);
 }
 
 // Work units per tile, chosen so that every SM gets the same share of a
@@ -346,6 +430,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   prm.staged = g_opt.gather_staged.load() ? 1 : 0;
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.flat_ctas = 0;
+  prm.small_ctas = 0;
   prm.tile_vec = 0;  // single-CTA launches: the kernel's own tile
   int grid = 1;
   if (!single) {
@@ -357,9 +442,10 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       const uint64_t cap = forced > 0 ? static_cast<uint64_t>(forced)
                                       : static_cast<uint64_t>(sms) * static_cast<uint64_t>(occ);
       grid = plan_split(prm, std::min<uint64_t>(cap, 0x7FFFFFFFull));
-      if (grid == 0) {  // one CTA cannot hold both parts: every CTA takes the realigning path
+      if (grid == 0) {  // fewer CTAs than parts: every CTA takes the realigning path
         prm.staged = 0;
         prm.flat_ctas = 0;
+        prm.small_ctas = 0;
         mode = gather_mode_of(prm);
       }
     }
@@ -398,6 +484,77 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   }
   return check_launch(launch_gather(prm, grid, single, g_opt.pdl.load() != 0, stream), "all-gather",
                       single ? 1 : grid);
+}
+
+// One 16-byte aligned gather on the TMA engine (dc_bulk.cu).  Chunks: with
+// more than one full chunk (bulk_chunk_bytes) per CTA slot (SMs x
+// bulk_ctas_per_sm), R = ceil(total / (slots x full)) rounds of equal chunks
+// of total / (slots x R) bytes; a smaller output is cut into chunks of at
+// least bulk_chunk_min bytes, one per CTA.  Chunks are rounded up to 128
+// bytes (whole L2 lines; rounding up only lowers the chunk count, so no CTA
+// gets an extra round).  The ring has bulk_stages stages, fewer when a CTA
+// has fewer chunks, and never more than fit kBulkMaxSmem.
+struct BulkPlan {
+  uint64_t chunk;
+  int stages;
+  int grid;
+};
+
+BulkPlan plan_bulk(uint64_t total, int sms) {
+  const uint64_t cps = static_cast<uint64_t>(std::min(std::max(g_opt.bulk_ctas_per_sm.load(), 1LL), 32LL));
+  const uint64_t full = std::max<uint64_t>(16, static_cast<uint64_t>(g_opt.bulk_chunk_bytes.load()) & ~15ull);
+  const uint64_t cmin = std::min(full, std::max<uint64_t>(16, static_cast<uint64_t>(g_opt.bulk_chunk_min.load())));
+  const uint64_t slots = static_cast<uint64_t>(std::max(sms, 1)) * cps;
+  auto round_up = [](uint64_t x, uint64_t g) { return (x + g - 1) / g * g; };
+  uint64_t chunk;
+  if (total > slots * full) {
+    const uint64_t rounds = (total + slots * full - 1) / (slots * full);
+    chunk = (total + slots * rounds - 1) / (slots * rounds);
+  } else {
+    const uint64_t g = std::max<uint64_t>(1, std::min(slots, total / cmin));
+    chunk = (total + g - 1) / g;
+  }
+  chunk = chunk >= 128 ? round_up(chunk, 128) : round_up(chunk, 16);
+  const uint64_t nchunks = (total + chunk - 1) / chunk;
+  const uint64_t grid = std::min<uint64_t>(nchunks, slots);
+  const uint64_t per_cta = (nchunks + grid - 1) / grid;
+  uint64_t S = std::min<uint64_t>(std::max(g_opt.bulk_stages.load(), 1LL), 32);
+  S = std::min(S, per_cta);
+  const uint64_t fit = kBulkMaxSmem / (chunk + 8);
+  S = std::max<uint64_t>(1, std::min(S, fit));
+  const long long forced = g_opt.grid_ctas.load();
+  const uint64_t g = forced > 0 ? std::min<uint64_t>(static_cast<uint64_t>(forced), nchunks) : grid;
+  return BulkPlan{chunk, static_cast<int>(S), static_cast<int>(std::min<uint64_t>(g, 0x7FFFFFFFull))};
+}
+
+dc_status_t launch_bulk_plan(const GatherTensor& t, int P, uint64_t total, cudaStream_t stream) {
+  if (g_opt.test_fail_launch.load())
+    return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
+  int dev = 0, sms = 0;
+  dc_status_t st = current_device(&dev);
+  if (st != DC_OK) return st;
+  st = sm_count(dev, &sms);
+  if (st != DC_OK) return st;
+  BulkParams bp{};
+  bp.out = t.out;
+  bp.bytes = t.bytes;
+  bp.total = total;
+  bp.P = P;
+  for (int r = 0; r < P; ++r) bp.src[r] = reinterpret_cast<uint64_t>(t.peers[r]);
+  const BulkPlan plan = plan_bulk(total, sms);
+  bp.chunk = plan.chunk;
+  bp.stages = plan.stages;
+  // L2 prefetch distance in chunks per CTA, at most 64 MB ahead over the grid
+  const uint64_t pf_cap = (64ull << 20) / (plan.chunk * static_cast<uint64_t>(plan.grid));
+  bp.prefetch = g_opt.prefetch.load()
+                    ? static_cast<int32_t>(std::min<uint64_t>(
+                          std::min<uint64_t>(static_cast<uint64_t>(g_opt.bulk_prefetch.load()), 1024),
+                          std::max<uint64_t>(pf_cap, 1)))
+                    : 0;
+  bp.wait_ns = static_cast<uint64_t>(std::max(g_opt.wait_limit_ns.load(), 1000LL));
+  bp.test_flags = g_opt.test_bulk_short_tx.load() ? kBulkTestShortTx : 0u;
+  return check_launch(launch_gather_bulk(bp, plan.grid, g_opt.pdl.load() != 0, stream), "all-gather (bulk)",
+                      plan.grid);
 }
 
 // --------------------------------------------------------------- reduce ---
@@ -643,9 +800,15 @@ dc_status_t dc_all_gather(const void* const* peer_ptrs, int P, size_t bytes_per_
     if (overlaps(o, total, s, B))
       return fail(DC_ERR_OVERLAP, "output overlaps the payload of rank %d", r);
   }
-  GatherParams1 prm{};
   GatherTensor t{o, B, peer_ptrs};
-  fill_gather(prm, &t, 1, P, g_opt.force_generic.load() == 0);
+  const bool allow_flat = g_opt.force_generic.load() == 0;
+  // 16-byte aligned and not sent to one CTA: the TMA-engine copy
+  if (allow_flat && g_opt.gather_bulk.load() && tensor_aligned(t, P, true) &&
+      total >= static_cast<uint64_t>(g_opt.bulk_min_bytes.load()) &&
+      !use_single(total, g_opt.gather_single_max.load()))
+    return launch_bulk_plan(t, P, total, static_cast<cudaStream_t>(stream));
+  GatherParams1 prm{};
+  fill_gather(prm, &t, 1, P, allow_flat);
   return launch_gather_plan(prm, 0, total, static_cast<cudaStream_t>(stream));
 }
 
@@ -683,20 +846,8 @@ dc_status_t dc_all_gather_many(const void* const* peer_ptrs, const size_t* bytes
     }
   }
   if (live == 0) return ok();
-  // every output against every output and every payload
-  for (int t = 0; t < T; ++t) {
-    if (ts[t].bytes == 0) continue;
-    const uint64_t ot = ts[t].out, nt = ts[t].bytes * P;
-    for (int u = 0; u < T; ++u) {
-      if (ts[u].bytes == 0) continue;
-      if (u > t && overlaps(ot, nt, ts[u].out, ts[u].bytes * P))
-        return fail(DC_ERR_OVERLAP, "outputs of tensors %d and %d overlap", t, u);
-      for (int r = 0; r < P; ++r)
-        if (overlaps(ot, nt, reinterpret_cast<uint64_t>(ts[u].peers[r]), ts[u].bytes))
-          return fail(DC_ERR_OVERLAP, "output of tensor %d overlaps the payload of tensor %d rank %d",
-                      t, u, r);
-    }
-  }
+  const dc_status_t ov = check_gather_overlaps(ts, T, P);
+  if (ov != DC_OK) return ov;
   const bool allow_flat = g_opt.force_generic.load() == 0;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (live <= kManySmallTensors && live * P <= kManySmallSegments) {
@@ -764,6 +915,129 @@ dc_status_t dc_inject_delay_ns(unsigned long long ns, dc_stream_t stream) {
   if (g_opt.test_fail_launch.load())
     return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
   return check_launch(launch_delay(ns, static_cast<cudaStream_t>(stream)), "delay", 1);
+}
+
+size_t dc_fused_workspace_bytes(int P) {
+  return P < 1 || P > kMaxRanks ? 0 : fused_workspace_bytes(P);
+}
+
+dc_status_t dc_fused_all_gather(const void* const* in_ptrs, void* const* staging, void* const* outs, int P,
+                                size_t bytes_per_rank, void* workspace, unsigned int epoch, dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (bytes_per_rank == 0) return ok();
+  if (!in_ptrs || !staging || !outs) return fail(DC_ERR_INVALID, "in_ptrs, staging and outs must not be NULL");
+  if (!workspace) return fail(DC_ERR_INVALID, "workspace is NULL");
+  if (epoch == 0) return fail(DC_ERR_INVALID, "epoch 0 is reserved for a cleared workspace");
+  const uint64_t B = bytes_per_rank;
+  if (B > UINT64_MAX / static_cast<uint64_t>(P)) return fail(DC_ERR_INVALID, "P * bytes_per_rank overflows");
+  const uint64_t total = B * static_cast<uint64_t>(P);
+  const uint64_t ws = reinterpret_cast<uint64_t>(workspace), wsb = fused_workspace_bytes(P);
+  if ((B & 15u) || (ws & 15u))
+    return fail(DC_ERR_ALIGN, "bytes_per_rank and the workspace must be multiples of 16 bytes");
+  // written ranges (staging buffers, outputs, workspace) may overlap nothing;
+  // inputs may overlap each other
+  struct R {
+    uint64_t lo, hi;
+    int kind, rank;  // kind 0 input, 1 staging, 2 output, 3 workspace
+  };
+  std::vector<R> v;
+  v.reserve(3 * static_cast<size_t>(P) + 1);
+  v.push_back(R{ws, ws + wsb, 3, 0});
+  for (int r = 0; r < P; ++r) {
+    const uint64_t a[3] = {reinterpret_cast<uint64_t>(in_ptrs[r]), reinterpret_cast<uint64_t>(staging[r]),
+                           reinterpret_cast<uint64_t>(outs[r])};
+    const uint64_t n[3] = {B, B, total};
+    for (int k = 0; k < 3; ++k) {
+      if (!a[k]) return fail(DC_ERR_INVALID, "a pointer of rank %d is NULL", r);
+      if (a[k] & 15u) return fail(DC_ERR_ALIGN, "the buffers of rank %d must be 16-byte aligned", r);
+      if (a[k] + n[k] < a[k]) return fail(DC_ERR_INVALID, "a buffer of rank %d wraps around", r);
+      v.push_back(R{a[k], a[k] + n[k], k, r});
+    }
+  }
+  std::sort(v.begin(), v.end(), [](const R& x, const R& y) { return x.lo < y.lo; });
+  static const char* const kKind[4] = {"input", "staging buffer", "output", "workspace"};
+  const R* far_any = nullptr;  // the range reaching furthest so far
+  const R* far_w = nullptr;    // the written range reaching furthest so far
+  for (const R& x : v) {
+    const R* hit = x.kind == 0 ? far_w : far_any;
+    if (hit && hit->hi > x.lo)
+      return fail(DC_ERR_OVERLAP, "%s of rank %d overlaps %s of rank %d", kKind[x.kind], x.rank,
+                  kKind[hit->kind], hit->rank);
+    if (!far_any || x.hi > far_any->hi) far_any = &x;
+    if (x.kind != 0 && (!far_w || x.hi > far_w->hi)) far_w = &x;
+  }
+  if (g_opt.test_fail_launch.load())
+    return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
+  int dev = 0, sms = 0;
+  dc_status_t st = current_device(&dev);
+  if (st != DC_OK) return st;
+  st = sm_count(dev, &sms);
+  if (st != DC_OK) return st;
+  // G chunks per rank (one CTA each): chunks of at least fused_chunk_min
+  // bytes, at most kFusedMaxChunks, and all P * G CTAs resident at once
+  const uint64_t resident = static_cast<uint64_t>(sms) *
+                            static_cast<uint64_t>(occupancy(dev, 127, [] { return fused_ctas_per_sm(); }));
+  if (resident < static_cast<uint64_t>(P))
+    return fail(DC_ERR_INVALID, "%d ranks need %d CTAs resident at once; the GPU holds %llu", P, P,
+                static_cast<unsigned long long>(resident));
+  const uint64_t cmin = static_cast<uint64_t>(std::max(16LL, g_opt.fused_chunk_min.load()));
+  uint64_t G = std::min<uint64_t>({(B + cmin - 1) / cmin, static_cast<uint64_t>(kFusedMaxChunks),
+                                   resident / static_cast<uint64_t>(P)});
+  G = std::max<uint64_t>(G, 1);
+  const uint64_t chunk = ((B + G - 1) / G + 15) / 16 * 16;
+  G = (B + chunk - 1) / chunk;
+  FusedParams fp{};
+  for (int r = 0; r < P; ++r) {
+    fp.in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
+    fp.staging[r] = reinterpret_cast<uint64_t>(staging[r]);
+    fp.out[r] = reinterpret_cast<uint64_t>(outs[r]);
+  }
+  fp.bytes = B;
+  fp.chunk = chunk;
+  fp.wait_ns = static_cast<uint64_t>(std::max(g_opt.wait_limit_ns.load(), 1000LL));
+  fp.ws = ws;
+  fp.absent = static_cast<uint64_t>(g_opt.test_fused_absent.load());
+  fp.epoch = epoch;
+  fp.P = P;
+  fp.G = static_cast<int32_t>(G);
+  return check_launch(launch_fused_gather(fp, static_cast<cudaStream_t>(stream)), "fused all-gather",
+                      static_cast<int>(P * G));
+}
+
+dc_status_t dc_fused_reset(void* workspace, int P, dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (!workspace) return fail(DC_ERR_INVALID, "workspace is NULL");
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, fused_workspace_bytes(P), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DC_ERR_CUDA, "clearing the workspace failed: %s", cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+dc_status_t dc_check_device(void) {
+  read_env_once();
+  uint32_t bits = 0, fused[4] = {0, 0, 0, 0};
+  cudaError_t e = take_bulk_faults(&bits);
+  if (e == cudaSuccess) e = take_fused_faults(fused);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DC_ERR_CUDA, "device check failed: %s", cudaGetErrorString(e));
+  }
+  if (fused[0] & kFaultFusedWait) {
+    const uint32_t phase = fused[1] >> 24, rank = (fused[1] >> 12) & 0xFFFu, peer = fused[1] & 0xFFFu;
+    return fail(DC_ERR_TIMEOUT,
+                "fused all-gather: rank %u gave up waiting for rank %u's %s flag of chunk %u (epoch %u) "
+                "after wait_limit_ns; clear the workspace (dc_fused_reset) and start again at epoch 1",
+                rank, peer, phase == 1 ? "staged" : "done", fused[2], fused[3]);
+  }
+  if (bits & kFaultBulkWait)
+    return fail(DC_ERR_TIMEOUT,
+                "a bulk-copy all-gather gave up waiting for its loads after wait_limit_ns; "
+                "its output is incomplete");
+  return ok();
 }
 
 const char* dc_last_error(void) { return g_err; }

@@ -7,6 +7,73 @@
 
 namespace dc {
 
+// ------------------------------------------------------ bounds checks ---
+// Built with -DDC_DEBUG_BOUNDS (the checked library, libdc_bounds.so), every
+// global load, store and L2 prefetch of the kernels is first checked against
+// the range its job allows: for a load or prefetch the 16-byte-block hull of
+// the source it reads (a realigning copy reads whole aligned blocks around an
+// unaligned span), for a store the exact output range.  An access outside is
+// skipped, never made, and the first one is recorded in a device word of its
+// translation unit, which dc_check_device reads, clears and reports as
+// DC_ERR_BOUNDS; the kernel never traps.  In the normal build every check is
+// the constant true and compiles to nothing.
+struct BoundsFault {
+  unsigned int count;  // accesses outside their range since the last read
+  unsigned int site;   // where the first one was (kSite* of its file)
+  unsigned long long addr, len, lo, hi;
+};
+#ifdef DC_DEBUG_BOUNDS
+static __device__ BoundsFault g_bounds_fault;
+#endif
+
+// True if [a, a + len) lies in [lo, hi); else (checked build) records it.
+__device__ __forceinline__ bool in_bounds(const void* a, uint64_t len, uint64_t lo, uint64_t hi,
+                                          uint32_t site) {
+#ifdef DC_DEBUG_BOUNDS
+  const uint64_t x = reinterpret_cast<uint64_t>(a);
+  if (x >= lo && x <= hi && len <= hi - x) return true;
+  if (atomicAdd(&g_bounds_fault.count, 1u) == 0u) {
+    g_bounds_fault.site = site;
+    g_bounds_fault.addr = x;
+    g_bounds_fault.len = len;
+    g_bounds_fault.lo = lo;
+    g_bounds_fault.hi = hi;
+    __threadfence();
+  }
+  return false;
+#else
+  (void)a, (void)len, (void)lo, (void)hi, (void)site;
+  return true;
+#endif
+}
+
+// Defines `cudaError_t NAME(BoundsFault*)`, the host reader of this file's
+// record (synchronises the device, reads, clears).
+#ifdef DC_DEBUG_BOUNDS
+#define DC_BOUNDS_READER(NAME)                                                   \
+  cudaError_t NAME(BoundsFault* f) {                                             \
+    *f = BoundsFault{};                                                          \
+    cudaError_t e = cudaDeviceSynchronize();                                     \
+    if (e != cudaSuccess) return e;                                              \
+    e = cudaMemcpyFromSymbol(f, g_bounds_fault, sizeof(BoundsFault));            \
+    if (e != cudaSuccess || f->count == 0) return e;                             \
+    const BoundsFault zero{};                                                    \
+    return cudaMemcpyToSymbol(g_bounds_fault, &zero, sizeof(BoundsFault));       \
+  }
+#else
+#define DC_BOUNDS_READER(NAME)   \
+  cudaError_t NAME(BoundsFault* f) { \
+    *f = BoundsFault{};          \
+    return cudaSuccess;          \
+  }
+#endif
+
+// The 16-byte-block hull of [a, a + n): [hull_lo(a), hull_hi(a, n)).
+__host__ __device__ __forceinline__ uint64_t hull_lo(uint64_t a) { return a & ~static_cast<uint64_t>(15); }
+__host__ __device__ __forceinline__ uint64_t hull_hi(uint64_t a, uint64_t n) {
+  return (a + n + 15) & ~static_cast<uint64_t>(15);
+}
+
 // Programmatic dependent launch.  When a kernel is launched with
 // programmatic stream serialization, the GPU may start it before the previous
 // kernel in the stream has finished; griddepcontrol.wait then blocks until

@@ -1,0 +1,213 @@
+// dc_fused.cu -- the staged all-gather protocol of a multi-rank deterministic
+// collective (stage -> gather -> complete), with every wait bounded.
+//
+// "perf(cuda): vectorize the deterministic all-gather copy and right-size its
+// single-block path" (RL-Kernel PR 491) describes the deployment behind the
+// copy: a backend named cuda_ipc_fixed_tree whose ranks exchange payloads
+// through staging buffers that their peers map and read, in a CUDA-graph-safe
+// fused protocol of three steps -- each rank stages its payload, gathers its
+// peers' staged payloads, and completes, after which its staging buffer may be
+// reused (author's replies).  The page leaves open that a failed launch leaves
+// that protocol pending with no abort path, and that when a rank dies its
+// peers wait until the process-group timeout (section "Not in this PR" and the
+// review threads on the pending state and on the distributed test).
+//
+// Here the P ranks are groups of CTAs of ONE cooperative launch on one GPU:
+// the cooperative launch makes every CTA of the grid resident at once, so a
+// CTA may wait for another without deadlock.  Rank r owns an input, a staging
+// buffer and an output; its B bytes are cut into G chunks, and CTA (r, c)
+// handles chunk c of rank r:
+//   stage:    in_r[chunk c] -> staging_r[chunk c]; then staged[r][c] = epoch
+//             (release store, after a device-scope fence by every thread);
+//   gather:   for each rank q (starting with itself): wait until
+//             staged[q][c] == epoch (acquire load), then staging_q[chunk c] ->
+//             out_r[q*B + chunk c] (loads through L2 only: staging_q is
+//             written by other CTAs);
+//   complete: done[r][c] = epoch, then wait until done[q][c] == epoch for
+//             every q: chunk c of staging_r has been read by every rank and
+//             may be overwritten by the next epoch.
+// The flags live in a caller-owned workspace of P x kFusedMaxChunks x 2
+// words, zero before the first call; each call carries a new epoch (1, 2,
+// 3, ...), so no flag is ever reset between calls.  Every wait is bounded by
+// wait_ns of the global timer and a poll count.  A wait that runs out records
+// the first fault (phase, waiting rank, awaited rank, chunk, epoch) in a
+// device fault word read by dc_check_device, and the CTA returns: a rank that
+// never arrives makes its peers report DC_ERR_TIMEOUT within the bound
+// instead of hanging.  The caller then clears the workspace and starts again
+// at epoch 1 (dc_fused_reset): that is the abort path.
+#include <atomic>
+
+#include "dc_device.cuh"
+#include "dc_internal.h"
+
+namespace dc {
+namespace {
+
+// First fault of a fused launch: [0] kFaultFusedWait bits, [1] phase << 24 |
+// waiting rank << 12 | awaited rank, [2] chunk, [3] epoch.  Sticky until
+// take_fused_faults reads and clears it.
+__device__ unsigned int g_fused_fault[4];
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 16-byte load through L2 only (no L1 line that could hold an older epoch's
+// bytes of a staging buffer).
+__device__ __forceinline__ uint4 ld_cg16(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Waits until *f == want, for at most limit_ns of the global timer and at
+// most 2^24 polls.  False: it ran out.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t want, uint64_t limit_ns) {
+  if (ld_acquire_u32(f) == want) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    __nanosleep(64);
+    if (ld_acquire_u32(f) == want) return true;
+    if (global_ns() - t0 >= limit_ns) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void record_fault(uint32_t phase, uint32_t rank, uint32_t peer, uint32_t chunk,
+                                             uint32_t epoch) {
+  if (atomicCAS(&g_fused_fault[0], 0u, kFaultFusedWait) == 0u) {
+    g_fused_fault[1] = (phase << 24) | (rank << 12) | peer;
+    g_fused_fault[2] = chunk;
+    g_fused_fault[3] = epoch;
+    __threadfence();
+  }
+}
+
+// n bytes (a multiple of 16; both pointers 16-byte aligned) copied by the
+// CTA's threads, four 16-byte vectors in flight per thread.
+template <bool THROUGH_L2>
+__device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uint64_t n) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  const uint64_t nv = n >> 4;
+  for (uint64_t i = threadIdx.x; i < nv; i += 4ull * kFusedBlock) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t k = i + static_cast<uint64_t>(u) * kFusedBlock;
+      if (k < nv) v[u] = THROUGH_L2 ? ld_cg16(s + k) : ld_stream(s + k);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t k = i + static_cast<uint64_t>(u) * kFusedBlock;
+      if (k < nv) st16(d + k, v[u]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __grid_constant__ FusedParams p) {
+  __shared__ int s_ok[kMaxRanks + 1];
+  const uint32_t P = static_cast<uint32_t>(p.P), G = static_cast<uint32_t>(p.G);
+  const uint32_t r = blockIdx.x / G, c = blockIdx.x % G;
+  if (r >= P) return;
+  if ((p.absent >> r) & 1ull) return;  // (test only: a rank that never arrives)
+  uint32_t* staged = reinterpret_cast<uint32_t*>(p.ws);
+  uint32_t* done = staged + static_cast<uint64_t>(P) * kFusedMaxChunks;
+  const uint64_t lo = static_cast<uint64_t>(c) * p.chunk;
+  const uint64_t n = lo < p.bytes ? min(p.chunk, p.bytes - lo) : 0;
+  const uint32_t epoch = p.epoch;
+
+  // stage
+  copy_chunk<false>(reinterpret_cast<const uint8_t*>(p.in[r]) + lo, reinterpret_cast<uint8_t*>(p.staging[r]) + lo,
+                    n);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) st_release_u32(&staged[r * kFusedMaxChunks + c], epoch);
+
+  // gather, own rank first
+  for (uint32_t i = 0; i < P; ++i) {
+    const uint32_t q = r + i < P ? r + i : r + i - P;
+    if (threadIdx.x == 0) {
+      const bool ok = wait_flag(&staged[q * kFusedMaxChunks + c], epoch, p.wait_ns);
+      if (!ok) record_fault(1, r, q, c, epoch);
+      __threadfence();
+      s_ok[i] = ok;
+    }
+    __syncthreads();
+    if (!s_ok[i]) return;
+    copy_chunk<true>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
+                     reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n);
+  }
+
+  // complete
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    st_release_u32(&done[r * kFusedMaxChunks + c], epoch);
+    for (uint32_t q = 0; q < P; ++q)
+      if (!wait_flag(&done[q * kFusedMaxChunks + c], epoch, p.wait_ns)) {
+        record_fault(2, r, q, c, epoch);
+        break;
+      }
+  }
+}
+
+}  // namespace
+
+int fused_ctas_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_fused_gather_kernel, kFusedBlock, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_fused_gather(const FusedParams& p, cudaStream_t s) {
+  if (p.P < 1 || p.P > kMaxRanks || p.G < 1 || p.G > kFusedMaxChunks || (p.chunk & 15u) || (p.bytes & 15u) ||
+      p.epoch == 0 || static_cast<uint64_t>(p.G) * p.chunk < p.bytes)
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.P * p.G));
+  cfg.blockDim = dim3(kFusedBlock);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dc_fused_gather_kernel, p);
+}
+
+cudaError_t take_fused_faults(uint32_t* info) {
+  for (int i = 0; i < 4; ++i) info[i] = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  unsigned int v[4] = {0, 0, 0, 0};
+  e = cudaMemcpyFromSymbol(v, g_fused_fault, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v[0]) {
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    e = cudaMemcpyToSymbol(g_fused_fault, zero, sizeof zero);
+  }
+  for (int i = 0; i < 4; ++i) info[i] = v[i];
+  return e;
+}
+
+}  // namespace dc

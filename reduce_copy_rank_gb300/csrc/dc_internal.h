@@ -67,6 +67,8 @@ __host__ __device__ constexpr int reduce_pt(int P) { return P == 2 || P == 4 || 
 // at most kMaxRanks * 127 bytes, and the vector machinery would cost more
 // than it saves.
 constexpr uint64_t kGatherSmallBytes = 128;
+// Threads per 16-byte output vector in the small-job part of all_gather_many.
+constexpr int kSmallSplit = 4;
 
 // ------------------------------------------------------------- gather ---
 enum : uint32_t {
@@ -91,6 +93,10 @@ template <int MAXJ, int MAXS>
 struct GatherParams {
   uint64_t total_vec;   // sum of nvec over the jobs
   uint64_t flat_vec;    // jobs are ordered aligned (kJobFlat) first: their vectors are [0, flat_vec)
+  uint64_t small_vec;   // ... then the other jobs of at least kGatherSmallBytes per rank, then the
+                        // kJobSmall jobs, whose vectors are [small_vec, total_vec)
+  int32_t small_job0;   // index of the first kJobSmall job (njobs if none)
+  int32_t small_ctas;   // split launch: the last small_ctas CTAs copy the kJobSmall jobs
   int32_t njobs;
   int32_t P;
   int32_t staged;       // stage aligned copies through shared memory with cp.async
@@ -104,6 +110,55 @@ struct GatherParams {
 using GatherParams1 = GatherParams<1, kMaxRanks>;
 using GatherParamsS = GatherParams<kManySmallTensors, kManySmallSegments>;
 using GatherParamsL = GatherParams<kManyMaxTensors, kManyMaxSegments>;
+
+// One 16-byte aligned gather (out, bytes and every source 16-byte aligned)
+// copied by the TMA engine: the output is cut into chunks of `chunk` bytes
+// (a multiple of 16), CTA c takes chunks c, c + G, ... and moves each through
+// one of `stages` shared-memory stages with 1-D bulk copies.
+struct BulkParams {
+  uint64_t out;
+  uint64_t bytes;      // per rank
+  uint64_t total;      // P * bytes
+  uint64_t chunk;      // bytes per chunk
+  uint64_t wait_ns;    // limit of one wait for a stage's loads (global timer)
+  int32_t P;
+  int32_t stages;      // ring stages per CTA (1..32)
+  int32_t prefetch;    // chunks whose sources a CTA prefetches into L2 ahead of its loads
+  uint32_t test_flags; // kBulkTestShortTx: a test makes the first stage's wait run out
+  uint64_t src[kMaxRanks];
+};
+enum : uint32_t { kBulkTestShortTx = 1u };
+// Device fault bits (sticky until read by dc_check_device).
+enum : uint32_t { kFaultBulkWait = 1u, kFaultFusedWait = 2u };
+
+// The staged all-gather protocol (dc_fused.cu): P ranks, each a group of G
+// CTAs of one cooperative launch; rank r's bytes are cut into G chunks of
+// `chunk` bytes.  The workspace holds uint32 staged[P][kFusedMaxChunks] and
+// done[P][kFusedMaxChunks] epoch flags.
+constexpr int kFusedBlock = 256;
+constexpr int kFusedMaxChunks = 128;
+struct FusedParams {
+  uint64_t in[kMaxRanks];
+  uint64_t staging[kMaxRanks];
+  uint64_t out[kMaxRanks];
+  uint64_t bytes;      // per rank, a multiple of 16
+  uint64_t chunk;      // a multiple of 16; G * chunk >= bytes
+  uint64_t wait_ns;    // limit of one wait (global timer)
+  uint64_t ws;         // workspace (device address)
+  uint64_t absent;     // (tests) bit r: rank r never arrives
+  uint32_t epoch;      // nonzero, new for every call since the workspace was cleared
+  int32_t P;
+  int32_t G;
+};
+__host__ __device__ constexpr size_t fused_workspace_bytes(int P) {
+  return static_cast<size_t>(P) * kFusedMaxChunks * 2 * sizeof(uint32_t);
+}
+cudaError_t launch_fused_gather(const FusedParams& p, cudaStream_t s);
+int fused_ctas_per_sm();
+// Reads and clears the first fault of the fused kernel on the current device
+// (synchronous): info[0] fault bits, [1] phase << 24 | rank << 12 | peer,
+// [2] chunk, [3] epoch.
+cudaError_t take_fused_faults(uint32_t* info);
 
 // ---------------------------------------------------------- reduction ---
 enum : int { kBF16 = 0, kF16 = 1, kF32 = 2 };              // element types
@@ -182,6 +237,29 @@ cudaError_t launch_reduce(const Params& p, int dtype, int order, int grid, bool 
     default: return launch_reduce_bf16(p, order, grid, single, pdl, s);
   }
 }
+
+// The TMA-engine gather (dc_bulk.cu): `grid` CTAs, each with `stages` *
+// `chunk` bytes of dynamic shared memory (plus its mbarriers).
+cudaError_t launch_gather_bulk(const BulkParams& p, int grid, bool pdl, cudaStream_t s);
+size_t bulk_smem_bytes(uint64_t chunk, int stages);
+constexpr size_t kBulkMaxSmem = 227 * 1024;  // dynamic shared memory one bulk CTA may ask for
+// Reads and clears the fault bits that the kernels of dc_bulk.cu recorded on
+// the current device (synchronous).
+cudaError_t take_bulk_faults(uint32_t* bits);
+
+// Bounds-check records of the checked build (-DDC_DEBUG_BOUNDS), one per
+// kernel file; each reads and clears its file's record (synchronous), or
+// returns an empty one in the normal build.  bounds_file names the file of
+// reader i (i < kBoundsReaders).
+struct BoundsFault;
+constexpr int kBoundsReaders = 6;
+cudaError_t take_bounds_gather(BoundsFault* f);
+cudaError_t take_bounds_bulk(BoundsFault* f);
+cudaError_t take_bounds_fused(BoundsFault* f);
+cudaError_t take_bounds_reduce_bf16(BoundsFault* f);
+cudaError_t take_bounds_reduce_f16(BoundsFault* f);
+cudaError_t take_bounds_reduce_f32(BoundsFault* f);
+bool bounds_checked_build();
 
 // One-thread delay of `ns` nanoseconds of the global timer (rank-skew
 // calibration); defined in dc_delay.cu.

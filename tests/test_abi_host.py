@@ -136,6 +136,69 @@ def test_many_zero_sized_tensors_are_skipped(no_launch):
     assert dc.dc_all_gather_many(peers, [0, 32], [0, BASE + 4096], 2, 2) == CUDA
 
 
+def _many_overlap_model(peers, sizes, outs, T, P):
+    """The rule of dc_all_gather_many, pair by pair: an output may overlap no
+    other output and no payload; payloads may overlap each other."""
+    if not any(sizes[:T]):
+        return OK  # nothing to gather: a no-op
+    rng = []
+    for t in range(T):
+        if sizes[t] == 0:
+            continue
+        rng.append((outs[t], outs[t] + P * sizes[t], True))
+        rng.extend((peers[t * P + r], peers[t * P + r] + sizes[t], False) for r in range(P))
+    for i in range(len(rng)):
+        for k in range(i + 1, len(rng)):
+            a, b = rng[i], rng[k]
+            if (a[2] or b[2]) and a[0] < b[1] and b[0] < a[1]:
+                return OVERLAP
+    return CUDA
+
+
+def test_many_overlap_check_matches_pairwise_model(no_launch):
+    import random
+
+    rnd = random.Random(0xDC17)
+    for _ in range(400):
+        P, T = rnd.randint(1, 5), rnd.randint(1, 6)
+        sizes = [rnd.choice([0, 1, 16, 100, 4096]) for _ in range(T)]
+        slots = [BASE + k * 8192 for k in range(10)]
+        peers = [rnd.choice(slots) + rnd.choice([0, 1, 16, 4000]) for _ in range(T * P)]
+        outs = [rnd.choice(slots) + rnd.choice([0, 3, 2048, 8000]) for _ in range(T)]
+        want = _many_overlap_model(peers, sizes, outs, T, P)
+        got = dc.dc_all_gather_many(peers, sizes, outs, T, P)
+        assert got == want, (peers, sizes, outs, T, P, dc.last_error())
+
+
+def test_many_overlap_check_at_the_table_limits(no_launch):
+    """T = 256 tensors x P = 4 ranks (1024 payloads): a clean layout passes,
+    one planted payload inside an output, or two touching outputs that
+    overlap by one byte, are found; the check is a sort and one sweep, so a
+    call costs microseconds of host time, not the ~0.3 M range tests of an
+    all-pairs check."""
+    import time
+
+    T, P, B = 256, 4, 4096
+    peers = [BASE + (t * P + r) * 2 * B for t in range(T) for r in range(P)]
+    out0 = BASE + (T * P + 16) * 2 * B
+    outs = [out0 + t * P * B for t in range(T)]  # back to back, not overlapping
+    assert dc.dc_all_gather_many(peers, [B] * T, outs, T, P) == CUDA
+    t0 = time.perf_counter()
+    for _ in range(20):
+        dc.dc_all_gather_many(peers, [B] * T, outs, T, P)
+    per_call_us = (time.perf_counter() - t0) / 20 * 1e6
+    print(f"all_gather_many validation at T={T}, P={P}: {per_call_us:.1f} us of host time per call")
+    assert per_call_us < 20000
+    planted = list(peers)
+    planted[T * P - 1] = outs[100] + 17  # tensor 255 rank 3's payload inside output 100
+    assert dc.dc_all_gather_many(planted, [B] * T, outs, T, P) == OVERLAP
+    assert "output of tensor 100 overlaps the payload of tensor 255 rank 3" in dc.last_error()
+    bumped = list(outs)
+    bumped[201] -= 1  # output 201 starts one byte inside output 200
+    assert dc.dc_all_gather_many(peers, [B] * T, bumped, T, P) == OVERLAP
+    assert "outputs of tensors 200 and 201 overlap" in dc.last_error()
+
+
 # ------------------------------------------------------------- reductions ---
 
 def test_reduce_rejects_misaligned_bf16():
@@ -346,3 +409,46 @@ def test_tensors_on_another_device_are_rejected(monkeypatch):
     with pytest.raises(ValueError, match="current device"):
         dc.all_reduce([_FakeCudaTensor(64, 0), _FakeCudaTensor(64, 0)],
                       [_FakeCudaTensor(64, 0), _FakeCudaTensor(64, 3)])
+
+
+# ------------------------------------------------------- fused all-gather ---
+
+def _fused_layout(P, B, base=BASE):
+    """Disjoint, 256-byte spaced inputs, staging buffers, outputs and workspace."""
+    step = ((P * B + 255) // 256) * 256 + 256
+    ins = [base + r * step for r in range(P)]
+    stg = [base + (P + r) * step for r in range(P)]
+    outs = [base + (2 * P + r) * step for r in range(P)]
+    ws = base + 3 * P * step
+    return ins, stg, outs, ws
+
+
+def test_fused_workspace_size():
+    assert dc.dc_fused_workspace_bytes(0) == 0 and dc.dc_fused_workspace_bytes(65) == 0
+    assert dc.dc_fused_workspace_bytes(8) == 8 * 128 * 2 * 4
+
+
+def test_fused_argument_checks(no_launch):
+    P, B = 4, 4096
+    ins, stg, outs, ws = _fused_layout(P, B)
+    assert dc.dc_fused_all_gather(ins, stg, outs, P, B, ws, 1) == CUDA  # valid: reaches the launch
+    assert dc.dc_fused_all_gather(ins, stg, outs, P, 0, ws, 1) == OK  # zero bytes: a no-op
+    assert dc.dc_fused_all_gather(ins, stg, outs, 0, B, ws, 1) == INVALID
+    assert dc.dc_fused_all_gather(ins, stg, outs, P, B, ws, 0) == INVALID  # epoch 0 is reserved
+    assert dc.dc_fused_all_gather(ins, stg, outs, P, B, 0, 1) == INVALID
+    assert dc.dc_fused_all_gather(ins, stg, outs, P, B + 8, ws, 1) == ALIGN
+    assert dc.dc_fused_all_gather(ins, stg, [outs[0] + 8] + outs[1:], P, B, ws, 1) == ALIGN
+    assert dc.dc_fused_all_gather(ins, [0] + stg[1:], outs, P, B, ws, 1) == INVALID
+    # inputs may overlap inputs (the same payload on every rank)
+    assert dc.dc_fused_all_gather([ins[0]] * P, stg, outs, P, B, ws, 1) == CUDA
+    # a staging buffer inside another rank's input, an output over the workspace,
+    # two staging buffers on one another
+    assert dc.dc_fused_all_gather(ins, [ins[1]] + stg[1:], outs, P, B, ws, 1) == OVERLAP
+    assert "staging buffer of rank 0" in dc.last_error() or "input of rank 1" in dc.last_error()
+    assert dc.dc_fused_all_gather(ins, stg, outs[:-1] + [ws - 16], P, B, ws, 1) == OVERLAP
+    assert dc.dc_fused_all_gather(ins, [stg[0], stg[0] + 16] + stg[2:], outs, P, B, ws, 1) == OVERLAP
+
+
+def test_fused_reset_checks():
+    assert dc.dc_fused_reset(0, 4) == INVALID
+    assert dc.dc_fused_reset(BASE, 0) == INVALID

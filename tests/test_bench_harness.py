@@ -67,13 +67,13 @@ def test_traffic_record_matches_only_current_sources(tmp_path, monkeypatch):
     digest = bench.kernel_source_digest()
     (prof / "traffic.txt").write_text(
         "# comment\n"
-        f"kernel=k1 source={digest} bytes_per_launch=123.5\n"
+        f"kernel=k1 source={digest} bytes_per_launch=123.5 ncu_us_per_launch=4.25\n"
         "kernel=k2 source=0000 bytes_per_launch=99\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_digest", lambda: digest)
-    assert bench.load_traffic("k1") == 123.5
-    assert bench.load_traffic("k2") is None  # taken from other kernel sources
-    assert bench.load_traffic("k3") is None
+    assert bench.load_traffic("k1") == {"bytes_per_launch": 123.5, "ncu_us_per_launch": 4.25}
+    assert bench.load_traffic("k2") == {}  # taken from other kernel sources
+    assert bench.load_traffic("k3") == {}
 
 
 def test_reference_arm_nonzero_rank_does_no_work(monkeypatch, capsys):
@@ -90,6 +90,20 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == bench.WORKLOAD
+    assert line["config"] == bench.workload_config(1)  # the GPU arm prints the same dict
+
+
+def test_by_size_rows_fractions():
+    MiB = 1 << 20
+    table = [{"P": P, "bytes_per_rank": B, "kernel": "k", "us_median": 10.0}
+             for P in (8, 2) for B in (MiB, 4 * MiB)]
+    b2b = [{"P": P, "bytes_per_rank": B, "us": 5.0} for P in (8, 2) for B in (MiB, 4 * MiB)]
+    rows = bench.by_size_rows(table, b2b, 6000.0)
+    assert [(r["P"], r["bytes_per_rank"]) for r in rows] == [(8, 4 * MiB), (8, MiB), (2, 4 * MiB), (2, MiB)]
+    r = rows[0]
+    assert r["alone_gbs"] == 2 * 8 * 4 * MiB / 10.0 / 1e3
+    assert r["alone_frac_measured"] == r["alone_gbs"] / 6000.0
+    assert r["back_to_back_frac_nominal"] == r["back_to_back_gbs"] / 8000.0
 
 
 def _free_port():

@@ -67,7 +67,7 @@ def test_config2_aligned_sweep(case):
     peers = [W.random_bf16_patterns(case.seed, r, case.bytes_per_rank // 2).view(np.uint8)
              for r in range(case.P)]
     want = oracle.all_gather(peers)
-    for opts in ({}, {"gather_staged": 1}):
+    for opts in ({}, {"gather_staged": 0}, {"gather_bulk": 1}):
         got, guards = run_gather(peers, [0] * case.P, 0, **opts)
         assert np.array_equal(got, want), opts
         assert guards

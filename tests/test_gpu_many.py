@@ -128,6 +128,60 @@ def test_many_all_unaligned(grid):
     assert guards
 
 
+@pytest.mark.parametrize("opts", [{}, {"grid_ctas": 1}, {"grid_ctas": 2}, {"grid_ctas": 3},
+                                  {"grid_ctas": 5000}, {"gather_many_single_max_bytes": 0},
+                                  {"gather_many_single_max_bytes": 1 << 20}],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "default")
+def test_many_tiny_tensors(opts):
+    """120 tensors x 8 ranks of 3..100 B at random offsets: every job is
+    assembled from bytes by the split launch's small-job CTAs (tables in
+    shared memory), or by one CTA, or on the general path when the grid is
+    too small to split."""
+    rng = np.random.default_rng(W.seed_for(5, 9005))
+    P, T = 8, 120
+    tensors = [[rng.integers(0, 256, int(B), dtype=np.uint8) for _ in range(P)]
+               for B in rng.integers(3, 101, T)]
+    in_offs = [[int(x) for x in rng.integers(0, 16, P)] for _ in range(T)]
+    out_offs = [int(x) for x in rng.integers(0, 16, T)]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, in_offs, out_offs, **opts)
+    for t in range(T):
+        assert np.array_equal(got[t], want[t]), (t, opts)
+    assert guards
+
+
+@pytest.mark.parametrize("grid", [0, 2, 3, 4, 9, 5000])
+def test_many_three_parts(grid):
+    """Aligned, unaligned and small tensors in one launch: three parts of the
+    grid (or fewer CTAs than parts: the general path)."""
+    rng = np.random.default_rng(W.seed_for(5, 9006))
+    P = 8
+    sizes = [5, 4096, 127, 100003, 1, 65536, 77, 300000 + 16, 2000, 3]
+    tensors = [[rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)] for B in sizes]
+    in_offs = [[0] * P if B % 16 == 0 else [int(x) for x in rng.integers(0, 16, P)] for B in sizes]
+    out_offs = [0 if B % 16 == 0 else int(rng.integers(1, 16)) for B in sizes]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, in_offs, out_offs, grid_ctas=grid)
+    for t in range(len(sizes)):
+        assert np.array_equal(got[t], want[t]), (t, grid)
+    assert guards
+
+
+def test_many_small_jobs_at_the_table_limit():
+    """P = 64 ranks x 16 tensors of 1..127 B (1024 sources): the shared
+    pointer table of the small-job CTAs at its largest."""
+    rng = np.random.default_rng(W.seed_for(5, 9007))
+    P, T = 64, 16
+    tensors = [[rng.integers(0, 256, int(B), dtype=np.uint8) for _ in range(P)]
+               for B in rng.integers(1, 128, T)]
+    in_offs = [[int(x) for x in rng.integers(0, 16, P)] for _ in range(T)]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, in_offs, [int(x) for x in rng.integers(0, 16, T)])
+    for t in range(T):
+        assert np.array_equal(got[t], want[t]), t
+    assert guards
+
+
 def test_many_large_table():
     """More tensors than the small parameter block holds (T=100, P=8)."""
     rng = np.random.default_rng(W.seed_for(5, 9001))
