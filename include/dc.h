@@ -237,6 +237,38 @@ dc_status_t dc_fused_all_gather(const void *const *in_ptrs, void *const *staging
 dc_status_t dc_fused_reset(void *workspace, int P, dc_stream_t stream);
 
 /*
+ * dc_fused_all_gather_static -- dc_fused_all_gather for callers that cannot
+ * allocate device memory.  The pages describe no such entry point: it is this
+ * library's own addition.  Some callers are given only their input and output
+ * buffers and may not call cudaMalloc themselves: a plug-in run by a host
+ * framework that owns every device allocation, code whose device memory was
+ * planned once up front, or code that must not call cudaMalloc/cudaFree
+ * because those can synchronise the device.  This form needs no workspace and
+ * no staging buffers from them.
+ *
+ * It computes what dc_fused_all_gather computes (outs[r] = in_ptrs[0] ||
+ * in_ptrs[1] || ... for every r; same argument rules for in_ptrs, outs, P and
+ * bytes_per_rank), with the epoch flags and the P staging buffers in one
+ * static device array of the library: 16 MiB of staging after 64 KiB of
+ * flags, held by every GPU that loads the library until the process exits.
+ * Limit: P * (bytes_per_rank rounded up to 256) <= 16 MiB; a larger call is
+ * rejected with DC_ERR_INVALID before anything is launched.
+ *
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  Each call enqueues on `stream` a clear of the flags
+ * (cudaMemsetAsync, 64 KiB at most) and one kernel.  The first call made with
+ * a device current looks up the array's device address on that device
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call in the process uses the same array on a given GPU, which keeps
+ * the last call's contents: calls whose work overlaps on the GPU (issued on
+ * different streams, or from different host threads) race and corrupt each
+ * other's results; issue them on one stream.  Waits are bounded as in
+ * dc_fused_all_gather and reported by dc_check_device.
+ */
+dc_status_t dc_fused_all_gather_static(const void *const *in_ptrs, void *const *outs, int P,
+                                       size_t bytes_per_rank, dc_stream_t stream);
+
+/*
  * dc_check_device -- reports the faults that this library's kernels recorded
  * on the current device since the last check, and clears them.
  *

@@ -90,10 +90,12 @@ def lib() -> ctypes.CDLL:
         L.dc_fused_workspace_bytes.restype = Z
         L.dc_fused_all_gather.argtypes = [A, A, A, I, Z, _VP, ctypes.c_uint, _VP]
         L.dc_fused_reset.argtypes = [_VP, I, _VP]
+        L.dc_fused_all_gather_static.argtypes = [A, A, I, Z, _VP]
         for f in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
                   "dc_reduce_scatter_bf16", "dc_all_reduce", "dc_reduce_scatter",
                   "dc_all_reduce_many", "dc_reduce_scatter_many", "dc_inject_delay_ns",
-                  "dc_check_device", "dc_fused_all_gather", "dc_fused_reset"):
+                  "dc_check_device", "dc_fused_all_gather", "dc_fused_reset",
+                  "dc_fused_all_gather_static"):
             getattr(L, f).restype = ctypes.c_int
         L.dc_last_error.argtypes = []
         L.dc_last_error.restype = ctypes.c_char_p
@@ -208,6 +210,16 @@ def dc_fused_all_gather(in_ptrs: Sequence[int], staging: Sequence[int], outs: Se
 
 def dc_fused_reset(workspace: int, P: int, stream: int = 0) -> int:
     return lib().dc_fused_reset(workspace, P, stream)
+
+
+def dc_fused_all_gather_static(in_ptrs: Sequence[int], outs: Sequence[int], P: int, bytes_per_rank: int,
+                               stream: int = 0) -> int:
+    """dc_fused_all_gather for callers that cannot allocate device memory:
+    its flags and staging buffers live in the library's static scratch
+    (P * bytes_per_rank rounded up to 256 bytes per rank, 16 MiB at most);
+    calls that overlap on the GPU race."""
+    a, b = _u64(in_ptrs), _u64(outs)
+    return lib().dc_fused_all_gather_static(_addr(a), _addr(b), P, bytes_per_rank, stream)
 
 
 # ---------------------------------------------------------- tensor API ---

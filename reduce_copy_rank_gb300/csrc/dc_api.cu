@@ -1005,6 +1005,82 @@ dc_status_t dc_fused_all_gather(const void* const* in_ptrs, void* const* staging
                       static_cast<int>(P * G));
 }
 
+dc_status_t dc_fused_all_gather_static(const void* const* in_ptrs, void* const* outs, int P,
+                                       size_t bytes_per_rank, dc_stream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (bytes_per_rank == 0) return ok();
+  if (!in_ptrs || !outs) return fail(DC_ERR_INVALID, "in_ptrs and outs must not be NULL");
+  const uint64_t B = bytes_per_rank;
+  if (B & 15u) return fail(DC_ERR_ALIGN, "bytes_per_rank must be a multiple of 16 bytes");
+  if (B > kFusedStaticStagingBytes ||
+      fused_static_stride(B) * static_cast<uint64_t>(P) > kFusedStaticStagingBytes)
+    return fail(DC_ERR_INVALID,
+                "%d ranks x %llu bytes need %llu bytes of staging; the static scratch holds %llu",
+                P, static_cast<unsigned long long>(B),
+                static_cast<unsigned long long>(fused_static_stride(std::min<uint64_t>(B, 1ull << 40)) * P),
+                static_cast<unsigned long long>(kFusedStaticStagingBytes));
+  const uint64_t total = B * static_cast<uint64_t>(P);
+  // outputs may overlap nothing; inputs may overlap inputs
+  struct R {
+    uint64_t lo, hi;
+    bool out;
+    int rank;
+  };
+  std::vector<R> v;
+  v.reserve(2 * static_cast<size_t>(P));
+  for (int r = 0; r < P; ++r) {
+    const uint64_t a = reinterpret_cast<uint64_t>(in_ptrs[r]), o = reinterpret_cast<uint64_t>(outs[r]);
+    if (!a || !o) return fail(DC_ERR_INVALID, "a pointer of rank %d is NULL", r);
+    if ((a | o) & 15u) return fail(DC_ERR_ALIGN, "the buffers of rank %d must be 16-byte aligned", r);
+    if (a + B < a || o + total < o) return fail(DC_ERR_INVALID, "a buffer of rank %d wraps around", r);
+    v.push_back(R{a, a + B, false, r});
+    v.push_back(R{o, o + total, true, r});
+  }
+  std::sort(v.begin(), v.end(), [](const R& x, const R& y) { return x.lo < y.lo; });
+  const R* far_any = nullptr;
+  const R* far_out = nullptr;
+  for (const R& x : v) {
+    const R* hit = x.out ? far_any : far_out;
+    if (hit && hit->hi > x.lo)
+      return fail(DC_ERR_OVERLAP, "%s of rank %d overlaps %s of rank %d", x.out ? "output" : "input", x.rank,
+                  hit->out ? "the output" : "the input", hit->rank);
+    if (!far_any || x.hi > far_any->hi) far_any = &x;
+    if (x.out && (!far_out || x.hi > far_out->hi)) far_out = &x;
+  }
+  if (g_opt.test_fail_launch.load())
+    return fail(DC_ERR_CUDA, "launch failure injected by the test_fail_launch option");
+  int dev = 0, sms = 0;
+  dc_status_t st = current_device(&dev);
+  if (st != DC_OK) return st;
+  st = sm_count(dev, &sms);
+  if (st != DC_OK) return st;
+  const uint64_t resident = static_cast<uint64_t>(sms) *
+                            static_cast<uint64_t>(occupancy(dev, 127, [] { return fused_ctas_per_sm(); }));
+  if (resident < static_cast<uint64_t>(P))
+    return fail(DC_ERR_INVALID, "%d ranks need %d CTAs resident at once; the GPU holds %llu", P, P,
+                static_cast<unsigned long long>(resident));
+  const uint64_t cmin = static_cast<uint64_t>(std::max(16LL, g_opt.fused_chunk_min.load()));
+  uint64_t G = std::min<uint64_t>({(B + cmin - 1) / cmin, static_cast<uint64_t>(kFusedMaxChunks),
+                                   resident / static_cast<uint64_t>(P)});
+  G = std::max<uint64_t>(G, 1);
+  const uint64_t chunk = ((B + G - 1) / G + 15) / 16 * 16;
+  G = (B + chunk - 1) / chunk;
+  FusedParams fp{};
+  for (int r = 0; r < P; ++r) {
+    fp.in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
+    fp.out[r] = reinterpret_cast<uint64_t>(outs[r]);
+  }
+  fp.bytes = B;
+  fp.chunk = chunk;
+  fp.wait_ns = static_cast<uint64_t>(std::max(g_opt.wait_limit_ns.load(), 1000LL));
+  fp.absent = 0;
+  fp.P = P;
+  fp.G = static_cast<int32_t>(G);
+  return check_launch(launch_fused_gather_static(fp, static_cast<cudaStream_t>(stream)),
+                      "fused all-gather (static scratch)", static_cast<int>(P * G));
+}
+
 dc_status_t dc_fused_reset(void* workspace, int P, dc_stream_t stream) {
   read_env_once();
   if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);

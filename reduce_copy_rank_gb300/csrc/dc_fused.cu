@@ -36,6 +36,7 @@
 // instead of hanging.  The caller then clears the workspace and starts again
 // at epoch 1 (dc_fused_reset): that is the abort path.
 #include <atomic>
+#include <mutex>
 
 #include "dc_device.cuh"
 #include "dc_internal.h"
@@ -193,6 +194,59 @@ cudaError_t launch_fused_gather(const FusedParams& p, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, dc_fused_gather_kernel, p);
+}
+
+// ------------------------------------------------ allocation-free form ---
+// Scratch of dc_fused_all_gather_static, for callers that cannot allocate
+// device memory: the epoch flags of kMaxRanks ranks (64 KiB), then
+// kFusedStaticStagingBytes (16 MiB) of staging buffers.  The array is part of
+// this file's device code, so every GPU that loads it holds these bytes until
+// the process exits; every call shares them.  In host code the name
+// g_fused_scratch only stands in for the array: its device address comes from
+// cudaGetSymbolAddress, once per device (static_scratch below).
+constexpr size_t kFusedStaticFlagBytes = fused_workspace_bytes(kMaxRanks);
+static __device__ __align__(256) unsigned char g_fused_scratch[kFusedStaticFlagBytes + kFusedStaticStagingBytes];
+
+namespace {
+
+// The device address of g_fused_scratch on the current device, looked up on
+// the first call made with that device current and remembered.
+cudaError_t static_scratch(unsigned char** ptr) {
+  constexpr int kDevices = 64;
+  static std::mutex mu;
+  static unsigned char* addr[kDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fused_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_fused_gather_static(FusedParams p, cudaStream_t s) {
+  const uint64_t stride = fused_static_stride(p.bytes);
+  if (p.P < 1 || p.P > kMaxRanks || stride * static_cast<uint64_t>(p.P) > kFusedStaticStagingBytes)
+    return cudaErrorInvalidValue;
+  unsigned char* base = nullptr;
+  cudaError_t e = static_scratch(&base);
+  if (e != cudaSuccess) return e;
+  // the flags must start at zero: the previous call left its epoch in them
+  e = cudaMemsetAsync(base, 0, fused_workspace_bytes(p.P), s);
+  if (e != cudaSuccess) return e;
+  p.ws = reinterpret_cast<uint64_t>(base);
+  for (int r = 0; r < p.P; ++r)
+    p.staging[r] = reinterpret_cast<uint64_t>(base + kFusedStaticFlagBytes + stride * static_cast<uint64_t>(r));
+  p.epoch = 1;
+  return launch_fused_gather(p, s);
 }
 
 cudaError_t take_fused_faults(uint32_t* info) {

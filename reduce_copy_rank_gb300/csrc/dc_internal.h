@@ -155,6 +155,14 @@ __host__ __device__ constexpr size_t fused_workspace_bytes(int P) {
 }
 cudaError_t launch_fused_gather(const FusedParams& p, cudaStream_t s);
 int fused_ctas_per_sm();
+// The allocation-free form (dc_fused_all_gather_static): the flags and the
+// staging buffers live in a static device array of this many staging bytes
+// (rank r's buffer at r * fused_static_stride(bytes)) after the flags of
+// kMaxRanks ranks.  launch_fused_gather_static fills p.ws, p.staging and
+// p.epoch from it, clears the flags on `s` and launches.
+constexpr size_t kFusedStaticStagingBytes = 16u << 20;
+__host__ __device__ constexpr uint64_t fused_static_stride(uint64_t bytes) { return (bytes + 255) / 256 * 256; }
+cudaError_t launch_fused_gather_static(FusedParams p, cudaStream_t s);
 // Reads and clears the first fault of the fused kernel on the current device
 // (synchronous): info[0] fault bits, [1] phase << 24 | rank << 12 | peer,
 // [2] chunk, [3] epoch.
