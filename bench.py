@@ -95,8 +95,10 @@ def parse_args(argv=None):
                     help="profiling helper: run one call REPS times and exit, e.g. "
                          "gather:8:4194304:3, ugather:8:4194305:3 (unaligned), "
                          "allreduce:8:268435456:2, allreduce_mis:8:67108864:2 (rank 1 one "
-                         "element off; BYTES per rank) or "
-                         "many:8:0:3 (the all_gather_many workload)")
+                         "element off; BYTES per rank), "
+                         "many:8:0:3 (the all_gather_many workload), manytiny:8:0:3 (120 tiny "
+                         "tensors), gatherbulk:8:4194304:3 (the opt-in bulk-copy gather) or "
+                         "fused:8:4194304:3 (the staged protocol)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps must be >= 1 and --warmup >= 0")
@@ -443,10 +445,21 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     tens = [[W.random_bytes_device(W.seed_for(5, 2), r, B + 1, device, tensor=t)[1:] for r in range(8)]
             for t, B in enumerate(sizes)]
     outs = [torch.empty(8 * B, dtype=torch.uint8, device=device) for B in sizes]
-    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather_many(tens, outs)], 5)[0])
+    # (timed from a CUDA graph: flush, event, the call, event; the binding's
+    # host-side marshalling of 1080 tensors takes longer than the flush, so
+    # an eager call's events would count host time)
+    g, evs = build_step_graph(torch, flush, [lambda: dc.all_gather_many(tens, outs)])
+    t = []
+    for _ in range(5):
+        g.replay()
+        torch.cuda.synchronize()
+        t.append(evs[0].elapsed_time(evs[1]) * 1e3)
+    us = statistics.median(t)
+    del g
     nbytes = 2 * 8 * sum(sizes)
     rows.append({"op": "all_gather_many_tiny", "P": 8, "count": len(sizes),
-                 "shape": "120 tensors of 3..100 B per rank, payloads at +1 B", "us": us,
+                 "shape": "120 tensors of 3..100 B per rank, payloads at +1 B; call alone after a "
+                          "flush, from a CUDA graph", "us": us,
                  "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     del tens, outs
     # the staged protocol (stage -> gather -> complete), P = 8 ranks x 4 MiB:
@@ -1079,6 +1092,28 @@ def run_case(args) -> int:
         ins = [store[r][(1 if r == 1 else 0):(1 if r == 1 else 0) + nbytes // 2] for r in range(P)]
         outs = [torch.empty(nbytes // 2, dtype=torch.bfloat16, device=device) for _ in range(P)]
         fn = lambda: dc.all_reduce(ins, outs)  # noqa: E731
+    elif op == "gatherbulk":  # the opt-in TMA bulk-copy path of the aligned gather
+        peers = [torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=device) for _ in range(P)]
+        out = torch.empty(P * nbytes, dtype=torch.uint8, device=device)
+        dc.set_option("gather_bulk", 1)
+        fn = lambda: dc.all_gather(peers, out)  # noqa: E731
+    elif op == "manytiny":  # 120 tensors of 3..100 B per rank at +1 B (BYTES unused)
+        rng = np.random.default_rng(W.seed_for(5, 9005))
+        sizes = [int(x) for x in rng.integers(3, 101, 120)]
+        tens = [[torch.randint(0, 256, (B + 1,), dtype=torch.uint8, device=device)[1:] for _ in range(P)]
+                for B in sizes]
+        outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in sizes]
+        fn = lambda: dc.all_gather_many(tens, outs)  # noqa: E731
+    elif op == "fused":  # the staged all-gather protocol, P ranks x BYTES
+        ins = [torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=device) for _ in range(P)]
+        stg = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(P)]
+        outs = [torch.empty(P * nbytes, dtype=torch.uint8, device=device) for _ in range(P)]
+        ws = dc.fused_workspace(P, device)
+        epoch = [0]
+
+        def fn():
+            epoch[0] += 1
+            dc.fused_all_gather(ins, stg, outs, ws, epoch[0])
     elif op == "reducescatter":
         ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
         outs = [torch.empty(nbytes // 2 // P, dtype=torch.bfloat16, device=device) for _ in range(P)]
@@ -1088,6 +1123,7 @@ def run_case(args) -> int:
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()
+    dc.check_device()
     print(f"ran {op} P={P} bytes_per_rank={nbytes} x{reps}")
     return 0
 

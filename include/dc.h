@@ -48,7 +48,9 @@ typedef enum {
     DC_ERR_OVERLAP = 3,  /* an output range overlaps an input or another output */
     DC_ERR_TOO_MANY = 4, /* all_gather_many table larger than the limits below */
     DC_ERR_CUDA = 5,     /* the CUDA runtime refused the launch */
-    DC_ERR_TIMEOUT = 6   /* a bounded device wait ran out (reported by dc_check_device) */
+    DC_ERR_TIMEOUT = 6,  /* a bounded device wait ran out (reported by dc_check_device) */
+    DC_ERR_BOUNDS = 7    /* bounds-checked build only: a kernel skipped an access outside its
+                            job's range (reported by dc_check_device) */
 } dc_status_t;
 
 /* Element types and summation orders of the reductions. */
@@ -282,9 +284,11 @@ dc_status_t dc_fused_all_gather_static(const void *const *in_ptrs, void *const *
  * arrives.
  *
  * Synchronous: it first waits for all work on the current device
- * (cudaDeviceSynchronize), then reads and clears the fault word.
- * Returns DC_OK if no wait ran out, DC_ERR_TIMEOUT if one did, DC_ERR_CUDA if
- * the synchronisation or the read failed (the CUDA error in dc_last_error()).
+ * (cudaDeviceSynchronize), then reads and clears the fault words.
+ * Returns DC_OK if no wait ran out, DC_ERR_TIMEOUT if one did, DC_ERR_BOUNDS
+ * (bounds-checked build only, see dc_bounds_checked) if a kernel skipped an
+ * access outside its range, DC_ERR_CUDA if the synchronisation or the read
+ * failed (the CUDA error in dc_last_error()).
  */
 dc_status_t dc_check_device(void);
 
@@ -384,6 +388,20 @@ int dc_last_grid(void);
 
 /* ABI version: 1. */
 int dc_version(void);
+
+/*
+ * 1 in the bounds-checked build of the library (libdc_bounds.so, compiled
+ * with DC_DEBUG_BOUNDS), 0 in the normal one.  In the checked build every
+ * global load, store and L2 prefetch of every kernel is first checked against
+ * the range its job allows -- for a load, the 16-byte-block hull of the
+ * source bytes the job reads (realigning copies read whole aligned blocks
+ * around an unaligned span); for a store, the exact output range.  An access
+ * outside is skipped (never made) and the first one is recorded;
+ * dc_check_device then returns DC_ERR_BOUNDS with the file, site, address and
+ * allowed range.  The kernels never trap.  It is a test build: slower, and
+ * otherwise the same results.
+ */
+int dc_bounds_checked(void);
 
 #ifdef __cplusplus
 }

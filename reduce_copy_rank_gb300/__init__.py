@@ -34,9 +34,11 @@ __all__ = [
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdc.so")
+# The bounds-checked test build, loaded instead when DC_LIBRARY=bounds.
+LIB_BOUNDS_PATH = os.path.join(_HERE, "libdc_bounds.so")
 
 STATUS = {0: "DC_OK", 1: "DC_ERR_INVALID", 2: "DC_ERR_ALIGN", 3: "DC_ERR_OVERLAP",
-          4: "DC_ERR_TOO_MANY", 5: "DC_ERR_CUDA", 6: "DC_ERR_TIMEOUT"}
+          4: "DC_ERR_TOO_MANY", 5: "DC_ERR_CUDA", 6: "DC_ERR_TIMEOUT", 7: "DC_ERR_BOUNDS"}
 
 MAX_RANKS = 64
 MANY_MAX_TENSORS = 256
@@ -70,11 +72,12 @@ def lib() -> ctypes.CDLL:
     """The loaded C library (loaded on first use)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
+        path = LIB_BOUNDS_PATH if os.environ.get("DC_LIBRARY") == "bounds" else LIB_PATH
+        if not os.path.exists(path):
             raise LibraryMissing(
-                f"{LIB_PATH} is missing: build it with `python -m reduce_copy_rank_gb300._build` "
-                "(or __graft_entry__.build()); there is no fallback path")
-        L = ctypes.CDLL(LIB_PATH)
+                f"{path} is missing: build it with `python -m reduce_copy_rank_gb300._build` "
+                "(--bounds for the checked build, or __graft_entry__.build()); there is no fallback path")
+        L = ctypes.CDLL(path)
         A, I, Z = _VP, ctypes.c_int, ctypes.c_size_t  # A: address of a host array
         L.dc_all_gather.argtypes = [A, I, Z, _VP, _VP]
         L.dc_all_gather_many.argtypes = [A, A, A, I, I, _VP]
@@ -111,6 +114,8 @@ def lib() -> ctypes.CDLL:
         L.dc_last_grid.restype = ctypes.c_int
         L.dc_version.argtypes = []
         L.dc_version.restype = ctypes.c_int
+        L.dc_bounds_checked.argtypes = []
+        L.dc_bounds_checked.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -360,28 +365,27 @@ def all_gather_many(peers_per_tensor: Sequence[Sequence], outs: Sequence, stream
     if T == 0:
         return outs
     P = len(peers_per_tensor[0])
-    dev = None
+    dev = _cur_dev()
     ptrs, sizes = [], []
+    # one pass, few property reads per tensor (they dominate the host time of
+    # large batches); on any mismatch the slow checks below name the culprit
     for t, peers in enumerate(peers_per_tensor):
         if len(peers) != P:
             raise ValueError("every tensor needs the same number of peers")
-        B = _nbytes(peers[0])
+        B = peers[0].nbytes
         for r, p in enumerate(peers):
-            _device_tensor(p, f"peers_per_tensor[{t}][{r}]")
-            if _nbytes(p) != B:
-                raise ValueError(f"tensor {t}: all peers must have the same number of bytes")
-            if dev is None:
-                dev = _cur_dev()
-            if p.get_device() != dev:
+            if not (p.is_cuda and p.is_contiguous()) or p.nbytes != B or p.get_device() != dev:
+                _device_tensor(p, f"peers_per_tensor[{t}][{r}]")
+                if p.nbytes != B:
+                    raise ValueError(f"tensor {t}: all peers must have the same number of bytes")
                 _wrong_device(f"peers_per_tensor[{t}][{r}]", p, dev)
-        _device_tensor(outs[t], f"outs[{t}]")
-        if dev is None:
-            dev = _cur_dev()
-        if outs[t].get_device() != dev:
-            _wrong_device(f"outs[{t}]", outs[t], dev)
-        if _nbytes(outs[t]) != P * B:
-            raise ValueError(f"outs[{t}] holds {_nbytes(outs[t])} bytes, expected {P * B}")
-        ptrs.extend(p.data_ptr() for p in peers)
+            ptrs.append(p.data_ptr())
+        o = outs[t]
+        if not (o.is_cuda and o.is_contiguous()) or o.get_device() != dev:
+            _device_tensor(o, f"outs[{t}]")
+            _wrong_device(f"outs[{t}]", o, dev)
+        if o.nbytes != P * B:
+            raise ValueError(f"outs[{t}] holds {o.nbytes} bytes, expected {P * B}")
         sizes.append(B)
     _check(dc_all_gather_many(ptrs, sizes, [o.data_ptr() for o in outs], T, P,
                               _stream_handle(stream)))

@@ -28,6 +28,7 @@
 #include <vector>
 
 #include "dc.h"
+#include "dc_device.cuh"
 #include "dc_internal.h"
 
 namespace {
@@ -328,7 +329,9 @@ void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_f
 // Split of a launch's CTAs (at most `cap`) between its three parts: the
 // jobs of fewer than kGatherSmallBytes per rank get one CTA per kGatherBlock
 // threads, kSmallSplit threads per output vector (so all their byte loads
-// are in flight at once), at the end of the grid; the rest goes to the
+// are in flight at once), at most kMaxSmallCtas, at the end of the grid, each
+// CTA a contiguous run of small_per vectors whose first and last jobs
+// small_tab records; the rest goes to the
 // aligned jobs (tiles of kSplitVectors vectors per thread) and the other
 // unaligned jobs (tiles of kSplitRealignVectors), in proportion to their
 // work: a realigned 16-byte vector counts gather_split_cost_pct / 100 staged
@@ -344,7 +347,25 @@ int plan_split(Params& prm, uint64_t cap) {
   const uint64_t fv = prm.flat_vec, gv = prm.small_vec - prm.flat_vec, sv = prm.total_vec - prm.small_vec;
   const uint64_t others = (fv > 0 ? 1 : 0) + (gv > 0 ? 1 : 0);
   if (cap < others + (sv > 0 ? 1 : 0)) return 0;
-  const uint64_t sc = std::min((sv * kSmallSplit + kGatherBlock - 1) / kGatherBlock, cap - others);
+  constexpr size_t kTab = sizeof(prm.small_tab) / sizeof(prm.small_tab[0]);
+  uint64_t sc = 0;
+  if (sv > 0) {
+    if (kTab < 2) return 0;  // (parameter blocks of one job have no small-job part)
+    // one CTA per kGatherBlock / kSmallSplit vectors, each CTA a contiguous run
+    sc = std::min<uint64_t>({(sv * kSmallSplit + kGatherBlock - 1) / kGatherBlock, cap - others,
+                             static_cast<uint64_t>(kTab - 1)});
+    const uint64_t per = (sv + sc - 1) / sc;
+    sc = (sv + per - 1) / per;
+    prm.small_per = static_cast<uint32_t>(per);
+    // small_tab[c]: the job of CTA c's first vector; small_tab[sc]: the last job
+    int j = prm.small_job0;
+    for (uint64_t c = 0; c < sc; ++c) {
+      const uint64_t v = prm.small_vec + c * per;
+      while (j + 1 < prm.njobs && prm.job[j + 1].vfirst <= v) ++j;
+      prm.small_tab[c] = static_cast<uint16_t>(j - prm.small_job0);
+    }
+    prm.small_tab[sc] = static_cast<uint16_t>(prm.njobs - 1 - prm.small_job0);
+  }
   cap -= sc;
   const uint64_t ftile = static_cast<uint64_t>(kGatherBlock) * kSplitVectors;
   const uint64_t gtile = static_cast<uint64_t>(kGatherBlock) * kSplitRealignVectors;
@@ -1098,10 +1119,35 @@ dc_status_t dc_check_device(void) {
   uint32_t bits = 0, fused[4] = {0, 0, 0, 0};
   cudaError_t e = take_bulk_faults(&bits);
   if (e == cudaSuccess) e = take_fused_faults(fused);
+  // bounds-check records of the checked build (empty in the normal build)
+  static cudaError_t (*const kReaders[kBoundsReaders])(BoundsFault*) = {
+      take_bounds_gather, take_bounds_bulk, take_bounds_fused,
+      take_bounds_reduce_bf16, take_bounds_reduce_f16, take_bounds_reduce_f32};
+  static const char* const kFiles[kBoundsReaders] = {"dc_gather.cu", "dc_bulk.cu", "dc_fused.cu",
+                                                     "dc_reduce_bf16.cu", "dc_reduce_f16.cu", "dc_reduce_f32.cu"};
+  BoundsFault first{};
+  int first_file = -1;
+  unsigned long long outside = 0;
+  for (int i = 0; i < kBoundsReaders && e == cudaSuccess; ++i) {
+    BoundsFault f{};
+    e = kReaders[i](&f);
+    if (e == cudaSuccess && f.count) {
+      outside += f.count;
+      if (first_file < 0) {
+        first = f;
+        first_file = i;
+      }
+    }
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(DC_ERR_CUDA, "device check failed: %s", cudaGetErrorString(e));
   }
+  if (first_file >= 0)
+    return fail(DC_ERR_BOUNDS,
+                "%llu access(es) outside their job's range skipped; first: %s site %u, %llu bytes at 0x%llx, "
+                "allowed [0x%llx, 0x%llx)",
+                outside, kFiles[first_file], first.site, first.len, first.addr, first.lo, first.hi);
   if (fused[0] & kFaultFusedWait) {
     const uint32_t phase = fused[1] >> 24, rank = (fused[1] >> 12) & 0xFFFu, peer = fused[1] & 0xFFFu;
     return fail(DC_ERR_TIMEOUT,
@@ -1127,6 +1173,7 @@ const char* dc_status_name(int status) {
     case DC_ERR_TOO_MANY: return "DC_ERR_TOO_MANY";
     case DC_ERR_CUDA: return "DC_ERR_CUDA";
     case DC_ERR_TIMEOUT: return "DC_ERR_TIMEOUT";
+    case DC_ERR_BOUNDS: return "DC_ERR_BOUNDS";
     default: return "DC_ERR_UNKNOWN";
   }
 }
@@ -1155,5 +1202,13 @@ unsigned long long dc_launch_count(void) { return g_launches.load(); }
 int dc_last_grid(void) { return g_last_grid; }
 
 int dc_version(void) { return 1; }
+
+int dc_bounds_checked(void) {
+#ifdef DC_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 }  // extern "C"

@@ -126,14 +126,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // Output bytes [o0, o0 + len) of the gather come from rank r = o / B at
 // offset o - r*B, one piece per rank they cross: f(o, piece bytes, rank's
-// source address) for each piece.
+// source address) for each piece whose source range passes the bounds check
+// of the checked build (the rank's whole source).
+enum : uint32_t { kSiteBulkLoad = 300, kSiteBulkStore = 301, kSiteBulkPrefetch = 302 };
 template <class F>
-__device__ __forceinline__ void for_each_piece(const BulkParams& p, uint64_t o0, uint64_t len, F f) {
+__device__ __forceinline__ void for_each_piece(const BulkParams& p, uint64_t o0, uint64_t len, uint32_t site,
+                                               F f) {
   const uint64_t B = p.bytes, end = o0 + len;
   uint64_t r = o0 / B, o = o0;
   while (o < end) {
     const uint64_t rend = min((r + 1) * B, end);
-    f(o, rend - o, reinterpret_cast<const uint8_t*>(p.src[r]) + (o - r * B));
+    const uint8_t* a = reinterpret_cast<const uint8_t*>(p.src[r]) + (o - r * B);
+    if (in_bounds(a, rend - o, p.src[r], p.src[r] + B, site)) f(o, rend - o, a);
     o = rend;
     ++r;
   }
@@ -156,7 +160,8 @@ __global__ void __launch_bounds__(32) dc_gather_bulk_kernel(const __grid_constan
   const uint64_t pf = static_cast<uint64_t>(p.prefetch);
   auto prefetch_chunk = [&](uint64_t c) {
     if (c >= cend) return;
-    for_each_piece(p, c * chunk, min(chunk, total - c * chunk), [](uint64_t, uint64_t n, const uint8_t* a) {
+    for_each_piece(p, c * chunk, min(chunk, total - c * chunk), kSiteBulkPrefetch,
+                   [](uint64_t, uint64_t n, const uint8_t* a) {
       for (uint64_t q = 0; q < n; q += 32768)
         prefetch_l2(a + q, static_cast<uint32_t>(min(n - q, static_cast<uint64_t>(32768))));
     });
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(32) dc_gather_bulk_kernel(const __grid_constan
     // (test only: announce 16 bytes that never come, so that this wait runs out)
     const uint32_t extra = (p.test_flags & kBulkTestShortTx) && c == c0 ? 16u : 0u;
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(len) + extra);
-    for_each_piece(p, o0, len, [&](uint64_t o, uint64_t n, const uint8_t* a) {
+    for_each_piece(p, o0, len, kSiteBulkLoad, [&](uint64_t o, uint64_t n, const uint8_t* a) {
       bulk_load(dst + static_cast<uint32_t>(o - o0), a, static_cast<uint32_t>(n), bar);
     });
     inflight |= 1u << k;
@@ -195,9 +200,10 @@ __global__ void __launch_bounds__(32) dc_gather_bulk_kernel(const __grid_constan
     phase ^= 1u << k;
     inflight &= ~(1u << k);
     fence_proxy_async_smem();
-    const uint64_t o0 = c * chunk;
-    bulk_store(reinterpret_cast<uint8_t*>(p.out) + o0, buf + k * static_cast<uint32_t>(chunk),
-               static_cast<uint32_t>(min(chunk, total - o0)));
+    const uint64_t o0 = c * chunk, len = min(chunk, total - o0);
+    uint8_t* d = reinterpret_cast<uint8_t*>(p.out) + o0;
+    if (in_bounds(d, len, p.out, p.out + total, kSiteBulkStore))
+      bulk_store(d, buf + k * static_cast<uint32_t>(chunk), static_cast<uint32_t>(len));
     bulk_commit();
     if (S == 1) {  // one stage: refill it once its store has read it
       if (c + step < cend) {
@@ -246,6 +252,8 @@ cudaError_t launch_gather_bulk(const BulkParams& p, int grid, bool pdl, cudaStre
   }
   return launch_ex(dc_gather_bulk_kernel, grid, 32, pdl, s, p, smem);
 }
+
+DC_BOUNDS_READER(take_bounds_bulk)
 
 cudaError_t take_bulk_faults(uint32_t* bits) {
   *bits = 0;

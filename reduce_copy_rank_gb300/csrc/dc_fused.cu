@@ -99,10 +99,15 @@ __device__ __forceinline__ void record_fault(uint32_t phase, uint32_t rank, uint
   }
 }
 
+// Sites of the checked build's bounds checks (in_bounds).
+enum : uint32_t { kSiteFusedStage = 400, kSiteFusedGather = 401, kSiteFusedFlag = 402 };
+
 // n bytes (a multiple of 16; both pointers 16-byte aligned) copied by the
-// CTA's threads, four 16-byte vectors in flight per thread.
+// CTA's threads, four 16-byte vectors in flight per thread.  Checked build:
+// loads inside [slo, shi), stores inside [dlo, dhi).
 template <bool THROUGH_L2>
-__device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uint64_t n) {
+__device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uint64_t n, uint64_t slo,
+                                           uint64_t shi, uint64_t dlo, uint64_t dhi, uint32_t site) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
   uint4* d = reinterpret_cast<uint4*>(dst);
   const uint64_t nv = n >> 4;
@@ -111,12 +116,12 @@ __device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uin
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const uint64_t k = i + static_cast<uint64_t>(u) * kFusedBlock;
-      if (k < nv) v[u] = THROUGH_L2 ? ld_cg16(s + k) : ld_stream(s + k);
+      if (k < nv && in_bounds(s + k, 16, slo, shi, site)) v[u] = THROUGH_L2 ? ld_cg16(s + k) : ld_stream(s + k);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const uint64_t k = i + static_cast<uint64_t>(u) * kFusedBlock;
-      if (k < nv) st16(d + k, v[u]);
+      if (k < nv && in_bounds(d + k, 16, dlo, dhi, site)) st16(d + k, v[u]);
     }
   }
 }
@@ -135,16 +140,19 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
 
   // stage
   copy_chunk<false>(reinterpret_cast<const uint8_t*>(p.in[r]) + lo, reinterpret_cast<uint8_t*>(p.staging[r]) + lo,
-                    n);
+                    n, p.in[r], p.in[r] + p.bytes, p.staging[r], p.staging[r] + p.bytes, kSiteFusedStage);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) st_release_u32(&staged[r * kFusedMaxChunks + c], epoch);
+  const uint64_t ws_lo = p.ws, ws_hi = p.ws + fused_workspace_bytes(static_cast<int>(P));
+  if (threadIdx.x == 0 && in_bounds(&staged[r * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag))
+    st_release_u32(&staged[r * kFusedMaxChunks + c], epoch);
 
   // gather, own rank first
   for (uint32_t i = 0; i < P; ++i) {
     const uint32_t q = r + i < P ? r + i : r + i - P;
     if (threadIdx.x == 0) {
-      const bool ok = wait_flag(&staged[q * kFusedMaxChunks + c], epoch, p.wait_ns);
+      const bool ok = in_bounds(&staged[q * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag) &&
+                      wait_flag(&staged[q * kFusedMaxChunks + c], epoch, p.wait_ns);
       if (!ok) record_fault(1, r, q, c, epoch);
       __threadfence();
       s_ok[i] = ok;
@@ -152,16 +160,19 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
     __syncthreads();
     if (!s_ok[i]) return;
     copy_chunk<true>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
-                     reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n);
+                     reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n,
+                     p.staging[q], p.staging[q] + p.bytes, p.out[r], p.out[r] + P * p.bytes, kSiteFusedGather);
   }
 
   // complete
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    st_release_u32(&done[r * kFusedMaxChunks + c], epoch);
+    if (in_bounds(&done[r * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag))
+      st_release_u32(&done[r * kFusedMaxChunks + c], epoch);
     for (uint32_t q = 0; q < P; ++q)
-      if (!wait_flag(&done[q * kFusedMaxChunks + c], epoch, p.wait_ns)) {
+      if (!in_bounds(&done[q * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag) ||
+          !wait_flag(&done[q * kFusedMaxChunks + c], epoch, p.wait_ns)) {
         record_fault(2, r, q, c, epoch);
         break;
       }
@@ -248,6 +259,8 @@ cudaError_t launch_fused_gather_static(FusedParams p, cudaStream_t s) {
   p.epoch = 1;
   return launch_fused_gather(p, s);
 }
+
+DC_BOUNDS_READER(take_bounds_fused)
 
 cudaError_t take_fused_faults(uint32_t* info) {
   for (int i = 0; i < 4; ++i) info[i] = 0;

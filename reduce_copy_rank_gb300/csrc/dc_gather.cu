@@ -752,42 +752,48 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
 
 // The jobs of fewer than kGatherSmallBytes bytes per rank of a split launch
 // (jobs [small_job0, njobs), global vectors [small_vec, total_vec)), copied by
-// the launch's last `nctas` CTAs.  Each such CTA first copies these jobs'
-// entries and source pointers from the parameter block into shared memory,
-// so that the per-byte source reads of lanes that sit in different jobs or
-// ranks are shared-memory loads instead of parameter reads at lane-dependent
-// addresses (served one address at a time); then SPLIT threads share each
-// 16-byte output vector (thread i of the part takes bytes [(i % SPLIT) *
-// 16/SPLIT, ...) of vector small_vec + i / SPLIT), find the vector's job by
-// binary search in the shared table and assemble their bytes, all loads
-// issued before the store.  No thread walks the job table.  Measured on GB300
+// the launch's last `nctas` CTAs.  CTA c takes the contiguous run of
+// small_per vectors starting small_per * c after small_vec; the host wrote in
+// small_tab[c] and small_tab[c + 1] the jobs of its first and last vector.
+// The CTA first copies those jobs' entries and source pointers from the
+// parameter block into shared memory -- only those: parameters read at
+// lane-dependent addresses are served one address at a time, and after an L2
+// flush each new line is a miss, so copying the whole table of a large batch
+// cost 138 us per call (120 tensors x 8 ranks) against 5 us warm -- so that
+// the per-byte source reads of lanes in different jobs or ranks become
+// shared-memory loads.  Then SPLIT threads share each 16-byte output vector
+// (thread i takes bytes [(i % SPLIT) * 16/SPLIT, ...) of the CTA's vector i /
+// SPLIT), find the vector's job by binary search in the shared table and
+// assemble their bytes, all loads issued before the store.  Measured on GB300
 // (120 tensors of 3..100 B x 8 ranks at +1 B, 20 calls back to back): 23 us
 // per call before this part existed; 6.1, 5.1 and 5.15 us with 1, 2 and 4
-// threads per vector (4 spreads the part over 4x the SMs and was best for
-// 250 tensors of 1..40 B x 4 ranks, 6.5 us, and for 16 tensors x 64 ranks,
-// 3.9 us); reading the parameters at warp-uniform addresses instead (one
+// threads per vector (4 spreads the part over 4x the SMs and was best for 250
+// tensors of 1..40 B x 4 ranks, 6.5 us, and for 16 tensors x 64 ranks, 3.9
+// us); reading the parameters at warp-uniform addresses instead (one
 // broadcast per word, 32 words per lane round) was 0.9-1.3 us slower.
 template <int BLOCK, int SPLIT, int MAXJ, int MAXS>
-__device__ __forceinline__ void copy_small_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta,
-                                                uint32_t nctas) {
+__device__ __forceinline__ void copy_small_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta) {
   static_assert(SPLIT == 1 || SPLIT == 2 || SPLIT == 4, "16 bytes per vector");
+  static_assert(MAXJ > 1, "split launches only");
   constexpr uint32_t kBytes = 16 / SPLIT;
   extern __shared__ uint4 stage_buf[];
-  const int j0 = p.small_job0, nsj = p.njobs - j0;
-  if (nsj <= 0) return;
+  if (cta >= static_cast<uint32_t>(kMaxSmallCtas)) return;
+  const int jlo = p.small_job0 + p.small_tab[cta], jhi = p.small_job0 + p.small_tab[cta + 1];
+  if (jlo > jhi || jhi >= p.njobs) return;
+  const int nj = jhi - jlo + 1;
   const uint32_t P = static_cast<uint32_t>(p.P);
   GatherJob* sj = reinterpret_cast<GatherJob*>(stage_buf);
-  uint64_t* ssrc = reinterpret_cast<uint64_t*>(sj + nsj);
-  const uint32_t s0 = p.job[j0].src0, ns = static_cast<uint32_t>(nsj) * P;
-  for (int i = threadIdx.x; i < nsj; i += BLOCK) sj[i] = p.job[j0 + i];
+  uint64_t* ssrc = reinterpret_cast<uint64_t*>(sj + nj);
+  const uint32_t s0 = p.job[jlo].src0, ns = static_cast<uint32_t>(nj) * P;
+  for (int i = threadIdx.x; i < nj; i += BLOCK) sj[i] = p.job[jlo + i];
   for (uint32_t i = threadIdx.x; i < ns; i += BLOCK) ssrc[i] = p.src[s0 + i];
   __syncthreads();
-  const uint64_t nthreads = static_cast<uint64_t>(nctas) * BLOCK;
-  for (uint64_t g = static_cast<uint64_t>(cta) * BLOCK + threadIdx.x;
-       g < (p.total_vec - p.small_vec) * SPLIT; g += nthreads) {
-    const uint64_t k = p.small_vec + g / SPLIT;
+  const uint64_t k0 = p.small_vec + static_cast<uint64_t>(cta) * p.small_per;
+  const uint64_t k1 = min(k0 + p.small_per, p.total_vec);
+  for (uint64_t g = threadIdx.x; k0 + g / SPLIT < k1; g += BLOCK) {
+    const uint64_t k = k0 + g / SPLIT;
     const uint32_t part = static_cast<uint32_t>(g % SPLIT) * kBytes;
-    int lo = 0, hi = nsj - 1;  // the last job whose first vector is at or before k
+    int lo = 0, hi = nj - 1;  // the last job whose first vector is at or before k
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (sj[mid].vfirst <= k)
@@ -961,9 +967,9 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     const uint64_t fc = static_cast<uint64_t>(p.flat_ctas), sc = static_cast<uint64_t>(p.small_ctas);
     if (first < fc)
       gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, first, fc);
-    else if (first + sc >= step)
-      copy_small_jobs<BLOCK, kSmallSplit>(p, static_cast<uint32_t>(first + sc - step),
-                                          static_cast<uint32_t>(sc));
+    else if (first + sc >= step) {
+      if constexpr (MAXJ > 1) copy_small_jobs<BLOCK, kSmallSplit>(p, static_cast<uint32_t>(first + sc - step));
+    }
     else
       gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
           p, first - fc, step - fc - sc, p.flat_vec, p.small_vec);

@@ -69,6 +69,8 @@ __host__ __device__ constexpr int reduce_pt(int P) { return P == 2 || P == 4 || 
 constexpr uint64_t kGatherSmallBytes = 128;
 // Threads per 16-byte output vector in the small-job part of all_gather_many.
 constexpr int kSmallSplit = 4;
+// At most this many CTAs copy the small jobs of one launch (one table entry each).
+constexpr int kMaxSmallCtas = 512;
 
 // ------------------------------------------------------------- gather ---
 enum : uint32_t {
@@ -103,8 +105,13 @@ struct GatherParams {
   int32_t flat_ctas;    // split launch: CTAs [0, flat_ctas) copy the aligned jobs
   int32_t prefetch;     // one aligned job: tiles per CTA prefetched into L2 before the PDL wait
   int32_t tile_vec;     // one job, staged (modes 3, 5): vectors per tile (at most BLOCK*V)
+  uint32_t small_per;   // split launch: small-job vectors per small-job CTA (a contiguous run)
+  int32_t pad0;
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
+  // split launch: small-job CTA c covers jobs small_job0 + small_tab[c] ..
+  // small_job0 + small_tab[c + 1] (the jobs of its first and last vector)
+  uint16_t small_tab[MAXJ > 1 ? kMaxSmallCtas + 1 : 1];
 };
 
 using GatherParams1 = GatherParams<1, kMaxRanks>;

@@ -163,24 +163,58 @@ __device__ __forceinline__ uint8_t* out_ptr(const ReduceParams<MAXJ, MAXPTR>& p,
   return reinterpret_cast<uint8_t*>(p.ptr[J.out0 + m]);
 }
 
-// The 16 input bytes at `a`.  A job whose inputs all share the outputs'
-// address mod 16 loads them with one aligned load; a realigning job (inputs
-// at other offsets) loads the aligned block holding `a` and, if `a` is not
-// 16-byte aligned, the next one, and funnel-shifts them.  Both blocks hold
-// bytes of [a, a + 16), so they lie in the input buffer; a thread's second
-// block is its neighbour's first (coherent, L1-allocating load: a job may
-// run in place).
-template <bool REALIGN>
-__device__ __forceinline__ uint4 ld_input(const uint8_t* a) {
+// Bounds checks of the checked build (in_bounds): job J may read of input q
+// the 16-byte-block hull of its element range [in_q + in_off*s, in_q +
+// (in_off + count)*s), and write of output m exactly [out_m, out_m +
+// count*s).  Sites, for the fault record: kSiteRed* below.
+enum : uint32_t {
+  kSiteRedScalar = 200, kSiteRedVec = 201, kSiteRedStaged = 202, kSiteRedPrefetch = 203,
+};
+template <int DT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ bool input_ok(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J, int q,
+                                         const void* a, uint64_t len, uint32_t site) {
+  const uint64_t base = reinterpret_cast<uint64_t>(in_ptr(p, J, q)) + J.in_off * Elem<DT>::kSize;
+  return in_bounds(a, len, hull_lo(base), hull_hi(base, J.count * Elem<DT>::kSize), site);
+}
+template <int DT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ bool output_ok(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J, int m,
+                                          const void* a, uint64_t len, uint32_t site) {
+  const uint64_t base = reinterpret_cast<uint64_t>(out_ptr(p, J, m));
+  return in_bounds(a, len, base, base + J.count * Elem<DT>::kSize, site);
+}
+
+// The 16 input bytes of rank q at `a`.  A job whose inputs all share the
+// outputs' address mod 16 loads them with one aligned load; a realigning job
+// (inputs at other offsets) loads the aligned block holding `a` and, if `a`
+// is not 16-byte aligned, the next one, and funnel-shifts them.  Both blocks
+// hold bytes of [a, a + 16), so they lie in the input buffer; a thread's
+// second block is its neighbour's first (coherent, L1-allocating load: a job
+// may run in place).
+template <bool REALIGN, int DT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ uint4 ld_input(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J, int q,
+                                          const uint8_t* a) {
+  uint4 lo = make_uint4(0, 0, 0, 0);
   if constexpr (!REALIGN) {
-    return ld_stream(reinterpret_cast<const uint4*>(a));
+    const uint4* v = reinterpret_cast<const uint4*>(a);
+    if (input_ok<DT>(p, J, q, v, 16, kSiteRedVec)) lo = ld_stream(v);
+    return lo;
   } else {
     const uint32_t s = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a) & 15u);
     const uint4* blk = reinterpret_cast<const uint4*>(a - s);
-    const uint4 lo = ld_cached(blk);
-    const uint4 hi = s ? ld_cached(blk + 1) : lo;
+    if (input_ok<DT>(p, J, q, blk, 16, kSiteRedVec)) lo = ld_cached(blk);
+    uint4 hi = lo;
+    if (s && input_ok<DT>(p, J, q, blk + 1, 16, kSiteRedVec)) hi = ld_cached(blk + 1);
     return realign16(lo, hi, s);
   }
+}
+
+// One element of rank q at `a` (checked build: inside the job's range).
+template <int DT, int MAXJ, int MAXPTR>
+__device__ __forceinline__ float ld_element(const ReduceParams<MAXJ, MAXPTR>& p, const ReduceJob& J, int q,
+                                            const uint8_t* a) {
+  using Raw = typename Elem<DT>::Raw;
+  if (!input_ok<DT>(p, J, q, a, sizeof(Raw), kSiteRedScalar)) return 0.0f;
+  return Elem<DT>::widen1(*reinterpret_cast<const Raw*>(a));
 }
 
 // Elements [e0, e1) (step `step`) of job J, one at a time.
@@ -195,18 +229,19 @@ __device__ __forceinline__ void fold_scalar(const ReduceParams<MAXJ, MAXPTR>& p,
     if (ORDER == kOrderTree) {
       TreeStack<1> st;
       for (int q = 0; q < p.P; ++q) {
-        float x[1] = {T::widen1(*reinterpret_cast<const Raw*>(in_ptr(p, J, q) + off))};
+        float x[1] = {ld_element<DT>(p, J, q, in_ptr(p, J, q) + off)};
         st.push(x);
       }
       st.finish(acc);
     } else {
-      acc[0] = T::widen1(*reinterpret_cast<const Raw*>(in_ptr(p, J, 0) + off));
-      for (int q = 1; q < p.P; ++q)
-        acc[0] = __fadd_rn(acc[0], T::widen1(*reinterpret_cast<const Raw*>(in_ptr(p, J, q) + off)));
+      acc[0] = ld_element<DT>(p, J, 0, in_ptr(p, J, 0) + off);
+      for (int q = 1; q < p.P; ++q) acc[0] = __fadd_rn(acc[0], ld_element<DT>(p, J, q, in_ptr(p, J, q) + off));
     }
     const Raw y = T::narrow1(acc[0]);
-    for (uint32_t m = 0; m < J.nout; ++m)
-      *reinterpret_cast<Raw*>(out_ptr(p, J, m) + i * T::kSize) = y;
+    for (uint32_t m = 0; m < J.nout; ++m) {
+      Raw* d = reinterpret_cast<Raw*>(out_ptr(p, J, m) + i * T::kSize);
+      if (output_ok<DT>(p, J, m, d, sizeof(Raw), kSiteRedScalar)) *d = y;
+    }
   }
 }
 
@@ -244,7 +279,7 @@ __device__ __forceinline__ void fold_vector(const ReduceParams<MAXJ, MAXPTR>& p,
       const int nb = min(8, p.P - q0);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (k < nb) w[k] = ld_input<REALIGN>(in_ptr(p, J, q0 + k) + off);
+        if (k < nb) w[k] = ld_input<REALIGN, DT>(p, J, q0 + k, in_ptr(p, J, q0 + k) + off);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (k < nb) {
@@ -288,7 +323,7 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>&
           const uint64_t off = (J.in_off + J.head + E * (u - hu)) * T::kSize;
 #pragma unroll
           for (int q = 0; q < PT; ++q)
-            v[k][q] = ld_input<REALIGN>(in_ptr(p, J, q) + off);
+            v[k][q] = ld_input<REALIGN, DT>(p, J, q, in_ptr(p, J, q) + off);
         }
       }
     }
@@ -303,8 +338,10 @@ __device__ __forceinline__ void reduce_job_vec(const ReduceParams<MAXJ, MAXPTR>&
                                             acc);
         const uint4 y = T::narrow(acc);
         const uint64_t byte_off = (J.head + E * (u - hu)) * T::kSize;
-        for (uint32_t m = 0; m < J.nout; ++m)
-          st16(reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off), y);
+        for (uint32_t m = 0; m < J.nout; ++m) {
+          uint4* d = reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off);
+          if (output_ok<DT>(p, J, m, d, 16, kSiteRedVec)) st16(d, y);
+        }
       }
     }
   }
@@ -357,8 +394,9 @@ __device__ __forceinline__ void reduce_prefetch_tile(const ReduceParams<MAXJ, MA
     const uint64_t a = max(max(g0, J.ufirst) - J.ufirst, hu);
     const uint64_t b = min(min(g1, J.ufirst + J.nunits) - J.ufirst, body_end);
     if (a >= b) continue;
-    prefetch_l2(in_ptr(p, J, threadIdx.x) + (J.in_off + J.head + E * (a - hu)) * T::kSize,
-                static_cast<uint32_t>((b - a) * 16));
+    const uint8_t* src = in_ptr(p, J, threadIdx.x) + (J.in_off + J.head + E * (a - hu)) * T::kSize;
+    if (input_ok<DT>(p, J, threadIdx.x, src, (b - a) * 16, kSiteRedPrefetch))
+      prefetch_l2(src, static_cast<uint32_t>((b - a) * 16));
   }
 }
 
@@ -408,8 +446,10 @@ __device__ __forceinline__ void reduce_realign_staged(const ReduceParams<MAXJ, M
         const uint64_t a = in0(q) + 16 * b;
         const uint64_t blk = a & ~static_cast<uint64_t>(15);
         const uint32_t dst = sbase + kRank * (slot * PT + q);
-        cp_async16(dst, reinterpret_cast<const void*>(blk));
-        if ((a & 15u) && last) cp_async16(dst + 16u, reinterpret_cast<const void*>(blk + 16));
+        if (input_ok<DT>(p, J, q, reinterpret_cast<const void*>(blk), 16, kSiteRedStaged))
+          cp_async16(dst, reinterpret_cast<const void*>(blk));
+        if ((a & 15u) && last && input_ok<DT>(p, J, q, reinterpret_cast<const void*>(blk + 16), 16, kSiteRedStaged))
+          cp_async16(dst + 16u, reinterpret_cast<const void*>(blk + 16));
       }
     }
     cp_async_commit();
@@ -443,7 +483,10 @@ __device__ __forceinline__ void reduce_realign_staged(const ReduceParams<MAXJ, M
       fold_vector<DT, ORDER, PT, true>(p, J, 0, v, acc);
       const uint4 y = T::narrow(acc);
       const uint64_t byte_off = (J.head + static_cast<uint64_t>(E) * b) * T::kSize;
-      for (uint32_t m = 0; m < J.nout; ++m) st16(reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off), y);
+      for (uint32_t m = 0; m < J.nout; ++m) {
+        uint4* d = reinterpret_cast<uint4*>(out_ptr(p, J, m) + byte_off);
+        if (output_ok<DT>(p, J, m, d, 16, kSiteRedStaged)) st16(d, y);
+      }
     }
     __syncwarp();
     issue(slot, t_issue);
@@ -465,8 +508,11 @@ __device__ __forceinline__ void realign_prefetch(const ReduceParams<MAXJ, MAXPTR
   const uint64_t a = reinterpret_cast<uint64_t>(in_ptr(p, J, threadIdx.x)) + (J.in_off + J.head) * T::kSize;
   const uint64_t lo = (a + 16 * b0) & ~static_cast<uint64_t>(15);
   const uint64_t hi = (a + 16 * b1 + 15) & ~static_cast<uint64_t>(15);
-  for (uint64_t c = lo; c < hi; c += 32768)
-    prefetch_l2(reinterpret_cast<const void*>(c), static_cast<uint32_t>(min(static_cast<uint64_t>(32768), hi - c)));
+  for (uint64_t c = lo; c < hi; c += 32768) {
+    const uint64_t n = min(static_cast<uint64_t>(32768), hi - c);
+    if (input_ok<DT>(p, J, threadIdx.x, reinterpret_cast<const void*>(c), n, kSiteRedPrefetch))
+      prefetch_l2(reinterpret_cast<const void*>(c), static_cast<uint32_t>(n));
+  }
 }
 
 template <int DT, int MAXJ, int MAXPTR>
@@ -647,4 +693,5 @@ int occupancy_dtype(int order, int P) {
       default: return red::occupancy_dtype<DT, kManyMaxReduceJobs, kManyMaxReducePtrs>(order, P); \
     }                                                                                              \
   }                                                                                                \
+  DC_BOUNDS_READER(take_bounds_reduce_##NAME)                                                      \
   }  // namespace dc

@@ -56,6 +56,12 @@ def test_library_exports_every_declared_function():
     assert not missing, missing
 
 
+def test_which_build_is_loaded():
+    """libdc.so unless DC_LIBRARY=bounds selects the bounds-checked build."""
+    want = 1 if os.environ.get("DC_LIBRARY") == "bounds" else 0
+    assert dc.lib().dc_bounds_checked() == want
+
+
 def test_version_and_status_names():
     assert dc.lib().dc_version() == 1
     for code, name in dc.STATUS.items():
