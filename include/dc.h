@@ -361,7 +361,8 @@ const char *dc_status_name(int status);
  *   "test_bulk_short_tx"      1 = every bulk CTA's first wait runs out (tests
  *                             of dc_check_device)
  *   "fused_chunk_min"         dc_fused_all_gather: smallest chunk per CTA
- *                             (default 65536 bytes)
+ *                             (default 32768 bytes; measured, 8 ranks x 4 MiB:
+ *                             75.8 us at 32 KiB, 81.9 us at 64 KiB)
  *   "test_fused_absent_ranks" bit r set: rank r of dc_fused_all_gather never
  *                             arrives (tests of its bounded waits)
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching

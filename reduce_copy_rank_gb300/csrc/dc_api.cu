@@ -79,7 +79,7 @@ struct Options {
   std::atomic<long long> bulk_stages{6};
   std::atomic<long long> bulk_ctas_per_sm{2};
   std::atomic<long long> bulk_prefetch{2};
-  std::atomic<long long> fused_chunk_min{65536};
+  std::atomic<long long> fused_chunk_min{32768};
   std::atomic<long long> test_fused_absent{0};
   std::atomic<long long> wait_limit_ns{1000000000};
   std::atomic<long long> test_bulk_short_tx{0};

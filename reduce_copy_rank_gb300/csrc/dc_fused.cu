@@ -19,10 +19,10 @@
 // handles chunk c of rank r:
 //   stage:    in_r[chunk c] -> staging_r[chunk c]; then staged[r][c] = epoch
 //             (release store, after a device-scope fence by every thread);
-//   gather:   for each rank q (starting with itself): wait until
-//             staged[q][c] == epoch (acquire load), then staging_q[chunk c] ->
-//             out_r[q*B + chunk c] (loads through L2 only: staging_q is
-//             written by other CTAs);
+//   gather:   wait until staged[q][c] == epoch for every rank q, starting
+//             with itself (acquire loads), then staging_q[chunk c] ->
+//             out_r[q*B + chunk c] for every q (loads through L2 only:
+//             staging_q is written by other CTAs);
 //   complete: done[r][c] = epoch, then wait until done[q][c] == epoch for
 //             every q: chunk c of staging_r has been read by every rank and
 //             may be overwritten by the next epoch.
@@ -103,23 +103,23 @@ __device__ __forceinline__ void record_fault(uint32_t phase, uint32_t rank, uint
 enum : uint32_t { kSiteFusedStage = 400, kSiteFusedGather = 401, kSiteFusedFlag = 402 };
 
 // n bytes (a multiple of 16; both pointers 16-byte aligned) copied by the
-// CTA's threads, four 16-byte vectors in flight per thread.  Checked build:
+// CTA's threads, U 16-byte vectors in flight per thread.  Checked build:
 // loads inside [slo, shi), stores inside [dlo, dhi).
-template <bool THROUGH_L2>
+template <bool THROUGH_L2, int U>
 __device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uint64_t n, uint64_t slo,
                                            uint64_t shi, uint64_t dlo, uint64_t dhi, uint32_t site) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
   uint4* d = reinterpret_cast<uint4*>(dst);
   const uint64_t nv = n >> 4;
-  for (uint64_t i = threadIdx.x; i < nv; i += 4ull * kFusedBlock) {
-    uint4 v[4];
+  for (uint64_t i = threadIdx.x; i < nv; i += static_cast<uint64_t>(U) * kFusedBlock) {
+    uint4 v[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const uint64_t k = i + static_cast<uint64_t>(u) * kFusedBlock;
       if (k < nv && in_bounds(s + k, 16, slo, shi, site)) v[u] = THROUGH_L2 ? ld_cg16(s + k) : ld_stream(s + k);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const uint64_t k = i + static_cast<uint64_t>(u) * kFusedBlock;
       if (k < nv && in_bounds(d + k, 16, dlo, dhi, site)) st16(d + k, v[u]);
     }
@@ -127,7 +127,7 @@ __device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uin
 }
 
 __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __grid_constant__ FusedParams p) {
-  __shared__ int s_ok[kMaxRanks + 1];
+  __shared__ int s_ok[1];
   const uint32_t P = static_cast<uint32_t>(p.P), G = static_cast<uint32_t>(p.G);
   const uint32_t r = blockIdx.x / G, c = blockIdx.x % G;
   if (r >= P) return;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
   const uint32_t epoch = p.epoch;
 
   // stage
-  copy_chunk<false>(reinterpret_cast<const uint8_t*>(p.in[r]) + lo, reinterpret_cast<uint8_t*>(p.staging[r]) + lo,
+  copy_chunk<false, 8>(reinterpret_cast<const uint8_t*>(p.in[r]) + lo, reinterpret_cast<uint8_t*>(p.staging[r]) + lo,
                     n, p.in[r], p.in[r] + p.bytes, p.staging[r], p.staging[r] + p.bytes, kSiteFusedStage);
   __threadfence();
   __syncthreads();
@@ -147,21 +147,28 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
   if (threadIdx.x == 0 && in_bounds(&staged[r * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag))
     st_release_u32(&staged[r * kFusedMaxChunks + c], epoch);
 
-  // gather, own rank first
+  // gather: thread 0 waits until every rank has published chunk c (its own
+  // rank first), then the CTA copies the P staged chunks without a barrier
+  // between them (a barrier per peer drained the loads in flight each time)
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    for (uint32_t i = 0; i < P && ok; ++i) {
+      const uint32_t q = r + i < P ? r + i : r + i - P;
+      ok = in_bounds(&staged[q * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag) &&
+           wait_flag(&staged[q * kFusedMaxChunks + c], epoch, p.wait_ns);
+      if (!ok) record_fault(1, r, q, c, epoch);
+    }
+    __threadfence();
+    s_ok[0] = ok;
+  }
+  __syncthreads();
+  if (!s_ok[0]) return;
   for (uint32_t i = 0; i < P; ++i) {
     const uint32_t q = r + i < P ? r + i : r + i - P;
-    if (threadIdx.x == 0) {
-      const bool ok = in_bounds(&staged[q * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag) &&
-                      wait_flag(&staged[q * kFusedMaxChunks + c], epoch, p.wait_ns);
-      if (!ok) record_fault(1, r, q, c, epoch);
-      __threadfence();
-      s_ok[i] = ok;
-    }
-    __syncthreads();
-    if (!s_ok[i]) return;
-    copy_chunk<true>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
-                     reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n,
-                     p.staging[q], p.staging[q] + p.bytes, p.out[r], p.out[r] + P * p.bytes, kSiteFusedGather);
+    copy_chunk<true, 8>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
+                        reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n,
+                        p.staging[q], p.staging[q] + p.bytes, p.out[r], p.out[r] + P * p.bytes,
+                        kSiteFusedGather);
   }
 
   // complete
