@@ -360,6 +360,11 @@ const char *dc_status_name(int status);
  *                             at least 1000)
  *   "test_bulk_short_tx"      1 = every bulk CTA's first wait runs out (tests
  *                             of dc_check_device)
+ *   "gather_realign_warp"     1 (default) = a dc_all_gather whose payloads or
+ *                             output are not 16-byte aligned (at least 128
+ *                             bytes per rank, output under 4 GiB) realigns its
+ *                             vectors across the lanes of a warp, in
+ *                             registers; 0 = through a shared-memory ring
  *   "fused_chunk_min"         dc_fused_all_gather: smallest chunk per CTA
  *                             (default 32768 bytes; measured, 8 ranks x 4 MiB:
  *                             75.8 us at 32 KiB, 81.9 us at 64 KiB)
@@ -372,7 +377,7 @@ const char *dc_status_name(int status);
  * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
  * DC_REDUCE_TILE_MIN, DC_REDUCE_STAGED, DC_GATHER_BULK, DC_GATHER_BULK_MIN_BYTES,
  * DC_BULK_CHUNK_BYTES, DC_BULK_CHUNK_MIN, DC_BULK_STAGES, DC_BULK_CTAS_PER_SM,
- * DC_BULK_PREFETCH, DC_FUSED_CHUNK_MIN and DC_WAIT_LIMIT_NS set the initial values (read once,
+ * DC_BULK_PREFETCH, DC_GATHER_REALIGN_WARP, DC_FUSED_CHUNK_MIN and DC_WAIT_LIMIT_NS set the initial values (read once,
  * at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.

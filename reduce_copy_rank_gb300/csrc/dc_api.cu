@@ -80,6 +80,7 @@ struct Options {
   std::atomic<long long> bulk_ctas_per_sm{2};
   std::atomic<long long> bulk_prefetch{2};
   std::atomic<long long> fused_chunk_min{32768};
+  std::atomic<long long> realign_warp{1};
   std::atomic<long long> test_fused_absent{0};
   std::atomic<long long> wait_limit_ns{1000000000};
   std::atomic<long long> test_bulk_short_tx{0};
@@ -115,6 +116,7 @@ const OptionKey kKeys[] = {
     {"bulk_ctas_per_sm", "DC_BULK_CTAS_PER_SM", &g_opt.bulk_ctas_per_sm},
     {"bulk_prefetch", "DC_BULK_PREFETCH", &g_opt.bulk_prefetch},
     {"fused_chunk_min", "DC_FUSED_CHUNK_MIN", &g_opt.fused_chunk_min},
+    {"gather_realign_warp", "DC_GATHER_REALIGN_WARP", &g_opt.realign_warp},
     {"test_fused_absent_ranks", nullptr, &g_opt.test_fused_absent},
     {"wait_limit_ns", "DC_WAIT_LIMIT_NS", &g_opt.wait_limit_ns},
     {"test_bulk_short_tx", nullptr, &g_opt.test_bulk_short_tx},
@@ -449,6 +451,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
                                       : family == 0 ? g_opt.gather_single_max.load()
                                                     : g_opt.gather_many_single_max.load());
   prm.staged = g_opt.gather_staged.load() ? 1 : 0;
+  prm.realign_warp = g_opt.realign_warp.load() ? 1 : 0;
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.flat_ctas = 0;
   prm.small_ctas = 0;
@@ -476,6 +479,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       const int unroll = mode == 0   ? kGatherUnrollGeneral
                          : mode == 3 ? kStagedVectors
                          : mode == 5 ? kRealignVectors
+                         : mode == 6 ? kWarpRealignVectors
                                      : kGatherUnroll;
       uint64_t tile = static_cast<uint64_t>(kGatherBlock) * unroll;
       // The staged single-job kernels take even tiles: the aligned one (mode
@@ -493,13 +497,15 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
       // MiB+1) 3-6 % slower.  Mode 5 with 64-bit indices keeps full tiles.
       // Mode 5 adds one CTA for the rank-boundary vectors (copy_boundaries),
       // and keeps a slot free for it.
-      const int reserve = mode == 5 ? 1 : 0;
+      // Mode 6 (one unaligned job realigned across warps, registers) takes
+      // even tiles of at least gather_tile_min vectors, whole warps each.
+      const int reserve = (mode == 5 || mode == 6) ? 1 : 0;
       const bool wide = mode == 5 && (prm.total_vec * 16 >= (1ull << 32) || prm.job[0].bytes >= (1ull << 32));
-      if ((mode == 2 || mode == 3 || mode == 5) && !wide)
+      if ((mode == 2 || mode == 3 || mode == 5 || mode == 6) && !wide)
         tile = even_tile(prm.total_vec, sms, occ, tile,
                          mode == 5 ? static_cast<long long>(tile) : g_opt.tile_min.load(), mode == 5 ? 2 : 32,
                          reserve);
-      if (mode == 2 || mode == 3 || mode == 5) prm.tile_vec = static_cast<int32_t>(tile);
+      if (mode == 2 || mode == 3 || mode == 5 || mode == 6) prm.tile_vec = static_cast<int32_t>(tile);
       grid = plan_grid((prm.total_vec + tile - 1) / tile, sms, occ, reserve) + reserve;
     }
   }

@@ -71,7 +71,7 @@ struct Cursor {
 enum : uint32_t {
   kSiteBytes = 100, kSiteFlat1 = 101, kSiteStaged1 = 102, kSiteStagedRing = 103, kSiteStagedJobs = 104,
   kSiteSpan = 105, kSiteBoundary = 106, kSiteRealign = 107, kSiteSmallVec = 108, kSiteRealignJobs = 109,
-  kSiteSmallJobs = 110, kSiteGeneral = 111, kSitePrefetch = 112,
+  kSiteSmallJobs = 110, kSiteGeneral = 111, kSitePrefetch = 112, kSiteWarpRealign = 113,
 };
 template <int MAXJ, int MAXS>
 __device__ __forceinline__ bool load_ok(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J, uint32_t r,
@@ -598,6 +598,72 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
   cp_async_wait<0>();
 }
 
+// One unaligned job (at least kGatherSmallBytes per rank, 32-bit indices),
+// realigned across the lanes of a warp: the register path with far fewer
+// instructions per vector than the shared-memory ring of
+// gather_tiles_staged_realign, which ncu showed issue-bound (8 x (1 MiB+1 B):
+// 3.9 M warp instructions against 1.2 M for the aligned copy, issue slots 66 %
+// busy, almost no memory stalls).  Tiles as there; thread i of a tile takes
+// vectors i, i + BLOCK, ... (V of them), so the 32 lanes of a warp hold 32
+// consecutive output vectors.  A vector k inside rank r (k in [klo, khi), see
+// RankWalk) is bytes [16k + s, 16k + s + 16) of the 16-byte blocks base_r +
+// 16k and base_r + 16(k+1): each lane loads only the first block, straight
+// into registers, and takes the second from the next lane (__shfl_down_sync),
+// which loaded it as its own first block -- unless the next lane's vector is
+// not vector k + 1 of the same rank (lane 31, the tile's last vector, the
+// rank's last whole vector), in which case the lane loads its second block
+// itself, in the same round of loads.  All loads of a thread's V vectors are
+// issued before the first shuffle and store.  The vectors that are not inside
+// one rank are left to the launch's last CTA (copy_boundaries), as in mode 5.
+template <int BLOCK, int V, int MAXS>
+__device__ __forceinline__ void gather_tiles_warp_realign(const GatherParams<1, MAXS>& p, uint32_t first,
+                                                          uint32_t step) {
+  const GatherJob& J = p.job[0];
+  const uint32_t tile = static_cast<uint32_t>(p.tile_vec);  // <= BLOCK*V
+  const uint32_t total = static_cast<uint32_t>(p.total_vec);
+  const uint32_t ntiles = (total + tile - 1) / tile;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
+  uint4* const out = reinterpret_cast<uint4*>(xbase);
+  RankWalk<uint32_t> w{0, 0, 0, 0, 0, true};
+  for (uint32_t t = first; t < ntiles; t += step) {
+    uint4 lo[V], hi[V];
+    uint32_t meta[V];  // s | inside << 4 | own second block << 5
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint32_t i = u * BLOCK + threadIdx.x, k = t * tile + i;
+      meta[u] = 0;
+      if (i < tile && k < total) {
+        walk_to(w, p, J, xbase, k);
+        if (k >= w.klo && k < w.khi) {
+          const bool own_hi = w.s != 0 && (lane == 31u || k + 1 >= w.khi || i + 1 >= tile);
+          const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * static_cast<uint64_t>(k));
+          if (load_ok(p, J, w.r, blk, 16, kSiteWarpRealign)) lo[u] = ld_nc_cached(blk);
+          if (own_hi && load_ok(p, J, w.r, blk + 1, 16, kSiteWarpRealign)) hi[u] = ld_nc_cached(blk + 1);
+          meta[u] = w.s | 16u | (own_hi ? 32u : 0u);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      // every lane takes part in the shuffles; a lane whose next lane holds
+      // vector k + 1 of the same rank uses that lane's first block
+      uint4 nb;
+      nb.x = __shfl_down_sync(0xffffffffu, lo[u].x, 1);
+      nb.y = __shfl_down_sync(0xffffffffu, lo[u].y, 1);
+      nb.z = __shfl_down_sync(0xffffffffu, lo[u].z, 1);
+      nb.w = __shfl_down_sync(0xffffffffu, lo[u].w, 1);
+      const uint32_t m = meta[u];
+      if (m & 16u) {
+        const uint32_t sh = m & 15u;
+        const uint4 second = (m & 32u) ? hi[u] : nb;
+        const uint32_t k = t * tile + u * BLOCK + threadIdx.x;
+        if (store_ok(p, J, out + k, 16, kSiteWarpRealign)) st16(out + k, sh ? realign16(lo[u], second, sh) : lo[u]);
+      }
+    }
+  }
+}
+
 // The rank-boundary vectors of one unaligned job (at least
 // kGatherSmallBytes per rank): thread b copies the vector holding d_b = out +
 // b*B, b in [0, P], if d_b is not 16-byte aligned (the byte before d_b is
@@ -936,6 +1002,7 @@ enum Mode : int {
   kFlat1Staged = 3,
   kManySplit = 4,
   kGeneral1Staged = 5,  // one unaligned job (>= kGatherSmallBytes per rank) through shared memory
+  kGeneral1Warp = 6,    // the same, realigned across the lanes of a warp (32-bit indices)
 };
 
 template <int BLOCK, int UNROLL, int MODE, bool SINGLE = false, int MAXJ, int MAXS>
@@ -947,6 +1014,15 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
   else if constexpr (MODE == kFlat1Staged && MAXJ == 1)
     gather_tiles_staged<BLOCK, kStagedVectors, kStagedStages>(p, static_cast<uint32_t>(first),
                                                               static_cast<uint32_t>(step));
+  else if constexpr (MODE == kGeneral1Warp && MAXJ == 1) {
+    // the last CTA copies the rank-boundary vectors, the others the rest
+    if (first + 1 == step) {
+      copy_boundaries<BLOCK>(p);
+      return;
+    }
+    gather_tiles_warp_realign<BLOCK, kWarpRealignVectors>(p, static_cast<uint32_t>(first),
+                                                          static_cast<uint32_t>(step - 1));
+  }
   else if constexpr (MODE == kGeneral1Staged && MAXJ == 1) {
     // the last CTA copies the rank-boundary vectors, the others the rest
     if (first + 1 == step) {
@@ -1030,8 +1106,8 @@ __device__ __forceinline__ void prefetch_unaligned(const GatherParams<1, MAXS>& 
 // Multi-CTA gather: CTA c copies tiles c, c + gridDim.x, ...
 template <int MAXJ, int MAXS, int MODE>
 __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat1Staged) ? 4
-                                                : MODE == kGeneral1Staged             ? 3
-                                                                                      : 2)
+                                                : MODE == kGeneral1Staged ? 3 : MODE == kGeneral1Warp ? 2
+                                                                                                     : 2)
     dc_gather_kernel(const __grid_constant__ GatherParams<MAXJ, MAXS> p) {
   if constexpr (MAXJ == 1 && (MODE == kFlat1 || MODE == kFlat1Staged)) {
     pdl_launch_dependents();
@@ -1042,7 +1118,7 @@ __global__ void __launch_bounds__(kGatherBlock, (MODE == kFlat1 || MODE == kFlat
         prefetch_vectors(p, t * tile, (t + 1) * tile);
     }
     pdl_wait();
-  } else if constexpr (MAXJ == 1 && MODE == kGeneral1Staged) {
+  } else if constexpr (MAXJ == 1 && (MODE == kGeneral1Staged || MODE == kGeneral1Warp)) {
     // the first p.prefetch tiles of each tile CTA (all but the last CTA)
     // prefetched before the wait; dependents are let in after it (measured:
     // 8 x (256 KiB+1) back to back 2.87 us, 3.21 us with the trigger first,
@@ -1088,8 +1164,13 @@ template <int MAXJ, int MAXS>
 int mode_of(const GatherParams<MAXJ, MAXS>& p) {
   const bool all_flat = p.flat_vec == p.total_vec;
   if (MAXJ > 1 && p.staged) return kManySplit;
-  if (!all_flat)
-    return MAXJ == 1 && p.staged && !(p.job[0].flags & kJobSmall) ? kGeneral1Staged : kGeneral;
+  if (!all_flat) {
+    if (MAXJ != 1 || !p.staged || (p.job[0].flags & kJobSmall)) return kGeneral;
+    // the warp path uses 32-bit indices: outputs (from out rounded down to
+    // 16) and ranks under 4 GiB
+    const bool narrow = p.total_vec * 16 < (1ull << 32) && p.job[0].bytes < (1ull << 32);
+    return p.realign_warp && narrow ? kGeneral1Warp : kGeneral1Staged;
+  }
   if (MAXJ == 1 && p.total_vec < (1ull << 31)) return p.staged ? kFlat1Staged : kFlat1;
   return kFlat;
 }
@@ -1144,7 +1225,7 @@ cudaError_t launch_mode(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
   }
   if (single) {  // small outputs: staging buys nothing, use the register path
     constexpr int kMode = MODE == kFlat1Staged ? kFlat1
-                          : (MODE == kManySplit || MODE == kGeneral1Staged) ? kGeneral
+                          : (MODE == kManySplit || MODE == kGeneral1Staged || MODE == kGeneral1Warp) ? kGeneral
                                                                             : MODE;
     constexpr int block = kMode == kGeneral ? kGatherSingleBlockGeneral : kGatherSingleBlock;
     return launch_ex(dc_gather_single_kernel<MAXJ, MAXS, kMode>, 1, block, pdl, s, p);
@@ -1177,6 +1258,13 @@ cudaError_t launch_impl(const GatherParams<MAXJ, MAXS>& p, int grid, bool single
         return launch_mode<MAXJ, MAXS, kGeneral1Staged>(p, grid, single, pdl, s);
       }
       return cudaErrorInvalidValue;
+    case kGeneral1Warp:
+      if constexpr (MAXJ == 1) {  // grid: at least one tile CTA and the boundary CTA
+        if (!single && (grid < 2 || p.tile_vec < 1 || p.tile_vec > kGatherBlock * kWarpRealignVectors))
+          return cudaErrorInvalidValue;
+        return launch_mode<MAXJ, MAXS, kGeneral1Warp>(p, grid, single, pdl, s);
+      }
+      return cudaErrorInvalidValue;
     case kFlat1:
       if constexpr (MAXJ == 1) return launch_mode<MAXJ, MAXS, kFlat1>(p, grid, single, pdl, s);
       return cudaErrorInvalidValue;
@@ -1200,7 +1288,10 @@ int occupancy_impl(int mode) {
   else if (mode == kFlat || (MAXJ != 1 && mode != kManySplit) || (MAXJ != 1 && mode == kGeneral1Staged))
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kFlat>,
                                                       kGatherBlock, 0);
-  else if (mode == kGeneral1Staged && MAXJ == 1) {
+  else if (mode == kGeneral1Warp && MAXJ == 1) {
+    constexpr int kM = MAXJ == 1 ? kGeneral1Warp : kGeneral;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_gather_kernel<MAXJ, MAXS, kM>, kGatherBlock, 0);
+  } else if (mode == kGeneral1Staged && MAXJ == 1) {
     constexpr int kM = MAXJ == 1 ? kGeneral1Staged : kGeneral;
     e = allow_smem<MAXJ, MAXS, kM>();
     if (e == cudaSuccess)

@@ -44,6 +44,9 @@ constexpr int kSplitRealignVectors = 2;
 // per SM).
 constexpr int kRealignStages = 2;
 constexpr int kRealignVectors = 2;
+// One unaligned job realigned across a warp (mode 6): output vectors in
+// flight per thread, loaded straight into registers.
+constexpr int kWarpRealignVectors = 4;
 constexpr int kReduceBlock = 256;
 constexpr int kReduceSingleBlock = 512;
 constexpr int kReduceUnroll = 2;         // 8-element groups in flight per thread (P = 8 or any P)
@@ -106,7 +109,7 @@ struct GatherParams {
   int32_t prefetch;     // one aligned job: tiles per CTA prefetched into L2 before the PDL wait
   int32_t tile_vec;     // one job, staged (modes 3, 5): vectors per tile (at most BLOCK*V)
   uint32_t small_per;   // split launch: small-job vectors per small-job CTA (a contiguous run)
-  int32_t pad0;
+  int32_t realign_warp; // one unaligned job: realign across the warp's lanes (mode 6), not through a ring
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
   // split launch: small-job CTA c covers jobs small_job0 + small_tab[c] ..
@@ -312,9 +315,11 @@ int gather_ctas_per_sm(int which, int mode);  // which: 0 one job, 1 small many,
 // Kernel mode a launch will use: 0 general, 1 aligned jobs, 2 one aligned job,
 // 3 one aligned job staged through shared memory, 4 (kGatherModeSplit) several
 // jobs, the aligned ones staged by the first flat_ctas CTAs, 5 one unaligned
-// job staged through shared memory.
+// job staged through shared memory, 6 (kGatherModeWarpRealign) one unaligned
+// job realigned across the lanes of a warp.
 constexpr int kGatherModeSplit = 4;
-constexpr int kGatherModes = 6;
+constexpr int kGatherModeWarpRealign = 6;
+constexpr int kGatherModes = 7;
 int gather_mode_of(const GatherParams1& p);
 int gather_mode_of(const GatherParamsS& p);
 int gather_mode_of(const GatherParamsL& p);

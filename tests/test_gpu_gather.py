@@ -172,6 +172,9 @@ def test_page_size_list_all_offsets():
     {"prefetch": 0}, {"prefetch": 4, "force_path": 2, "grid_ctas": 2},
     {"gather_tile_min": 32}, {"gather_tile_min": 33}, {"gather_tile_min": 1 << 20},
     {"gather_tile_min": 33, "force_path": 2, "grid_ctas": 5}, {"gather_tile_min": 33, "prefetch": 3},
+    {"gather_realign_warp": 0}, {"gather_realign_warp": 0, "force_path": 2, "grid_ctas": 2},
+    {"gather_realign_warp": 1, "force_path": 2, "grid_ctas": 2},
+    {"gather_realign_warp": 1, "gather_tile_min": 33}, {"gather_realign_warp": 1, "grid_ctas": 7},
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_path_and_grid_independence(opts):
     """The bytes never depend on the path, the grid or the flat/generic
@@ -190,14 +193,15 @@ def test_path_and_grid_independence(opts):
 @pytest.mark.parametrize("B", [4 * 1024 * 1024 + 1, 32 * 1024 * 1024 + 1])
 def test_large_unaligned_full_size(B):
     """The bench's unaligned rows at full size (8 ranks, payloads at +1 B,
-    output at +3 B; the staged realigning path), byte for byte against the
-    oracle, with per-rank offsets varied as well."""
+    output at +3 B; the warp realigning path, and the shared-memory ring once),
+    byte for byte against the oracle, with per-rank offsets varied as well."""
     rng = np.random.default_rng(W.seed_for(3, 9100))
     P = 8
     peers = [rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)]
     want = oracle.all_gather(peers)
-    for in_offs, out_off in (([1] * P, 3), ([int(x) for x in rng.integers(0, 16, P)], 9)):
-        got, guards = run_gather(peers, in_offs, out_off)
+    for in_offs, out_off, opts in (([1] * P, 3, {}), ([int(x) for x in rng.integers(0, 16, P)], 9, {}),
+                                   ([1] * P, 3, {"gather_realign_warp": 0})):
+        got, guards = run_gather(peers, in_offs, out_off, **opts)
         assert np.array_equal(got, want), (B, in_offs, out_off)
         assert guards
 
