@@ -76,9 +76,11 @@ typedef enum { DC_ORDER_LINEAR = 0, DC_ORDER_TREE = 1 } dc_order_t;
  *            not overlap any peer range (DC_ERR_OVERLAP).
  * Bytes outside [out, out + P*bytes_per_rank) are never written.
  * Path: the 16-byte flat vector copy when out, bytes_per_rank and every peer
- * are 16-byte aligned, the realigning per-rank copy otherwise; one CTA below
- * the measured single-block threshold (output bytes), a grid sized from the
- * 16-byte vector count and the SM count above it.
+ * are 16-byte aligned (staged through shared memory with cp.async, or, with
+ * the gather_bulk option, bulk copies on the TMA engine); the realigning copy
+ * otherwise (across the lanes of a warp, or through a shared-memory ring);
+ * one CTA below the measured single-block threshold (output bytes), a grid
+ * sized from the 16-byte vector count and the SM count above it.
  */
 dc_status_t dc_all_gather(const void *const *peer_ptrs, int P, size_t bytes_per_rank,
                           void *out, dc_stream_t stream);
