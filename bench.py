@@ -581,11 +581,13 @@ def comparators_block(torch, dc, device, stream, flush, reps=10):
     return {"all_gather_vs_torch_cat": gathers, "all_reduce_bf16_vs_torch_loop": reduces}
 
 
-def back_to_back_block(torch, dc, device, flush, per_size=8, replays=10):
+def back_to_back_block(torch, dc, device, flush, per_size=14, replays=10):
     """Per-call time of each sweep size in the back-to-back regime: one CUDA
     graph of `per_size` calls of that size on distinct buffers (so every
     call reads inputs no kernel has touched since the L2 flush that opens
-    the graph), timed by events around the calls; median over replays."""
+    the graph), timed by events around the calls; median over replays.
+    14 calls per graph, as many as the step has, so the first call's launch
+    (which nothing overlaps) weighs as much as in the step."""
     rows = []
     for (P, B, seed) in sweep_cases():
         bufs = []
