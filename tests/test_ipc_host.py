@@ -1,0 +1,123 @@
+"""The staged all-gather across processes (reduce_copy_rank_gb300.ipc), its
+host protocol on CPU: gloo process groups of 2 and 3 ranks, host buffers in
+shared memory standing in for the device staging buffers.
+
+Checked: every rank's output is the rank-ordered concatenation over several
+epochs; ranks that disagree on the collective all raise DC_ERR_INVALID when it
+is built; a rank that never arrives, or that dies, makes the others raise
+DC_ERR_TIMEOUT within the bound (seconds, not the process group's minutes),
+naming the step and the epoch, and every later call raises at once.
+
+Page, by title: "perf(cuda): vectorize the deterministic all-gather copy and
+right-size its single-block path" (author's replies: stage, gather, complete
+over CUDA IPC; section "Not in this PR" and the review threads: no abort path,
+peers of a dead rank wait for the process-group timeout).
+"""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import time
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import oracle
+import workloads as W
+
+
+def _port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, case, outdir):
+    import torch.distributed as dist
+
+    import reduce_copy_rank_gb300 as dc
+    from reduce_copy_rank_gb300.ipc import SharedMemoryTransport, StagedAllGather
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    res = {"rank": rank}
+    B = 4099
+    try:
+        if case == "mismatch":
+            try:
+                StagedAllGather(None, B + (rank == 1), SharedMemoryTransport(), timeout=2.0)
+                res["raised"] = None
+            except dc.DCError as e:
+                res["raised"] = e.status
+            return
+        coll = StagedAllGather(None, B, SharedMemoryTransport(), timeout=2.0)
+        if case == "parity":
+            res["ok"] = []
+            for epoch in range(1, 4):
+                payloads = [W.random_bytes(W.seed_for(2, 800 + epoch), q, B) for q in range(world)]
+                out = np.zeros(world * B, dtype=np.uint8)
+                coll.all_gather(payloads[rank], out)
+                res["ok"].append(bool(np.array_equal(out, oracle.all_gather(payloads))))
+            coll.close()
+        elif case in ("absent", "dead"):
+            payload = W.random_bytes(W.seed_for(2, 810), rank, B)
+            out = np.zeros(world * B, dtype=np.uint8)
+            coll.all_gather(payload, out)  # epoch 1: everyone
+            if rank == world - 1:
+                if case == "dead":
+                    os._exit(0)  # between steps, nothing in flight
+                time.sleep(8.0)  # never arrives at epoch 2
+                return
+            t0 = time.time()
+            try:
+                coll.all_gather(payload, out)
+                res["raised"] = None
+            except dc.DCError as e:
+                res["raised"], res["msg"] = e.status, str(e)
+            res["seconds"] = time.time() - t0
+            t1 = time.time()
+            try:
+                coll.all_gather(payload, out)
+                res["again"] = None
+            except dc.DCError as e:
+                res["again"] = e.status
+            res["again_seconds"] = time.time() - t1
+    finally:
+        with open(os.path.join(outdir, f"r{rank}.json"), "w") as fh:
+            json.dump(res, fh)
+
+
+def _run(world, case, tmp_path):
+    mp.spawn(_worker, args=(world, _port(), case, str(tmp_path)), nprocs=world, join=True)
+    out = {}
+    for r in range(world):
+        p = tmp_path / f"r{r}.json"
+        if p.exists():
+            out[r] = json.load(open(p))
+    return out
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_parity_over_epochs(world, tmp_path):
+    res = _run(world, "parity", tmp_path)
+    assert len(res) == world
+    for r in range(world):
+        assert res[r]["ok"] == [True, True, True], res[r]
+
+
+def test_signature_mismatch_raises_on_every_rank(tmp_path):
+    res = _run(2, "mismatch", tmp_path)
+    assert [res[r]["raised"] for r in range(2)] == [1, 1]  # DC_ERR_INVALID
+
+
+@pytest.mark.parametrize("case", ["absent", "dead"])
+def test_rank_that_never_arrives_times_out(case, tmp_path):
+    world = 3
+    res = _run(world, case, tmp_path)
+    for r in range(world - 1):
+        assert res[r]["raised"] == 6, res[r]  # DC_ERR_TIMEOUT
+        assert "stage of epoch 2" in res[r]["msg"], res[r]["msg"]
+        assert res[r]["seconds"] < 30.0, res[r]  # the bound, not the process group's default
+        assert res[r]["again"] == 6 and res[r]["again_seconds"] < 0.5, res[r]  # aborted: at once
