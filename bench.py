@@ -90,6 +90,13 @@ def parse_args(argv=None):
     ap.add_argument("--skew-modes", nargs="+", choices=["graph", "eager"], default=["graph", "eager"])
     ap.add_argument("--skew-trials", type=int, default=50)
     ap.add_argument("--skew-warmup", type=int, default=10)
+    ap.add_argument("--ipc", action="store_true",
+                    help="the staged all-gather across processes: one process per rank on this "
+                         "GPU, staging buffers shared by CUDA IPC, host handshakes (one JSON "
+                         "line per rank count and size)")
+    ap.add_argument("--ipc-ranks", nargs="+", type=int, default=[2, 4])
+    ap.add_argument("--ipc-sizes", nargs="+", type=int, default=[4096, 1 << 20, 4 << 20])
+    ap.add_argument("--ipc-handshakes", nargs="+", choices=["shm", "gloo"], default=["shm", "gloo"])
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
     ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
                     help="profiling helper: run one call REPS times and exit, e.g. "
@@ -98,7 +105,8 @@ def parse_args(argv=None):
                          "element off; BYTES per rank), "
                          "many:8:0:3 (the all_gather_many workload), manytiny:8:0:3 (120 tiny "
                          "tensors), gatherbulk:8:4194304:3 (the opt-in bulk-copy gather) or "
-                         "fused:8:4194304:3 (the staged protocol)")
+                         "fused:8:4194304:3 (the staged protocol), fill:8:33554432:2 (torch's "
+                         "write-only fill of P * BYTES, a comparator)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps must be >= 1 and --warmup >= 0")
@@ -477,10 +485,20 @@ def reductions_block(torch, dc, device, stream, flush, peak):
 
     us = statistics.median(timed_calls(torch, stream, flush, [fused], 5)[0])
     dc.check_device()
+    # its DRAM traffic is mostly writes (P*P*B of outputs + P*B of staging):
+    # torch's own fill of as many bytes (one buffer), timed the same way, is
+    # the write-only rate it is held against
+    fill = torch.empty(P * P * B, dtype=torch.uint8, device=device)
+    fill_us = statistics.median(timed_calls(torch, stream, flush, [fill.zero_], 5)[0])
+    del fill
     nbytes = 2 * P * B + 2 * P * P * B
     rows.append({"op": "fused_all_gather", "P": P, "count": B,
                  "shape": "4 MiB per rank, every rank's own output (stage, gather, complete)", "us": us,
-                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes,
+                 "written_bytes": P * P * B + P * B,
+                 "torch_fill_outputs_us": fill_us,
+                 "write_gbs": (P * P * B + P * B) / us / 1e3,
+                 "torch_fill_write_gbs": P * P * B / fill_us / 1e3})
     return rows
 
 
@@ -1027,6 +1045,112 @@ def run_crossover(args) -> int:
     return 0
 
 
+def _ipc_worker(rank, world, port, sizes, handshakes, steps, warmup, outfile):
+    """One rank of `--ipc` (a spawned process)."""
+    import torch
+    import torch.distributed as dist
+
+    import reduce_copy_rank_gb300 as dc
+    from reduce_copy_rank_gb300.ipc import CudaIpcTransport, StagedAllGather
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    lines = []
+    for hs, B in [(h, b) for h in handshakes for b in sizes]:
+        coll = StagedAllGather(None, B, CudaIpcTransport(), timeout=60.0, handshake=hs)
+        payloads = [W.random_bytes_device(W.seed_for(2, 950), q, B, "cuda") for q in range(world)]
+        expect = torch.cat(payloads)
+        out = torch.empty(world * B, dtype=torch.uint8, device="cuda")
+        for _ in range(warmup):
+            coll.all_gather(payloads[rank], out)
+        coll.seconds = dict.fromkeys(coll.seconds, 0.0)
+        dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            coll.all_gather(payloads[rank], out)
+        epoch_s = (time.perf_counter() - t0) / steps
+        exact = bool(torch.equal(out, expect))
+        # the gather kernel alone over the mapped staging buffers, one rank at a
+        # time: a CUDA graph of 20 back-to-back gathers (eager calls from
+        # Python would time the host's launch rate instead)
+        kernel_us = 0.0
+        for q in range(world):
+            dist.barrier()
+            if q == rank:
+                views = [b[:B] for b in coll.peers]
+                side = torch.cuda.Stream()
+                with torch.cuda.stream(side):
+                    dc.all_gather(views, out)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=side):
+                        for _ in range(20):
+                            dc.all_gather(views, out)
+                torch.cuda.synchronize()
+                times = []
+                for _ in range(5):
+                    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s_ev.record()
+                    g.replay()
+                    e_ev.record()
+                    torch.cuda.synchronize()
+                    times.append(s_ev.elapsed_time(e_ev) * 1e3 / 20)
+                kernel_us = statistics.median(times)
+                del g, views
+        dist.barrier()
+        vals = torch.tensor([epoch_s] + [coll.seconds[k] / steps for k in coll.seconds] + [kernel_us, float(not exact)],
+                            dtype=torch.float64)
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+        del payloads, expect, out
+        coll.close()
+        if rank == 0:
+            v = vals.tolist()
+            lines.append({
+                "metric": "staged all-gather across processes on one GPU: us per epoch",
+                "impl": "dc-ipc", "P": world, "bytes_per_rank": B, "epochs": steps, "warmup": warmup,
+                "us_per_epoch": v[0] * 1e6,
+                "phases_us": {k: x * 1e6 for k, x in zip(coll.seconds, v[1:5])},
+                "gather_kernel_us": v[5],
+                "gather_kernel_gbs": algorithmic_bytes(world, B) / (v[5] * 1e3) if v[5] > 0 else None,
+                "bit_exact": v[6] == 0.0,
+                "timing": "host clock around each epoch (max over ranks); the kernel by CUDA events "
+                          "around a graph of 20 back-to-back gathers over the mapped buffers, one rank "
+                          "at a time (median of 5 replays)",
+                "handshake": {"shm": "node-local shared-memory arrival counters, bounded",
+                              "gloo": "gloo monitored_barrier, bounded"}[hs],
+            })
+    if rank == 0:
+        with open(outfile, "w") as fh:
+            for ln in lines:
+                fh.write(json.dumps(ln) + "\n")
+    dist.destroy_process_group()
+
+
+def run_ipc(args) -> int:
+    """`--ipc`: the staged all-gather across processes, ranks as processes
+    sharing this GPU (CUDA IPC staging buffers, host handshakes)."""
+    import socket
+    import tempfile
+
+    import torch.multiprocessing as mp
+
+    steps = min(args.steps, 200)
+    warmup = max(args.warmup, 3)
+    for world in args.ipc_ranks:
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        with tempfile.TemporaryDirectory() as td:
+            path = os.path.join(td, "ipc.jsonl")
+            mp.spawn(_ipc_worker, args=(world, port, list(args.ipc_sizes), list(args.ipc_handshakes),
+                                        steps, warmup, path),
+                     nprocs=world, join=True)
+            with open(path) as fh:
+                for ln in fh:
+                    print(ln.strip(), flush=True)
+    return 0
+
+
 def run_skew(args) -> int:
     """Rank-skew calibration (the page "[Benchmark] Add all-reduce rank-skew
     calibration", section "Test Plan"): BF16 all_reduce of each shape per
@@ -1116,6 +1240,9 @@ def run_case(args) -> int:
         def fn():
             epoch[0] += 1
             dc.fused_all_gather(ins, stg, outs, ws, epoch[0])
+    elif op == "fill":  # torch's own write-only fill of P * BYTES bytes (a comparator)
+        buf = torch.empty(P * nbytes, dtype=torch.uint8, device=device)
+        fn = buf.zero_
     elif op == "reducescatter":
         ins = [torch.randn(nbytes // 2, device=device).to(torch.bfloat16) for _ in range(P)]
         outs = [torch.empty(nbytes // 2 // P, dtype=torch.bfloat16, device=device) for _ in range(P)]
@@ -1148,6 +1275,8 @@ def main(argv=None) -> int:
         return run_case(args)
     if args.skew:
         return run_skew(args)
+    if args.ipc:
+        return run_ipc(args)
     return run_dc(args)
 
 

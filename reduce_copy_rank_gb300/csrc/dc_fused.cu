@@ -147,13 +147,18 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
   if (threadIdx.x == 0 && in_bounds(&staged[r * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag))
     st_release_u32(&staged[r * kFusedMaxChunks + c], epoch);
 
-  // gather: thread 0 waits until every rank has published chunk c (its own
-  // rank first), then the CTA copies the P staged chunks without a barrier
-  // between them (a barrier per peer drained the loads in flight each time)
+  // gather: thread 0 waits until every rank has published chunk c, then the
+  // CTA copies the P staged chunks without a barrier between them (a barrier
+  // per peer drained the loads in flight each time).  Peers are taken in the
+  // order c, c+1, ... (mod P), the same for every rank: the P CTAs of chunk c
+  // read staging_q's chunk at about the same time, while it is in L2 (in a
+  // per-rank order the P reads of one chunk spread over the whole gather and
+  // the output traffic evicted the chunk in between).
+  const uint32_t q0 = c % P;
   if (threadIdx.x == 0) {
     bool ok = true;
     for (uint32_t i = 0; i < P && ok; ++i) {
-      const uint32_t q = r + i < P ? r + i : r + i - P;
+      const uint32_t q = q0 + i < P ? q0 + i : q0 + i - P;
       ok = in_bounds(&staged[q * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag) &&
            wait_flag(&staged[q * kFusedMaxChunks + c], epoch, p.wait_ns);
       if (!ok) record_fault(1, r, q, c, epoch);
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
   __syncthreads();
   if (!s_ok[0]) return;
   for (uint32_t i = 0; i < P; ++i) {
-    const uint32_t q = r + i < P ? r + i : r + i - P;
+    const uint32_t q = q0 + i < P ? q0 + i : q0 + i - P;
     copy_chunk<true, 8>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
                         reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n,
                         p.staging[q], p.staging[q] + p.bytes, p.out[r], p.out[r] + P * p.bytes,

@@ -18,17 +18,29 @@ buffers; no kernel ever waits for another process.  Each step is
 
   stage:    copy the local payload into the local staging buffer and wait for
             the copy to finish;
-  barrier:  every rank has staged this epoch (a monitored barrier of the
-            process group, bounded by `timeout`);
+  barrier:  every rank has staged this epoch (bounded by `timeout`);
   gather:   dc_all_gather over the P staging buffers into the local output,
             wait for it to finish;
   barrier:  every rank has read every staging buffer (same bound), so the
             next epoch may overwrite them.
 
+The barriers are either a monitored barrier of the process group
+(handshake="gloo") or arrival counters in node-local shared memory
+(handshake="shm": one 64-bit word per rank, polled; a few microseconds instead
+of the process group's message round trips).  CUDA IPC only maps memory
+between processes of one node, so the node-local handshake loses nothing
+there, and it is the CUDA transport's default.  It is correct for payloads in
+device memory on any host: a rank stores its counter only after its stream
+synchronisation returned, so a peer that sees the counter launches its reads
+after the copy finished.  For host payloads (SharedMemoryTransport) the
+payload's stores would have to become visible before the counter's, which
+weakly ordered hosts do not promise, so that transport defaults to gloo.
+
 A barrier that runs out (a rank that never arrives, or died) raises
 DCError(DC_ERR_TIMEOUT) naming the epoch and step; the collective is then
-aborted: every later call raises at once, before it touches a peer's buffer,
-and close() releases the mappings.  Signatures (world size, bytes per rank,
+aborted: every later call raises at once, before it touches a peer's buffer.
+close() drops the mappings of the peers' buffers, waits until every rank has
+(within the bound), then releases the own buffer.  Signatures (world size, bytes per rank,
 transport) are compared once, when the collective is built: a mismatch raises
 DCError(DC_ERR_INVALID) on every rank.
 
@@ -41,43 +53,139 @@ must support monitored_barrier (gloo).
 from __future__ import annotations
 
 import datetime
+import os
+import time
 
-from . import DCError, STATUS
+from . import DCError
 
 _TIMEOUT = 6  # DC_ERR_TIMEOUT
 _INVALID = 1  # DC_ERR_INVALID
 
 
+class _SharedBytes:
+    """A file in node-local shared memory (/dev/shm, a tmpfs; the temporary
+    directory where there is none) mapped into this process.  The creator
+    names it and unlinks it; the others open it by path."""
+
+    def __init__(self, size: int = 0, path: str | None = None):
+        import mmap
+        import tempfile
+        import uuid
+
+        self.owner = path is None
+        if self.owner:
+            d = "/dev/shm" if os.path.isdir("/dev/shm") else tempfile.gettempdir()
+            path = os.path.join(d, f"dc_{uuid.uuid4().hex}")
+            fd = os.open(path, os.O_CREAT | os.O_EXCL | os.O_RDWR, 0o600)
+            os.ftruncate(fd, max(size, 8))
+        else:
+            fd = os.open(path, os.O_RDWR)
+        try:
+            self.size = os.fstat(fd).st_size
+            self.mm = mmap.mmap(fd, self.size)
+        finally:
+            os.close(fd)
+        self.path = path
+
+    def array(self, dtype, count: int):
+        import numpy as np
+
+        return np.frombuffer(self.mm, dtype=dtype, count=count)
+
+    def unlink(self) -> None:
+        """Remove the name (creator only).  The mappings stay valid, so once
+        every process has opened the file it is unlinked: nothing is left
+        behind even if a process dies."""
+        if self.owner:
+            self.owner = False
+            try:
+                os.unlink(self.path)
+            except FileNotFoundError:
+                pass
+
+    def close(self) -> None:
+        try:
+            self.mm.close()
+        except BufferError:  # an array still views it: the mapping goes with the last one
+            pass
+        self.unlink()
+
+
+class ShmHandshake:
+    """Node-local barrier: one 64-bit arrival counter per rank in shared
+    memory.  wait() stores the caller's next sequence number in its word,
+    then polls until every word has reached it (spinning briefly, then
+    sleeping 20 us between polls), for at most `timeout` seconds; it returns
+    the ranks that had not arrived, or [] once all have.  A rank is at most
+    one barrier ahead of any other, so `>=` is the arrival test."""
+
+    kind = "shm"
+
+    def __init__(self, group, rank: int, world: int, timeout: float):
+        import numpy as np
+        import torch.distributed as dist
+
+        self.rank, self.world, self.timeout = rank, world, timeout
+        mem = _SharedBytes(8 * world) if rank == 0 else None
+        paths = [None] * world
+        dist.all_gather_object(paths, mem.path if mem else None, group=group)
+        self._mem = mem if mem else _SharedBytes(path=paths[0])
+        self.slots = self._mem.array(np.uint64, world)
+        self.seq = 0
+
+    def wait(self) -> list:
+        self.seq += 1
+        seq = self.seq
+        slots = self.slots
+        slots[self.rank] = seq
+        t0 = time.perf_counter()
+        polls = 0
+        while int(slots.min()) < seq:
+            polls += 1
+            if polls > 200:
+                time.sleep(20e-6)
+            if time.perf_counter() - t0 > self.timeout:
+                return [q for q in range(self.world) if int(slots[q]) < seq]
+        return []
+
+    def opened_by_all(self) -> None:
+        self._mem.unlink()
+
+    def close(self) -> None:
+        if self._mem is None:
+            return
+        self.slots = None
+        self._mem.close()
+        self._mem = None
+
+
 class SharedMemoryTransport:
-    """Host buffers in POSIX shared memory (multiprocessing.shared_memory);
-    stage and gather are numpy copies.  For the protocol's tests."""
+    """Host buffers in node-local shared memory; stage and gather are numpy
+    copies.  For the protocol's tests on machines without a GPU."""
 
     kind = "shared-memory"
+    default_handshake = "gloo"
 
     def __init__(self):
         self._owned = []
         self._opened = []
 
     def alloc(self, nbytes: int):
-        from multiprocessing import shared_memory
-
         import numpy as np
 
-        shm = shared_memory.SharedMemory(create=True, size=max(nbytes, 1))
-        self._owned.append(shm)
-        return np.ndarray((nbytes,), dtype=np.uint8, buffer=shm.buf), shm.name
+        mem = _SharedBytes(nbytes)
+        self._owned.append(mem)
+        return mem.array(np.uint8, nbytes), mem.path
 
     def export(self, buf) -> object:
         return buf[1]
 
     def open(self, desc):
-        from multiprocessing import shared_memory
-
         import numpy as np
 
-        shm = shared_memory.SharedMemory(name=desc)
-        self._opened.append(shm)
-        return np.ndarray((shm.size,), dtype=np.uint8, buffer=shm.buf), desc
+        mem = _SharedBytes(path=desc)
+        self._opened.append(mem)
+        return mem.array(np.uint8, mem.size), desc
 
     def stage(self, buf, payload) -> None:
         buf[0][: payload.nbytes] = payload.view("u1").reshape(-1)
@@ -86,13 +194,19 @@ class SharedMemoryTransport:
         for q, b in enumerate(bufs):
             out[q * nbytes:(q + 1) * nbytes] = b[0][:nbytes]
 
-    def close(self) -> None:
-        for shm in self._opened:
-            shm.close()
-        for shm in self._owned:
-            shm.close()
-            shm.unlink()
-        self._opened, self._owned = [], []
+    def opened_by_all(self) -> None:
+        for mem in self._owned:
+            mem.unlink()
+
+    def close_peers(self) -> None:
+        for mem in self._opened:
+            mem.close()
+        self._opened = []
+
+    def release(self) -> None:
+        for mem in self._owned:
+            mem.close()
+        self._owned = []
 
 
 class CudaIpcTransport:
@@ -103,6 +217,7 @@ class CudaIpcTransport:
     other's memory (here: processes on one GPU)."""
 
     kind = "cuda-ipc"
+    default_handshake = "shm"
 
     def __init__(self, device=None):
         import torch
@@ -135,8 +250,16 @@ class CudaIpcTransport:
         all_gather([b[:nbytes] for b in bufs], out.reshape(-1).view(self.torch.uint8))
         self.torch.cuda.current_stream().synchronize()
 
-    def close(self) -> None:
+    def opened_by_all(self) -> None:
+        pass
+
+    def close_peers(self) -> None:
         self._opened = []
+        self.torch.cuda.synchronize()
+
+    def release(self) -> None:
+        # frees this process's shared blocks once every peer has dropped them
+        self.torch.cuda.ipc_collect()
 
 
 class StagedAllGather:
@@ -145,7 +268,7 @@ class StagedAllGather:
     bytes).  Payloads and outputs are contiguous byte buffers of the
     transport's kind (numpy arrays or CUDA tensors)."""
 
-    def __init__(self, group, nbytes: int, transport, timeout: float = 5.0):
+    def __init__(self, group, nbytes: int, transport, timeout: float = 5.0, handshake: str | None = None):
         import torch.distributed as dist
 
         self.dist, self.group, self.nbytes, self.transport = dist, group, int(nbytes), transport
@@ -154,48 +277,95 @@ class StagedAllGather:
         self.timeout = datetime.timedelta(seconds=timeout)
         self.epoch = 0
         self.aborted = None
-        sig = {"world": self.world, "nbytes": self.nbytes, "transport": transport.kind}
+        self.closed = False
+        # host seconds spent in each step, summed over the epochs
+        self.seconds = dict.fromkeys(("stage", "stage_barrier", "gather", "complete_barrier"), 0.0)
+        self.handshake = transport.default_handshake if handshake is None else handshake
+        if self.handshake not in ("gloo", "shm"):
+            raise ValueError(f"handshake must be 'gloo' or 'shm', not {self.handshake!r}")
+        self._hs = None
+        sig = {"world": self.world, "nbytes": self.nbytes, "transport": transport.kind,
+               "handshake": self.handshake}
         sigs = [None] * self.world
         dist.all_gather_object(sigs, sig, group=group)
         if any(s != sig for s in sigs):
             raise DCError(_INVALID, f"ranks disagree on the collective: {sigs}")
+        if self.handshake == "shm":
+            self._hs = ShmHandshake(group, self.rank, self.world, timeout)
         self.local = transport.alloc(self.nbytes)
+        # one descriptor per peer (CUDA IPC counts the references it hands
+        # out: one export per process that opens it)
+        mine = [None if q == self.rank else transport.export(self.local) for q in range(self.world)]
         descs = [None] * self.world
-        dist.all_gather_object(descs, transport.export(self.local), group=group)
-        self.peers = [self.local if q == self.rank else transport.open(d) for q, d in enumerate(descs)]
+        dist.all_gather_object(descs, mine, group=group)
+        self.peers = [self.local if q == self.rank else transport.open(descs[q][self.rank])
+                      for q in range(self.world)]
         self._barrier("setup")
+        # every rank has opened every shared buffer: their names can go
+        self.transport.opened_by_all()
+        if self._hs is not None:
+            self._hs.opened_by_all()
 
-    def _barrier(self, step: str) -> None:
+    def _wait_all(self) -> str | None:
+        """One barrier; None once every rank arrived, else what went wrong."""
+        if self._hs is not None:
+            missing = self._hs.wait()
+            return f"ranks {missing} did not arrive within {self.timeout.total_seconds()} s" if missing else None
         try:
             self.dist.monitored_barrier(group=self.group, timeout=self.timeout, wait_all_ranks=True)
         except RuntimeError as e:
-            self.aborted = f"{step} of epoch {self.epoch} on rank {self.rank}: {e}"
-            raise DCError(_TIMEOUT, self.aborted) from e
+            return str(e)
+        return None
+
+    def _barrier(self, step: str) -> None:
+        err = self._wait_all()
+        if err is not None:
+            self.aborted = f"{step} of epoch {self.epoch} on rank {self.rank}: {err}"
+            raise DCError(_TIMEOUT, self.aborted)
 
     def all_gather(self, payload, out):
         """Stage, barrier, gather, barrier (see the module docstring)."""
         if self.aborted:
             raise DCError(_TIMEOUT, "the collective was aborted: " + self.aborted)
+        if self.closed:
+            raise ValueError("the collective is closed")
         if payload.nbytes != self.nbytes or out.nbytes != self.world * self.nbytes:
             raise ValueError(f"need a payload of {self.nbytes} bytes and an output of "
                              f"{self.world * self.nbytes}")
         self.epoch += 1
+        t0 = time.perf_counter()
         self.transport.stage(self.local, payload)
+        t1 = time.perf_counter()
         self._barrier("stage")
+        t2 = time.perf_counter()
         self.transport.gather(self.peers, out, self.nbytes)
+        t3 = time.perf_counter()
         self._barrier("complete")
+        t4 = time.perf_counter()
+        sec = self.seconds
+        sec["stage"] += t1 - t0
+        sec["stage_barrier"] += t2 - t1
+        sec["gather"] += t3 - t2
+        sec["complete_barrier"] += t4 - t3
         return out
 
     def close(self) -> None:
-        """Release the peers' mappings, then (if the collective is healthy)
-        wait until every rank has, so that no buffer is freed while mapped."""
+        """Drop the peers' mappings, wait (if the collective is healthy, within
+        the bound) until every rank has dropped them, then release the own
+        staging buffer.  Idempotent; later calls of all_gather raise."""
+        if self.closed:
+            return
+        self.closed = True
         self.peers = []
-        self.transport.close()
+        self.transport.close_peers()
         if not self.aborted:
-            try:
-                self.dist.monitored_barrier(group=self.group, timeout=self.timeout, wait_all_ranks=True)
-            except RuntimeError:
-                pass
+            err = self._wait_all()
+            if err is not None:
+                self.aborted = f"close on rank {self.rank}: {err}"
+        self.local = None
+        self.transport.release()
+        if self._hs is not None:
+            self._hs.close()
 
 
-__all__ = ["StagedAllGather", "CudaIpcTransport", "SharedMemoryTransport", "STATUS"]
+__all__ = ["StagedAllGather", "CudaIpcTransport", "SharedMemoryTransport", "ShmHandshake"]

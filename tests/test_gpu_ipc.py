@@ -4,8 +4,9 @@ processes map through CUDA IPC, the gather the library's kernel over the
 mapped buffers.  Every rank's output is compared with the oracle, bit for bit,
 over several epochs and at aligned, unaligned and multi-tile sizes.
 
-No kernel waits for another process: the handshakes are host barriers of a
-gloo process group, so the processes' launches never depend on one another.
+No kernel waits for another process: the handshakes are host barriers (the
+node-local shared-memory counters, and the gloo process group's monitored
+barrier), so the processes' launches never depend on one another.
 The failure cases (a rank that never arrives or dies) are covered on CPU.
 
 Page, by title: "perf(cuda): vectorize the deterministic all-gather copy and
@@ -38,7 +39,7 @@ def _port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, outdir):
+def _worker(rank, world, port, handshake, outdir):
     import torch
     import torch.distributed as dist
 
@@ -52,7 +53,7 @@ def _worker(rank, world, port, outdir):
     try:
         n0 = dc.launch_count()
         for si, B in enumerate(SIZES):
-            coll = StagedAllGather(None, B, CudaIpcTransport(), timeout=30.0)
+            coll = StagedAllGather(None, B, CudaIpcTransport(), timeout=30.0, handshake=handshake)
             for epoch in range(1, 4):
                 payloads = [W.random_bytes(W.seed_for(3, 900 + 10 * si + epoch), q, B)
                             for q in range(world)]
@@ -83,11 +84,12 @@ def _compute_mode_default():
     return out in ("", "Default")
 
 
+@pytest.mark.parametrize("handshake", ["shm", "gloo"])
 @pytest.mark.parametrize("world", [2, 3])
-def test_staged_all_gather_over_cuda_ipc(world, tmp_path):
+def test_staged_all_gather_over_cuda_ipc(world, handshake, tmp_path):
     if not _compute_mode_default():
         pytest.skip("GPU 0 is not in the default compute mode: one process per GPU only")
-    mp.spawn(_worker, args=(world, _port(), str(tmp_path)), nprocs=world, join=True)
+    mp.spawn(_worker, args=(world, _port(), handshake, str(tmp_path)), nprocs=world, join=True)
     for r in range(world):
         res = json.load(open(tmp_path / f"r{r}.json"))
         assert "error" not in res, res

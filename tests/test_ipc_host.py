@@ -34,7 +34,7 @@ def _port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, case, outdir):
+def _worker(rank, world, port, case, handshake, outdir):
     import torch.distributed as dist
 
     import reduce_copy_rank_gb300 as dc
@@ -47,12 +47,13 @@ def _worker(rank, world, port, case, outdir):
     try:
         if case == "mismatch":
             try:
-                StagedAllGather(None, B + (rank == 1), SharedMemoryTransport(), timeout=2.0)
+                StagedAllGather(None, B + (rank == 1), SharedMemoryTransport(), timeout=2.0,
+                                handshake=handshake)
                 res["raised"] = None
             except dc.DCError as e:
                 res["raised"] = e.status
             return
-        coll = StagedAllGather(None, B, SharedMemoryTransport(), timeout=2.0)
+        coll = StagedAllGather(None, B, SharedMemoryTransport(), timeout=2.0, handshake=handshake)
         if case == "parity":
             res["ok"] = []
             for epoch in range(1, 4):
@@ -61,6 +62,12 @@ def _worker(rank, world, port, case, outdir):
                 coll.all_gather(payloads[rank], out)
                 res["ok"].append(bool(np.array_equal(out, oracle.all_gather(payloads))))
             coll.close()
+            coll.close()  # idempotent
+            try:
+                coll.all_gather(payloads[rank], out)
+                res["after_close"] = None
+            except ValueError:
+                res["after_close"] = "ValueError"
         elif case in ("absent", "dead"):
             payload = W.random_bytes(W.seed_for(2, 810), rank, B)
             out = np.zeros(world * B, dtype=np.uint8)
@@ -84,13 +91,14 @@ def _worker(rank, world, port, case, outdir):
             except dc.DCError as e:
                 res["again"] = e.status
             res["again_seconds"] = time.time() - t1
+            coll.close()  # aborted: releases without waiting for the missing rank
     finally:
         with open(os.path.join(outdir, f"r{rank}.json"), "w") as fh:
             json.dump(res, fh)
 
 
-def _run(world, case, tmp_path):
-    mp.spawn(_worker, args=(world, _port(), case, str(tmp_path)), nprocs=world, join=True)
+def _run(world, case, tmp_path, handshake="gloo"):
+    mp.spawn(_worker, args=(world, _port(), case, handshake, str(tmp_path)), nprocs=world, join=True)
     out = {}
     for r in range(world):
         p = tmp_path / f"r{r}.json"
@@ -99,25 +107,39 @@ def _run(world, case, tmp_path):
     return out
 
 
+# The shared-memory handshake with host payloads relies on the payload's
+# stores becoming visible before the counter's: true on x86 (where these
+# tests run), not promised on weakly ordered hosts, where that transport
+# defaults to the gloo handshake.  With device payloads (the CUDA transport)
+# it holds on any host.
+HANDSHAKES = ["gloo", "shm"]
+
+
+@pytest.mark.parametrize("handshake", HANDSHAKES)
 @pytest.mark.parametrize("world", [2, 3])
-def test_parity_over_epochs(world, tmp_path):
-    res = _run(world, "parity", tmp_path)
+def test_parity_over_epochs(world, handshake, tmp_path):
+    res = _run(world, "parity", tmp_path, handshake)
     assert len(res) == world
     for r in range(world):
         assert res[r]["ok"] == [True, True, True], res[r]
+        assert res[r]["after_close"] == "ValueError", res[r]
 
 
-def test_signature_mismatch_raises_on_every_rank(tmp_path):
-    res = _run(2, "mismatch", tmp_path)
+@pytest.mark.parametrize("handshake", HANDSHAKES)
+def test_signature_mismatch_raises_on_every_rank(handshake, tmp_path):
+    res = _run(2, "mismatch", tmp_path, handshake)
     assert [res[r]["raised"] for r in range(2)] == [1, 1]  # DC_ERR_INVALID
 
 
+@pytest.mark.parametrize("handshake", HANDSHAKES)
 @pytest.mark.parametrize("case", ["absent", "dead"])
-def test_rank_that_never_arrives_times_out(case, tmp_path):
+def test_rank_that_never_arrives_times_out(case, handshake, tmp_path):
     world = 3
-    res = _run(world, case, tmp_path)
+    res = _run(world, case, tmp_path, handshake)
     for r in range(world - 1):
         assert res[r]["raised"] == 6, res[r]  # DC_ERR_TIMEOUT
         assert "stage of epoch 2" in res[r]["msg"], res[r]["msg"]
+        if handshake == "shm":
+            assert f"ranks [{world - 1}] did not arrive" in res[r]["msg"], res[r]["msg"]
         assert res[r]["seconds"] < 30.0, res[r]  # the bound, not the process group's default
         assert res[r]["again"] == 6 and res[r]["again_seconds"] < 0.5, res[r]  # aborted: at once
