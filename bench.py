@@ -248,6 +248,32 @@ class ClockSampler:
 
 # ------------------------------------------------------- the oracle arm ---
 
+_ARM_PARTS = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2",
+              "0xd4f": "Neoverse-V2", "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model as /proc/cpuinfo gives it (x86: the model name;
+    Arm: implementer and part, named where the part is a known Neoverse)."""
+    import platform
+
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                k, _, v = ln.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    part = fields.get("CPU part")
+    if part:
+        return (f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {part}"
+                + (f" ({_ARM_PARTS[part]})" if part in _ARM_PARTS else ""))
+    return platform.processor() or platform.machine()
+
+
 def cpu_oracle_sample(seconds: float):
     """Time the oracle (single-threaded C byte-loop gather) on the host over
     whole passes of the sweep until `seconds` have elapsed (at least one)."""
@@ -267,6 +293,7 @@ def cpu_oracle_sample(seconds: float):
         if el >= seconds:
             break
     return {"value": step_bytes * passes / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{passes} full passes of the 14-gather sweep ({step_bytes} algorithmic bytes "
                       f"each) through the single-threaded C oracle, {el:.1f} s"}
 
@@ -300,7 +327,7 @@ def cpu_oracle_threaded(seconds: float):
         t.join()
     el = time.perf_counter() - t0
     return {"value": step_bytes * sum(done) / el / 1e9, "unit": UNIT, "cores": nthreads,
-            "kind": "oracle, one thread per core",
+            "kind": "oracle, one thread per core", "cpu_model": cpu_model(),
             "sample": f"{sum(done)} full passes of the 14-gather sweep over {nthreads} threads, "
                       f"{el:.1f} s"}
 
@@ -332,6 +359,7 @@ def run_reference(args) -> int:
         "config": workload_config(int(os.environ.get("WORLD_SIZE", "1"))),
         "timing": "host oracle on the host cores: whole passes of the sweep, wall clock",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"{args.steps} full passes of the 14-gather sweep through the "
                                    "single-threaded C oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
