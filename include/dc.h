@@ -161,6 +161,34 @@ dc_status_t dc_reduce_scatter(const void *const *in_ptrs, void *const *out_ptrs,
                               dc_stream_t stream);
 
 /*
+ * dc_reduce -- one rank's share of a reduction: the P inputs folded into ONE
+ * output, as dc_all_reduce / dc_reduce_scatter fold them:
+ *
+ *   out[i] = round(fold over q = 0..P-1 of in_ptrs[q][in_offset + i]),  i < count
+ *
+ * When every rank is its own process ([PR491] author's replies: the
+ * collective's ranks exchange payloads through buffers their peers map),
+ * rank r computes only its own output: its all_reduce output (in_offset 0,
+ * count = elements per rank) or its reduce_scatter shard (in_offset =
+ * r * count_per_shard, count = count_per_shard), from the P mapped buffers.
+ * The result is bit-identical to the same rank's output of dc_all_reduce /
+ * dc_reduce_scatter.
+ *
+ * in_ptrs: host array of P device pointers (read during the call), each to
+ *          at least in_offset + count elements; aligned to the element size
+ *          (DC_ERR_ALIGN).  Inputs may overlap each other.
+ * out:     device pointer to count elements, aligned to the element size.
+ *          It may be exactly the range of one input that is read (in_ptrs[q]
+ *          + in_offset elements: in place); any other overlap with the
+ *          elements read is DC_ERR_OVERLAP.
+ * count:   0 is a successful no-op.  in_offset + count must not overflow
+ *          (DC_ERR_INVALID).
+ * One kernel on `stream`; nothing allocated, no synchronisation.
+ */
+dc_status_t dc_reduce(const void *const *in_ptrs, int P, size_t in_offset, size_t count, void *out,
+                      dc_dtype_t dtype, dc_order_t order, dc_stream_t stream);
+
+/*
  * dc_all_reduce_many / dc_reduce_scatter_many -- T independent reductions of
  * the same P, type and order in one launch ([PR491] "Tests":
  * reduce_scatter_many(..., outs=) with caller-given outputs).

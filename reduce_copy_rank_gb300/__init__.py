@@ -25,7 +25,7 @@ from typing import Sequence
 
 __all__ = [
     "DCError", "LibraryMissing", "all_gather", "all_gather_many", "all_reduce",
-    "reduce_scatter", "all_reduce_many", "reduce_scatter_many", "inject_delay", "check_device",
+    "reduce_scatter", "reduce", "all_reduce_many", "reduce_scatter_many", "inject_delay", "check_device",
     "fused_all_gather", "fused_workspace", "fused_reset",
     "set_option",
     "get_option",
@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
         L.dc_reduce_scatter_bf16.argtypes = [A, A, I, Z, _VP]
         L.dc_all_reduce.argtypes = [A, A, I, Z, I, I, _VP]
         L.dc_reduce_scatter.argtypes = L.dc_all_reduce.argtypes
+        L.dc_reduce.argtypes = [A, I, Z, Z, _VP, I, I, _VP]
         L.dc_all_reduce_many.argtypes = [A, A, A, I, I, I, I, _VP]
         L.dc_reduce_scatter_many.argtypes = L.dc_all_reduce_many.argtypes
         L.dc_inject_delay_ns.argtypes = [ctypes.c_ulonglong, _VP]
@@ -95,7 +96,7 @@ def lib() -> ctypes.CDLL:
         L.dc_fused_reset.argtypes = [_VP, I, _VP]
         L.dc_fused_all_gather_static.argtypes = [A, A, I, Z, _VP]
         for f in ("dc_all_gather", "dc_all_gather_many", "dc_all_reduce_bf16",
-                  "dc_reduce_scatter_bf16", "dc_all_reduce", "dc_reduce_scatter",
+                  "dc_reduce_scatter_bf16", "dc_all_reduce", "dc_reduce_scatter", "dc_reduce",
                   "dc_all_reduce_many", "dc_reduce_scatter_many", "dc_inject_delay_ns",
                   "dc_check_device", "dc_fused_all_gather", "dc_fused_reset",
                   "dc_fused_all_gather_static"):
@@ -179,6 +180,12 @@ def dc_reduce_scatter(in_ptrs: Sequence[int], out_ptrs: Sequence[int], P: int,
                       count_per_shard: int, dtype: int = 0, order: int = 0, stream: int = 0) -> int:
     a, b = _u64(in_ptrs), _u64(out_ptrs)
     return lib().dc_reduce_scatter(_addr(a), _addr(b), P, count_per_shard, dtype, order, stream)
+
+
+def dc_reduce(in_ptrs: Sequence[int], P: int, in_offset: int, count: int, out: int,
+              dtype: int = 0, order: int = 0, stream: int = 0) -> int:
+    a = _u64(in_ptrs)
+    return lib().dc_reduce(_addr(a), P, in_offset, count, out, dtype, order, stream)
 
 
 def dc_all_reduce_many(in_ptrs: Sequence[int], out_ptrs: Sequence[int], counts: Sequence[int],
@@ -474,6 +481,39 @@ def reduce_scatter(inputs: Sequence, outputs: Sequence, order: str = "linear", s
     _check(lib().dc_reduce_scatter(_addr(a), _addr(b), P, C, _dtype_code(inputs[0]),
                                    _order_code(order), _stream_handle(stream)))
     return outputs
+
+
+def reduce(inputs: Sequence, out, offset: int = 0, order: str = "linear", stream=None):
+    """One rank's share of a reduction: ``out`` (n elements) receives the
+    fixed-order fold of elements ``offset .. offset+n-1`` of every input, as
+    all_reduce / reduce_scatter compute them (their rank-r output, for
+    offset 0 or r*n).  For a rank that is its own process and reads its peers'
+    buffers.  ``out`` may be exactly that range of one input.  Returns out."""
+    P = len(inputs)
+    if P == 0:
+        raise ValueError("need at least one input")
+    dt = out.dtype
+    _device_tensor(out, "out")
+    n = out.numel()
+    if offset < 0:
+        raise ValueError(f"offset must be >= 0 (got {offset})")
+    dev = _cur_dev()
+    if out.get_device() != dev:
+        _wrong_device("out", out, dev)
+    ptrs = []
+    for i, t in enumerate(inputs):
+        _device_tensor(t, f"inputs[{i}]")
+        if t.dtype != dt:
+            raise ValueError(f"inputs[{i}] has dtype {t.dtype}, expected {dt}")
+        if t.numel() < offset + n:
+            raise ValueError(f"inputs[{i}] has {t.numel()} elements, fewer than offset + n = {offset + n}")
+        if t.get_device() != dev:
+            _wrong_device(f"inputs[{i}]", t, dev)
+        ptrs.append(t.data_ptr())
+    a = array.array("Q", ptrs)
+    _check(lib().dc_reduce(_addr(a), P, offset, n, out.data_ptr(), _dtype_code(out), _order_code(order),
+                           _stream_handle(stream)))
+    return out
 
 
 def _many(inputs_per_tensor, outputs_per_tensor, scatter: bool):

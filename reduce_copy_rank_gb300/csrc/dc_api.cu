@@ -626,11 +626,39 @@ dc_status_t check_reduce_overlaps(std::vector<Range>& v, bool scatter, const uin
   return DC_OK;
 }
 
+// A job's units: 16-byte units anchored at its outputs need every output at
+// the same address mod 16; inputs at that offset too load whole vectors,
+// inputs at other offsets are realigned.  Outputs that disagree: one element
+// per unit.  Sets head, flags and nunits of J (in0, out0, nout, in_off and
+// count already set); returns nunits.
+template <class Params>
+uint64_t classify_reduce_job(const Params& prm, ReduceJob& J, int P, int dtype) {
+  const int es = esize_of(dtype), epv = epv_of(dtype);
+  const uint64_t n = J.count;
+  const uint64_t off = J.in_off * es;
+  const uint32_t o = static_cast<uint32_t>(prm.ptr[J.out0] & 15u);
+  bool outs_agree = true, ins_agree = true;
+  for (int m = 0; m < J.nout; ++m) outs_agree = outs_agree && (prm.ptr[J.out0 + m] & 15u) == o;
+  for (int q = 0; q < P; ++q) ins_agree = ins_agree && ((prm.ptr[J.in0 + q] + off) & 15u) == o;
+  if (outs_agree) {
+    uint64_t head = ((16u - o) & 15u) / es;
+    if (head > n) head = n;
+    const uint64_t rest = n - head;
+    J.head = static_cast<uint8_t>(head);
+    J.flags = ins_agree ? kJobVec : (kJobVec | kJobRealign);
+    J.nunits = (head ? 1 : 0) + rest / epv + ((rest % epv) ? 1 : 0);
+  } else {
+    J.head = 0;
+    J.flags = 0;
+    J.nunits = n;
+  }
+  return J.nunits;
+}
+
 template <class Params>
 void fill_reduce(Params& prm, int P, int dtype, bool scatter, const std::vector<int>& live,
                  const void* const* in_ptrs, void* const* out_ptrs, const size_t* counts) {
   const int nz = static_cast<int>(live.size());
-  const int es = esize_of(dtype), epv = epv_of(dtype);
   prm.P = P;
   for (int k = 0; k < nz; ++k) {
     const int t = live[k];
@@ -651,28 +679,8 @@ void fill_reduce(Params& prm, int P, int dtype, bool scatter, const std::vector<
       J.nout = static_cast<uint16_t>(scatter ? 1 : P);
       J.in_off = scatter ? static_cast<uint64_t>(r) * n : 0;
       J.count = n;
-      // 16-byte units are anchored at the outputs: they need every output at
-      // the same address mod 16; inputs at that offset too load whole
-      // vectors, inputs at other offsets are realigned.
-      const uint64_t off = J.in_off * es;
-      const uint32_t o = static_cast<uint32_t>(prm.ptr[J.out0] & 15u);
-      bool outs_agree = true, ins_agree = true;
-      for (int m = 0; m < J.nout; ++m) outs_agree = outs_agree && (prm.ptr[J.out0 + m] & 15u) == o;
-      for (int q = 0; q < P; ++q) ins_agree = ins_agree && ((prm.ptr[J.in0 + q] + off) & 15u) == o;
-      if (outs_agree) {
-        uint64_t head = ((16u - o) & 15u) / es;
-        if (head > n) head = n;
-        const uint64_t rest = n - head;
-        J.head = static_cast<uint8_t>(head);
-        J.flags = ins_agree ? kJobVec : (kJobVec | kJobRealign);
-        J.nunits = (head ? 1 : 0) + rest / epv + ((rest % epv) ? 1 : 0);
-      } else {
-        J.head = 0;
-        J.flags = 0;
-        J.nunits = n;
-      }
       J.ufirst = units;
-      units += J.nunits;
+      units += classify_reduce_job(prm, J, P, dtype);
     }
   }
   prm.njobs = nj;
@@ -803,6 +811,57 @@ dc_status_t reduce_entry(const void* const* in_ptrs, void* const* out_ptrs, cons
   return launch_reduce_plan(prm, 2, dtype, order, in_bytes_per_rank, stream, what);
 }
 
+// One rank's share of a reduction: P inputs folded into one output,
+// element i of the output from element in_offset + i of every input.
+dc_status_t reduce_one_entry(const void* const* in_ptrs, int P, uint64_t in_offset, uint64_t count,
+                             void* out, int dtype, int order, cudaStream_t stream) {
+  read_env_once();
+  if (P < 1 || P > kMaxRanks) return fail(DC_ERR_INVALID, "P = %d is outside 1..%d", P, kMaxRanks);
+  if (dtype < kBF16 || dtype > kF32) return fail(DC_ERR_INVALID, "unknown element type %d", dtype);
+  if (order != kOrderLinear && order != kOrderTree)
+    return fail(DC_ERR_INVALID, "unknown summation order %d", order);
+  if (count == 0) return ok();
+  if (!in_ptrs || !out) return fail(DC_ERR_INVALID, "in_ptrs and out must not be NULL");
+  const uint64_t es = static_cast<uint64_t>(esize_of(dtype));
+  if (in_offset > UINT64_MAX / es || count > UINT64_MAX / es - in_offset)
+    return fail(DC_ERR_INVALID, "in_offset + count overflows");
+  const uint64_t o = reinterpret_cast<uint64_t>(out);
+  const uint64_t out_b = count * es, skip = in_offset * es;
+  if (o & (es - 1))
+    return fail(DC_ERR_ALIGN, "out: %s pointers must be %d-byte aligned", dtype_name(dtype), static_cast<int>(es));
+  if (o + out_b < o) return fail(DC_ERR_INVALID, "output wraps around the address space");
+  std::vector<Range> ranges;
+  ranges.push_back(Range{o, o + out_b, 0, 0, true});
+  for (int q = 0; q < P; ++q) {
+    const uint64_t i = reinterpret_cast<uint64_t>(in_ptrs[q]);
+    if (!i) return fail(DC_ERR_INVALID, "in_ptrs[%d] is NULL", q);
+    if (i & (es - 1))
+      return fail(DC_ERR_ALIGN, "in_ptrs[%d]: %s pointers must be %d-byte aligned", q, dtype_name(dtype),
+                  static_cast<int>(es));
+    if (i + skip < i || i + skip + out_b < i + skip) return fail(DC_ERR_INVALID, "input %d wraps around", q);
+    // the elements read: [in_q + skip, in_q + skip + out_b); the output may be
+    // exactly that range of one input (in place)
+    ranges.push_back(Range{i + skip, i + skip + out_b, 0, q, false});
+  }
+  const uint64_t zero = 0;
+  dc_status_t st = check_reduce_overlaps(ranges, false, &zero);
+  if (st != DC_OK) return st;
+  ReduceParams1 prm{};
+  prm.P = P;
+  for (int q = 0; q < P; ++q) prm.ptr[q] = reinterpret_cast<uint64_t>(in_ptrs[q]);
+  prm.ptr[P] = o;
+  ReduceJob& J = prm.job[0];
+  J.in0 = 0;
+  J.out0 = static_cast<uint16_t>(P);
+  J.nout = 1;
+  J.in_off = in_offset;
+  J.count = count;
+  J.ufirst = 0;
+  prm.njobs = 1;
+  prm.total_units = classify_reduce_job(prm, J, P, dtype);
+  return launch_reduce_plan(prm, 0, dtype, order, out_b, stream, "reduce");
+}
+
 }  // namespace
 
 extern "C" {
@@ -916,6 +975,12 @@ dc_status_t dc_reduce_scatter(const void* const* in_ptrs, void* const* out_ptrs,
   return reduce_entry(in_ptrs, out_ptrs, &count_per_shard, 1, P, static_cast<int>(dtype),
                       static_cast<int>(order), true, static_cast<cudaStream_t>(stream),
                       "reduce_scatter");
+}
+
+dc_status_t dc_reduce(const void* const* in_ptrs, int P, size_t in_offset, size_t count, void* out,
+                      dc_dtype_t dtype, dc_order_t order, dc_stream_t stream) {
+  return reduce_one_entry(in_ptrs, P, in_offset, count, out, static_cast<int>(dtype), static_cast<int>(order),
+                          static_cast<cudaStream_t>(stream));
 }
 
 dc_status_t dc_all_reduce_many(const void* const* in_ptrs, void* const* out_ptrs,

@@ -1,26 +1,27 @@
-"""The staged all-gather across processes: one process per rank, each with
+"""The staged collectives across processes: one process per rank, each with
 its own buffers, the ranks' staging buffers shared between the processes.
 
 Page, by title: "perf(cuda): vectorize the deterministic all-gather copy and
 right-size its single-block path".  Its collective runs over CUDA IPC (the
 backend id cuda_ipc_fixed_tree, in the author's replies): every rank stages
-its payload in a buffer its peers have mapped, gathers the peers' staged
-payloads in rank order, and completes once every peer has read its buffer.
-What happens when a rank fails part-way is left open there: the review's
-reliability finding notes that an interrupted staged gather leaves pending
-state with no coordinated abort, and a review thread on the multi-process
-test notes that peers of a failed rank block until the process-group
-timeout (minutes).
+its payload in a buffer its peers have mapped, reads the peers' staged
+payloads, and completes once every peer has read its buffer.  What happens
+when a rank fails part-way is left open there: the review's reliability
+finding notes that an interrupted staged gather leaves pending state with no
+coordinated abort, and a review thread on the multi-process test notes that
+peers of a failed rank block until the process-group timeout (minutes).
 
-Here the handshakes run on the host, between the processes, and the gather
-runs in the library's kernel (dc_all_gather) over the peers' mapped staging
-buffers; no kernel ever waits for another process.  Each step is
+Here the handshakes run on the host, between the processes, and the work
+runs in the library's kernels over the peers' mapped staging buffers; no
+kernel ever waits for another process.  Each call (an epoch) is
 
   stage:    copy the local payload into the local staging buffer and wait for
             the copy to finish;
   barrier:  every rank has staged this epoch (bounded by `timeout`);
-  gather:   dc_all_gather over the P staging buffers into the local output,
-            wait for it to finish;
+  compute:  this rank's output from the P staging buffers, and wait for it:
+            the rank-ordered gather (dc_all_gather), or the fixed-order fold
+            of every buffer (dc_reduce) -- the whole buffer for all_reduce,
+            shard r of it for rank r of reduce_scatter;
   barrier:  every rank has read every staging buffer (same bound), so the
             next epoch may overwrite them.
 
@@ -32,28 +33,33 @@ between processes of one node, so the node-local handshake loses nothing
 there, and it is the CUDA transport's default.  It is correct for payloads in
 device memory on any host: a rank stores its counter only after its stream
 synchronisation returned, so a peer that sees the counter launches its reads
-after the copy finished.  For host payloads (SharedMemoryTransport) the
-payload's stores would have to become visible before the counter's, which
-weakly ordered hosts do not promise, so that transport defaults to gloo.
+after the copy finished.  (A transport whose payloads live in host memory
+would need the payload's stores to become visible before the counter's,
+which weakly ordered hosts do not promise: such a transport should keep the
+gloo handshake.)
 
 A barrier that runs out (a rank that never arrives, or died) raises
 DCError(DC_ERR_TIMEOUT) naming the epoch and step; the collective is then
 aborted: every later call raises at once, before it touches a peer's buffer.
 close() drops the mappings of the peers' buffers, waits until every rank has
-(within the bound), then releases the own buffer.  Signatures (world size, bytes per rank,
-transport) are compared once, when the collective is built: a mismatch raises
-DCError(DC_ERR_INVALID) on every rank.
+(within the bound), then releases the own buffer.  Signatures (operation,
+world size, sizes, element type, order, transport, handshake and, for the
+shared-memory handshake, the host) are compared once, when the collective is
+built: a mismatch raises DCError(DC_ERR_INVALID) on every rank.
 
-Transports: CudaIpcTransport (device buffers shared through CUDA IPC handles
-by torch's own tensor sharing; the gather is dc_all_gather) and
-SharedMemoryTransport (host buffers in POSIX shared memory, gathered on the
-host; for testing the protocol on machines without a GPU).  The process group
-must support monitored_barrier (gloo).
+A transport provides: kind, default_handshake, alloc(nbytes) -> buffer,
+export(buffer) -> descriptor (one per peer that opens it), open(descriptor)
+-> the peer's buffer, opened_by_all(), stage(buffer, payload),
+gather(buffers, out, nbytes), reduce(buffers, out, nbytes, offset, order),
+close_peers(), release().  CudaIpcTransport is the product's: device buffers
+shared through CUDA IPC handles, the work in dc_all_gather / dc_reduce.  The
+process group must support monitored_barrier (gloo).
 """
 from __future__ import annotations
 
 import datetime
 import os
+import socket
 import time
 
 from . import DCError
@@ -61,8 +67,11 @@ from . import DCError
 _TIMEOUT = 6  # DC_ERR_TIMEOUT
 _INVALID = 1  # DC_ERR_INVALID
 
+# element types of the reductions and their sizes in bytes
+ELEMENT_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
 
-class _SharedBytes:
+
+class SharedBytes:
     """A file in node-local shared memory (/dev/shm, a tmpfs; the temporary
     directory where there is none) mapped into this process.  The creator
     names it and unlinks it; the others open it by path."""
@@ -126,10 +135,10 @@ class ShmHandshake:
         import torch.distributed as dist
 
         self.rank, self.world, self.timeout = rank, world, timeout
-        mem = _SharedBytes(8 * world) if rank == 0 else None
+        mem = SharedBytes(8 * world) if rank == 0 else None
         paths = [None] * world
         dist.all_gather_object(paths, mem.path if mem else None, group=group)
-        self._mem = mem if mem else _SharedBytes(path=paths[0])
+        self._mem = mem if mem else SharedBytes(path=paths[0])
         self.slots = self._mem.array(np.uint64, world)
         self.seq = 0
 
@@ -159,62 +168,12 @@ class ShmHandshake:
         self._mem = None
 
 
-class SharedMemoryTransport:
-    """Host buffers in node-local shared memory; stage and gather are numpy
-    copies.  For the protocol's tests on machines without a GPU."""
-
-    kind = "shared-memory"
-    default_handshake = "gloo"
-
-    def __init__(self):
-        self._owned = []
-        self._opened = []
-
-    def alloc(self, nbytes: int):
-        import numpy as np
-
-        mem = _SharedBytes(nbytes)
-        self._owned.append(mem)
-        return mem.array(np.uint8, nbytes), mem.path
-
-    def export(self, buf) -> object:
-        return buf[1]
-
-    def open(self, desc):
-        import numpy as np
-
-        mem = _SharedBytes(path=desc)
-        self._opened.append(mem)
-        return mem.array(np.uint8, mem.size), desc
-
-    def stage(self, buf, payload) -> None:
-        buf[0][: payload.nbytes] = payload.view("u1").reshape(-1)
-
-    def gather(self, bufs, out, nbytes: int) -> None:
-        for q, b in enumerate(bufs):
-            out[q * nbytes:(q + 1) * nbytes] = b[0][:nbytes]
-
-    def opened_by_all(self) -> None:
-        for mem in self._owned:
-            mem.unlink()
-
-    def close_peers(self) -> None:
-        for mem in self._opened:
-            mem.close()
-        self._opened = []
-
-    def release(self) -> None:
-        for mem in self._owned:
-            mem.close()
-        self._owned = []
-
-
 class CudaIpcTransport:
     """Device staging buffers shared between processes through CUDA IPC
-    (torch's tensor sharing, torch.multiprocessing.reductions); the gather
-    is the library's dc_all_gather over the mapped peer buffers on the
-    current stream.  The processes' devices must be able to reach each
-    other's memory (here: processes on one GPU)."""
+    (torch's tensor sharing, torch.multiprocessing.reductions); the work is
+    the library's dc_all_gather / dc_reduce over the mapped peer buffers on
+    the current stream.  The processes' devices must be able to reach each
+    other's memory (processes on one node)."""
 
     kind = "cuda-ipc"
     default_handshake = "shm"
@@ -240,6 +199,9 @@ class CudaIpcTransport:
         self._opened.append(t)
         return t
 
+    def opened_by_all(self) -> None:
+        pass
+
     def stage(self, buf, payload) -> None:
         buf[: payload.nbytes].copy_(payload.reshape(-1).view(self.torch.uint8))
         self.torch.cuda.current_stream().synchronize()
@@ -250,8 +212,11 @@ class CudaIpcTransport:
         all_gather([b[:nbytes] for b in bufs], out.reshape(-1).view(self.torch.uint8))
         self.torch.cuda.current_stream().synchronize()
 
-    def opened_by_all(self) -> None:
-        pass
+    def reduce(self, bufs, out, nbytes: int, offset: int, order: str) -> None:
+        from . import reduce
+
+        reduce([b[:nbytes].view(out.dtype) for b in bufs], out.reshape(-1), offset=offset, order=order)
+        self.torch.cuda.current_stream().synchronize()
 
     def close_peers(self) -> None:
         self._opened = []
@@ -262,16 +227,19 @@ class CudaIpcTransport:
         self.torch.cuda.ipc_collect()
 
 
-class StagedAllGather:
-    """The staged all-gather of one process group: rank r's all_gather(payload,
-    out) leaves in `out` the P ranks' payloads in rank order (P * nbytes
-    bytes).  Payloads and outputs are contiguous byte buffers of the
-    transport's kind (numpy arrays or CUDA tensors)."""
+class _Staged:
+    """The protocol shared by the staged collectives: signature check,
+    buffers and handshake at construction, stage / barrier / compute /
+    barrier per call, abort and close."""
 
-    def __init__(self, group, nbytes: int, transport, timeout: float = 5.0, handshake: str | None = None):
+    op = ""
+
+    def __init__(self, group, staging_bytes: int, transport, timeout: float, handshake: str | None,
+                 extra: dict):
         import torch.distributed as dist
 
-        self.dist, self.group, self.nbytes, self.transport = dist, group, int(nbytes), transport
+        self.dist, self.group, self.transport = dist, group, transport
+        self.staging_bytes = int(staging_bytes)
         self.rank = dist.get_rank(group)
         self.world = dist.get_world_size(group)
         self.timeout = datetime.timedelta(seconds=timeout)
@@ -279,20 +247,22 @@ class StagedAllGather:
         self.aborted = None
         self.closed = False
         # host seconds spent in each step, summed over the epochs
-        self.seconds = dict.fromkeys(("stage", "stage_barrier", "gather", "complete_barrier"), 0.0)
+        self.seconds = dict.fromkeys(("stage", "stage_barrier", "compute", "complete_barrier"), 0.0)
         self.handshake = transport.default_handshake if handshake is None else handshake
         if self.handshake not in ("gloo", "shm"):
             raise ValueError(f"handshake must be 'gloo' or 'shm', not {self.handshake!r}")
         self._hs = None
-        sig = {"world": self.world, "nbytes": self.nbytes, "transport": transport.kind,
-               "handshake": self.handshake}
+        sig = {"op": self.op, "world": self.world, "staging_bytes": self.staging_bytes,
+               "transport": transport.kind, "handshake": self.handshake, **extra}
+        if self.handshake == "shm":
+            sig["host"] = socket.gethostname()
         sigs = [None] * self.world
         dist.all_gather_object(sigs, sig, group=group)
         if any(s != sig for s in sigs):
             raise DCError(_INVALID, f"ranks disagree on the collective: {sigs}")
         if self.handshake == "shm":
             self._hs = ShmHandshake(group, self.rank, self.world, timeout)
-        self.local = transport.alloc(self.nbytes)
+        self.local = transport.alloc(self.staging_bytes)
         # one descriptor per peer (CUDA IPC counts the references it hands
         # out: one export per process that opens it)
         mine = [None if q == self.rank else transport.export(self.local) for q in range(self.world)]
@@ -323,36 +293,36 @@ class StagedAllGather:
             self.aborted = f"{step} of epoch {self.epoch} on rank {self.rank}: {err}"
             raise DCError(_TIMEOUT, self.aborted)
 
-    def all_gather(self, payload, out):
-        """Stage, barrier, gather, barrier (see the module docstring)."""
+    def _run(self, payload, out, payload_bytes: int, out_bytes: int, compute):
+        """Stage, barrier, compute, barrier (the module docstring)."""
         if self.aborted:
             raise DCError(_TIMEOUT, "the collective was aborted: " + self.aborted)
         if self.closed:
             raise ValueError("the collective is closed")
-        if payload.nbytes != self.nbytes or out.nbytes != self.world * self.nbytes:
-            raise ValueError(f"need a payload of {self.nbytes} bytes and an output of "
-                             f"{self.world * self.nbytes}")
+        if payload.nbytes != payload_bytes or out.nbytes != out_bytes:
+            raise ValueError(f"{self.op} needs a payload of {payload_bytes} bytes and an output of "
+                             f"{out_bytes} (got {payload.nbytes} and {out.nbytes})")
         self.epoch += 1
         t0 = time.perf_counter()
         self.transport.stage(self.local, payload)
         t1 = time.perf_counter()
         self._barrier("stage")
         t2 = time.perf_counter()
-        self.transport.gather(self.peers, out, self.nbytes)
+        compute()
         t3 = time.perf_counter()
         self._barrier("complete")
         t4 = time.perf_counter()
         sec = self.seconds
         sec["stage"] += t1 - t0
         sec["stage_barrier"] += t2 - t1
-        sec["gather"] += t3 - t2
+        sec["compute"] += t3 - t2
         sec["complete_barrier"] += t4 - t3
         return out
 
     def close(self) -> None:
         """Drop the peers' mappings, wait (if the collective is healthy, within
         the bound) until every rank has dropped them, then release the own
-        staging buffer.  Idempotent; later calls of all_gather raise."""
+        staging buffer.  Idempotent; later calls raise."""
         if self.closed:
             return
         self.closed = True
@@ -368,4 +338,69 @@ class StagedAllGather:
             self._hs.close()
 
 
-__all__ = ["StagedAllGather", "CudaIpcTransport", "SharedMemoryTransport", "ShmHandshake"]
+class StagedAllGather(_Staged):
+    """Rank r's all_gather(payload, out) leaves in `out` the P ranks'
+    payloads in rank order (P * nbytes bytes).  Payloads and outputs are
+    contiguous buffers of the transport's kind."""
+
+    op = "all_gather"
+
+    def __init__(self, group, nbytes: int, transport, timeout: float = 5.0, handshake: str | None = None):
+        self.nbytes = int(nbytes)
+        super().__init__(group, self.nbytes, transport, timeout, handshake, {})
+
+    def all_gather(self, payload, out):
+        return self._run(payload, out, self.nbytes, self.world * self.nbytes,
+                         lambda: self.transport.gather(self.peers, out, self.nbytes))
+
+
+class StagedAllReduce(_Staged):
+    """Rank r's all_reduce(payload, out): `out` (count elements of `dtype`,
+    "bf16" / "f16" / "f32") receives the fixed-order fold of the P ranks'
+    payloads -- bit-identical to rank r's output of dc_all_reduce over the
+    same P buffers."""
+
+    op = "all_reduce"
+
+    def __init__(self, group, count: int, dtype: str, transport, order: str = "linear",
+                 timeout: float = 5.0, handshake: str | None = None):
+        if dtype not in ELEMENT_BYTES:
+            raise ValueError(f"dtype must be one of {sorted(ELEMENT_BYTES)} (got {dtype!r})")
+        self.count, self.dtype, self.order = int(count), dtype, order
+        self.nbytes = self.count * ELEMENT_BYTES[dtype]
+        super().__init__(group, self.nbytes, transport, timeout, handshake,
+                         {"count": self.count, "dtype": dtype, "order": order})
+
+    def all_reduce(self, payload, out):
+        return self._run(payload, out, self.nbytes, self.nbytes,
+                         lambda: self.transport.reduce(self.peers, out, self.nbytes, 0, self.order))
+
+
+class StagedReduceScatter(_Staged):
+    """Rank r's reduce_scatter(payload, out): the payload holds P shards of
+    count_per_shard elements; `out` receives the fixed-order fold of shard r
+    of every rank's payload -- bit-identical to rank r's output of
+    dc_reduce_scatter."""
+
+    op = "reduce_scatter"
+
+    def __init__(self, group, count_per_shard: int, dtype: str, transport, order: str = "linear",
+                 timeout: float = 5.0, handshake: str | None = None):
+        import torch.distributed as dist
+
+        if dtype not in ELEMENT_BYTES:
+            raise ValueError(f"dtype must be one of {sorted(ELEMENT_BYTES)} (got {dtype!r})")
+        self.count, self.dtype, self.order = int(count_per_shard), dtype, order
+        self.shard_bytes = self.count * ELEMENT_BYTES[dtype]
+        P = dist.get_world_size(group)
+        super().__init__(group, P * self.shard_bytes, transport, timeout, handshake,
+                         {"count_per_shard": self.count, "dtype": dtype, "order": order})
+
+    def reduce_scatter(self, payload, out):
+        return self._run(payload, out, self.world * self.shard_bytes, self.shard_bytes,
+                         lambda: self.transport.reduce(self.peers, out, self.world * self.shard_bytes,
+                                                       self.rank * self.count, self.order))
+
+
+__all__ = ["StagedAllGather", "StagedAllReduce", "StagedReduceScatter", "CudaIpcTransport", "ShmHandshake",
+           "SharedBytes", "ELEMENT_BYTES"]

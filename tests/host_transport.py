@@ -1,0 +1,66 @@
+"""A transport for the staged collectives' host protocol on machines without
+a GPU (tests only): staging buffers are host memory in node-local shared
+memory files, the gather is a byte copy and the reduction is the oracle's
+fold.  It exercises everything of reduce_copy_rank_gb300.ipc but the device
+work: signatures, descriptor exchange, handshakes, timeouts, abort, close.
+
+Payloads are numpy arrays (bytes for the gather; 16- or 32-bit patterns for
+the reductions, as the oracle takes them)."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from reduce_copy_rank_gb300.ipc import SharedBytes
+
+
+class HostTransport:
+    kind = "host-shared-memory"
+    # the shared-memory handshake needs the payload's stores visible before
+    # the counter's: x86 (where these tests run) promises it, weakly ordered
+    # hosts do not, so the default is the process group's barrier
+    default_handshake = "gloo"
+
+    def __init__(self, dtype: str = "u8"):
+        self.dtype = dtype
+        self._owned = []
+        self._opened = []
+
+    def alloc(self, nbytes: int):
+        mem = SharedBytes(nbytes)
+        self._owned.append(mem)
+        return mem.array(np.uint8, nbytes), mem.path
+
+    def export(self, buf) -> object:
+        return buf[1]
+
+    def open(self, desc):
+        mem = SharedBytes(path=desc)
+        self._opened.append(mem)
+        return mem.array(np.uint8, mem.size), desc
+
+    def opened_by_all(self) -> None:
+        for mem in self._owned:
+            mem.unlink()
+
+    def stage(self, buf, payload) -> None:
+        buf[0][: payload.nbytes] = np.ascontiguousarray(payload).view(np.uint8).reshape(-1)
+
+    def gather(self, bufs, out, nbytes: int) -> None:
+        for q, b in enumerate(bufs):
+            out[q * nbytes:(q + 1) * nbytes] = b[0][:nbytes]
+
+    def reduce(self, bufs, out, nbytes: int, offset: int, order: str) -> None:
+        n = out.size
+        cols = [b[0][:nbytes].view(out.dtype)[offset:offset + n] for b in bufs]
+        out[:] = oracle.all_reduce(cols, self.dtype, order).view(out.dtype)
+
+    def close_peers(self) -> None:
+        for mem in self._opened:
+            mem.close()
+        self._opened = []
+
+    def release(self) -> None:
+        for mem in self._owned:
+            mem.close()
+        self._owned = []

@@ -417,6 +417,51 @@ def test_tensors_on_another_device_are_rejected(monkeypatch):
                       [_FakeCudaTensor(64, 0), _FakeCudaTensor(64, 3)])
 
 
+# ------------------------------------------------- one rank's reduction ---
+
+def test_reduce_rejects_bad_arguments():
+    ins = [BASE, BASE + 4096]
+    out = BASE + 8192
+    assert dc.dc_reduce(ins, 0, 0, 8, out) == INVALID
+    assert dc.dc_reduce([BASE] * 65, 65, 0, 8, out) == INVALID
+    assert dc.dc_reduce(ins, 2, 0, 8, out, dtype=3) == INVALID
+    assert dc.dc_reduce(ins, 2, 0, 8, out, order=2) == INVALID
+    assert dc.dc_reduce([BASE, 0], 2, 0, 8, out) == INVALID
+    assert dc.dc_reduce(ins, 2, 0, 8, 0) == INVALID
+    assert dc.dc_reduce(ins, 2, 1 << 63, 1 << 63, out) == INVALID  # offset + count overflows
+    assert "overflows" in dc.last_error()
+
+
+def test_reduce_alignment_follows_the_element_type(no_launch):
+    ins = [BASE, BASE + 4096]
+    assert dc.dc_reduce(ins, 2, 0, 8, BASE + 8193) == ALIGN           # BF16 output at an odd byte
+    assert dc.dc_reduce([BASE + 1, BASE + 4096], 2, 0, 8, BASE + 8192) == ALIGN
+    assert dc.dc_reduce(ins, 2, 0, 8, BASE + 8194, dtype=2) == ALIGN  # FP32 at 2 mod 4
+    assert dc.dc_reduce(ins, 2, 0, 8, BASE + 8194) == CUDA            # BF16 at 2 mod 16: fine
+
+
+def test_reduce_zero_count_is_a_noop_without_launch():
+    before = dc.launch_count()
+    assert dc.dc_reduce([0, 0], 2, 0, 0, 0) == OK
+    assert dc.launch_count() == before
+
+
+@pytest.mark.parametrize("shift", [-2, 2, 14])
+def test_reduce_rejects_partial_overlap_with_the_elements_read(shift):
+    ins = [BASE, BASE + 4096]
+    # reads elements [16, 24) of every input (BF16): bytes [32, 48) of each
+    assert dc.dc_reduce(ins, 2, 16, 8, BASE + 4096 + 32 + shift) == OVERLAP
+    assert "overlaps" in dc.last_error()
+
+
+def test_reduce_in_place_and_unread_overlaps_are_allowed(no_launch):
+    ins = [BASE, BASE + 4096]
+    assert dc.dc_reduce(ins, 2, 16, 8, BASE + 4096 + 32) == CUDA  # exactly the range read: in place
+    assert dc.dc_reduce(ins, 2, 16, 8, BASE + 4096) == CUDA       # input 1's unread elements [0, 8)
+    assert dc.dc_reduce(ins, 2, 16, 8, BASE + 4096 + 48) == CUDA  # just past the range read
+    assert dc.dc_reduce([BASE, BASE], 2, 0, 8, BASE + 4096) == CUDA  # inputs may repeat
+
+
 # ------------------------------------------------------- fused all-gather ---
 
 def _fused_layout(P, B, base=BASE):

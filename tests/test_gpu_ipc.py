@@ -1,8 +1,9 @@
-"""The staged all-gather across processes on the GPU: ranks as separate
+"""The staged collectives across processes on the GPU: ranks as separate
 processes on one GPU, each staging buffer a device allocation that the other
-processes map through CUDA IPC, the gather the library's kernel over the
-mapped buffers.  Every rank's output is compared with the oracle, bit for bit,
-over several epochs and at aligned, unaligned and multi-tile sizes.
+processes map through CUDA IPC, the gather or the fixed-order fold the
+library's kernel over the mapped buffers.  Every rank's output is compared
+with the oracle, bit for bit (NaN by class), over several epochs, at aligned,
+unaligned and multi-tile sizes and for every element type.
 
 No kernel waits for another process: the handshakes are host barriers (the
 node-local shared-memory counters, and the gloo process group's monitored
@@ -39,7 +40,7 @@ def _port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, handshake, outdir):
+def _worker(rank, world, port, handshake, outdir, op="gather"):
     import torch
     import torch.distributed as dist
 
@@ -52,6 +53,11 @@ def _worker(rank, world, port, handshake, outdir):
     res = {"rank": rank, "ok": [], "launches": 0}
     try:
         n0 = dc.launch_count()
+        if op != "gather":
+            _reductions(rank, world, handshake, op, res)
+            res["launches"] = dc.launch_count() - n0
+            dc.check_device()
+            return
         for si, B in enumerate(SIZES):
             coll = StagedAllGather(None, B, CudaIpcTransport(), timeout=30.0, handshake=handshake)
             for epoch in range(1, 4):
@@ -70,6 +76,47 @@ def _worker(rank, world, port, handshake, outdir):
         with open(os.path.join(outdir, f"r{rank}.json"), "w") as fh:
             json.dump(res, fh)
         dist.destroy_process_group()
+
+
+RED_CASES = [("bf16", "linear", 4099), ("f16", "tree", 1 << 18), ("f32", "linear", (1 << 18) + 3)]
+
+
+def _reductions(rank, world, handshake, op, res):
+    """all_reduce / reduce_scatter over CUDA IPC for each (dtype, order, n),
+    three epochs each, against the oracle's fold and the single-process
+    entry point's output for this rank."""
+    import torch
+
+    from gpu_util import NP_OF, is_nan_typed, torch_dtype, typed_bits, typed_tensor
+    from reduce_copy_rank_gb300.ipc import CudaIpcTransport, StagedAllReduce, StagedReduceScatter
+
+    for ci, (dtype, order, n) in enumerate(RED_CASES):
+        if op == "allreduce":
+            coll = StagedAllReduce(None, n, dtype, CudaIpcTransport(), order=order, timeout=30.0,
+                                   handshake=handshake)
+            total = n
+        else:
+            coll = StagedReduceScatter(None, n, dtype, CudaIpcTransport(), order=order, timeout=30.0,
+                                       handshake=handshake)
+            total = world * n
+        for epoch in range(1, 4):
+            cols = []
+            for q in range(world):
+                g = np.random.default_rng(np.random.SeedSequence([W.seed_for(4, 930 + 10 * ci + epoch), q]))
+                hi = np.iinfo(NP_OF[dtype]).max
+                cols.append(g.integers(0, hi, total, dtype=np.uint64).astype(NP_OF[dtype]))
+            mine = typed_tensor(cols[rank], dtype)
+            out = torch.empty(n, dtype=torch_dtype(dtype), device="cuda")
+            if op == "allreduce":
+                coll.all_reduce(mine, out)
+                want = oracle.all_reduce(cols, dtype, order)
+            else:
+                coll.reduce_scatter(mine, out)
+                want = oracle.reduce_scatter(cols, dtype, order)[rank]
+            got, w = typed_bits(out, dtype), want.view(NP_OF[dtype])
+            gn, wn = is_nan_typed(got, dtype), is_nan_typed(w, dtype)  # NaN compared by class
+            res["ok"].append(bool(np.array_equal(gn, wn) and np.array_equal(got[~wn], w[~wn])))
+        coll.close()
 
 
 def _compute_mode_default():
@@ -95,3 +142,16 @@ def test_staged_all_gather_over_cuda_ipc(world, handshake, tmp_path):
         assert "error" not in res, res
         assert res["ok"] == [True] * (3 * len(SIZES)), res
         assert res["launches"] == 3 * len(SIZES), res  # one gather kernel per epoch
+
+
+@pytest.mark.parametrize("op", ["allreduce", "reducescatter"])
+@pytest.mark.parametrize("world", [2, 3])
+def test_staged_reductions_over_cuda_ipc(world, op, tmp_path):
+    if not _compute_mode_default():
+        pytest.skip("GPU 0 is not in the default compute mode: one process per GPU only")
+    mp.spawn(_worker, args=(world, _port(), "shm", str(tmp_path), op), nprocs=world, join=True)
+    for r in range(world):
+        res = json.load(open(tmp_path / f"r{r}.json"))
+        assert "error" not in res, res
+        assert res["ok"] == [True] * (3 * len(RED_CASES)), res
+        assert res["launches"] == 3 * len(RED_CASES), res  # one reduction kernel per epoch

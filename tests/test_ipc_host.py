@@ -1,10 +1,11 @@
-"""The staged all-gather across processes (reduce_copy_rank_gb300.ipc), its
+"""The staged collectives across processes (reduce_copy_rank_gb300.ipc), their
 host protocol on CPU: gloo process groups of 2 and 3 ranks, host buffers in
-shared memory standing in for the device staging buffers.
+shared memory standing in for the device staging buffers (tests/host_transport.py).
 
-Checked: every rank's output is the rank-ordered concatenation over several
-epochs; ranks that disagree on the collective all raise DC_ERR_INVALID when it
-is built; a rank that never arrives, or that dies, makes the others raise
+Checked: every rank's output is the rank-ordered concatenation (all_gather),
+or the oracle's fold of every rank's payload (all_reduce) or of its own shard
+(reduce_scatter), over several epochs; ranks that disagree on the collective
+all raise DC_ERR_INVALID when it is built; a rank that never arrives, or that dies, makes the others raise
 DC_ERR_TIMEOUT within the bound (seconds, not the process group's minutes),
 naming the step and the epoch, and every later call raises at once.
 
@@ -17,6 +18,7 @@ from __future__ import annotations
 
 import json
 import os
+import platform
 import socket
 import time
 
@@ -38,7 +40,8 @@ def _worker(rank, world, port, case, handshake, outdir):
     import torch.distributed as dist
 
     import reduce_copy_rank_gb300 as dc
-    from reduce_copy_rank_gb300.ipc import SharedMemoryTransport, StagedAllGather
+    from host_transport import HostTransport
+    from reduce_copy_rank_gb300.ipc import StagedAllGather, StagedAllReduce, StagedReduceScatter
 
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -47,13 +50,47 @@ def _worker(rank, world, port, case, handshake, outdir):
     try:
         if case == "mismatch":
             try:
-                StagedAllGather(None, B + (rank == 1), SharedMemoryTransport(), timeout=2.0,
+                StagedAllGather(None, B + (rank == 1), HostTransport(), timeout=2.0,
                                 handshake=handshake)
                 res["raised"] = None
             except dc.DCError as e:
                 res["raised"] = e.status
             return
-        coll = StagedAllGather(None, B, SharedMemoryTransport(), timeout=2.0, handshake=handshake)
+        if case == "mismatch_dtype":
+            try:
+                StagedAllReduce(None, 64, "bf16" if rank == 0 else "f16", HostTransport(), timeout=2.0,
+                                handshake=handshake)
+                res["raised"] = None
+            except dc.DCError as e:
+                res["raised"] = e.status
+            return
+        if case.startswith(("allreduce", "reducescatter")):
+            op, dtype, order = case.split(":")
+            n = 1001
+            np_t = np.uint32 if dtype == "f32" else np.uint16
+            if op == "allreduce":
+                coll = StagedAllReduce(None, n, dtype, HostTransport(dtype), order=order, timeout=2.0,
+                                       handshake=handshake)
+            else:
+                coll = StagedReduceScatter(None, n, dtype, HostTransport(dtype), order=order, timeout=2.0,
+                                           handshake=handshake)
+            res["ok"] = []
+            for epoch in range(1, 4):
+                total = n if op == "allreduce" else world * n
+                rng = [np.random.default_rng(np.random.SeedSequence([W.seed_for(4, 820 + epoch), q]))
+                       for q in range(world)]
+                payloads = [g.integers(0, np.iinfo(np_t).max, total, dtype=np.uint64).astype(np_t) for g in rng]
+                out = np.zeros(n, dtype=np_t)
+                if op == "allreduce":
+                    coll.all_reduce(payloads[rank], out)
+                    want = oracle.all_reduce(payloads, dtype, order)
+                else:
+                    coll.reduce_scatter(payloads[rank], out)
+                    want = oracle.reduce_scatter(payloads, dtype, order)[rank]
+                res["ok"].append(bool(np.array_equal(out, want.view(np_t))))
+            coll.close()
+            return
+        coll = StagedAllGather(None, B, HostTransport(), timeout=2.0, handshake=handshake)
         if case == "parity":
             res["ok"] = []
             for epoch in range(1, 4):
@@ -112,7 +149,9 @@ def _run(world, case, tmp_path, handshake="gloo"):
 # tests run), not promised on weakly ordered hosts, where that transport
 # defaults to the gloo handshake.  With device payloads (the CUDA transport)
 # it holds on any host.
-HANDSHAKES = ["gloo", "shm"]
+HANDSHAKES = ["gloo", pytest.param("shm", marks=pytest.mark.skipif(
+    platform.machine() not in ("x86_64", "AMD64"),
+    reason="host payloads with the shared-memory handshake need a host that keeps store order"))]
 
 
 @pytest.mark.parametrize("handshake", HANDSHAKES)
@@ -123,6 +162,21 @@ def test_parity_over_epochs(world, handshake, tmp_path):
     for r in range(world):
         assert res[r]["ok"] == [True, True, True], res[r]
         assert res[r]["after_close"] == "ValueError", res[r]
+
+
+@pytest.mark.parametrize("handshake", HANDSHAKES)
+@pytest.mark.parametrize("case", ["allreduce:bf16:linear", "allreduce:f32:tree", "reducescatter:bf16:tree",
+                                  "reducescatter:f16:linear"])
+def test_reductions_over_epochs(case, handshake, tmp_path):
+    world = 3
+    res = _run(world, case, tmp_path, handshake)
+    for r in range(world):
+        assert res[r]["ok"] == [True, True, True], res[r]
+
+
+def test_reduction_dtype_mismatch_raises_on_every_rank(tmp_path):
+    res = _run(2, "mismatch_dtype", tmp_path, "gloo")
+    assert [res[r]["raised"] for r in range(2)] == [1, 1]
 
 
 @pytest.mark.parametrize("handshake", HANDSHAKES)
