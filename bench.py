@@ -481,22 +481,41 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     tens = [[W.random_bytes_device(W.seed_for(5, 2), r, B + 1, device, tensor=t)[1:] for r in range(8)]
             for t, B in enumerate(sizes)]
     outs = [torch.empty(8 * B, dtype=torch.uint8, device=device) for B in sizes]
-    # (timed from a CUDA graph: flush, event, the call, event; the binding's
-    # host-side marshalling of 1080 tensors takes longer than the flush, so
-    # an eager call's events would count host time)
-    g, evs = build_step_graph(torch, flush, [lambda: dc.all_gather_many(tens, outs)])
-    t = []
-    for _ in range(5):
-        g.replay()
-        torch.cuda.synchronize()
-        t.append(evs[0].elapsed_time(evs[1]) * 1e3)
-    us = statistics.median(t)
-    del g
+    # (timed from CUDA graphs: flush, event, the call -- or 20 of them back
+    # to back --, event; the binding's host-side marshalling of a thousand
+    # tensors takes longer than the flush, so an eager call's events would
+    # count host time)
+    def graph_us(fn, n):
+        g, evs = build_step_graph(torch, flush, [fn] * n)
+        t = []
+        for _ in range(5):
+            g.replay()
+            torch.cuda.synchronize()
+            t.append(evs[0].elapsed_time(evs[1]) * 1e3 / n)
+        del g
+        return statistics.median(t)
+
+    many = lambda: dc.all_gather_many(tens, outs)  # noqa: E731
+    us, b2b = graph_us(many, 1), graph_us(many, 20)
     nbytes = 2 * 8 * sum(sizes)
     rows.append({"op": "all_gather_many_tiny", "P": 8, "count": len(sizes),
                  "shape": "120 tensors of 3..100 B per rank, payloads at +1 B; call alone after a "
-                          "flush, from a CUDA graph", "us": us,
+                          "flush, from a CUDA graph", "us": us, "back_to_back_us": b2b,
                  "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    del tens, outs
+    # many mid-size tensors: 250 tensors x 4 ranks of 128..4096 B at +1 B
+    # (the realigning part with a long job table)
+    sizes = [int(x) for x in rng.integers(128, 4097, 250)]
+    tens = [[W.random_bytes_device(W.seed_for(5, 3), r, B + 1, device, tensor=t)[1:] for r in range(4)]
+            for t, B in enumerate(sizes)]
+    outs = [torch.empty(4 * B, dtype=torch.uint8, device=device) for B in sizes]
+    us, b2b = graph_us(many, 1), graph_us(many, 20)
+    nbytes = 2 * 4 * sum(sizes)
+    rows.append({"op": "all_gather_many_mid", "P": 4, "count": len(sizes),
+                 "shape": "250 tensors of 128..4096 B per rank, payloads at +1 B; call alone after a "
+                          "flush, and 20 back to back, from CUDA graphs", "us": us, "back_to_back_us": b2b,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes,
+                 "back_to_back_gbs": nbytes / b2b / 1e3})
     del tens, outs
     # the staged protocol (stage -> gather -> complete), P = 8 ranks x 4 MiB:
     # P*B read + P*B written to stage, P*P*B read + P*P*B written to gather

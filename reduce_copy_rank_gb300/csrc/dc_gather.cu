@@ -36,7 +36,9 @@
 //    or two aligned blocks) or from bytes, with their loads issued before
 //    their stores; in mode 5 one extra CTA copies them beside the ring.
 //  * all_gather_many (mode 4): the aligned jobs come first and are staged by
-//    the first part of the grid, the unaligned ones by the rest.
+//    the first part of the grid, the unaligned ones by the rest; in these
+//    parts each CTA takes a contiguous run of tiles, starting at a job the
+//    host looked up, so that a thread enters only the jobs of its run.
 //  * Jobs with fewer than kGatherSmallBytes per rank are assembled from bytes.
 //  * Programmatic dependent launch: the single-job staged kernels prefetch
 //    their first tile into L2 before they wait for the previous kernel of
@@ -346,22 +348,32 @@ __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>&
 // ordered aligned first), staged like gather_tiles_staged but over a job
 // table: the issuing side walks jobs and ranks forward with a Cursor, the
 // draining side walks jobs only (it needs each vector's output address).
+// CTA `cta` of the part takes the contiguous run of p.flat_per tiles from
+// tile cta * flat_per, starting at job p.flat_tab[cta] (written by the
+// host): a thread's vectors then lie close together and it enters only the
+// few jobs of its run.  (With tiles dealt round robin over the part, a
+// thread's consecutive tiles were the whole grid's share apart, so it
+// crossed many jobs per tile, each a dependent read of the job table and a
+// division: 250 aligned jobs of 4-64 KiB x 4 ranks took 38 us.)
 template <int BLOCK, int V, int S, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ, MAXS>& p,
-                                                         uint64_t first, uint64_t step) {
+__device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta) {
   extern __shared__ uint4 stage_buf[];  // [S][V][BLOCK]
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
   const uint64_t total = p.flat_vec;
   const uint64_t ntiles = (total + kTile - 1) / kTile;
+  const uint64_t t0 = static_cast<uint64_t>(cta) * p.flat_per;
+  const uint64_t t1 = min(t0 + p.flat_per, ntiles);
+  if (t0 >= t1) return;
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
-  Cursor c = cursor_at(p, first * kTile + threadIdx.x);
+  const int j0 = MAXJ > 1 ? static_cast<int>(p.flat_tab[cta]) : 0;
+  Cursor c{j0, p.job[j0].vfirst, p.job[j0].vfirst + p.job[j0].nvec, true, 0, 0, 0};
   int jd = c.j;
   uint64_t dbeg = c.jbeg, dend = c.jend;
   auto issue = [&](uint32_t slot, uint64_t t) {
 #pragma unroll
     for (int u = 0; u < V; ++u) {
       const uint64_t k = t * kTile + static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
-      if (t < ntiles && k < total) {
+      if (t < t1 && k < total) {
         cursor_to_job(p, c, k);
         const uint4* a = flat_source(p, c, p.job[c.j], k - c.jbeg);
         if (load_ok(p, p.job[c.j], c.r, a, 16, kSiteStagedJobs)) cp_async16(sbase + 16u * BLOCK * (slot * V + u), a);
@@ -369,14 +381,14 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
     }
     cp_async_commit();
   };
-  uint64_t t_issue = first;
+  uint64_t t_issue = t0;
 #pragma unroll
   for (int s = 0; s < S; ++s) {
     issue(s, t_issue);
-    t_issue += step;
+    ++t_issue;
   }
   uint32_t slot = 0;
-  for (uint64_t t = first; t < ntiles; t += step) {
+  for (uint64_t t = t0; t < t1; ++t) {
     cp_async_wait<S - 1>();
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -392,7 +404,7 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
       }
     }
     issue(slot, t_issue);
-    t_issue += step;
+    ++t_issue;
     slot = (slot + 1 == S) ? 0 : slot + 1;
   }
   cp_async_wait<0>();
@@ -724,17 +736,24 @@ __device__ __forceinline__ void copy_small_vector(const GatherParams<MAXJ, MAXS>
 // issued before its stores, so it costs one memory round trip.
 template <int BLOCK, int V, int S, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherParams<MAXJ, MAXS>& p,
-                                                                 uint64_t first, uint64_t step,
-                                                                 uint64_t voff, uint64_t vend) {
+                                                                 uint32_t cta, uint64_t voff, uint64_t vend) {
   static_assert(S * V * 5 <= 32, "ring notes must fit one register");
   extern __shared__ uint4 stage_buf[];  // [S][V][2][BLOCK]
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
   const uint64_t total = vend;
   const uint64_t ntiles = (total - voff + kTile - 1) / kTile;
+  // CTA `cta` of the part: the contiguous run of p.real_per tiles from tile
+  // cta * real_per, starting at job p.real_tab[cta] (written by the host;
+  // a binary search here spilled registers, and walking the table from its
+  // start cost a dependent read per job: 250 jobs of 128 B-4 KiB x 4 ranks
+  // at +1 B took 36 us)
+  const uint64_t t0 = static_cast<uint64_t>(cta) * p.real_per;
+  const uint64_t t1 = min(t0 + p.real_per, ntiles);
+  if (t0 >= t1) return;
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
   // issuing side: job j (vectors [jbeg, jend)), its ranks
-  int j = 0;  // (a binary search here, as in the other job kernels, spilled registers)
-  uint64_t jbeg = p.job[0].vfirst, jend = jbeg + p.job[0].nvec;
+  int j = MAXJ > 1 ? static_cast<int>(p.real_tab[cta]) : 0;
+  uint64_t jbeg = p.job[j].vfirst, jend = jbeg + p.job[j].nvec;
   RankWalk<uint64_t> w{0, 0, 0, 0, 0, true};
   // draining side: job jd (vectors [dbeg, dend))
   int jd = j;
@@ -748,7 +767,7 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
 #pragma unroll
     for (int u = 0; u < V; ++u) {
       const uint64_t k = voff + t * kTile + static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
-      if (t < ntiles && k < total) {
+      if (t < t1 && k < total) {
         while (k >= jend) {
           ++j;
           jbeg = p.job[j].vfirst;
@@ -772,14 +791,14 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
     }
     cp_async_commit();
   };
-  uint64_t t_issue = first;
+  uint64_t t_issue = t0;
 #pragma unroll
   for (int i = 0; i < S; ++i) {
     issue(i, t_issue);
-    t_issue += step;
+    ++t_issue;
   }
   uint32_t slot = 0;
-  for (uint64_t t = first; t < ntiles; t += step) {
+  for (uint64_t t = t0; t < t1; ++t) {
     cp_async_wait<S - 1>();
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -810,7 +829,7 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
       }
     }
     issue(slot, t_issue);
-    t_issue += step;
+    ++t_issue;
     slot = (slot + 1 == S) ? 0 : slot + 1;
   }
   cp_async_wait<0>();
@@ -1042,13 +1061,13 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     // the other unaligned jobs
     const uint64_t fc = static_cast<uint64_t>(p.flat_ctas), sc = static_cast<uint64_t>(p.small_ctas);
     if (first < fc)
-      gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, first, fc);
+      gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, static_cast<uint32_t>(first));
     else if (first + sc >= step) {
       if constexpr (MAXJ > 1) copy_small_jobs<BLOCK, kSmallSplit>(p, static_cast<uint32_t>(first + sc - step));
     }
     else
       gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
-          p, first - fc, step - fc - sc, p.flat_vec, p.small_vec);
+          p, static_cast<uint32_t>(first - fc), p.flat_vec, p.small_vec);
   } else
     gather_tiles<BLOCK, UNROLL, MODE != kGeneral, SINGLE>(p, first, step);
 }

@@ -74,6 +74,8 @@ constexpr uint64_t kGatherSmallBytes = 128;
 constexpr int kSmallSplit = 4;
 // At most this many CTAs copy the small jobs of one launch (one table entry each).
 constexpr int kMaxSmallCtas = 512;
+// split launch: CTAs of its aligned part and of its realigning part, each at most
+constexpr int kMaxPartCtas = 1024;
 
 // ------------------------------------------------------------- gather ---
 enum : uint32_t {
@@ -110,11 +112,17 @@ struct GatherParams {
   int32_t tile_vec;     // one job, staged (modes 3, 5): vectors per tile (at most BLOCK*V)
   uint32_t small_per;   // split launch: small-job vectors per small-job CTA (a contiguous run)
   int32_t realign_warp; // one unaligned job: realign across the warp's lanes (mode 6), not through a ring
+  uint32_t flat_per;    // split launch: tiles per aligned-part CTA (a contiguous run)
+  uint32_t real_per;    // split launch: tiles per realigning-part CTA (a contiguous run)
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
   // split launch: small-job CTA c covers jobs small_job0 + small_tab[c] ..
   // small_job0 + small_tab[c + 1] (the jobs of its first and last vector)
   uint16_t small_tab[MAXJ > 1 ? kMaxSmallCtas + 1 : 1];
+  // split launch: the job of the first vector of aligned-part CTA c
+  // (flat_tab[c]) and of realigning-part CTA c (real_tab[c])
+  uint16_t flat_tab[MAXJ > 1 ? kMaxPartCtas : 1];
+  uint16_t real_tab[MAXJ > 1 ? kMaxPartCtas : 1];
 };
 
 using GatherParams1 = GatherParams<1, kMaxRanks>;
