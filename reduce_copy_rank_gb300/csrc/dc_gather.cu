@@ -348,21 +348,28 @@ __device__ __forceinline__ void gather_tiles_staged(const GatherParams<1, MAXS>&
 // ordered aligned first), staged like gather_tiles_staged but over a job
 // table: the issuing side walks jobs and ranks forward with a Cursor, the
 // draining side walks jobs only (it needs each vector's output address).
-// CTA `cta` of the part takes the contiguous run of p.flat_per tiles from
-// tile cta * flat_per, starting at job p.flat_tab[cta] (written by the
-// host): a thread's vectors then lie close together and it enters only the
-// few jobs of its run.  (With tiles dealt round robin over the part, a
-// thread's consecutive tiles were the whole grid's share apart, so it
-// crossed many jobs per tile, each a dependent read of the job table and a
-// division: 250 aligned jobs of 4-64 KiB x 4 ranks took 38 us.)
+// With many jobs (p.flat_per > 0), CTA `cta` of the part takes the
+// contiguous run of flat_per tiles from tile cta * flat_per: a thread's
+// vectors then lie close together and it enters only the few jobs of its
+// run.  (With tiles dealt round robin, a thread's consecutive tiles are the
+// whole part's share apart, so it crossed many jobs per tile, each a
+// dependent read of the job table and a division: 250 aligned jobs of 4-64
+// KiB x 4 ranks took 38 us.)  With few jobs (flat_per == 0) tiles are dealt
+// round robin over the part's `nctas` CTAs, so that all CTAs sweep the
+// buffers together (the six-tensor batch with 8 x 32 MiB in it: 2-3 %
+// faster that way).  Either way the CTA starts at job p.flat_tab[cta],
+// the job of its first vector (written by the host).
 template <int BLOCK, int V, int S, int MAXJ, int MAXS>
-__device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta) {
+__device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta,
+                                                         uint32_t nctas) {
   extern __shared__ uint4 stage_buf[];  // [S][V][BLOCK]
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
   const uint64_t total = p.flat_vec;
   const uint64_t ntiles = (total + kTile - 1) / kTile;
-  const uint64_t t0 = static_cast<uint64_t>(cta) * p.flat_per;
-  const uint64_t t1 = min(t0 + p.flat_per, ntiles);
+  const bool runs = p.flat_per != 0;
+  const uint64_t t0 = runs ? static_cast<uint64_t>(cta) * p.flat_per : cta;
+  const uint64_t t1 = runs ? min(t0 + p.flat_per, ntiles) : ntiles;
+  const uint64_t ts = runs ? 1 : nctas;
   if (t0 >= t1) return;
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
   const int j0 = MAXJ > 1 ? static_cast<int>(p.flat_tab[cta]) : 0;
@@ -385,10 +392,10 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
 #pragma unroll
   for (int s = 0; s < S; ++s) {
     issue(s, t_issue);
-    ++t_issue;
+    t_issue += ts;
   }
   uint32_t slot = 0;
-  for (uint64_t t = t0; t < t1; ++t) {
+  for (uint64_t t = t0; t < t1; t += ts) {
     cp_async_wait<S - 1>();
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -404,7 +411,7 @@ __device__ __forceinline__ void gather_tiles_staged_jobs(const GatherParams<MAXJ
       }
     }
     issue(slot, t_issue);
-    ++t_issue;
+    t_issue += ts;
     slot = (slot + 1 == S) ? 0 : slot + 1;
   }
   cp_async_wait<0>();
@@ -736,19 +743,24 @@ __device__ __forceinline__ void copy_small_vector(const GatherParams<MAXJ, MAXS>
 // issued before its stores, so it costs one memory round trip.
 template <int BLOCK, int V, int S, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherParams<MAXJ, MAXS>& p,
-                                                                 uint32_t cta, uint64_t voff, uint64_t vend) {
+                                                                 uint32_t cta, uint32_t nctas, uint64_t voff,
+                                                                 uint64_t vend) {
   static_assert(S * V * 5 <= 32, "ring notes must fit one register");
   extern __shared__ uint4 stage_buf[];  // [S][V][2][BLOCK]
   constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
   const uint64_t total = vend;
   const uint64_t ntiles = (total - voff + kTile - 1) / kTile;
-  // CTA `cta` of the part: the contiguous run of p.real_per tiles from tile
-  // cta * real_per, starting at job p.real_tab[cta] (written by the host;
-  // a binary search here spilled registers, and walking the table from its
+  // CTA `cta` of the part: with many jobs (p.real_per > 0) the contiguous
+  // run of real_per tiles from tile cta * real_per, with few jobs tiles cta,
+  // cta + nctas, ... (as gather_tiles_staged_jobs); either way starting at
+  // job p.real_tab[cta], the job of its first vector, written by the host
+  // (a binary search here spilled registers, and walking the table from its
   // start cost a dependent read per job: 250 jobs of 128 B-4 KiB x 4 ranks
   // at +1 B took 36 us)
-  const uint64_t t0 = static_cast<uint64_t>(cta) * p.real_per;
-  const uint64_t t1 = min(t0 + p.real_per, ntiles);
+  const bool runs = p.real_per != 0;
+  const uint64_t t0 = runs ? static_cast<uint64_t>(cta) * p.real_per : cta;
+  const uint64_t t1 = runs ? min(t0 + p.real_per, ntiles) : ntiles;
+  const uint64_t ts = runs ? 1 : nctas;
   if (t0 >= t1) return;
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_buf)) + 16u * threadIdx.x;
   // issuing side: job j (vectors [jbeg, jend)), its ranks
@@ -795,10 +807,10 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
 #pragma unroll
   for (int i = 0; i < S; ++i) {
     issue(i, t_issue);
-    ++t_issue;
+    t_issue += ts;
   }
   uint32_t slot = 0;
-  for (uint64_t t = t0; t < t1; ++t) {
+  for (uint64_t t = t0; t < t1; t += ts) {
     cp_async_wait<S - 1>();
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -829,7 +841,7 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
       }
     }
     issue(slot, t_issue);
-    ++t_issue;
+    t_issue += ts;
     slot = (slot + 1 == S) ? 0 : slot + 1;
   }
   cp_async_wait<0>();
@@ -1061,13 +1073,14 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     // the other unaligned jobs
     const uint64_t fc = static_cast<uint64_t>(p.flat_ctas), sc = static_cast<uint64_t>(p.small_ctas);
     if (first < fc)
-      gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, static_cast<uint32_t>(first));
+      gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, static_cast<uint32_t>(first),
+                                                                   static_cast<uint32_t>(fc));
     else if (first + sc >= step) {
       if constexpr (MAXJ > 1) copy_small_jobs<BLOCK, kSmallSplit>(p, static_cast<uint32_t>(first + sc - step));
     }
     else
       gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
-          p, static_cast<uint32_t>(first - fc), p.flat_vec, p.small_vec);
+          p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc), p.flat_vec, p.small_vec);
   } else
     gather_tiles<BLOCK, UNROLL, MODE != kGeneral, SINGLE>(p, first, step);
 }
