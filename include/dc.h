@@ -353,6 +353,9 @@ const char *dc_status_name(int status);
  *                             tensors: cost of a realigned 16-byte vector in
  *                             percent of a staged aligned one, for splitting
  *                             the grid between the two (default 250, measured)
+ *   "gather_split_cost_warp_pct" the same when the unaligned part (more than
+ *                             16 tensors) realigns across warps (default 100,
+ *                             measured)
  *   "prefetch"                tiles per CTA whose inputs are prefetched into
  *                             L2 before the kernel waits for the previous
  *                             kernel in the stream (dc_all_gather on its
@@ -392,9 +395,11 @@ const char *dc_status_name(int status);
  *                             of dc_check_device)
  *   "gather_realign_warp"     1 (default) = a dc_all_gather whose payloads or
  *                             output are not 16-byte aligned (at least 128
- *                             bytes per rank, output under 4 GiB) realigns its
- *                             vectors across the lanes of a warp, in
- *                             registers; 0 = through a shared-memory ring
+ *                             bytes per rank, output under 4 GiB), and the
+ *                             unaligned tensors of a dc_all_gather_many with
+ *                             more than 16 of them, realign their vectors
+ *                             across the lanes of a warp, in registers;
+ *                             0 = through a shared-memory ring
  *   "fused_chunk_min"         dc_fused_all_gather: smallest chunk per CTA
  *                             (default 32768 bytes; measured, 8 ranks x 4 MiB:
  *                             75.8 us at 32 KiB, 81.9 us at 64 KiB)
@@ -404,7 +409,7 @@ const char *dc_status_name(int status);
  * Environment variables DC_FORCE_PATH, DC_FORCE_GENERIC,
  * DC_GATHER_SINGLE_MAX_BYTES, DC_GATHER_MANY_SINGLE_MAX_BYTES,
  * DC_REDUCE_SINGLE_MAX_BYTES, DC_GRID_CTAS, DC_PDL,
- * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
+ * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_GATHER_SPLIT_COST_WARP_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
  * DC_REDUCE_TILE_MIN, DC_REDUCE_STAGED, DC_GATHER_BULK, DC_GATHER_BULK_MIN_BYTES,
  * DC_BULK_CHUNK_BYTES, DC_BULK_CHUNK_MIN, DC_BULK_STAGES, DC_BULK_CTAS_PER_SM,
  * DC_BULK_PREFETCH, DC_GATHER_REALIGN_WARP, DC_FUSED_CHUNK_MIN and DC_WAIT_LIMIT_NS set the initial values (read once,

@@ -67,7 +67,8 @@ struct Options {
   std::atomic<long long> test_fail_launch{0};
   std::atomic<long long> pdl{1};
   std::atomic<long long> gather_staged{1};
-  std::atomic<long long> split_cost_pct{250};  // see plan_split
+  std::atomic<long long> split_cost_pct{250};       // see plan_split
+  std::atomic<long long> split_cost_warp_pct{100};  // see plan_split
   std::atomic<long long> prefetch{1};
   std::atomic<long long> tile_min{512};  // see staged_tile
   std::atomic<long long> reduce_tile_min{64};  // see launch_reduce_plan
@@ -104,6 +105,7 @@ const OptionKey kKeys[] = {
     {"pdl", "DC_PDL", &g_opt.pdl},
     {"gather_staged", "DC_GATHER_STAGED", &g_opt.gather_staged},
     {"gather_split_cost_pct", "DC_GATHER_SPLIT_COST_PCT", &g_opt.split_cost_pct},
+    {"gather_split_cost_warp_pct", "DC_GATHER_SPLIT_COST_WARP_PCT", &g_opt.split_cost_warp_pct},
     {"prefetch", "DC_PREFETCH", &g_opt.prefetch},
     {"gather_tile_min", "DC_GATHER_TILE_MIN", &g_opt.tile_min},
     {"reduce_tile_min", "DC_REDUCE_TILE_MIN", &g_opt.reduce_tile_min},
@@ -341,9 +343,23 @@ void fill_gather(Params& prm, const GatherTensor* ts, int T, int P, bool allow_f
 // tensors of the all_gather_many workload (P = 8), both parts staged: 100 %
 // -> 115 us, 150 % -> 108.5 us, 200 % -> 108 us, 250 % -> 100.6 us, 300 %
 // -> 104 us; every CTA on the register realigning path instead: 141 us.
+// A realigning part of more than kRoundRobinJobs jobs realigns across the
+// lanes of a warp instead (gather_realign_warp on), with boundary CTAs for
+// its rank-boundary vectors, and its vectors count
+// gather_split_cost_warp_pct / 100 staged ones.  Measured (20 calls back to
+// back, payloads of every other tensor at +1 B; ring at 250 % -> warp at 250
+// % / 100 %): 60 tensors x 8 ranks of 1-128 KiB 13.3 -> 13.3 / 10.8 us, 100
+// x 8 of 16 B-64 KiB 11.6 -> 11.3 / 9.7 us; all unaligned, 250 x 4 of 4-64
+// KiB 17.3 -> 11.6 us, 60 x 8 of 1-128 KiB 13.3 -> 9.8 us.  The six mixed
+// tensors (one unaligned job of 7 MiB+5 B) stay on the ring: on the warp path
+// they took 113-114 us against 109 us.
 // Each part gets the fewest CTAs that finish its tiles in the same number of
 // rounds.  Returns the total grid, 0 if no split is possible (fewer CTAs than
 // parts with work).
+// Parts of all_gather_many with more jobs than this take contiguous runs
+// of tiles per CTA (and the realigning part realigns across warps).
+constexpr int kRoundRobinJobs = 16;
+
 template <class Params>
 int plan_split(Params& prm, uint64_t cap) {
   const uint64_t fv = prm.flat_vec, gv = prm.small_vec - prm.flat_vec, sv = prm.total_vec - prm.small_vec;
@@ -369,6 +385,20 @@ int plan_split(Params& prm, uint64_t cap) {
     prm.small_tab[sc] = static_cast<uint16_t>(prm.njobs - 1 - prm.small_job0);
   }
   cap -= sc;
+  // the realigning part: across warps (with CTAs for its jobs' rank-boundary
+  // vectors, one per kGatherBlock (job, boundary) pairs, at most
+  // kMaxBoundaryCtas) when it has more than kRoundRobinJobs jobs, else the ring
+  int nflat = 0;
+  while (nflat < prm.njobs && (prm.job[nflat].flags & kJobFlat)) ++nflat;
+  const int nreal = prm.small_job0 - nflat;
+  uint64_t bc = 0;
+  prm.realign_warp = prm.realign_warp && gv > 0 && nreal > kRoundRobinJobs ? 1 : 0;
+  if (prm.realign_warp) {
+    const uint64_t pairs = static_cast<uint64_t>(nreal) * static_cast<uint64_t>(prm.P + 1);
+    bc = std::min<uint64_t>((pairs + kGatherBlock - 1) / kGatherBlock, kMaxBoundaryCtas);
+    if (cap < others + bc) return 0;
+    cap -= bc;
+  }
   const uint64_t ftile = static_cast<uint64_t>(kGatherBlock) * kSplitVectors;
   const uint64_t gtile = static_cast<uint64_t>(kGatherBlock) * kSplitRealignVectors;
   const uint64_t ft = (fv + ftile - 1) / ftile, gt = (gv + gtile - 1) / gtile;
@@ -380,7 +410,8 @@ int plan_split(Params& prm, uint64_t cap) {
     gf = 0;
     gg = std::min(cap, gt);
   } else {
-    const double cost = static_cast<double>(std::max(1LL, g_opt.split_cost_pct.load())) / 100.0;
+    const long long pct = prm.realign_warp ? g_opt.split_cost_warp_pct.load() : g_opt.split_cost_pct.load();
+    const double cost = static_cast<double>(std::max(1LL, pct)) / 100.0;
     const double wf = static_cast<double>(fv), wg = cost * static_cast<double>(gv);
     gf = static_cast<uint64_t>(static_cast<double>(cap) * wf / (wf + wg) + 0.5);
     gf = std::min(std::max<uint64_t>(gf, 1), cap - 1);
@@ -403,12 +434,6 @@ int plan_split(Params& prm, uint64_t cap) {
   // round robin.  tab[c] is the job of CTA c's first vector, found by one
   // forward walk over the jobs.
   constexpr uint64_t kPartTab = sizeof(prm.flat_tab) / sizeof(prm.flat_tab[0]);
-  constexpr int kRoundRobinJobs = 16;
-  const int nflat = [&prm] {
-    int n = 0;
-    while (n < prm.njobs && (prm.job[n].flags & kJobFlat)) ++n;
-    return n;
-  }();
   auto deal = [&](uint64_t tiles, uint64_t g, uint64_t tile, uint64_t v0, int njobs_part, uint16_t* tab,
                      uint32_t* per_out) {
     if (g == 0 || tiles == 0) {
@@ -433,10 +458,11 @@ int plan_split(Params& prm, uint64_t cap) {
     return g;
   };
   gf = deal(ft, gf, ftile, 0, nflat, prm.flat_tab, &prm.flat_per);
-  gg = deal(gt, gg, gtile, fv, prm.small_job0 - nflat, prm.real_tab, &prm.real_per);
+  gg = deal(gt, gg, gtile, fv, nreal, prm.real_tab, &prm.real_per);
   prm.flat_ctas = static_cast<int32_t>(gf);
   prm.small_ctas = static_cast<int32_t>(sc);
-  return static_cast<int>(gf + gg + sc);
+  prm.bnd_ctas = static_cast<int32_t>(gg ? bc : 0);
+  return static_cast<int>(gf + gg + prm.bnd_ctas + sc);
 }
 
 // Work units per tile, chosen so that every SM gets the same share of a
@@ -496,6 +522,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
   prm.prefetch = static_cast<int32_t>(std::min<long long>(g_opt.prefetch.load(), 64));
   prm.flat_ctas = 0;
   prm.small_ctas = 0;
+  prm.bnd_ctas = 0;
   prm.tile_vec = 0;  // single-CTA launches: the kernel's own tile
   int grid = 1;
   if (!single) {
@@ -511,6 +538,7 @@ dc_status_t launch_gather_plan(Params& prm, int family, uint64_t out_bytes, cuda
         prm.staged = 0;
         prm.flat_ctas = 0;
         prm.small_ctas = 0;
+        prm.bnd_ctas = 0;
         mode = gather_mode_of(prm);
       }
     }

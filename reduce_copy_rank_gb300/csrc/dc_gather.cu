@@ -74,6 +74,7 @@ enum : uint32_t {
   kSiteBytes = 100, kSiteFlat1 = 101, kSiteStaged1 = 102, kSiteStagedRing = 103, kSiteStagedJobs = 104,
   kSiteSpan = 105, kSiteBoundary = 106, kSiteRealign = 107, kSiteSmallVec = 108, kSiteRealignJobs = 109,
   kSiteSmallJobs = 110, kSiteGeneral = 111, kSitePrefetch = 112, kSiteWarpRealign = 113,
+  kSiteWarpRealignJobs = 114,
 };
 template <int MAXJ, int MAXS>
 __device__ __forceinline__ bool load_ok(const GatherParams<MAXJ, MAXS>& p, const GatherJob& J, uint32_t r,
@@ -847,6 +848,99 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
   cp_async_wait<0>();
 }
 
+// The unaligned jobs of a split launch (global vectors [voff, vend)),
+// realigned across the lanes of a warp in registers, as
+// gather_tiles_warp_realign does for one job: lane i of a warp loads the
+// first source block of its vector k and takes the second one from lane
+// i + 1, which holds vector k + 1; a lane whose neighbour is in another rank
+// or job, lane 31, and the last vector of a tile load their own second block.
+// Tiles are dealt as in gather_tiles_staged_realign_jobs (runs for many
+// jobs, round robin for few, from the job p.real_tab[cta]); a thread walks
+// jobs and ranks forward.  The vectors not inside one rank (at most P+1 per
+// job) are skipped here and copied by the part's boundary CTAs
+// (copy_boundaries_jobs), beside the tiles: copied inline, their byte
+// assembly spilled this part's registers.
+template <int BLOCK, int V, int MAXJ, int MAXS>
+__device__ __forceinline__ void gather_tiles_warp_realign_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta,
+                                                               uint32_t nctas, uint64_t voff, uint64_t vend) {
+  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
+  const uint64_t ntiles = (vend - voff + kTile - 1) / kTile;
+  const bool runs = p.real_per != 0;
+  const uint64_t t0 = runs ? static_cast<uint64_t>(cta) * p.real_per : cta;
+  const uint64_t t1 = runs ? min(t0 + p.real_per, ntiles) : ntiles;
+  const uint64_t ts = runs ? 1 : nctas;
+  const uint32_t lane = threadIdx.x & 31u;
+  int j = MAXJ > 1 ? static_cast<int>(p.real_tab[cta]) : 0;
+  uint64_t jbeg = p.job[j].vfirst, jend = jbeg + p.job[j].nvec;
+  RankWalk<uint64_t> w{0, 0, 0, 0, 0, true};
+  for (uint64_t t = t0; t < t1; t += ts) {
+    uint4 lo[V], hi[V];
+    uint64_t dst[V];
+    uint32_t meta[V];  // s | inside << 4 | own second block << 5 | store in bounds << 6
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint64_t i = static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
+      const uint64_t k = voff + t * kTile + i;
+      meta[u] = 0;
+      if (k < vend) {
+        while (k >= jend) {
+          ++j;
+          jbeg = p.job[j].vfirst;
+          jend = jbeg + p.job[j].nvec;
+          w.fresh = true;
+        }
+        const GatherJob& J = p.job[j];
+        const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
+        const uint64_t kl = k - jbeg;
+        walk_to(w, p, J, xbase, kl);
+        dst[u] = xbase + 16 * kl;
+        if (kl >= w.klo && kl < w.khi) {
+          const bool own_hi = w.s != 0 && (lane == 31u || kl + 1 >= w.khi || i + 1 >= kTile);
+          const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * kl);
+          if (load_ok(p, J, w.r, blk, 16, kSiteWarpRealignJobs)) lo[u] = ld_nc_cached(blk);
+          if (own_hi && load_ok(p, J, w.r, blk + 1, 16, kSiteWarpRealignJobs)) hi[u] = ld_nc_cached(blk + 1);
+          // (the checked build tests the store against this vector's job
+          // here: by the store, the thread may have entered the next job)
+          const bool sok = store_ok(p, J, reinterpret_cast<void*>(dst[u]), 16, kSiteWarpRealignJobs);
+          meta[u] = w.s | 16u | (own_hi ? 32u : 0u) | (sok ? 64u : 0u);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      uint4 nb;  // every lane takes part in the shuffles
+      nb.x = __shfl_down_sync(0xffffffffu, lo[u].x, 1);
+      nb.y = __shfl_down_sync(0xffffffffu, lo[u].y, 1);
+      nb.z = __shfl_down_sync(0xffffffffu, lo[u].z, 1);
+      nb.w = __shfl_down_sync(0xffffffffu, lo[u].w, 1);
+      const uint32_t m = meta[u];
+      if (m & 16u) {
+        const uint32_t sh = m & 15u;
+        const uint4 second = (m & 32u) ? hi[u] : nb;
+        if (m & 64u) st16(reinterpret_cast<uint4*>(dst[u]), sh ? realign16(lo[u], second, sh) : lo[u]);
+      }
+    }
+  }
+}
+
+// The rank-boundary vectors of the unaligned jobs of a split launch (jobs
+// [p.real_tab[0], p.small_job0)), copied by `nctas` CTAs: pair (job j, b),
+// b in [0, P], is the vector holding d_b = out_j + b*B_j if d_b is not
+// 16-byte aligned (as copy_boundaries does for one job).
+template <int BLOCK, int MAXJ, int MAXS>
+__device__ __forceinline__ void copy_boundaries_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta,
+                                                     uint32_t nctas) {
+  const uint32_t j0 = MAXJ > 1 ? p.real_tab[0] : 0;
+  const uint32_t P1 = static_cast<uint32_t>(p.P) + 1;
+  const uint32_t pairs = (static_cast<uint32_t>(p.small_job0) - j0) * P1;
+  for (uint32_t idx = cta * BLOCK + threadIdx.x; idx < pairs; idx += nctas * BLOCK) {
+    const uint32_t jj = idx / P1, b = idx - jj * P1;
+    const GatherJob& J = p.job[j0 + jj];
+    const uint64_t d = J.out + static_cast<uint64_t>(b) * J.bytes;
+    if (d & 15u) copy_boundary(p, J, d & ~static_cast<uint64_t>(15), b == 0 ? 0u : b - 1);
+  }
+}
+
 // The jobs of fewer than kGatherSmallBytes bytes per rank of a split launch
 // (jobs [small_job0, njobs), global vectors [small_vec, total_vec)), copied by
 // the launch's last `nctas` CTAs.  CTA c takes the contiguous run of
@@ -1069,15 +1163,23 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
       gather_tiles_staged_realign<BLOCK, kRealignVectors, kRealignStages, uint64_t>(p, first, step);
   }
   else if constexpr (MODE == kManySplit) {
-    // CTAs [0, fc): aligned jobs; [step - sc, step): the small jobs; the rest:
-    // the other unaligned jobs
+    // CTAs [0, fc): aligned jobs; [step - sc, step): the small jobs; [step -
+    // sc - bc, step - sc): the rank-boundary vectors of the unaligned jobs
+    // (warp realigning only); the rest: the other unaligned jobs
     const uint64_t fc = static_cast<uint64_t>(p.flat_ctas), sc = static_cast<uint64_t>(p.small_ctas);
+    const uint64_t bc = static_cast<uint64_t>(p.bnd_ctas);
     if (first < fc)
       gather_tiles_staged_jobs<BLOCK, kSplitVectors, kSplitStages>(p, static_cast<uint32_t>(first),
                                                                    static_cast<uint32_t>(fc));
     else if (first + sc >= step) {
       if constexpr (MAXJ > 1) copy_small_jobs<BLOCK, kSmallSplit>(p, static_cast<uint32_t>(first + sc - step));
     }
+    else if (first + sc + bc >= step)
+      copy_boundaries_jobs<BLOCK>(p, static_cast<uint32_t>(first + sc + bc - step), static_cast<uint32_t>(bc));
+    else if (p.realign_warp)
+      gather_tiles_warp_realign_jobs<BLOCK, kSplitRealignVectors>(
+          p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc - bc), p.flat_vec,
+          p.small_vec);
     else
       gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
           p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc), p.flat_vec, p.small_vec);

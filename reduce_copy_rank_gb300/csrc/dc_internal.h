@@ -76,6 +76,8 @@ constexpr int kSmallSplit = 4;
 constexpr int kMaxSmallCtas = 512;
 // split launch: CTAs of its aligned part and of its realigning part, each at most
 constexpr int kMaxPartCtas = 1024;
+// split launch, warp realigning: CTAs that copy the unaligned jobs' rank-boundary vectors, at most
+constexpr int kMaxBoundaryCtas = 4;
 
 // ------------------------------------------------------------- gather ---
 enum : uint32_t {
@@ -114,6 +116,8 @@ struct GatherParams {
   int32_t realign_warp; // one unaligned job: realign across the warp's lanes (mode 6), not through a ring
   uint32_t flat_per;    // split launch: tiles per aligned-part CTA (a contiguous run)
   uint32_t real_per;    // split launch: tiles per realigning-part CTA (a contiguous run)
+  int32_t bnd_ctas;     // split launch, warp realigning: CTAs after the realigning part that copy
+                        // its jobs' rank-boundary vectors
   GatherJob job[MAXJ];
   uint64_t src[MAXS];   // tensor-major: job j's rank r is src[job[j].src0 + r]
   // split launch: small-job CTA c covers jobs small_job0 + small_tab[c] ..

@@ -195,6 +195,30 @@ def test_many_large_table():
     assert guards
 
 
+@pytest.mark.parametrize("opts", [{}, {"gather_realign_warp": 0}, {"grid_ctas": 3}, {"grid_ctas": 4},
+                                  {"grid_ctas": 6}, {"grid_ctas": 40}, {"grid_ctas": 5000},
+                                  {"gather_split_cost_warp_pct": 400}],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "default")
+def test_many_jobs_runs_and_warp_realign(opts):
+    """More than 16 jobs in each part: contiguous runs of tiles per CTA from
+    the host's start-job tables; the unaligned part realigned across the
+    lanes of a warp, its rank-boundary vectors copied by their own CTAs (or
+    through the ring with gather_realign_warp=0); small grids fall back to
+    fewer parts."""
+    rng = np.random.default_rng(W.seed_for(5, 9010))
+    P, T = 4, 90
+    sizes = [int(B) for B in rng.integers(128, 70000, T)]
+    sizes = [((B + 15) // 16) * 16 if t % 3 == 0 else B for t, B in enumerate(sizes)]
+    tensors = [[rng.integers(0, 256, B, dtype=np.uint8) for _ in range(P)] for B in sizes]
+    in_offs = [[0] * P if t % 3 == 0 else [int(x) for x in rng.integers(0, 16, P)] for t in range(T)]
+    out_offs = [0 if t % 3 == 0 else int(rng.integers(0, 16)) for t in range(T)]
+    want = oracle.all_gather_many(tensors)
+    got, guards = run_many(tensors, in_offs, out_offs, **opts)
+    for t in range(T):
+        assert np.array_equal(got[t], want[t]), (t, opts)
+    assert guards
+
+
 def test_many_tensor_api():
     P = 4
     tensors = [[torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda") for _ in range(P)]
