@@ -262,19 +262,54 @@ class _Staged:
             raise DCError(_INVALID, f"ranks disagree on the collective: {sigs}")
         if self.handshake == "shm":
             self._hs = ShmHandshake(group, self.rank, self.world, timeout)
-        self.local = transport.alloc(self.staging_bytes)
         # one descriptor per peer (CUDA IPC counts the references it hands
-        # out: one export per process that opens it)
-        mine = [None if q == self.rank else transport.export(self.local) for q in range(self.world)]
+        # out: one export per process that opens it).  A rank that fails to
+        # allocate or export still takes part in the exchange, with its
+        # error, so that every rank raises instead of waiting for it.
+        try:
+            self.local = transport.alloc(self.staging_bytes)
+            mine = ("ok", [None if q == self.rank else transport.export(self.local) for q in range(self.world)])
+        except Exception as e:  # reported to every rank below
+            self.local = None
+            mine = ("error", f"rank {self.rank}: {e!r}")
         descs = [None] * self.world
         dist.all_gather_object(descs, mine, group=group)
-        self.peers = [self.local if q == self.rank else transport.open(descs[q][self.rank])
-                      for q in range(self.world)]
-        self._barrier("setup")
+        failed = [d[1] for d in descs if d[0] != "ok"]
+        if failed:
+            self.aborted = "setup: " + "; ".join(failed)
+            self._release_after_failed_setup()
+            raise DCError(_INVALID, self.aborted)
+        # a rank that fails to open a peer's buffer raises DC_ERR_INVALID and
+        # never reaches the setup barrier: the others time out there (within
+        # the bound), or fail to open its buffer once it released it; either
+        # way every rank releases its buffers before it raises
+        try:
+            self.peers = [self.local if q == self.rank else self._open(q, descs[q][1][self.rank])
+                          for q in range(self.world)]
+            self._barrier("setup")
+        except BaseException:
+            self._release_after_failed_setup()
+            raise
         # every rank has opened every shared buffer: their names can go
         self.transport.opened_by_all()
         if self._hs is not None:
             self._hs.opened_by_all()
+
+    def _open(self, q: int, desc):
+        try:
+            return self.transport.open(desc)
+        except Exception as e:
+            self.aborted = f"setup: rank {self.rank} could not open the buffer of rank {q}: {e!r}"
+            raise DCError(_INVALID, self.aborted) from e
+
+    def _release_after_failed_setup(self) -> None:
+        self.closed = True
+        self.peers = []
+        self.transport.close_peers()
+        self.local = None
+        self.transport.release()
+        if self._hs is not None:
+            self._hs.close()
 
     def _wait_all(self) -> str | None:
         """One barrier; None once every rank arrived, else what went wrong."""

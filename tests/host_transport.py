@@ -21,12 +21,15 @@ class HostTransport:
     # hosts do not, so the default is the process group's barrier
     default_handshake = "gloo"
 
-    def __init__(self, dtype: str = "u8"):
+    def __init__(self, dtype: str = "u8", fail_alloc: bool = False, fail_open: bool = False):
         self.dtype = dtype
+        self.fail_alloc, self.fail_open = fail_alloc, fail_open
         self._owned = []
         self._opened = []
 
     def alloc(self, nbytes: int):
+        if self.fail_alloc:  # (tests: an allocation that fails on this rank)
+            raise MemoryError("injected allocation failure")
         mem = SharedBytes(nbytes)
         self._owned.append(mem)
         return mem.array(np.uint8, nbytes), mem.path
@@ -35,6 +38,8 @@ class HostTransport:
         return buf[1]
 
     def open(self, desc):
+        if self.fail_open:  # (tests: a peer buffer that cannot be mapped here)
+            raise OSError("injected failure to open a peer's buffer")
         mem = SharedBytes(path=desc)
         self._opened.append(mem)
         return mem.array(np.uint8, mem.size), desc

@@ -56,6 +56,17 @@ def _worker(rank, world, port, case, handshake, outdir):
             except dc.DCError as e:
                 res["raised"] = e.status
             return
+        if case in ("fail_alloc", "fail_open"):
+            t0 = time.time()
+            try:
+                StagedAllGather(None, B, HostTransport(fail_alloc=(case == "fail_alloc" and rank == 1),
+                                                      fail_open=(case == "fail_open" and rank == 1)),
+                                timeout=2.0, handshake=handshake)
+                res["raised"] = None
+            except dc.DCError as e:
+                res["raised"], res["msg"] = e.status, str(e)
+            res["seconds"] = time.time() - t0
+            return
         if case == "mismatch_dtype":
             try:
                 StagedAllReduce(None, 64, "bf16" if rank == 0 else "f16", HostTransport(), timeout=2.0,
@@ -172,6 +183,25 @@ def test_reductions_over_epochs(case, handshake, tmp_path):
     res = _run(world, case, tmp_path, handshake)
     for r in range(world):
         assert res[r]["ok"] == [True, True, True], res[r]
+
+
+@pytest.mark.parametrize("handshake", HANDSHAKES)
+def test_setup_failure_on_one_rank_raises_on_every_rank(handshake, tmp_path):
+    """A rank whose allocation fails sends its error through the descriptor
+    exchange: every rank raises DC_ERR_INVALID at once.  A rank that cannot
+    open a peer's buffer raises DC_ERR_INVALID there; the others time out at
+    the setup barrier within the bound, or cannot open its buffer once it has
+    released it (DC_ERR_INVALID): none waits for the process group."""
+    res = _run(3, "fail_alloc", tmp_path, handshake)
+    for r in range(3):
+        assert res[r]["raised"] == 1 and "injected allocation failure" in res[r]["msg"], res[r]
+        assert res[r]["seconds"] < 10.0, res[r]
+    (tmp_path / "open").mkdir()
+    res = _run(3, "fail_open", tmp_path / "open", handshake)
+    assert res[1]["raised"] == 1 and "injected failure to open" in res[1]["msg"], res[1]
+    for r in (0, 2):
+        assert res[r]["raised"] in (1, 6) and "setup" in res[r]["msg"], res[r]
+        assert res[r]["seconds"] < 30.0, res[r]
 
 
 def test_reduction_dtype_mismatch_raises_on_every_rank(tmp_path):
