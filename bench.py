@@ -91,12 +91,14 @@ def parse_args(argv=None):
     ap.add_argument("--skew-trials", type=int, default=50)
     ap.add_argument("--skew-warmup", type=int, default=10)
     ap.add_argument("--ipc", action="store_true",
-                    help="the staged all-gather across processes: one process per rank on this "
+                    help="the staged collectives across processes: one process per rank on this "
                          "GPU, staging buffers shared by CUDA IPC, host handshakes (one JSON "
-                         "line per rank count and size)")
+                         "line per operation, rank count, handshake and size)")
     ap.add_argument("--ipc-ranks", nargs="+", type=int, default=[2, 4])
     ap.add_argument("--ipc-sizes", nargs="+", type=int, default=[4096, 1 << 20, 4 << 20])
     ap.add_argument("--ipc-handshakes", nargs="+", choices=["shm", "gloo"], default=["shm", "gloo"])
+    ap.add_argument("--ipc-ops", nargs="+", choices=["all_gather", "all_reduce", "reduce_scatter"],
+                    default=["all_gather", "all_reduce", "reduce_scatter"])
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
     ap.add_argument("--case", default=None, metavar="OP:P:BYTES:REPS",
                     help="profiling helper: run one call REPS times and exit, e.g. "
@@ -105,7 +107,8 @@ def parse_args(argv=None):
                          "element off; BYTES per rank), "
                          "many:8:0:3 (the all_gather_many workload), manytiny:8:0:3 (120 tiny "
                          "tensors), gatherbulk:8:4194304:3 (the opt-in bulk-copy gather) or "
-                         "fused:8:4194304:3 (the staged protocol), fill:8:33554432:2 (torch's "
+                         "fused:8:4194304:3 (the staged protocol), manymid:4:0:2 (250 tensors of 4-64 KiB at +1 B), "
+                         "fill:8:33554432:2 (torch's "
                          "write-only fill of P * BYTES, a comparator)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
@@ -1092,47 +1095,78 @@ def run_crossover(args) -> int:
     return 0
 
 
-def _ipc_worker(rank, world, port, sizes, handshakes, steps, warmup, outfile):
-    """One rank of `--ipc` (a spawned process)."""
+def _ipc_worker(rank, world, port, ops, sizes, handshakes, steps, warmup, outfile):
+    """One rank of `--ipc` (a spawned process).  For each operation,
+    handshake and payload size B (bytes per rank; BF16 for the reductions):
+    warm-up, `steps` timed epochs, a bit check against the single-process
+    entry point on local copies, and the kernel alone over the mapped
+    staging buffers."""
     import torch
     import torch.distributed as dist
 
     import reduce_copy_rank_gb300 as dc
-    from reduce_copy_rank_gb300.ipc import CudaIpcTransport, StagedAllGather
+    from reduce_copy_rank_gb300.ipc import CudaIpcTransport, StagedAllGather, StagedAllReduce, StagedReduceScatter
 
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     torch.cuda.set_device(0)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     lines = []
-    for hs, B in [(h, b) for h in handshakes for b in sizes]:
-        coll = StagedAllGather(None, B, CudaIpcTransport(), timeout=60.0, handshake=hs)
-        payloads = [W.random_bytes_device(W.seed_for(2, 950), q, B, "cuda") for q in range(world)]
-        expect = torch.cat(payloads)
-        out = torch.empty(world * B, dtype=torch.uint8, device="cuda")
+    for op, hs, B in [(o, h, b) for o in ops for h in handshakes for b in sizes]:
+        if op == "all_gather":
+            coll = StagedAllGather(None, B, CudaIpcTransport(), timeout=60.0, handshake=hs)
+            payloads = [W.random_bytes_device(W.seed_for(2, 950), q, B, "cuda") for q in range(world)]
+            expect = torch.cat(payloads)
+            out = torch.empty(world * B, dtype=torch.uint8, device="cuda")
+            run = lambda: coll.all_gather(payloads[rank], out)  # noqa: E731
+            kernel = lambda views: dc.all_gather(views, out)  # noqa: E731
+            alg = algorithmic_bytes(world, B)
+        else:
+            n = B // 2
+            payloads = [W.normal_bf16_device(W.seed_for(4, 950), q, n, "cuda") for q in range(world)]
+            if op == "all_reduce":
+                coll = StagedAllReduce(None, n, "bf16", CudaIpcTransport(), timeout=60.0, handshake=hs)
+                outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+                dc.all_reduce(payloads, outs)
+                expect = outs[rank]
+                out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+                run = lambda: coll.all_reduce(payloads[rank], out)  # noqa: E731
+                offset, alg = 0, (world + 1) * B
+            else:
+                C = n // world
+                coll = StagedReduceScatter(None, C, "bf16", CudaIpcTransport(), timeout=60.0, handshake=hs)
+                payloads = [x[:world * C] for x in payloads]
+                outs = [torch.empty(C, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+                dc.reduce_scatter(payloads, outs)
+                expect = outs[rank]
+                out = torch.empty(C, dtype=torch.bfloat16, device="cuda")
+                run = lambda: coll.reduce_scatter(payloads[rank], out)  # noqa: E731
+                offset, alg = rank * C, world * C * 2 + C * 2
+            nbytes = payloads[0].nbytes
+            kernel = lambda views: dc.reduce([v.view(torch.bfloat16) for v in views], out, offset=offset)  # noqa: E731
         for _ in range(warmup):
-            coll.all_gather(payloads[rank], out)
+            run()
         coll.seconds = dict.fromkeys(coll.seconds, 0.0)
         dist.barrier()
         t0 = time.perf_counter()
         for _ in range(steps):
-            coll.all_gather(payloads[rank], out)
+            run()
         epoch_s = (time.perf_counter() - t0) / steps
-        exact = bool(torch.equal(out, expect))
-        # the gather kernel alone over the mapped staging buffers, one rank at a
-        # time: a CUDA graph of 20 back-to-back gathers (eager calls from
-        # Python would time the host's launch rate instead)
+        exact = bool(torch.equal(out.view(torch.uint8), expect.view(torch.uint8)))
+        # the kernel alone over the mapped staging buffers, one rank at a
+        # time: a CUDA graph of 20 back-to-back calls (eager calls from Python
+        # would time the host's launch rate instead)
         kernel_us = 0.0
         for q in range(world):
             dist.barrier()
             if q == rank:
-                views = [b[:B] for b in coll.peers]
+                views = [b[:(B if op == "all_gather" else nbytes)] for b in coll.peers]
                 side = torch.cuda.Stream()
                 with torch.cuda.stream(side):
-                    dc.all_gather(views, out)
+                    kernel(views)
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=side):
                         for _ in range(20):
-                            dc.all_gather(views, out)
+                            kernel(views)
                 torch.cuda.synchronize()
                 times = []
                 for _ in range(5):
@@ -1148,21 +1182,21 @@ def _ipc_worker(rank, world, port, sizes, handshakes, steps, warmup, outfile):
         vals = torch.tensor([epoch_s] + [coll.seconds[k] / steps for k in coll.seconds] + [kernel_us, float(not exact)],
                             dtype=torch.float64)
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-        del payloads, expect, out
+        del payloads, expect, out, run, kernel
         coll.close()
         if rank == 0:
             v = vals.tolist()
             lines.append({
-                "metric": "staged all-gather across processes on one GPU: us per epoch",
-                "impl": "dc-ipc", "P": world, "bytes_per_rank": B, "epochs": steps, "warmup": warmup,
+                "metric": f"staged {op} across processes on one GPU: us per epoch",
+                "impl": "dc-ipc", "op": op, "P": world, "bytes_per_rank": B, "epochs": steps, "warmup": warmup,
                 "us_per_epoch": v[0] * 1e6,
                 "phases_us": {k: x * 1e6 for k, x in zip(coll.seconds, v[1:5])},
-                "gather_kernel_us": v[5],
-                "gather_kernel_gbs": algorithmic_bytes(world, B) / (v[5] * 1e3) if v[5] > 0 else None,
-                "bit_exact": v[6] == 0.0,
+                "kernel_us": v[5],
+                "kernel_gbs": alg / (v[5] * 1e3) if v[5] > 0 else None,
+                "bit_exact_vs_single_process_entry_point": v[6] == 0.0,
                 "timing": "host clock around each epoch (max over ranks); the kernel by CUDA events "
-                          "around a graph of 20 back-to-back gathers over the mapped buffers, one rank "
-                          "at a time (median of 5 replays)",
+                          "around a graph of 20 back-to-back calls over the mapped buffers, one rank "
+                          "at a time (median of 5 replays; buffers L2-resident)",
                 "handshake": {"shm": "node-local shared-memory arrival counters, bounded",
                               "gloo": "gloo monitored_barrier, bounded"}[hs],
             })
@@ -1174,7 +1208,7 @@ def _ipc_worker(rank, world, port, sizes, handshakes, steps, warmup, outfile):
 
 
 def run_ipc(args) -> int:
-    """`--ipc`: the staged all-gather across processes, ranks as processes
+    """`--ipc`: the staged collectives across processes, ranks as processes
     sharing this GPU (CUDA IPC staging buffers, host handshakes)."""
     import socket
     import tempfile
@@ -1189,8 +1223,8 @@ def run_ipc(args) -> int:
             port = so.getsockname()[1]
         with tempfile.TemporaryDirectory() as td:
             path = os.path.join(td, "ipc.jsonl")
-            mp.spawn(_ipc_worker, args=(world, port, list(args.ipc_sizes), list(args.ipc_handshakes),
-                                        steps, warmup, path),
+            mp.spawn(_ipc_worker, args=(world, port, list(args.ipc_ops), list(args.ipc_sizes),
+                                        list(args.ipc_handshakes), steps, warmup, path),
                      nprocs=world, join=True)
             with open(path) as fh:
                 for ln in fh:
@@ -1273,6 +1307,13 @@ def run_case(args) -> int:
     elif op == "manytiny":  # 120 tensors of 3..100 B per rank at +1 B (BYTES unused)
         rng = np.random.default_rng(W.seed_for(5, 9005))
         sizes = [int(x) for x in rng.integers(3, 101, 120)]
+        tens = [[torch.randint(0, 256, (B + 1,), dtype=torch.uint8, device=device)[1:] for _ in range(P)]
+                for B in sizes]
+        outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in sizes]
+        fn = lambda: dc.all_gather_many(tens, outs)  # noqa: E731
+    elif op == "manymid":  # 250 tensors of 4..64 KiB per rank at +1 B (BYTES unused)
+        rng = np.random.default_rng(W.seed_for(5, 9011))
+        sizes = [int(x) for x in rng.integers(4096, 65537, 250)]
         tens = [[torch.randint(0, 256, (B + 1,), dtype=torch.uint8, device=device)[1:] for _ in range(P)]
                 for B in sizes]
         outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in sizes]
