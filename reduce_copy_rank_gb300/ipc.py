@@ -135,12 +135,26 @@ class ShmHandshake:
         import torch.distributed as dist
 
         self.rank, self.world, self.timeout = rank, world, timeout
-        mem = SharedBytes(8 * world) if rank == 0 else None
+        self.seq = 0
+        self.error = None  # set if this rank could not create or open the counters
+        mem = None
+        if rank == 0:
+            try:
+                mem = SharedBytes(8 * world)
+            except OSError as e:
+                self.error = e
         paths = [None] * world
         dist.all_gather_object(paths, mem.path if mem else None, group=group)
-        self._mem = mem if mem else SharedBytes(path=paths[0])
-        self.slots = self._mem.array(np.uint64, world)
-        self.seq = 0
+        self._mem, self.slots = mem, None
+        if self._mem is None and paths[0] is not None:
+            try:
+                self._mem = SharedBytes(path=paths[0])
+            except OSError as e:
+                self.error = e
+        elif paths[0] is None and self.error is None:
+            self.error = RuntimeError("rank 0 could not create the arrival counters")
+        if self._mem is not None:
+            self.slots = self._mem.array(np.uint64, world)
 
     def wait(self) -> list:
         self.seq += 1
@@ -158,7 +172,8 @@ class ShmHandshake:
         return []
 
     def opened_by_all(self) -> None:
-        self._mem.unlink()
+        if self._mem is not None:
+            self._mem.unlink()
 
     def close(self) -> None:
         if self._mem is None:
@@ -264,9 +279,12 @@ class _Staged:
             self._hs = ShmHandshake(group, self.rank, self.world, timeout)
         # one descriptor per peer (CUDA IPC counts the references it hands
         # out: one export per process that opens it).  A rank that fails to
-        # allocate or export still takes part in the exchange, with its
-        # error, so that every rank raises instead of waiting for it.
+        # open the handshake's counters, allocate or export still takes part
+        # in the exchange, with its error, so that every rank raises instead
+        # of waiting for it.
         try:
+            if self._hs is not None and self._hs.error is not None:
+                raise self._hs.error
             self.local = transport.alloc(self.staging_bytes)
             mine = ("ok", [None if q == self.rank else transport.export(self.local) for q in range(self.world)])
         except Exception as e:  # reported to every rank below
