@@ -505,7 +505,7 @@ def reduce(inputs: Sequence, out, offset: int = 0, order: str = "linear", stream
         _device_tensor(t, f"inputs[{i}]")
         if t.dtype != dt:
             raise ValueError(f"inputs[{i}] has dtype {t.dtype}, expected {dt}")
-        if t.numel() < offset + n:
+        if n and t.numel() < offset + n:  # (nothing is read when n == 0)
             raise ValueError(f"inputs[{i}] has {t.numel()} elements, fewer than offset + n = {offset + n}")
         if t.get_device() != dev:
             _wrong_device(f"inputs[{i}]", t, dev)
