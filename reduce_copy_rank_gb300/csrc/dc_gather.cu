@@ -860,43 +860,43 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
 // job) are skipped here and copied by the part's boundary CTAs
 // (copy_boundaries_jobs), beside the tiles: copied inline, their byte
 // assembly spilled this part's registers.
-template <int BLOCK, int V, int MAXJ, int MAXS>
+template <int BLOCK, int V, typename Idx, int MAXJ, int MAXS>
 __device__ __forceinline__ void gather_tiles_warp_realign_jobs(const GatherParams<MAXJ, MAXS>& p, uint32_t cta,
-                                                               uint32_t nctas, uint64_t voff, uint64_t vend) {
-  constexpr uint64_t kTile = static_cast<uint64_t>(BLOCK) * V;
-  const uint64_t ntiles = (vend - voff + kTile - 1) / kTile;
+                                                               uint32_t nctas, Idx voff, Idx vend) {
+  constexpr Idx kTile = static_cast<Idx>(BLOCK) * V;
+  const Idx ntiles = (vend - voff + kTile - 1) / kTile;
   const bool runs = p.real_per != 0;
-  const uint64_t t0 = runs ? static_cast<uint64_t>(cta) * p.real_per : cta;
-  const uint64_t t1 = runs ? min(t0 + p.real_per, ntiles) : ntiles;
-  const uint64_t ts = runs ? 1 : nctas;
+  const Idx t0 = runs ? static_cast<Idx>(cta) * static_cast<Idx>(p.real_per) : static_cast<Idx>(cta);
+  const Idx t1 = runs ? min(t0 + static_cast<Idx>(p.real_per), ntiles) : ntiles;
+  const Idx ts = runs ? 1 : static_cast<Idx>(nctas);
   const uint32_t lane = threadIdx.x & 31u;
   int j = MAXJ > 1 ? static_cast<int>(p.real_tab[cta]) : 0;
-  uint64_t jbeg = p.job[j].vfirst, jend = jbeg + p.job[j].nvec;
-  RankWalk<uint64_t> w{0, 0, 0, 0, 0, true};
-  for (uint64_t t = t0; t < t1; t += ts) {
+  Idx jbeg = static_cast<Idx>(p.job[j].vfirst), jend = jbeg + static_cast<Idx>(p.job[j].nvec);
+  RankWalk<Idx> w{0, 0, 0, 0, 0, true};
+  for (Idx t = t0; t < t1; t += ts) {
     uint4 lo[V], hi[V];
     uint64_t dst[V];
     uint32_t meta[V];  // s | inside << 4 | own second block << 5 | store in bounds << 6
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-      const uint64_t i = static_cast<uint64_t>(u) * BLOCK + threadIdx.x;
-      const uint64_t k = voff + t * kTile + i;
+      const Idx i = static_cast<Idx>(u) * BLOCK + threadIdx.x;
+      const Idx k = voff + t * kTile + i;
       meta[u] = 0;
       if (k < vend) {
         while (k >= jend) {
           ++j;
-          jbeg = p.job[j].vfirst;
-          jend = jbeg + p.job[j].nvec;
+          jbeg = static_cast<Idx>(p.job[j].vfirst);
+          jend = jbeg + static_cast<Idx>(p.job[j].nvec);
           w.fresh = true;
         }
         const GatherJob& J = p.job[j];
         const uint64_t xbase = J.out & ~static_cast<uint64_t>(15);
-        const uint64_t kl = k - jbeg;
+        const Idx kl = k - jbeg;
         walk_to(w, p, J, xbase, kl);
-        dst[u] = xbase + 16 * kl;
+        dst[u] = xbase + 16 * static_cast<uint64_t>(kl);
         if (kl >= w.klo && kl < w.khi) {
           const bool own_hi = w.s != 0 && (lane == 31u || kl + 1 >= w.khi || i + 1 >= kTile);
-          const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * kl);
+          const uint4* blk = reinterpret_cast<const uint4*>(w.base + 16 * static_cast<uint64_t>(kl));
           if (load_ok(p, J, w.r, blk, 16, kSiteWarpRealignJobs)) lo[u] = ld_nc_cached(blk);
           if (own_hi && load_ok(p, J, w.r, blk + 1, 16, kSiteWarpRealignJobs)) hi[u] = ld_nc_cached(blk + 1);
           // (the checked build tests the store against this vector's job
@@ -1176,10 +1176,16 @@ __device__ __forceinline__ void gather_mode(const GatherParams<MAXJ, MAXS>& p, u
     }
     else if (first + sc + bc >= step)
       copy_boundaries_jobs<BLOCK>(p, static_cast<uint32_t>(first + sc + bc - step), static_cast<uint32_t>(bc));
-    else if (p.realign_warp)
-      gather_tiles_warp_realign_jobs<BLOCK, kSplitRealignVectors>(
-          p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc - bc), p.flat_vec,
-          p.small_vec);
+    else if (p.realign_warp) {
+      if (p.total_vec < (1ull << 28))  // 16 * vectors under 4 GiB
+        gather_tiles_warp_realign_jobs<BLOCK, kSplitRealignVectors, uint32_t>(
+            p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc - bc),
+            static_cast<uint32_t>(p.flat_vec), static_cast<uint32_t>(p.small_vec));
+      else
+        gather_tiles_warp_realign_jobs<BLOCK, kSplitRealignVectors, uint64_t>(
+            p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc - bc), p.flat_vec,
+            p.small_vec);
+    }
     else
       gather_tiles_staged_realign_jobs<BLOCK, kSplitRealignVectors, kSplitRealignStages>(
           p, static_cast<uint32_t>(first - fc), static_cast<uint32_t>(step - fc - sc), p.flat_vec, p.small_vec);
