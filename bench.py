@@ -756,41 +756,72 @@ def build_step_graph(torch, flush, calls):
     return g, evs
 
 
+def e2e_groups(cases, small=1 << 20):
+    """Consecutive calls of under `small` bytes per rank share one host copy
+    each way; larger calls have their own.  Returns lists of case indices."""
+    groups, cur = [], []
+    for i, (P, B, _s) in enumerate(cases):
+        if B < small:
+            cur.append(i)
+            continue
+        if cur:
+            groups.append(cur)
+            cur = []
+        groups.append([i])
+    if cur:
+        groups.append(cur)
+    return groups
+
+
 def e2e_measure(torch, dc, device, stream, cases, steps):
     """The same sweep through the public API with host buffers.  Each step
-    copies every call's P payloads from one pinned host buffer to the device
-    (copy stream), gathers on `stream` as soon as that call's copy is in, and
-    copies each output back to pinned host memory (a second copy stream), so
-    the two copy directions and the kernels overlap across calls.  The step
-    starts and ends on `stream`; all copies are inside the timed region."""
-    host_in, dev_in, dev_out, host_out = [], [], [], []
-    for (P, B, seed) in cases:
-        h = torch.empty(P * B, dtype=torch.uint8).pin_memory()
-        for r in range(P):
-            h[r * B:(r + 1) * B].copy_(torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)))
+    copies the inputs from pinned host memory to the device (copy stream),
+    gathers on `stream` as soon as a call's inputs are in, and copies the
+    outputs back to pinned host memory (a second copy stream), so the two
+    copy directions and the kernels overlap.  Calls under 1 MiB per rank
+    share one copy each way with their neighbours (e2e_groups: six copies
+    per direction instead of fourteen; a copy has a fixed cost of a few
+    microseconds).  The step starts and ends on `stream`; all copies are
+    inside the timed region."""
+    groups = e2e_groups(cases)
+    host_in, dev_in, dev_out, host_out, views, outs = [], [], [], [], {}, {}
+    for g in groups:
+        total = sum(cases[i][0] * cases[i][1] for i in g)
+        h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        di = torch.empty(total, dtype=torch.uint8, device=device)
+        do = torch.empty(total, dtype=torch.uint8, device=device)
+        off = 0
+        for i in g:
+            P, B, seed = cases[i]
+            for r in range(P):
+                h[off + r * B:off + (r + 1) * B].copy_(
+                    torch.from_numpy(W.random_bf16_patterns(seed, r, B // 2).view(np.uint8)))
+            views[i] = [di[off + r * B:off + (r + 1) * B] for r in range(P)]
+            outs[i] = do[off:off + P * B]
+            off += P * B
         host_in.append(h)
-        dev_in.append(torch.empty(P * B, dtype=torch.uint8, device=device))
-        dev_out.append(torch.empty(P * B, dtype=torch.uint8, device=device))
-        host_out.append(torch.empty(P * B, dtype=torch.uint8).pin_memory())
+        dev_in.append(di)
+        dev_out.append(do)
+        host_out.append(torch.empty(total, dtype=torch.uint8).pin_memory())
     h2d = sum(P * B for (P, B, _s) in cases)
     up, down = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
-    ev_in = [torch.cuda.Event() for _ in cases]
-    ev_g = [torch.cuda.Event() for _ in cases]
-    views = [[dev_in[i][r * B:(r + 1) * B] for r in range(P)] for i, (P, B, _s) in enumerate(cases)]
+    ev_in = [torch.cuda.Event() for _ in groups]
+    ev_g = [torch.cuda.Event() for _ in groups]
 
     def step():
         up.wait_stream(stream)  # the previous step is over before its inputs are overwritten
         with torch.cuda.stream(up):
-            for i in range(len(cases)):
-                dev_in[i].copy_(host_in[i], non_blocking=True)
-                ev_in[i].record(up)
-        for i in range(len(cases)):
-            stream.wait_event(ev_in[i])
-            dc.all_gather(views[i], dev_out[i], stream=stream)
-            ev_g[i].record(stream)
-            down.wait_event(ev_g[i])
+            for gi in range(len(groups)):
+                dev_in[gi].copy_(host_in[gi], non_blocking=True)
+                ev_in[gi].record(up)
+        for gi, g in enumerate(groups):
+            stream.wait_event(ev_in[gi])
+            for i in g:
+                dc.all_gather(views[i], outs[i], stream=stream)
+            ev_g[gi].record(stream)
+            down.wait_event(ev_g[gi])
             with torch.cuda.stream(down):
-                host_out[i].copy_(dev_out[i], non_blocking=True)
+                host_out[gi].copy_(dev_out[gi], non_blocking=True)
         stream.wait_stream(down)
 
     step()
@@ -803,13 +834,14 @@ def e2e_measure(torch, dc, device, stream, cases, steps):
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
-    for i in range(len(cases)):  # the round trip really happened
-        assert torch.equal(host_out[i], host_in[i]), "e2e output differs from its input payloads"
+    for gi in range(len(groups)):  # the round trip really happened
+        assert torch.equal(host_out[gi], host_in[gi]), "e2e output differs from its input payloads"
     step_bytes = sum(algorithmic_bytes(P, B) for (P, B, _s) in cases)
     return {"value": step_bytes / ms / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": steps,
-            "pipeline": "H2D copy stream -> gather on the compute stream -> D2H copy stream, "
-                        "per call, joined by events"}
+            "copies_per_direction": len(groups),
+            "pipeline": "H2D copy stream -> gathers on the compute stream -> D2H copy stream, per copy "
+                        "group (calls under 1 MiB per rank share one copy each way), joined by events"}
 
 
 def rank_max(value: float, dist=None, device=None) -> float:
