@@ -267,6 +267,14 @@ class _Staged:
         if self.handshake not in ("gloo", "shm"):
             raise ValueError(f"handshake must be 'gloo' or 'shm', not {self.handshake!r}")
         self._hs = None
+        # every rank is here (bounded) before the exchanges below, which would
+        # otherwise wait for a missing rank until the process group's timeout
+        try:
+            dist.monitored_barrier(group=group, timeout=self.timeout, wait_all_ranks=True)
+        except RuntimeError as e:
+            self.aborted = f"setup on rank {self.rank}: {e}"
+            self.closed = True
+            raise DCError(_TIMEOUT, self.aborted) from e
         sig = {"op": self.op, "world": self.world, "staging_bytes": self.staging_bytes,
                "transport": transport.kind, "handshake": self.handshake, **extra}
         if self.handshake == "shm":

@@ -67,6 +67,18 @@ def _worker(rank, world, port, case, handshake, outdir):
                 res["raised"], res["msg"] = e.status, str(e)
             res["seconds"] = time.time() - t0
             return
+        if case == "late":  # the last rank never builds the collective
+            if rank == world - 1:
+                time.sleep(6.0)
+                return
+            t0 = time.time()
+            try:
+                StagedAllGather(None, B, HostTransport(), timeout=2.0, handshake=handshake)
+                res["raised"] = None
+            except dc.DCError as e:
+                res["raised"], res["msg"] = e.status, str(e)
+            res["seconds"] = time.time() - t0
+            return
         if case == "mismatch_dtype":
             try:
                 StagedAllReduce(None, 64, "bf16" if rank == 0 else "f16", HostTransport(), timeout=2.0,
@@ -202,6 +214,16 @@ def test_setup_failure_on_one_rank_raises_on_every_rank(handshake, tmp_path):
     for r in (0, 2):
         assert res[r]["raised"] in (1, 6) and "setup" in res[r]["msg"], res[r]
         assert res[r]["seconds"] < 30.0, res[r]
+
+
+@pytest.mark.parametrize("handshake", HANDSHAKES)
+def test_rank_that_never_builds_the_collective(handshake, tmp_path):
+    """The others raise DC_ERR_TIMEOUT at the setup barrier within the bound,
+    not after the process group's timeout."""
+    res = _run(3, "late", tmp_path, handshake)
+    for r in range(2):
+        assert res[r]["raised"] == 6 and "setup" in res[r]["msg"], res[r]
+        assert res[r]["seconds"] < 10.0, res[r]
 
 
 def test_reduction_dtype_mismatch_raises_on_every_rank(tmp_path):
