@@ -15,8 +15,8 @@ Here the handshakes run on the host, between the processes, and the work
 runs in the library's kernels over the peers' mapped staging buffers; no
 kernel ever waits for another process.  Each call (an epoch) is
 
-  stage:    copy the local payload into the local staging buffer and wait for
-            the copy to finish;
+  stage:    copy the local payload into the local staging buffer (the
+            library's one-rank gather) and wait for the copy to finish;
   barrier:  every rank has staged this epoch (bounded by `timeout`);
   compute:  this rank's output from the P staging buffers, and wait for it:
             the rank-ordered gather (dc_all_gather), or the fixed-order fold
@@ -218,7 +218,10 @@ class CudaIpcTransport:
         pass
 
     def stage(self, buf, payload) -> None:
-        buf[: payload.nbytes].copy_(payload.reshape(-1).view(self.torch.uint8))
+        from . import all_gather
+
+        # a one-rank gather is a copy: the staging copy runs in the library too
+        all_gather([payload.reshape(-1).view(self.torch.uint8)], buf[: payload.nbytes])
         self.torch.cuda.current_stream().synchronize()
 
     def gather(self, bufs, out, nbytes: int) -> None:
