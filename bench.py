@@ -994,7 +994,9 @@ def run_dc(args) -> int:
                   "the same timed region",
         "l2": "flushed before every step and before every separately timed call (write + read of "
               "4x L2); each call's inputs are untouched since",
-        "library": {"programmatic_dependent_launch": bool(dc.get_option("pdl")),
+        "library": {"source_digest": kernel_source_digest(),
+                    "bounds_checked_build": bool(dc.lib().dc_bounds_checked()),
+                    "programmatic_dependent_launch": bool(dc.get_option("pdl")),
                     "gather_single_max_bytes": single_max,
                     "gather_bulk": dc.get_option("gather_bulk"),
                     "gather_bulk_min_bytes": dc.get_option("gather_bulk_min_bytes"),
