@@ -978,6 +978,12 @@ def run_dc(args) -> int:
         latency = warm_latency_block(torch, dc, device)
     back_to_back = back_to_back_block(torch, dc, device, flush)
     by_size = by_size_rows(table, back_to_back, peak)
+    # the floor of every "alone" figure: a 16-byte one-rank gather timed the
+    # same way (flush, event, launch, event)
+    tiny_in = [torch.zeros(16, dtype=torch.uint8, device=device)]
+    tiny_out = torch.empty(16, dtype=torch.uint8, device=device)
+    alone_floor_us = statistics.median(
+        timed_calls(torch, stream, flush, [lambda: dc.all_gather(tiny_in, tiny_out)], 21)[0])
     e2e = e2e_measure(torch, dc, device, stream, cases, min(args.steps, 20))
     e2e["value"] = job_throughput(world, step_bytes, rank_max(e2e["ms_per_step"], dist, device))
 
@@ -1019,7 +1025,10 @@ def run_dc(args) -> int:
                      "isolated": {"achieved": iso_achieved, "frac": iso_achieved / peak,
                                   "us_per_launch": kern_time[dom] / max(kern_launches[dom], 1),
                                   "share": kern_time[dom] / sum(kern_time.values())},
-                     "by_size": by_size},
+                     "by_size": by_size, "alone_event_floor_us": alone_floor_us,
+                     "alone_event_floor_note": "a 16-byte one-rank gather timed like the alone figures (flush, "
+                                               "event, launch, event): the fixed cost every alone figure includes; "
+                                               "this GPU's event clock advances in 2.05 us steps"},
         "headline_4MiB_P8": {"us": big["us_mean"], "gbs": big["gbs"], "frac": big["frac"]},
         "per_call": table,
         "per_call_back_to_back": back_to_back,
