@@ -431,7 +431,7 @@ __device__ __forceinline__ uint4 load_span(const uint8_t* a, uint64_t len, uint6
   uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
   if (in_bounds(b0, 16, hlo, hhi, kSiteSpan)) lo = ld_nc_stream(b0);
   if (in_bounds(b1, 16, hlo, hhi, kSiteSpan)) hi = ld_nc_stream(b1);
-  return realign16(lo, hi, static_cast<uint32_t>(ia & 15u));
+  return realign16_sel(lo, hi, static_cast<uint32_t>(ia & 15u));
 }
 
 // v's bytes moved up by n (0..15) places (byte i -> i + n; little-endian).
@@ -607,7 +607,7 @@ __device__ __forceinline__ void gather_tiles_staged_realign(const GatherParams<1
           const uint32_t sh = m & 15u;
           const uint4 lo = ld_shared16(slot_addr(slot, u, 0));
           const uint4 hi = sh ? ld_shared16(slot_addr(slot, u, 1)) : lo;
-          if (store_ok(p, J, out + k, 16, kSiteRealign)) st16(out + k, realign16(lo, hi, sh));
+          if (store_ok(p, J, out + k, 16, kSiteRealign)) st16(out + k, realign16_sel(lo, hi, sh));
         }
       }
     }
@@ -678,7 +678,7 @@ __device__ __forceinline__ void gather_tiles_warp_realign(const GatherParams<1, 
         const uint32_t sh = m & 15u;
         const uint4 second = (m & 32u) ? hi[u] : nb;
         const uint32_t k = t * tile + u * BLOCK + threadIdx.x;
-        if (store_ok(p, J, out + k, 16, kSiteWarpRealign)) st16(out + k, sh ? realign16(lo[u], second, sh) : lo[u]);
+        if (store_ok(p, J, out + k, 16, kSiteWarpRealign)) st16(out + k, sh ? realign16_sel(lo[u], second, sh) : lo[u]);
       }
     }
   }
@@ -831,7 +831,7 @@ __device__ __forceinline__ void gather_tiles_staged_realign_jobs(const GatherPar
           const uint4 lo = ld_shared16(slot_addr(slot, u, 0));
           const uint4 hi = sh ? ld_shared16(slot_addr(slot, u, 1)) : lo;
           uint4* d = reinterpret_cast<uint4*>(xbase) + kl;
-          if (store_ok(p, J, d, 16, kSiteRealignJobs)) st16(d, realign16(lo, hi, sh));
+          if (store_ok(p, J, d, 16, kSiteRealignJobs)) st16(d, realign16_sel(lo, hi, sh));
         } else {
           const uint64_t x = xbase + 16 * kl;
           if (J.flags & kJobSmall)
@@ -917,7 +917,7 @@ __device__ __forceinline__ void gather_tiles_warp_realign_jobs(const GatherParam
       if (m & 16u) {
         const uint32_t sh = m & 15u;
         const uint4 second = (m & 32u) ? hi[u] : nb;
-        if (m & 64u) st16(reinterpret_cast<uint4*>(dst[u]), sh ? realign16(lo[u], second, sh) : lo[u]);
+        if (m & 64u) st16(reinterpret_cast<uint4*>(dst[u]), sh ? realign16_sel(lo[u], second, sh) : lo[u]);
       }
     }
   }
@@ -1103,7 +1103,7 @@ __device__ __forceinline__ void gather_tiles(const GatherParams<MAXJ, MAXS>& p, 
       const uint32_t kind = (meta[u] >> 8) & 0xFFu;
       if (kind == 0) {
         if (store_ok(p, p.job[job[u]], reinterpret_cast<void*>(dst[u]), 16, kSiteGeneral))
-          st16(reinterpret_cast<uint4*>(dst[u]), realign16(lo[u], hi[u], meta[u] & 15u));
+          st16(reinterpret_cast<uint4*>(dst[u]), realign16_sel(lo[u], hi[u], meta[u] & 15u));
       }
       else if (!FAST_EDGES)  // (the multi-CTA kernel has no registers to spare)
         copy_bytes(p, p.job[job[u]], dst[u], meta[u] >> 16, kind == 2);
