@@ -432,7 +432,7 @@ def reductions_block(torch, dc, device, stream, flush, peak):
         seed = W.seed_for(4, list(W.CONFIG4_COUNTS).index(name))
         ins = [W.normal_bf16_device(seed, r, n, device) for r in range(P)]
         outs = [torch.empty_like(x) for x in ins]
-        us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_reduce(ins, outs)], 5)[0])
+        us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_reduce(ins, outs)], 11)[0])
         nbytes = 4 * P * n
         rows.append({"op": "all_reduce_bf16", "P": P, "count": n, "shape": name, "us": us,
                      "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
@@ -441,7 +441,7 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     n = c["rows"] * c["cols"]
     ins = [W.normal_bf16_device(W.seed_for(5, 0), r, n, device) for r in range(c["P"])]
     outs = [torch.empty(n // c["P"], dtype=torch.bfloat16, device=device) for _ in range(c["P"])]
-    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.reduce_scatter(ins, outs)], 5)[0])
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.reduce_scatter(ins, outs)], 11)[0])
     nbytes = 2 * c["P"] * n + 2 * n
     rows.append({"op": "reduce_scatter_bf16", "P": c["P"], "count": n, "shape": "16384x8192",
                  "us": us, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
@@ -453,7 +453,7 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     store = [W.normal_bf16_device(W.seed_for(4, 9920), r, n + 8, device) for r in range(P)]
     ins = [store[r][(1 if r == 1 else 0):(1 if r == 1 else 0) + n] for r in range(P)]
     outs = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
-    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_reduce(ins, outs)], 5)[0])
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_reduce(ins, outs)], 11)[0])
     nbytes = 4 * P * n
     rows.append({"op": "all_reduce_bf16_realigned", "P": P, "count": n,
                  "shape": "8627x8192, rank 1's input one element off 16 bytes", "us": us,
@@ -462,7 +462,7 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     for B in (4 * 1024 * 1024 + 1, 32 * 1024 * 1024 + 1):  # unaligned: payloads +1, output +3
         peers = [W.random_bytes_device(W.seed_for(3, 9000), r, B + 1, device)[1:] for r in range(8)]
         out = torch.empty(8 * B + 3, dtype=torch.uint8, device=device)[3:]
-        us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather(peers, out)], 5)[0])
+        us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather(peers, out)], 11)[0])
         nbytes = 2 * 8 * B
         rows.append({"op": "all_gather_unaligned", "P": 8, "count": B,
                      "shape": f"{B} B per rank, payloads at +1 B, output at +3 B", "us": us,
@@ -472,7 +472,7 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     tens = [[W.random_bytes_device(W.seed_for(5, 1), r, B, device, tensor=t) for r in range(P)]
             for t, B in enumerate(W.CONFIG5_MANY_SIZES)]
     outs = [torch.empty(P * B, dtype=torch.uint8, device=device) for B in W.CONFIG5_MANY_SIZES]
-    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather_many(tens, outs)], 5)[0])
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.all_gather_many(tens, outs)], 11)[0])
     nbytes = 2 * P * sum(W.CONFIG5_MANY_SIZES)
     rows.append({"op": "all_gather_many", "P": P, "count": len(W.CONFIG5_MANY_SIZES),
                  "shape": "{3 B, 4 KiB, 100000 B, 1 MiB, 7 MiB+5 B, 32 MiB}", "us": us,
@@ -533,13 +533,13 @@ def reductions_block(torch, dc, device, stream, flush, peak):
         epoch[0] += 1
         dc.fused_all_gather(ins, stg, outs, ws, epoch[0])
 
-    us = statistics.median(timed_calls(torch, stream, flush, [fused], 5)[0])
+    us = statistics.median(timed_calls(torch, stream, flush, [fused], 11)[0])
     dc.check_device()
     # its DRAM traffic is mostly writes (P*P*B of outputs + P*B of staging):
     # torch's own fill of as many bytes (one buffer), timed the same way, is
     # the write-only rate it is held against
     fill = torch.empty(P * P * B, dtype=torch.uint8, device=device)
-    fill_us = statistics.median(timed_calls(torch, stream, flush, [fill.zero_], 5)[0])
+    fill_us = statistics.median(timed_calls(torch, stream, flush, [fill.zero_], 11)[0])
     del fill
     nbytes = 2 * P * B + 2 * P * P * B
     rows.append({"op": "fused_all_gather", "P": P, "count": B,
