@@ -795,7 +795,13 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
     // SMs.  Several jobs (reduce_scatter, batches): full tiles, which do not
     // cut a job of a multiple of 512 units; a tile that straddles two jobs
     // runs their parts one after the other, and for 8 shards of 64 Ki BF16
-    // elements even tiles were slower (3.70 -> 4.04 us back to back).
+    // elements even tiles were slower (3.70 -> 4.04 us back to back) -- except
+    // launches of at most kEvenJobsMaxUnits units, which take even tiles of
+    // >= 64 units too, so that a small reduce_scatter reaches more than a few
+    // SMs.  Measured (P = 8 BF16 reduce_scatter, 14 calls back to back, per
+    // call; full -> even): 128 KiB per rank 3.35 -> 2.90 us, 256 KiB 3.36 ->
+    // 3.03 us, 512 KiB 3.48 -> 3.04 us; but 1 MiB 3.77 -> 3.92 us and 8 MiB
+    // 13.8 -> 14.9 us, hence the bound.
     // Measured on GB300 for one all_reduce (BF16, 12 calls back to back after
     // an L2 flush, per call; full tiles -> even tiles of >= 64 units): P = 8
     // x 8 KiB 3.36 -> 2.53 us, 8 x 256 KiB 3.56 -> 2.70 us, 8 x 512 KiB 4.21
@@ -803,7 +809,8 @@ dc_status_t launch_reduce_plan(Params& prm, int variant, int dtype, int order,
     // KiB 3.97 -> 2.51 us; P = 4 x 2 MiB 5.09 -> 3.88 us.  A 32-unit minimum
     // was no better, 128 and 256 were slower for 128-512 KiB per rank.
     const uint64_t full = static_cast<uint64_t>(kReduceBlock) * reduce_unroll(pt);
-    const uint64_t tile = prm.njobs == 1
+    constexpr uint64_t kEvenJobsMaxUnits = 32768;
+    const uint64_t tile = prm.njobs == 1 || prm.total_units <= kEvenJobsMaxUnits
                               ? even_tile(prm.total_units, sms, occ, full, g_opt.reduce_tile_min.load(), 32)
                               : full;
     prm.tile_units = static_cast<int32_t>(tile);
