@@ -446,6 +446,17 @@ def reductions_block(torch, dc, device, stream, flush, peak):
     rows.append({"op": "reduce_scatter_bf16", "P": c["P"], "count": n, "shape": "16384x8192",
                  "us": us, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
     del ins, outs
+    # one rank's share (dc_reduce), as a rank that is its own process
+    # computes it: rank 3's output of the 8627x8192 all_reduce, P = 8
+    n = W.CONFIG4_COUNTS["8627x8192"]
+    ins = [W.normal_bf16_device(W.seed_for(4, 9930), r, n, device) for r in range(P)]
+    out = torch.empty(n, dtype=torch.bfloat16, device=device)
+    us = statistics.median(timed_calls(torch, stream, flush, [lambda: dc.reduce(ins, out)], 11)[0])
+    nbytes = 2 * P * n + 2 * n
+    rows.append({"op": "reduce_one_rank_bf16", "P": P, "count": n,
+                 "shape": "8627x8192: P inputs folded into one output", "us": us,
+                 "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak, "bytes": nbytes})
+    del ins, out
     rows.extend(typed_rows(torch, dc, device, stream, flush, peak))
     # all_reduce with rank 1's input one element past the others' alignment
     # (8627x8192 per rank, P=8): the realigning path
