@@ -19,7 +19,8 @@ kernel ever waits for another process.  Each call (an epoch) is
             library's one-rank gather) and wait for the copy to finish;
   barrier:  every rank has staged this epoch (bounded by `timeout`);
   compute:  this rank's output from the P staging buffers, and wait for it:
-            the rank-ordered gather (dc_all_gather), or the fixed-order fold
+            the rank-ordered gather (dc_all_gather; dc_all_gather_many for
+            several tensors in one staging buffer), or the fixed-order fold
             of every buffer (dc_reduce) -- the whole buffer for all_reduce,
             shard r of it for rank r of reduce_scatter;
   barrier:  every rank has read every staging buffer (same bound), so the
@@ -51,7 +52,8 @@ A transport provides: kind, default_handshake, alloc(nbytes) -> buffer,
 export(buffer) -> descriptor (one per peer that opens it), open(descriptor)
 -> the peer's buffer, opened_by_all(), stage(buffer, payload),
 gather(buffers, out, nbytes), reduce(buffers, out, nbytes, offset, order),
-close_peers(), release().  CudaIpcTransport is the product's: device buffers
+stage_many(buffer, payloads, offsets), gather_many(buffers, outs, offsets,
+sizes), close_peers(), release().  CudaIpcTransport is the product's: device buffers
 shared through CUDA IPC handles, the work in dc_all_gather / dc_reduce.  The
 process group must support monitored_barrier (gloo).
 """
@@ -230,6 +232,25 @@ class CudaIpcTransport:
         all_gather([b[:nbytes] for b in bufs], out.reshape(-1).view(self.torch.uint8))
         self.torch.cuda.current_stream().synchronize()
 
+    def stage_many(self, buf, payloads, offsets) -> None:
+        from . import all_gather_many
+
+        # one launch: T one-rank gathers (copies) into the staging buffer
+        live = [(p, o) for p, o in zip(payloads, offsets) if p.nbytes]
+        if live:
+            all_gather_many([[p.reshape(-1).view(self.torch.uint8)] for p, _o in live],
+                            [buf[o:o + p.nbytes] for p, o in live])
+        self.torch.cuda.current_stream().synchronize()
+
+    def gather_many(self, bufs, outs, offsets, sizes) -> None:
+        from . import all_gather_many
+
+        live = [t for t, B in enumerate(sizes) if B]
+        if live:
+            all_gather_many([[b[offsets[t]:offsets[t] + sizes[t]] for b in bufs] for t in live],
+                            [outs[t].reshape(-1).view(self.torch.uint8) for t in live])
+        self.torch.cuda.current_stream().synchronize()
+
     def reduce(self, bufs, out, nbytes: int, offset: int, order: str) -> None:
         from . import reduce
 
@@ -359,16 +380,23 @@ class _Staged:
 
     def _run(self, payload, out, payload_bytes: int, out_bytes: int, compute):
         """Stage, barrier, compute, barrier (the module docstring)."""
+        self._check_open()
+        if payload.nbytes != payload_bytes or out.nbytes != out_bytes:
+            raise ValueError(f"{self.op} needs a payload of {payload_bytes} bytes and an output of "
+                             f"{out_bytes} (got {payload.nbytes} and {out.nbytes})")
+        self._steps(lambda: self.transport.stage(self.local, payload), compute)
+        return out
+
+    def _check_open(self) -> None:
         if self.aborted:
             raise DCError(_TIMEOUT, "the collective was aborted: " + self.aborted)
         if self.closed:
             raise ValueError("the collective is closed")
-        if payload.nbytes != payload_bytes or out.nbytes != out_bytes:
-            raise ValueError(f"{self.op} needs a payload of {payload_bytes} bytes and an output of "
-                             f"{out_bytes} (got {payload.nbytes} and {out.nbytes})")
+
+    def _steps(self, stage, compute) -> None:
         self.epoch += 1
         t0 = time.perf_counter()
-        self.transport.stage(self.local, payload)
+        stage()
         t1 = time.perf_counter()
         self._barrier("stage")
         t2 = time.perf_counter()
@@ -381,7 +409,6 @@ class _Staged:
         sec["stage_barrier"] += t2 - t1
         sec["compute"] += t3 - t2
         sec["complete_barrier"] += t4 - t3
-        return out
 
     def close(self) -> None:
         """Drop the peers' mappings, wait (if the collective is healthy, within
@@ -416,6 +443,39 @@ class StagedAllGather(_Staged):
     def all_gather(self, payload, out):
         return self._run(payload, out, self.nbytes, self.world * self.nbytes,
                          lambda: self.transport.gather(self.peers, out, self.nbytes))
+
+
+class StagedAllGatherMany(_Staged):
+    """Several gathers in one epoch: rank r's all_gather_many(payloads, outs)
+    leaves in outs[t] the P ranks' payloads of tensor t in rank order
+    (P * sizes[t] bytes).  The T payloads share one staging buffer per rank
+    (tensor t at a 256-byte aligned offset), staged by one launch, and the
+    gather is one dc_all_gather_many over the mapped buffers."""
+
+    op = "all_gather_many"
+
+    def __init__(self, group, sizes, transport, timeout: float = 5.0, handshake: str | None = None):
+        self.sizes = [int(b) for b in sizes]
+        if any(b < 0 for b in self.sizes):
+            raise ValueError("sizes must be >= 0")
+        self.offsets, off = [], 0
+        for b in self.sizes:
+            self.offsets.append(off)
+            off += (b + 255) // 256 * 256
+        super().__init__(group, off, transport, timeout, handshake, {"sizes": self.sizes})
+
+    def all_gather_many(self, payloads, outs):
+        self._check_open()
+        T = len(self.sizes)
+        if len(payloads) != T or len(outs) != T:
+            raise ValueError(f"{self.op} needs {T} payloads and {T} outputs")
+        for t, B in enumerate(self.sizes):
+            if payloads[t].nbytes != B or outs[t].nbytes != self.world * B:
+                raise ValueError(f"tensor {t}: need a payload of {B} bytes and an output of {self.world * B} "
+                                 f"(got {payloads[t].nbytes} and {outs[t].nbytes})")
+        self._steps(lambda: self.transport.stage_many(self.local, payloads, self.offsets),
+                    lambda: self.transport.gather_many(self.peers, outs, self.offsets, self.sizes))
+        return outs
 
 
 class StagedAllReduce(_Staged):
@@ -466,5 +526,5 @@ class StagedReduceScatter(_Staged):
                                                        self.rank * self.count, self.order))
 
 
-__all__ = ["StagedAllGather", "StagedAllReduce", "StagedReduceScatter", "CudaIpcTransport", "ShmHandshake",
-           "SharedBytes", "ELEMENT_BYTES"]
+__all__ = ["StagedAllGather", "StagedAllGatherMany", "StagedAllReduce", "StagedReduceScatter", "CudaIpcTransport",
+           "ShmHandshake", "SharedBytes", "ELEMENT_BYTES"]

@@ -55,6 +55,15 @@ class HostTransport:
         for q, b in enumerate(bufs):
             out[q * nbytes:(q + 1) * nbytes] = b[0][:nbytes]
 
+    def stage_many(self, buf, payloads, offsets) -> None:
+        for p, o in zip(payloads, offsets):
+            buf[0][o:o + p.nbytes] = np.ascontiguousarray(p).view(np.uint8).reshape(-1)
+
+    def gather_many(self, bufs, outs, offsets, sizes) -> None:
+        for t, (o, B) in enumerate(zip(offsets, sizes)):
+            for q, b in enumerate(bufs):
+                outs[t][q * B:(q + 1) * B] = b[0][o:o + B]
+
     def reduce(self, bufs, out, nbytes: int, offset: int, order: str) -> None:
         n = out.size
         cols = [b[0][:nbytes].view(out.dtype)[offset:offset + n] for b in bufs]

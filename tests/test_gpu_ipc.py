@@ -53,6 +53,11 @@ def _worker(rank, world, port, handshake, outdir, op="gather"):
     res = {"rank": rank, "ok": [], "launches": 0}
     try:
         n0 = dc.launch_count()
+        if op == "gathermany":
+            _gather_many(rank, world, handshake, res)
+            res["launches"] = dc.launch_count() - n0
+            dc.check_device()
+            return
         if op != "gather":
             _reductions(rank, world, handshake, op, res)
             res["launches"] = dc.launch_count() - n0
@@ -76,6 +81,28 @@ def _worker(rank, world, port, handshake, outdir, op="gather"):
         with open(os.path.join(outdir, f"r{rank}.json"), "w") as fh:
             json.dump(res, fh)
         dist.destroy_process_group()
+
+
+MANY_SIZES = [0, 1, 15, 4099, 256, 70001, (1 << 20) + 3]
+
+
+def _gather_many(rank, world, handshake, res):
+    """all_gather_many over CUDA IPC (one staging buffer per rank), three
+    epochs, against the oracle."""
+    import torch
+
+    from reduce_copy_rank_gb300.ipc import CudaIpcTransport, StagedAllGatherMany
+
+    coll = StagedAllGatherMany(None, MANY_SIZES, CudaIpcTransport(), timeout=30.0, handshake=handshake)
+    for epoch in range(1, 4):
+        tensors = [[W.random_bytes(W.seed_for(5, 940 + epoch), q, B, tensor=t) for q in range(world)]
+                   for t, B in enumerate(MANY_SIZES)]
+        mine = [torch.from_numpy(tensors[t][rank]).cuda() for t in range(len(MANY_SIZES))]
+        outs = [torch.full((world * B,), 0xA5, dtype=torch.uint8, device="cuda") for B in MANY_SIZES]
+        coll.all_gather_many(mine, outs)
+        want = oracle.all_gather_many(tensors)
+        res["ok"].append(all(bool(np.array_equal(o.cpu().numpy(), w)) for o, w in zip(outs, want)))
+    coll.close()
 
 
 RED_CASES = [("bf16", "linear", 4099), ("f16", "tree", 1 << 18), ("f32", "linear", (1 << 18) + 3)]
@@ -142,6 +169,18 @@ def test_staged_all_gather_over_cuda_ipc(world, handshake, tmp_path):
         assert "error" not in res, res
         assert res["ok"] == [True] * (3 * len(SIZES)), res
         assert res["launches"] == 2 * 3 * len(SIZES), res  # per epoch: the staging copy and the gather
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_staged_all_gather_many_over_cuda_ipc(world, tmp_path):
+    if not _compute_mode_default():
+        pytest.skip("GPU 0 is not in the default compute mode: one process per GPU only")
+    mp.spawn(_worker, args=(world, _port(), "shm", str(tmp_path), "gathermany"), nprocs=world, join=True)
+    for r in range(world):
+        res = json.load(open(tmp_path / f"r{r}.json"))
+        assert "error" not in res, res
+        assert res["ok"] == [True] * 3, res
+        assert res["launches"] == 2 * 3, res  # per epoch: one staging launch, one gather launch
 
 
 @pytest.mark.parametrize("op", ["allreduce", "reducescatter"])

@@ -41,7 +41,7 @@ def _worker(rank, world, port, case, handshake, outdir):
 
     import reduce_copy_rank_gb300 as dc
     from host_transport import HostTransport
-    from reduce_copy_rank_gb300.ipc import StagedAllGather, StagedAllReduce, StagedReduceScatter
+    from reduce_copy_rank_gb300.ipc import StagedAllGather, StagedAllGatherMany, StagedAllReduce, StagedReduceScatter
 
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -78,6 +78,27 @@ def _worker(rank, world, port, case, handshake, outdir):
             except dc.DCError as e:
                 res["raised"], res["msg"] = e.status, str(e)
             res["seconds"] = time.time() - t0
+            return
+        if case in ("gathermany", "mismatch_sizes"):
+            sizes = [0, 1, 15, 4099, 256, 70001]
+            if case == "mismatch_sizes":
+                try:
+                    StagedAllGatherMany(None, sizes if rank else sizes[:-1], HostTransport(), timeout=2.0,
+                                        handshake=handshake)
+                    res["raised"] = None
+                except dc.DCError as e:
+                    res["raised"] = e.status
+                return
+            coll = StagedAllGatherMany(None, sizes, HostTransport(), timeout=2.0, handshake=handshake)
+            res["ok"] = []
+            for epoch in range(1, 4):
+                tensors = [[W.random_bytes(W.seed_for(5, 830 + epoch), q, B, tensor=t) for q in range(world)]
+                           for t, B in enumerate(sizes)]
+                outs = [np.zeros(world * B, dtype=np.uint8) for B in sizes]
+                coll.all_gather_many([tensors[t][rank] for t in range(len(sizes))], outs)
+                want = oracle.all_gather_many(tensors)
+                res["ok"].append(all(bool(np.array_equal(o, w)) for o, w in zip(outs, want)))
+            coll.close()
             return
         if case == "mismatch_dtype":
             try:
@@ -224,6 +245,21 @@ def test_rank_that_never_builds_the_collective(handshake, tmp_path):
     for r in range(2):
         assert res[r]["raised"] == 6 and "setup" in res[r]["msg"], res[r]
         assert res[r]["seconds"] < 10.0, res[r]
+
+
+@pytest.mark.parametrize("handshake", HANDSHAKES)
+@pytest.mark.parametrize("world", [2, 3])
+def test_gather_many_over_epochs(world, handshake, tmp_path):
+    """Several tensors (0 B to 70 KB, odd sizes) in one staging buffer per
+    rank: every output is the oracle's gather of that tensor."""
+    res = _run(world, "gathermany", tmp_path, handshake)
+    for r in range(world):
+        assert res[r]["ok"] == [True, True, True], res[r]
+
+
+def test_gather_many_size_mismatch_raises_on_every_rank(tmp_path):
+    res = _run(2, "mismatch_sizes", tmp_path, "gloo")
+    assert [res[r]["raised"] for r in range(2)] == [1, 1]
 
 
 def test_reduction_dtype_mismatch_raises_on_every_rank(tmp_path):
