@@ -403,6 +403,13 @@ const char *dc_status_name(int status);
  *   "fused_chunk_min"         dc_fused_all_gather: smallest chunk per CTA
  *                             (default 32768 bytes; measured, 8 ranks x 4 MiB:
  *                             75.8 us at 32 KiB, 81.9 us at 64 KiB)
+ *   "fused_tma"               1 (default) = the protocol's gather step streams
+ *                             the staged chunks through the TMA engine (one
+ *                             thread per CTA, bulk loads and stores through a
+ *                             shared-memory ring); 0 = every thread copies
+ *                             16-byte vectors
+ *   "fused_stages", "fused_sub_bytes"  that ring: stages (1..32, default 3) of
+ *                             bytes each (a multiple of 16, default 32768)
  *   "test_fused_absent_ranks" bit r set: rank r of dc_fused_all_gather never
  *                             arrives (tests of its bounded waits)
  *   "test_fail_launch"        1 = report DC_ERR_CUDA instead of launching
@@ -412,7 +419,8 @@ const char *dc_status_name(int status);
  * DC_GATHER_STAGED, DC_GATHER_SPLIT_COST_PCT, DC_GATHER_SPLIT_COST_WARP_PCT, DC_PREFETCH, DC_GATHER_TILE_MIN,
  * DC_REDUCE_TILE_MIN, DC_REDUCE_STAGED, DC_GATHER_BULK, DC_GATHER_BULK_MIN_BYTES,
  * DC_BULK_CHUNK_BYTES, DC_BULK_CHUNK_MIN, DC_BULK_STAGES, DC_BULK_CTAS_PER_SM,
- * DC_BULK_PREFETCH, DC_GATHER_REALIGN_WARP, DC_FUSED_CHUNK_MIN and DC_WAIT_LIMIT_NS set the initial values (read once,
+ * DC_BULK_PREFETCH, DC_GATHER_REALIGN_WARP, DC_FUSED_CHUNK_MIN, DC_FUSED_TMA, DC_FUSED_STAGES,
+ * DC_FUSED_SUB_BYTES and DC_WAIT_LIMIT_NS set the initial values (read once,
  * at the first call).
  * dc_set_option returns 0, or -1 for an unknown key or a negative value.
  * dc_get_option returns the value, or -1 for an unknown key.

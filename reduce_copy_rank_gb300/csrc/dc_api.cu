@@ -81,6 +81,9 @@ struct Options {
   std::atomic<long long> bulk_ctas_per_sm{2};
   std::atomic<long long> bulk_prefetch{2};
   std::atomic<long long> fused_chunk_min{32768};
+  std::atomic<long long> fused_tma{1};
+  std::atomic<long long> fused_stages{3};
+  std::atomic<long long> fused_sub_bytes{32768};
   std::atomic<long long> realign_warp{1};
   std::atomic<long long> test_fused_absent{0};
   std::atomic<long long> wait_limit_ns{1000000000};
@@ -118,6 +121,9 @@ const OptionKey kKeys[] = {
     {"bulk_ctas_per_sm", "DC_BULK_CTAS_PER_SM", &g_opt.bulk_ctas_per_sm},
     {"bulk_prefetch", "DC_BULK_PREFETCH", &g_opt.bulk_prefetch},
     {"fused_chunk_min", "DC_FUSED_CHUNK_MIN", &g_opt.fused_chunk_min},
+    {"fused_tma", "DC_FUSED_TMA", &g_opt.fused_tma},
+    {"fused_stages", "DC_FUSED_STAGES", &g_opt.fused_stages},
+    {"fused_sub_bytes", "DC_FUSED_SUB_BYTES", &g_opt.fused_sub_bytes},
     {"gather_realign_warp", "DC_GATHER_REALIGN_WARP", &g_opt.realign_warp},
     {"test_fused_absent_ranks", nullptr, &g_opt.test_fused_absent},
     {"wait_limit_ns", "DC_WAIT_LIMIT_NS", &g_opt.wait_limit_ns},
@@ -938,6 +944,38 @@ dc_status_t reduce_one_entry(const void* const* in_ptrs, int P, uint64_t in_offs
   return launch_reduce_plan(prm, 0, dtype, order, out_b, stream, "reduce");
 }
 
+// The launch shape of a fused all-gather: G chunk CTAs per rank (chunks of
+// at least fused_chunk_min bytes, at most kFusedMaxChunks, and all P * G
+// CTAs resident at once: the cooperative launch needs them together), and
+// the gather step's TMA ring (fused_tma, fused_stages stages of
+// fused_sub_bytes), whose shared memory decides how many CTAs fit an SM.
+// Fills bytes, chunk, G, P, wait_ns, tma, stages and sub of fp.
+dc_status_t plan_fused(FusedParams& fp, uint64_t B, int P, int sms) {
+  fp.tma = g_opt.fused_tma.load() ? 1 : 0;
+  fp.stages = static_cast<int32_t>(std::min(std::max(g_opt.fused_stages.load(), 1LL), 32LL));
+  const long long sub = std::max(16LL, g_opt.fused_sub_bytes.load()) / 16 * 16;
+  fp.sub = static_cast<uint32_t>(std::min(sub, static_cast<long long>(kFusedMaxSmem)));
+  const size_t smem = fused_smem_bytes(fp.tma, fp.stages, fp.sub);
+  if (smem > kFusedMaxSmem)
+    return fail(DC_ERR_INVALID, "the fused TMA ring (%d stages of %u bytes) exceeds %zu bytes of shared memory",
+                fp.stages, fp.sub, kFusedMaxSmem);
+  const uint64_t resident = static_cast<uint64_t>(sms) * static_cast<uint64_t>(fused_ctas_per_sm(smem));
+  if (resident < static_cast<uint64_t>(P))
+    return fail(DC_ERR_INVALID, "%d ranks need %d CTAs resident at once; the GPU holds %llu", P, P,
+                static_cast<unsigned long long>(resident));
+  const uint64_t cmin = static_cast<uint64_t>(std::max(16LL, g_opt.fused_chunk_min.load()));
+  uint64_t G = std::min<uint64_t>({(B + cmin - 1) / cmin, static_cast<uint64_t>(kFusedMaxChunks),
+                                   resident / static_cast<uint64_t>(P)});
+  G = std::max<uint64_t>(G, 1);
+  const uint64_t chunk = ((B + G - 1) / G + 15) / 16 * 16;
+  fp.bytes = B;
+  fp.chunk = chunk;
+  fp.G = static_cast<int32_t>((B + chunk - 1) / chunk);
+  fp.P = P;
+  fp.wait_ns = static_cast<uint64_t>(std::max(g_opt.wait_limit_ns.load(), 1000LL));
+  return DC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1144,33 +1182,19 @@ dc_status_t dc_fused_all_gather(const void* const* in_ptrs, void* const* staging
   if (st != DC_OK) return st;
   // G chunks per rank (one CTA each): chunks of at least fused_chunk_min
   // bytes, at most kFusedMaxChunks, and all P * G CTAs resident at once
-  const uint64_t resident = static_cast<uint64_t>(sms) *
-                            static_cast<uint64_t>(occupancy(dev, 127, [] { return fused_ctas_per_sm(); }));
-  if (resident < static_cast<uint64_t>(P))
-    return fail(DC_ERR_INVALID, "%d ranks need %d CTAs resident at once; the GPU holds %llu", P, P,
-                static_cast<unsigned long long>(resident));
-  const uint64_t cmin = static_cast<uint64_t>(std::max(16LL, g_opt.fused_chunk_min.load()));
-  uint64_t G = std::min<uint64_t>({(B + cmin - 1) / cmin, static_cast<uint64_t>(kFusedMaxChunks),
-                                   resident / static_cast<uint64_t>(P)});
-  G = std::max<uint64_t>(G, 1);
-  const uint64_t chunk = ((B + G - 1) / G + 15) / 16 * 16;
-  G = (B + chunk - 1) / chunk;
   FusedParams fp{};
+  st = plan_fused(fp, B, P, sms);
+  if (st != DC_OK) return st;
   for (int r = 0; r < P; ++r) {
     fp.in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
     fp.staging[r] = reinterpret_cast<uint64_t>(staging[r]);
     fp.out[r] = reinterpret_cast<uint64_t>(outs[r]);
   }
-  fp.bytes = B;
-  fp.chunk = chunk;
-  fp.wait_ns = static_cast<uint64_t>(std::max(g_opt.wait_limit_ns.load(), 1000LL));
   fp.ws = ws;
   fp.absent = static_cast<uint64_t>(g_opt.test_fused_absent.load());
   fp.epoch = epoch;
-  fp.P = P;
-  fp.G = static_cast<int32_t>(G);
   return check_launch(launch_fused_gather(fp, static_cast<cudaStream_t>(stream)), "fused all-gather",
-                      static_cast<int>(P * G));
+                      P * fp.G);
 }
 
 dc_status_t dc_fused_all_gather_static(const void* const* in_ptrs, void* const* outs, int P,
@@ -1223,30 +1247,16 @@ dc_status_t dc_fused_all_gather_static(const void* const* in_ptrs, void* const* 
   if (st != DC_OK) return st;
   st = sm_count(dev, &sms);
   if (st != DC_OK) return st;
-  const uint64_t resident = static_cast<uint64_t>(sms) *
-                            static_cast<uint64_t>(occupancy(dev, 127, [] { return fused_ctas_per_sm(); }));
-  if (resident < static_cast<uint64_t>(P))
-    return fail(DC_ERR_INVALID, "%d ranks need %d CTAs resident at once; the GPU holds %llu", P, P,
-                static_cast<unsigned long long>(resident));
-  const uint64_t cmin = static_cast<uint64_t>(std::max(16LL, g_opt.fused_chunk_min.load()));
-  uint64_t G = std::min<uint64_t>({(B + cmin - 1) / cmin, static_cast<uint64_t>(kFusedMaxChunks),
-                                   resident / static_cast<uint64_t>(P)});
-  G = std::max<uint64_t>(G, 1);
-  const uint64_t chunk = ((B + G - 1) / G + 15) / 16 * 16;
-  G = (B + chunk - 1) / chunk;
   FusedParams fp{};
+  st = plan_fused(fp, B, P, sms);
+  if (st != DC_OK) return st;
   for (int r = 0; r < P; ++r) {
     fp.in[r] = reinterpret_cast<uint64_t>(in_ptrs[r]);
     fp.out[r] = reinterpret_cast<uint64_t>(outs[r]);
   }
-  fp.bytes = B;
-  fp.chunk = chunk;
-  fp.wait_ns = static_cast<uint64_t>(std::max(g_opt.wait_limit_ns.load(), 1000LL));
   fp.absent = 0;
-  fp.P = P;
-  fp.G = static_cast<int32_t>(G);
   return check_launch(launch_fused_gather_static(fp, static_cast<cudaStream_t>(stream)),
-                      "fused all-gather (static scratch)", static_cast<int>(P * G));
+                      "fused all-gather (static scratch)", P * fp.G);
 }
 
 dc_status_t dc_fused_reset(void* workspace, int P, dc_stream_t stream) {

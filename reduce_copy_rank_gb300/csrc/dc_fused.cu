@@ -19,10 +19,13 @@
 // handles chunk c of rank r:
 //   stage:    in_r[chunk c] -> staging_r[chunk c]; then staged[r][c] = epoch
 //             (release store, after a device-scope fence by every thread);
-//   gather:   wait until staged[q][c] == epoch for every rank q, starting
-//             with itself (acquire loads), then staging_q[chunk c] ->
-//             out_r[q*B + chunk c] for every q (loads through L2 only:
-//             staging_q is written by other CTAs);
+//   gather:   wait until staged[q][c] == epoch for every rank q (acquire
+//             loads), then staging_q[chunk c] -> out_r[q*B + chunk c] for
+//             every q: by default one thread streams the chunks through the
+//             TMA engine (gather_tma: bulk loads into a shared-memory ring,
+//             bulk stores out of it), else every thread copies 16-byte
+//             vectors (loads through L2 only: staging_q is written by other
+//             CTAs);
 //   complete: done[r][c] = epoch, then wait until done[q][c] == epoch for
 //             every q: chunk c of staging_r has been read by every rank and
 //             may be overwritten by the next epoch.
@@ -40,6 +43,7 @@
 
 #include "dc_device.cuh"
 #include "dc_internal.h"
+#include "dc_tma.cuh"
 
 namespace dc {
 namespace {
@@ -49,11 +53,7 @@ namespace {
 // take_fused_faults reads and clears it.
 __device__ unsigned int g_fused_fault[4];
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+using tma::global_ns;
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
@@ -126,6 +126,90 @@ __device__ __forceinline__ void copy_chunk(const uint8_t* src, uint8_t* dst, uin
   }
 }
 
+// The gather step on the TMA engine: thread 0 streams the P staged chunks
+// (peers in the order q0, q0+1, ...) through a ring of p.stages shared-memory
+// stages of p.sub bytes: each piece is one bulk load (staging_q -> stage,
+// completing on the stage's mbarrier) and one bulk store (stage -> out_r),
+// with p.stages - 1 pieces' loads in flight; the stores drain through the
+// TMA engine instead of the load-store units.  Every mbarrier wait is
+// bounded; one that runs out records the fault (phase 3), waits (bounded)
+// for the loads still in flight and returns false.  True: every load has
+// landed, so the staging chunks have been read.
+__device__ __forceinline__ bool gather_tma(const FusedParams& p, uint32_t r, uint32_t c, uint32_t q0, uint64_t lo,
+                                           uint64_t n) {
+  using namespace tma;
+  extern __shared__ __align__(128) uint8_t fused_smem[];  // [stages][sub], then the mbarriers
+  const uint32_t P = static_cast<uint32_t>(p.P), S = static_cast<uint32_t>(p.stages);
+  const uint64_t sub = p.sub, B = p.bytes;
+  const uint32_t buf = static_cast<uint32_t>(__cvta_generic_to_shared(fused_smem));
+  const uint32_t bars = buf + S * static_cast<uint32_t>(sub);
+  for (uint32_t k = 0; k < S; ++k) mbar_init(bars + 8u * k, 1);
+  mbar_init_fence();
+  // the staged bytes were published by other CTAs (release/acquire on the
+  // flags, generic proxy); the bulk loads below read them through the async proxy
+  fence_proxy_async_global();
+  const uint64_t per = (n + sub - 1) / sub, items = per * P;
+  auto piece = [&](uint64_t i, uint32_t& q, uint64_t& off) {
+    const uint64_t pi = i / per;
+    q = q0 + static_cast<uint32_t>(pi);
+    if (q >= P) q -= P;
+    off = (i - pi * per) * sub;
+  };
+  uint32_t inflight = 0, phase = 0;
+  auto issue = [&](uint32_t k, uint64_t i) {
+    uint32_t q;
+    uint64_t off;
+    piece(i, q, off);
+    const uint32_t len = static_cast<uint32_t>(min(sub, n - off));
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.staging[q]) + lo + off;
+    const bool ok = in_bounds(src, len, p.staging[q], p.staging[q] + B, kSiteFusedGather);
+    mbar_arrive_expect_tx(bars + 8u * k, ok ? len : 0u);
+    if (ok) bulk_load(buf + k * static_cast<uint32_t>(sub), src, len, bars + 8u * k);
+    inflight |= 1u << k;
+  };
+  for (uint32_t k = 0; k < S && k < items; ++k) issue(k, k);
+  bool ok = true;
+  uint32_t k = 0, kprev = S - 1;
+  for (uint64_t i = 0; i < items; ++i) {
+    if (!mbar_wait_bounded(bars + 8u * k, (phase >> k) & 1u, p.wait_ns)) {
+      uint32_t q;
+      uint64_t off;
+      piece(i, q, off);
+      record_fault(3, r, q, c, p.epoch);
+      inflight &= ~(1u << k);  // already waited for once
+      ok = false;
+      break;
+    }
+    phase ^= 1u << k;
+    inflight &= ~(1u << k);
+    fence_proxy_async_smem();
+    uint32_t q;
+    uint64_t off;
+    piece(i, q, off);
+    const uint32_t len = static_cast<uint32_t>(min(sub, n - off));
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * B + lo + off;
+    if (in_bounds(dst, len, p.out[r], p.out[r] + P * B, kSiteFusedGather))
+      bulk_store(dst, buf + k * static_cast<uint32_t>(sub), len);
+    bulk_commit();
+    if (S == 1) {  // one stage: refill it once its store has read it
+      if (i + 1 < items) {
+        bulk_wait_read<0>();
+        issue(0, i + 1);
+      }
+    } else if (i > 0 && i + S - 1 < items) {  // refill the stage drained one step ago
+      bulk_wait_read<1>();
+      issue(kprev, i + S - 1);
+    }
+    kprev = k;
+    k = (k + 1 == S) ? 0 : k + 1;
+  }
+  if (!ok)
+    for (uint32_t q = 0; q < S; ++q)
+      if ((inflight >> q) & 1u) mbar_wait_bounded(bars + 8u * q, (phase >> q) & 1u, p.wait_ns);
+  bulk_wait_read<0>();  // the stores have read the stages; their writes complete with the grid
+  return ok;
+}
+
 __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __grid_constant__ FusedParams p) {
   __shared__ int s_ok[1];
   const uint32_t P = static_cast<uint32_t>(p.P), G = static_cast<uint32_t>(p.G);
@@ -168,17 +252,23 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
   }
   __syncthreads();
   if (!s_ok[0]) return;
-  for (uint32_t i = 0; i < P; ++i) {
-    const uint32_t q = q0 + i < P ? q0 + i : q0 + i - P;
-    copy_chunk<true, 8>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
-                        reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n,
-                        p.staging[q], p.staging[q] + p.bytes, p.out[r], p.out[r] + P * p.bytes,
-                        kSiteFusedGather);
+  if (p.tma) {
+    // one thread drives the TMA ring; the others are done
+    if (threadIdx.x != 0) return;
+    if (!gather_tma(p, r, c, q0, lo, n)) return;  // fault recorded; no completion to publish
+  } else {
+    for (uint32_t i = 0; i < P; ++i) {
+      const uint32_t q = q0 + i < P ? q0 + i : q0 + i - P;
+      copy_chunk<true, 8>(reinterpret_cast<const uint8_t*>(p.staging[q]) + lo,
+                          reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<uint64_t>(q) * p.bytes + lo, n,
+                          p.staging[q], p.staging[q] + p.bytes, p.out[r], p.out[r] + P * p.bytes,
+                          kSiteFusedGather);
+    }
+    __threadfence();
+    __syncthreads();
   }
 
   // complete
-  __threadfence();
-  __syncthreads();
   if (threadIdx.x == 0) {
     if (in_bounds(&done[r * kFusedMaxChunks + c], 4, ws_lo, ws_hi, kSiteFusedFlag))
       st_release_u32(&done[r * kFusedMaxChunks + c], epoch);
@@ -193,9 +283,32 @@ __global__ void __launch_bounds__(kFusedBlock) dc_fused_gather_kernel(const __gr
 
 }  // namespace
 
-int fused_ctas_per_sm() {
+// Lets the kernel use `smem` bytes of dynamic shared memory (the TMA ring
+// needs more than the default 48 KB; the kernel's own static shared memory
+// counts against the same limit, so the attribute is raised to what a launch
+// asks for, per device, never lowered).
+cudaError_t allow_fused_smem(size_t smem) {
+  if (smem <= 48u * 1024u) return cudaSuccess;
+  constexpr int kDevices = 64;
+  static std::atomic<size_t> allowed[kDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+  if (allowed[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(dc_fused_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  size_t cur = allowed[dev].load(std::memory_order_relaxed);
+  while (cur < smem && !allowed[dev].compare_exchange_weak(cur, smem)) {
+  }
+  return cudaSuccess;
+}
+
+int fused_ctas_per_sm(size_t smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_fused_gather_kernel, kFusedBlock, 0) != cudaSuccess) {
+  if (allow_fused_smem(smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dc_fused_gather_kernel, kFusedBlock, smem) != cudaSuccess) {
     cudaGetLastError();
     return 1;
   }
@@ -206,10 +319,15 @@ cudaError_t launch_fused_gather(const FusedParams& p, cudaStream_t s) {
   if (p.P < 1 || p.P > kMaxRanks || p.G < 1 || p.G > kFusedMaxChunks || (p.chunk & 15u) || (p.bytes & 15u) ||
       p.epoch == 0 || static_cast<uint64_t>(p.G) * p.chunk < p.bytes)
     return cudaErrorInvalidValue;
+  const size_t smem = fused_smem_bytes(p.tma, p.stages, p.sub);
+  if (p.tma && (p.stages < 1 || p.stages > 32 || p.sub < 16 || (p.sub & 15u) || smem > kFusedMaxSmem))
+    return cudaErrorInvalidValue;
+  cudaError_t e = allow_fused_smem(smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.P * p.G));
   cfg.blockDim = dim3(kFusedBlock);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -171,12 +171,21 @@ struct FusedParams {
   uint32_t epoch;      // nonzero, new for every call since the workspace was cleared
   int32_t P;
   int32_t G;
+  int32_t tma;         // 1: the gather step streams the staged chunks through the TMA engine
+  int32_t stages;      // ... in a ring of `stages` shared-memory stages
+  uint32_t sub;        // ... of `sub` bytes (a multiple of 16)
 };
+// Dynamic shared memory of a fused launch (the TMA ring and its mbarriers),
+// at most kFusedMaxSmem (the kernel has static shared memory as well).
+constexpr size_t kFusedMaxSmem = 226 * 1024;
+__host__ __device__ constexpr size_t fused_smem_bytes(int tma, int stages, uint32_t sub) {
+  return tma ? static_cast<size_t>(stages) * (static_cast<size_t>(sub) + 8) : 0;
+}
 __host__ __device__ constexpr size_t fused_workspace_bytes(int P) {
   return static_cast<size_t>(P) * kFusedMaxChunks * 2 * sizeof(uint32_t);
 }
 cudaError_t launch_fused_gather(const FusedParams& p, cudaStream_t s);
-int fused_ctas_per_sm();
+int fused_ctas_per_sm(size_t smem);
 // The allocation-free form (dc_fused_all_gather_static): the flags and the
 // staging buffers live in a static device array of this many staging bytes
 // (rank r's buffer at r * fused_static_stride(bytes)) after the flags of
